@@ -1,0 +1,252 @@
+"""Pins of the oracle's quantizer and all-reduce (CPU only): scale hierarchy
+invariants, exactness on level-aligned inputs, Monte-Carlo unbiasedness, and
+the error orderings the pages state (correlated < independent rounding,
+butterfly < ring, more bits < fewer bits)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from quantized_hop_gradient_gb300 import synth
+
+
+def _sg(rs, scale=1.0):
+    return (rs.standard_normal(256) * scale).astype(np.float32)
+
+
+# --------------------------------------------------------------------------- scale hierarchy
+@pytest.mark.parametrize("mag", [1e-38, 1e-30, 1e-3, 1.0, 255.0, 256.0, 1e30])
+def test_scale_hierarchy_invariants(mag):
+    rs = np.random.default_rng(int(abs(math.log10(mag))) + 11)
+    for trial in range(20):
+        x = _sg(rs, mag) * np.exp(rs.normal(0, 2, 256)).astype(np.float32)
+        if trial % 5 == 0:
+            x[rs.integers(0, 16) * 16:][:16] = 0.0        # an all-zero group
+        E, u, codes = oracle.quantize_sg(x, 4, seed=trial)
+        s = np.abs(x.astype(np.float64)).reshape(16, 16).max(1)
+        S = s.max()
+        if S == 0:
+            assert E == 0 and np.all(u == 0)
+            continue
+        e = E - 127
+        assert -126 <= e <= 127
+        assert 255.0 * 2.0 ** e >= S
+        if e > -126:
+            assert 255.0 * 2.0 ** (e - 1) < S          # e is the smallest
+        d = 2.0 ** e
+        sigma = u.astype(np.float64) * d
+        assert np.all(sigma >= s)                         # scale rounded up
+        pos = u > 0
+        assert np.all((u[pos] - 1) * d < s[pos])          # u is the smallest
+        assert np.all((u == 0) == (s == 0))
+        if e > -126:
+            assert u.max() >= 128                          # >= 7 bits for the largest group
+
+
+# --------------------------------------------------------------------------- exactness
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("m", [-20, -3, 0, 5, 40])
+def test_exact_on_level_aligned_inputs(bits, m):
+    """x = 2^m q_k with every group reaching 2^m exactly: sigma = 2^m, y = q_k
+    exactly, so every coordinate decodes to itself whatever the uniforms."""
+    rs = np.random.default_rng(bits * 100 + m + 50)
+    q = oracle.level_table(bits, 1.0)
+    L = 1 << bits
+    k = rs.integers(0, L, 256)
+    k[::16] = L - 1 if rs.random() < 0.5 else 0       # a group max at +-2^m
+    x = (q[k].astype(np.float64) * 2.0 ** m).astype(np.float32)
+    for seed in range(3):
+        E, u, codes = oracle.quantize_sg(x, bits, seed=seed, round=seed)
+        assert np.all(u == 128)
+        assert np.array_equal(oracle.unpack_codes(codes, bits), k)
+        assert np.array_equal(oracle.dequantize_sg(E, u, codes, bits), x)
+
+
+def test_zero_supergroup_decodes_to_mean():
+    """A zero super-group is exact; constant super-groups normalise to zero,
+    so the all-reduce returns the exact sum."""
+    E, u, codes = oracle.quantize_sg(np.zeros(256, np.float32), 8)
+    assert E == 0 and np.all(u == 0)
+    assert np.all(oracle.dequantize_sg(E, u, codes, 8) == 0)
+    # all workers constant c on every super-group
+    N, J = 4, 6
+    c = np.array([0.5, -3.0, 0.0, 1024.0, 2.0 ** -10, -7.25], np.float32)
+    g = np.repeat(c, 256).astype(np.float32)
+    import torch
+    gb = torch.as_tensor(g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for butterfly in (False, True):
+        cfg = oracle.Config(N, 5.0, correlated=True)
+        _, out = oracle.allreduce(cfg, [gb] * N, butterfly=butterfly)
+        assert np.array_equal(out, N * g)
+
+
+# --------------------------------------------------------------------------- unbiasedness
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("correlated", [False, True])
+def test_quantizer_unbiased_monte_carlo(bits, correlated):
+    rs = np.random.default_rng(bits + 7 * correlated)
+    x = _sg(rs) * np.exp(rs.normal(0, 1, 256)).astype(np.float32)
+    R = 3000
+    acc = np.zeros(256)
+    acc2 = np.zeros(256)
+    for r in range(R):
+        E, u, codes = oracle.quantize_sg(x, bits, seed=5, round=r, n_ranks=8, correlated=correlated,
+                                         rank=r % 8, hop=r % 3, slot=r % 4, n_slots=4)
+        d = oracle.dequantize_sg(E, u, codes, bits).astype(np.float64)
+        acc += d
+        acc2 += d * d
+    mean = acc / R
+    sd = np.sqrt(np.maximum(acc2 / R - mean ** 2, 0))
+    se = sd / math.sqrt(R)
+    E, u, _ = oracle.quantize_sg(x, bits, seed=5)
+    sigma = np.repeat(u.astype(np.float64) * 2.0 ** (E - 127), 16)
+    bias_bound = sigma * 2.0 ** -16 * 2 + 1e-6 * np.abs(x)   # 16-bit uniforms, fp32 rounding
+    assert np.all(np.abs(mean - x) <= 5 * se + bias_bound)
+    z = (mean - x) / np.where(se > 0, se, 1)
+    assert abs(z.mean()) < 5 / math.sqrt(256)            # no systematic drift
+
+
+def test_allreduce_unbiased_monte_carlo():
+    """E[all-reduce output] = exact sum (ring and butterfly, N = 4)."""
+    w = synth.WORKLOADS["ring4_1m"].scaled(512)
+    gr = [synth.as_u16(g) for g in synth.generate(w, "cpu", seed=3)]
+    s = oracle.exact_sum(gr)
+    for butterfly in (False, True):
+        R = 600
+        acc = np.zeros_like(s)
+        acc2 = np.zeros_like(s)
+        for r in range(R):
+            _, out = oracle.allreduce(oracle.Config(4, 5.0, correlated=True, round=r), gr, butterfly=butterfly)
+            acc += out
+            acc2 += out.astype(np.float64) ** 2
+        mean = acc / R
+        se = np.sqrt(np.maximum(acc2 / R - mean ** 2, 0) / R)
+        tol = 5 * se + 1e-5 * np.abs(s) + 1e-30
+        assert np.mean(np.abs(mean - s) <= tol) > 0.999
+
+
+# --------------------------------------------------------------------------- error orderings
+def _vnmse(name, n, butterfly, correlated, budget=5.0, rounds=4, N=None):
+    w = synth.WORKLOADS[name]
+    w = w.scaled(n)
+    gr = [synth.as_u16(g) for g in synth.generate(w, "cpu", seed=9)]
+    N = N or w.n_ranks
+    gr = gr[:N]
+    v = []
+    for r in range(rounds):
+        cfg = oracle.Config(N, budget, correlated=correlated, round=r)
+        _, out = oracle.allreduce(cfg, gr, butterfly=butterfly)
+        v.append(oracle.vnmse(out, gr))
+    return float(np.mean(v))
+
+
+def test_correlated_rounding_lowers_error_in_butterfly():
+    """Workers that quantize the same coordinates in one butterfly stage share
+    stratified uniforms, so their rounding errors partly cancel in the sum."""
+    ind = _vnmse("bert_large_ring8", 1 << 16, True, False, rounds=6)
+    cor = _vnmse("bert_large_ring8", 1 << 16, True, True, rounds=6)
+    assert cor < ind
+    assert ind / cor < 2.5          # the scribe notes report "up to 2x"
+
+
+def test_butterfly_error_below_ring():
+    ring = _vnmse("llama1b_butterfly8", 1 << 16, False, True)
+    bfly = _vnmse("llama1b_butterfly8", 1 << 16, True, True)
+    assert bfly < ring
+
+
+def test_error_falls_with_budget():
+    v = [_vnmse("gemma1b_ring16", 1 << 16, False, True, budget=b, N=8) for b in (4.0, 5.0, 6.0)]
+    assert v[0] > v[1] > v[2]
+    # eight bits everywhere is far more accurate than two
+    assert _vnmse("ring4_1m", 1 << 14, False, True, budget=8.0) < 1e-3
+
+
+# --------------------------------------------------------------------------- message layout and schedule
+def test_message_bytes_formula():
+    for n2, n4, n8 in [(1, 0, 0), (0, 1, 0), (0, 0, 1), (3, 5, 7), (16, 0, 16), (0, 0, 0)]:
+        c = n2 + n4 + n8
+        assert oracle.message_bytes(n2, n4, n8) == -(-c // 16) * 16 + 16 * c + 64 * n2 + 128 * n4 + 256 * n8
+    # at 5 average code bits: (5 + 17*8/256)/8 bytes per coordinate
+    n2, n4, n8 = 0, 480, 160
+    assert 2 * n2 + 4 * n4 + 8 * n8 == 5 * 640
+    assert oracle.message_bytes(n2, n4, n8) / (640 * 256) == pytest.approx((5 + 17 * 8 / 256) / 8)
+
+
+def _ring_by_messages(cfg, gr, p):
+    N = cfg.n_ranks
+    lo = p.chunk_lo
+    N2, N4 = int(p.counts[0]), int(p.counts[1])
+    msg = {}
+    for t in range(N):
+        new = {}
+        for r in range(N):
+            c = (r - 1 - t) % N
+            if t == 0:
+                new[r] = oracle.compress(cfg, lo[c], lo[c + 1], N2, N4, r, 0, gr[r], p.M, p.perm)
+            else:
+                new[r], _ = oracle.dar(cfg, lo[c], lo[c + 1], N2, N4, r, t, msg[(r - 1) % N], gr[r], p.M,
+                                       p.perm, send=(lo[c], lo[c + 1]))
+        msg = new
+    out = np.zeros(p.b.size * 256, np.float32)
+    for c in range(N):
+        oracle.decode(cfg, lo[c], lo[c + 1], N2, N4, msg[c], p.M, p.perm, out)
+    return out
+
+
+def _butterfly_by_messages(cfg, gr, p):
+    N = cfg.n_ranks
+    L = N.bit_length() - 1
+    lo = p.chunk_lo
+    N2, N4 = int(p.counts[0]), int(p.counts[1])
+
+    def span(s, r, keep):
+        width = 1 << (L - s)
+        half = width >> 1
+        base = (r >> (L - s)) << (L - s)
+        my = (r >> (L - 1 - s)) & 1
+        a = base + (my if keep else 1 - my) * half
+        return lo[a], lo[a + half]
+
+    def slots(s, r):
+        n = 1 << (L - 1 - s)
+        return dict(slot=r & (n - 1), n_slots=n)
+
+    if L == 0:
+        out = np.zeros(p.b.size * 256, np.float32)
+        m = oracle.compress(cfg, lo[0], lo[1], N2, N4, 0, 0, gr[0], p.M, p.perm)
+        return oracle.decode(cfg, lo[0], lo[1], N2, N4, m, p.M, p.perm, out)
+    msg = {r: oracle.compress(cfg, *span(0, r, False), N2, N4, r, 0, gr[r], p.M, p.perm, **slots(0, r))
+           for r in range(N)}
+    part = {r: gr[r] for r in range(N)}
+    for s in range(1, L):
+        new_msg, new_part = {}, {}
+        for r in range(N):
+            a, b = span(s - 1, r, True)
+            new_msg[r], new_part[r] = oracle.dar(cfg, a, b, N2, N4, r, s, msg[r ^ (N >> s)], part[r], p.M,
+                                                 p.perm, send=span(s, r, False), keep=span(s, r, True),
+                                                 **slots(s, r))
+        msg, part = new_msg, new_part
+    fin = {}
+    for r in range(N):
+        fin[r], _ = oracle.dar(cfg, lo[r], lo[r + 1], N2, N4, r, L, msg[r ^ 1], part[r], p.M, p.perm,
+                               send=(lo[r], lo[r + 1]))
+    out = np.zeros(p.b.size * 256, np.float32)
+    for c in range(N):
+        oracle.decode(cfg, lo[c], lo[c + 1], N2, N4, fin[c], p.M, p.perm, out)
+    return out
+
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8])
+@pytest.mark.parametrize("correlated", [False, True])
+def test_message_path_equals_per_supergroup_path(N, correlated):
+    """The chunked, message-level schedule (compress / dar / decode over
+    layouts) gives bit-identical results to the per-super-group walk."""
+    w = synth.WORKLOADS["ring4_1m"].scaled(256 * 37)
+    gr = [synth.as_u16(g) for g in synth.generate(w.__class__(**{**w.__dict__, "n_ranks": N}), "cpu", seed=4)]
+    cfg = oracle.Config(N, 4.5, correlated=correlated, seed=3, round=2)
+    p, out = oracle.allreduce(cfg, gr, butterfly=False)
+    assert np.array_equal(_ring_by_messages(cfg, gr, p), out)
+    p, out = oracle.allreduce(cfg, gr, butterfly=True)
+    assert np.array_equal(_butterfly_by_messages(cfg, gr, p), out)
