@@ -1,0 +1,252 @@
+/*
+ * dq.h -- C ABI of libdq, a GB300 (sm_103a) implementation of the
+ * data-parallel hot path of DynamiQ, a gradient-quantization scheme for
+ * multi-hop all-reduce (arXiv 2602.08923).
+ *
+ * Sources, cited per entry point below:
+ *   [S] everythinginsigcomm.group scribe notes, "DynamiQ: Accelerating
+ *       Gradient Synchronization using Compressed Multi-hop All-reduce",
+ *       sections "Key idea and contribution" and "Evaluation".
+ *   [P] pith.science review of the same paper: "What carries the argument",
+ *       "Referee Report" (Summary, major comment 1, minor comment 1),
+ *       "Axiom & Free-Parameter Ledger", Fig. 2 and Fig. 3 captions.
+ *   [A] mlsanity.com page of the paper, Abstract.
+ *
+ * Vocabulary.  A group is 16 consecutive coordinates sharing one scale; a
+ * super-group (SG) is 16 groups = 256 consecutive coordinates sharing a
+ * bitwidth, a mean and a squared norm [P "What carries the argument"].
+ * n_sg = J is the number of super-groups of one worker's gradient (the
+ * gradient length is J * 256; pad with zeros).  N = n_ranks workers are
+ * simulated on one GPU: each worker's buffers are ordinary device buffers and
+ * a "hop" hands a message buffer from one simulated rank to the next.
+ *
+ * Conventions (all entry points):
+ *   - Device pointers are cudaMalloc/PyTorch device memory on the current
+ *     device; "host" marks the few host pointers.  The caller owns every
+ *     buffer; the library never allocates device memory.
+ *   - stream is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     enqueued asynchronously; only dq_plan synchronises (it reads three
+ *     counts back to the host).
+ *   - Gradient, message, mean and output pointers must be 16-byte aligned
+ *     (DQ_ERR_ALIGNMENT otherwise).
+ *   - The return value reports argument validation and the launch status
+ *     (cudaGetLastError); nothing is launched when validation fails.
+ *   - Calls on one stream are ordered; calls that share output buffers must
+ *     not overlap on different streams.
+ *   - Non-finite gradient values are outside the method's domain: results
+ *     are unspecified (no fault, no hang).
+ */
+#ifndef DQ_H
+#define DQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DQ_OK = 0,
+    DQ_ERR_INVALID_ARG = 1,        /* null pointer, bad size, bad range, bad N   */
+    DQ_ERR_ALIGNMENT = 2,          /* a pointer is not 16-byte aligned           */
+    DQ_ERR_BUDGET_INFEASIBLE = 3,  /* budget below 2 bits per coordinate         */
+    DQ_ERR_CUDA = 4                /* a CUDA call or kernel launch failed        */
+} dq_status;
+
+/* Parameters of one all-reduce round. */
+typedef struct {
+    int32_t  n_ranks;      /* N, 1 .. 65535 (butterfly: a power of two)              */
+    float    budget_bits;  /* B, average code bits per coordinate, >= 2             */
+    double   eps;          /* level shape: q = sign(r) |r|(eps+|r|)/(1+eps); > 0, or
+                              +inf for uniform levels; 1.0 by default              */
+    int32_t  correlated;   /* 1: correlated rounding across ranks, 0: independent  */
+    uint64_t seed;         /* key of the counter-based generator                    */
+    uint64_t round;        /* training round (part of the generator counter)        */
+} dq_config;
+
+/* Who quantizes, for the stochastic-rounding generator.  Independent
+ * rounding draws from a stream keyed by (seed, round, hop, rank, coordinate).
+ * Correlated rounding [S "Key idea and contribution": shared randomness
+ * across workers so that rounding errors cancel, up to 2x lower variance]
+ * draws one uniform per (seed, round, hop, coordinate), shared by all
+ * workers, and worker `slot` of the n_slots workers that quantize the same
+ * coordinates at the same stage shifts it by slot/n_slots (one uniform per
+ * stratum).  A fresh uniform per stage keeps every hop exactly unbiased.
+ * Ring stages and the owner's final quantization have n_slots = 1;
+ * butterfly step s (of L = log2 N) has n_slots = 2^(L-1-s), slot = the low
+ * L-1-s bits of the rank. */
+typedef struct {
+    int32_t rank;     /* quantizing worker, 0 .. N-1                       */
+    int32_t hop;      /* quantization stage of these coordinates, 0..65535 */
+    int32_t slot;     /* 0 .. n_slots-1                                    */
+    int32_t n_slots;  /* >= 1                                              */
+} dq_stage;
+
+/* A range of REORDERED super-groups [lo, hi).  After reordering, SGs
+ * [0, end2) are 2-bit, [end2, end4) 4-bit and [end4, J) 8-bit. */
+typedef struct {
+    int64_t lo, hi;
+    int64_t end2, end4;
+} dq_range;
+
+/* Version string of the library. */
+const char *dq_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char *dq_status_string(dq_status s);
+
+/* Bytes of the message that carries range r (host, pure).  Layout, for
+ * c = hi - lo SGs of which n2, n4, n8 have 2, 4, 8 bits:
+ *   [E: c exponent bytes, padded to a multiple of 16][u: 16 bytes per SG]
+ *   [2-bit codes, 64 B per SG][4-bit codes, 128 B per SG][8-bit, 256 B per SG]
+ * Coordinate i of an SG occupies bits [b*i, b*i+b) of the SG's code block,
+ * least significant bits first.  [S "Key idea and contribution": groups and
+ * super-groups; P Referee Report summary: hierarchical UINT8 group scaling] */
+size_t dq_message_bytes(dq_range r);
+
+/* Level table of the library for b in {2, 4, 8} (host, pure): writes 2^b
+ * fp32 levels to q_host.  [P ledger: Q = {f(eps, r)}; S "Key idea and
+ * contribution": more levels near zero] */
+dq_status dq_level_table(int32_t bits, double eps, float *q_host);
+
+/* Per-super-group statistics of ONE worker [S "Key idea and contribution":
+ * each worker computes the mean and squared l2 norm of each super-group;
+ * P major comment 1: F is computed before the mean is subtracted].
+ *   g_bf16: device, J*256 bf16 values.  mean, sq: device, J floats each.
+ *   Sums are fp32 in a fixed halving tree (16 coords of a group, then the 16
+ *   group partials); mean = sum / 256. */
+dq_status dq_stats(const void *g_bf16, int64_t n_sg, float *mean, float *sq, void *stream);
+
+/* Metadata all-reduce, simulated [S "Key idea and contribution": a
+ * lightweight all-reduce of the statistics; P Fig. 2(b)].
+ *   mean_all, sq_all: device, N x J row-major (row r = rank r's dq_stats).
+ *   M, F: device, J floats: M_j = sum of means, F_j = sum of squared norms,
+ *   each added in rank order 0..N-1 in fp32. */
+dq_status dq_stats_reduce(const float *mean_all, const float *sq_all, int32_t n_ranks,
+                          int64_t n_sg, float *M, float *F, void *stream);
+
+/* Device scratch needed by dq_allocate and dq_reorder for J super-groups. */
+size_t dq_workspace_bytes(int64_t n_sg);
+
+/* Bitwidth allocation [P "What carries the argument" and Fig. 3 caption:
+ * thresholds tied by T_{2,4} = 17/512 T_{4,8}, one scalar meets any budget].
+ *   b_j = 8 if 17 F_j >= 512 T, 4 if F_j >= T, else 2, where T is the
+ *   smallest non-negative fp32 with sum_j b_j <= floor(B * J).
+ *   F: device, J floats (finite, >= 0).  b: device, J bytes.  T_dev: device,
+ *   1 float.  counts_dev: device, 3 int64 (number of 2-, 4-, 8-bit SGs).
+ *   ws: device scratch of at least dq_workspace_bytes(J) bytes.
+ *   Errors: DQ_ERR_BUDGET_INFEASIBLE if budget < 2; J must be < 2^27. */
+dq_status dq_allocate(const float *F, int64_t n_sg, float budget, uint8_t *b, float *T_dev,
+                      int64_t *counts_dev, void *ws, size_t ws_bytes, void *stream);
+
+/* Reordering by bitwidth [S "Key idea and contribution": reorder the
+ * super-groups by bitwidth, same bitwidth contiguous; P Fig. 2(c)].
+ *   Stable partition 2-bit, 4-bit, 8-bit.  perm: device, J int32,
+ *   perm[new] = old.  ws as for dq_allocate. */
+dq_status dq_reorder(const uint8_t *b, int64_t n_sg, int32_t *perm, void *ws, size_t ws_bytes,
+                     void *stream);
+
+/* Chunk cuts of the reordered stream among n_chunks workers (host, pure):
+ * chunk_lo_host[c] = the smallest reordered index whose prefix of code bits
+ * reaches ceil(c * total / n_chunks); chunk_lo_host[n_chunks] = J.  Chunks
+ * carry near-equal code bits (equal bytes per hop). */
+dq_status dq_chunk_cuts(int64_t n2, int64_t n4, int64_t n8, int32_t n_chunks,
+                        int64_t *chunk_lo_host);
+
+/* First hop: quantize one worker's normalised gradient over range r
+ * [S "Key idea and contribution": each worker normalises by the global mean
+ * and quantizes; non-uniform levels, UINT8 second-level scales, correlated
+ * rounding].  x = fl(float(g[perm[j]*256 + i]) - M[perm[j]] / N).
+ *   hop: quantization stage index; rank: the quantizing rank (generator
+ *   counter and correlated offset).  msg_out: device, dq_message_bytes(r). */
+dq_status dq_compress(const dq_config *cfg, dq_range r, dq_stage stage, const void *g_bf16,
+                      const float *M, const int32_t *perm, uint8_t *msg_out, void *stream);
+
+/* One hop: decompress - accumulate - recompress, fused [S "Key idea and
+ * contribution": decompress the incoming partial sum, accumulate the local
+ * gradient, recompress, forward; S: a fused CUDA kernel; A].
+ *   x = fl(dec(msg_in) + addend) over range in.
+ *   addend: addend_is_fp32 = 0: the worker's bf16 gradient (full J*256, read
+ *   through perm, mean subtracted); = 1: fp32 partial sums, row j - in.lo.
+ *   SGs in `send` are requantized into msg_out (dq_message_bytes(send));
+ *   SGs in `keep` are written as fp32 to keep_out (row j - keep.lo).
+ *   send and keep must split `in` into two adjacent ranges (either may be
+ *   empty): a ring hop sends everything, a butterfly step sends one half and
+ *   keeps the other. */
+dq_status dq_dar(const dq_config *cfg, dq_range in, dq_stage stage, const uint8_t *msg_in,
+                 const void *addend, int32_t addend_is_fp32, const float *M, const int32_t *perm, dq_range send, uint8_t *msg_out,
+                 dq_range keep, float *keep_out, void *stream);
+
+/* Final decode [S "Key idea and contribution": restore the original
+ * super-group order and add back the subtracted mean; P Referee Report
+ * summary: the receiver unnormalises].  out[perm[j]*256 + i] =
+ * fl(dec + fl(fl(M/N) * N)), fp32 (out_is_bf16 = 0) or rounded to bf16. */
+dq_status dq_decode(const dq_config *cfg, dq_range r, const uint8_t *msg, const float *M,
+                    const int32_t *perm, void *out, int32_t out_is_bf16, void *stream);
+
+/* ---- the whole round: statistics to decode, N simulated ranks ---------- */
+
+/* Result of the planning phase, filled by dq_plan. */
+typedef struct {
+    float   T;            /* the threshold T_{2,4} */
+    int64_t n2, n4, n8;   /* SGs per bitwidth */
+} dq_plan_info;
+
+/* Device bytes dq_plan needs in plan_ws for N ranks and J super-groups. */
+size_t dq_plan_workspace_bytes(int32_t n_ranks, int64_t n_sg);
+
+/* Planning phase of one all-reduce round over N ranks [S "Key idea and
+ * contribution", statistics collection phase; P Fig. 2(a)-(c)]: per-rank
+ * statistics, metadata all-reduce, allocation and reordering.
+ *   grads_host: host array of N device pointers (J*256 bf16 each).
+ *   M, perm: device outputs (J floats, J int32) used by dq_exchange.
+ *   info_host: host output.  Synchronises `stream` once to read the counts.
+ *   plan_ws: device scratch of dq_plan_workspace_bytes(N, J). */
+dq_status dq_plan(const dq_config *cfg, const void *const *grads_host, int64_t n_sg,
+                  float *M, int32_t *perm, void *plan_ws, size_t plan_ws_bytes,
+                  dq_plan_info *info_host, void *stream);
+
+/* Optional record of the kernel launches of dq_exchange, for timing them on
+ * the launching stream.  events: host array of 2*capacity cudaEvent_t created
+ * by the caller (timing enabled); launch i is bracketed by events[2i] and
+ * events[2i+1].  kinds[i]: DQ_LAUNCH_*; sgs[i]: super-groups it processed.
+ * count: in, first free slot; out, slots used.  Launches beyond capacity
+ * are not recorded (they still run). */
+enum { DQ_LAUNCH_COMPRESS = 0, DQ_LAUNCH_DAR = 1, DQ_LAUNCH_DECODE = 2 };
+typedef struct {
+    void   **events;
+    int32_t *kinds;
+    int64_t *sgs;
+    int32_t  capacity;
+    int32_t  count;
+} dq_launch_log;
+
+/* Number of kernels libdq has launched in this process (all entry points). */
+uint64_t dq_launch_count(void);
+
+/* Device bytes dq_exchange needs (messages and butterfly partial sums). */
+size_t dq_exchange_workspace_bytes(const dq_config *cfg, int32_t butterfly, int64_t n_sg,
+                                   const dq_plan_info *info);
+
+/* Main all-reduce phase [S "Key idea and contribution": hop-by-hop
+ * decompress-accumulate-recompress, then restore order and add the mean;
+ * S "Evaluation": ring and butterfly topologies].  Ring: reduce-scatter of
+ * N-1 DAR hops, the owner's DAR giving the final chunk, all-gather forwarding
+ * the bytes unchanged.  Butterfly: recursive halving with split DAR (one half
+ * sent compressed, the other kept in fp32), the owner compressing its chunk
+ * once.  Every rank then decodes all chunks into outs_host[r] (device, J*256
+ * fp32, or bf16 if out_is_bf16).  final_msgs_host, if not NULL, receives the
+ * N device pointers (inside ws) of the final chunk messages.  log: NULL or
+ * a dq_launch_log to fill.  No sync. */
+dq_status dq_exchange(const dq_config *cfg, int32_t butterfly, const void *const *grads_host,
+                      int64_t n_sg, const float *M, const int32_t *perm,
+                      const dq_plan_info *info, void *ws, size_t ws_bytes,
+                      void *const *outs_host, int32_t out_is_bf16,
+                      const uint8_t **final_msgs_host, dq_launch_log *log, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DQ_H */

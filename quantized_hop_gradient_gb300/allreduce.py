@@ -1,0 +1,82 @@
+"""N simulated ranks on one GPU: one DynamiQ all-reduce round per call.
+
+Holds the device buffers of the planning and exchange phases and calls the
+two schedule entry points of libdq (``dq_plan``, ``dq_exchange``).  The
+workers' gradients are device tensors; a "hop" is a message buffer handed
+from one simulated rank to the next inside the exchange workspace.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import dq
+
+SG = dq.SG
+
+
+class DynamiQAllReduce:
+    def __init__(self, n_ranks: int, n_sg: int, *, budget: float = 5.0, eps: float = 1.0,
+                 correlated: bool = True, butterfly: bool = False, seed: int = 0,
+                 out_dtype: torch.dtype = torch.float32, device="cuda"):
+        self.n_ranks, self.n_sg = n_ranks, n_sg
+        self.budget, self.eps, self.correlated, self.butterfly = budget, eps, correlated, butterfly
+        self.seed = seed
+        self.out_dtype = out_dtype
+        self.device = torch.device(device)
+        dq.lib()
+        self.M = torch.empty(n_sg, dtype=torch.float32, device=self.device)
+        self.perm = torch.empty(n_sg, dtype=torch.int32, device=self.device)
+        nb = dq.dq_plan_workspace_bytes(n_ranks, n_sg)
+        self.plan_ws = torch.empty(nb, dtype=torch.uint8, device=self.device)
+        self.ws = torch.empty(0, dtype=torch.uint8, device=self.device)
+        self.info = None
+        self.final = None
+
+    def config(self, round: int = 0):
+        return dq.config(self.n_ranks, self.budget, self.eps, self.correlated, self.seed, round)
+
+    def plan(self, grads, round: int = 0, stream=None):
+        cfg = self.config(round)
+        self.info = dq.dq_plan(cfg, grads, self.n_sg, self.M, self.perm, self.plan_ws, self.plan_ws.numel(),
+                               stream)
+        return self.info
+
+    def reserve(self, nbytes: int):
+        if self.ws.numel() < nbytes:
+            self.ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+
+    def exchange(self, grads, outs, round: int = 0, stream=None, log=None):
+        cfg = self.config(round)
+        need = dq.dq_exchange_workspace_bytes(cfg, self.butterfly, self.n_sg, self.info)
+        if need == 0:
+            raise dq.DQError(dq.DQ_ERR_INVALID_ARG, "dq_exchange_workspace_bytes")
+        self.reserve(need)
+        self.final = dq.dq_exchange(cfg, self.butterfly, grads, self.n_sg, self.M, self.perm, self.info,
+                                    self.ws, self.ws.numel(), outs, self.out_dtype == torch.bfloat16, log,
+                                    stream)
+        return outs
+
+    def new_outputs(self):
+        return [torch.empty(self.n_sg * SG, dtype=self.out_dtype, device=self.device)
+                for _ in range(self.n_ranks)]
+
+    def __call__(self, grads, round: int = 0, outs=None, stream=None):
+        if len(grads) != self.n_ranks:
+            raise ValueError("one gradient per rank")
+        if outs is None:
+            outs = self.new_outputs()
+        self.plan(grads, round, stream)
+        return self.exchange(grads, outs, round, stream)
+
+    def chunk_lo(self):
+        i = self.info
+        return dq.dq_chunk_cuts(i.n2, i.n4, i.n8, self.n_ranks)
+
+    def final_message(self, c: int) -> torch.Tensor:
+        """Copy of the final message of chunk c (device bytes -> host uint8)."""
+        lo = self.chunk_lo()
+        i = self.info
+        r = dq.rng(lo[c], lo[c + 1], i.n2, i.n2 + i.n4)
+        nb = dq.dq_message_bytes(r)
+        off = self.final[c] - self.ws.data_ptr()
+        return self.ws[off:off + nb].cpu()

@@ -1,0 +1,33 @@
+// dq_internal.h -- declarations shared by the libdq translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dq_common.cuh"
+
+namespace dq {
+
+int sm_count();            // SMs of the current device (cached per device)
+void note_launches(int n);  // adds to the library's launch counter
+
+// Level tables for eps (host; cached).  Returns false for an invalid eps.
+bool build_tables(double eps, Tables *out);
+
+// Message view of range [lo, hi) with stream boundaries end2, end4.
+MsgView msg_view(uint8_t *base, int64_t lo, int64_t hi, int64_t end2, int64_t end4);
+size_t msg_bytes(int64_t c, int64_t n2, int64_t n4, int64_t n8);
+
+cudaError_t launch_stats(const uint16_t *g, int64_t n_sg, float *mean, float *sq, cudaStream_t st);
+cudaError_t launch_stats_reduce(const float *mean_all, const float *sq_all, int32_t n, int64_t n_sg,
+                                float *M, float *F, cudaStream_t st);
+cudaError_t launch_hop(const HopParams &P, bool has_in, bool add_f32, cudaStream_t st);
+cudaError_t launch_decode(const DecodeParams &P, cudaStream_t st);
+
+// Allocation (radix select of T) and reordering; ws is device scratch.
+size_t plan_scratch_bytes(int64_t n_sg);
+cudaError_t launch_allocate(const float *F, int64_t n_sg, int64_t cap_bits, uint8_t *b, float *T,
+                            int64_t *counts, void *ws, cudaStream_t st);
+cudaError_t launch_reorder(const uint8_t *b, int64_t n_sg, int32_t *perm, void *ws, cudaStream_t st);
+
+}  // namespace dq

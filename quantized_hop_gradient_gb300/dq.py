@@ -1,0 +1,273 @@
+"""Thin Python binding of libdq (argument marshalling only).
+
+Every function here has the name of a C entry point of ``include/dq.h`` and
+only converts arguments: torch tensors become device pointers, the current
+torch stream becomes the cudaStream_t, status codes become exceptions.  All
+computation runs in libdq's CUDA kernels; there is no fallback: loading fails
+loudly if the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+SG = 256
+DQ_OK, DQ_ERR_INVALID_ARG, DQ_ERR_ALIGNMENT, DQ_ERR_BUDGET_INFEASIBLE, DQ_ERR_CUDA = range(5)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DQError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class BudgetInfeasible(DQError):
+    pass
+
+
+class dq_config(C.Structure):
+    _fields_ = [("n_ranks", C.c_int32), ("budget_bits", C.c_float), ("eps", C.c_double),
+                ("correlated", C.c_int32), ("seed", C.c_uint64), ("round", C.c_uint64)]
+
+
+class dq_stage(C.Structure):
+    _fields_ = [("rank", C.c_int32), ("hop", C.c_int32), ("slot", C.c_int32), ("n_slots", C.c_int32)]
+
+
+class dq_range(C.Structure):
+    _fields_ = [("lo", C.c_int64), ("hi", C.c_int64), ("end2", C.c_int64), ("end4", C.c_int64)]
+
+
+class dq_launch_log(C.Structure):
+    _fields_ = [("events", C.c_void_p), ("kinds", C.c_void_p), ("sgs", C.c_void_p),
+                ("capacity", C.c_int32), ("count", C.c_int32)]
+
+
+DQ_LAUNCH_COMPRESS, DQ_LAUNCH_DAR, DQ_LAUNCH_DECODE = 0, 1, 2
+
+
+class dq_plan_info(C.Structure):
+    _fields_ = [("T", C.c_float), ("n2", C.c_int64), ("n4", C.c_int64), ("n8", C.c_int64)]
+
+
+_SIGS = {
+    "dq_version": ([], C.c_char_p),
+    "dq_launch_count": ([], C.c_uint64),
+    "dq_status_string": ([C.c_int], C.c_char_p),
+    "dq_message_bytes": ([dq_range], C.c_size_t),
+    "dq_level_table": ([C.c_int32, C.c_double, C.c_void_p], C.c_int),
+    "dq_stats": ([C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+    "dq_stats_reduce": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_int64, C.c_void_p, C.c_void_p,
+                         C.c_void_p], C.c_int),
+    "dq_workspace_bytes": ([C.c_int64], C.c_size_t),
+    "dq_allocate": ([C.c_void_p, C.c_int64, C.c_float, C.c_void_p, C.c_void_p, C.c_void_p,
+                     C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
+    "dq_reorder": ([C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
+    "dq_chunk_cuts": ([C.c_int64, C.c_int64, C.c_int64, C.c_int32, C.c_void_p], C.c_int),
+    "dq_compress": ([C.POINTER(dq_config), dq_range, dq_stage, C.c_void_p, C.c_void_p,
+                     C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+    "dq_dar": ([C.POINTER(dq_config), dq_range, dq_stage, C.c_void_p, C.c_void_p,
+                C.c_int32, C.c_void_p, C.c_void_p, dq_range, C.c_void_p, dq_range, C.c_void_p,
+                C.c_void_p], C.c_int),
+    "dq_decode": ([C.POINTER(dq_config), dq_range, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                   C.c_int32, C.c_void_p], C.c_int),
+    "dq_plan_workspace_bytes": ([C.c_int32, C.c_int64], C.c_size_t),
+    "dq_plan": ([C.POINTER(dq_config), C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p,
+                 C.c_size_t, C.POINTER(dq_plan_info), C.c_void_p], C.c_int),
+    "dq_exchange_workspace_bytes": ([C.POINTER(dq_config), C.c_int32, C.c_int64,
+                                     C.POINTER(dq_plan_info)], C.c_size_t),
+    "dq_exchange": ([C.POINTER(dq_config), C.c_int32, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
+                     C.POINTER(dq_plan_info), C.c_void_p, C.c_size_t, C.c_void_p, C.c_int32,
+                     C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib(build: bool = False):
+    """Loads libdq (building it first when ``build``).  Raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build else _build.LIB
+            if not os.path.exists(path):
+                raise ImportError(f"libdq is not built ({path}); run quantized_hop_gradient_gb300.build")
+            L = C.CDLL(path)
+            for name, (args, res) in _SIGS.items():
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = L
+    return _lib
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+def status_string(s: int) -> str:
+    return lib().dq_status_string(s).decode()
+
+
+def _check(status: int, what: str):
+    if status == DQ_ERR_BUDGET_INFEASIBLE:
+        raise BudgetInfeasible(status, what)
+    if status != DQ_OK:
+        raise DQError(status, what)
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def config(n_ranks: int, budget_bits: float = 5.0, eps: float = 1.0, correlated: bool = True,
+           seed: int = 0, round: int = 0) -> dq_config:
+    return dq_config(n_ranks, budget_bits, eps, int(correlated), seed, round)
+
+
+def rng(lo: int, hi: int, end2: int, end4: int) -> dq_range:
+    return dq_range(lo, hi, end2, end4)
+
+
+def stage(rank: int, hop: int, slot: int = 0, n_slots: int = 1) -> dq_stage:
+    return dq_stage(rank, hop, slot, n_slots)
+
+
+# ------------------------------------------------------------------ entry points (same names as dq.h)
+def dq_version() -> str:
+    return lib().dq_version().decode()
+
+
+def dq_launch_count() -> int:
+    return lib().dq_launch_count()
+
+
+def dq_message_bytes(r: dq_range) -> int:
+    return lib().dq_message_bytes(r)
+
+
+def dq_level_table(bits: int, eps: float = 1.0):
+    import numpy as np
+    q = np.zeros(1 << bits, np.float32)
+    _check(lib().dq_level_table(bits, eps, q.ctypes.data), "dq_level_table")
+    return q
+
+
+def dq_stats(g, n_sg, mean, sq, stream=None):
+    _check(lib().dq_stats(_ptr(g), n_sg, _ptr(mean), _ptr(sq), _stream(stream)), "dq_stats")
+
+
+def dq_stats_reduce(mean_all, sq_all, n_ranks, n_sg, M, F, stream=None):
+    _check(lib().dq_stats_reduce(_ptr(mean_all), _ptr(sq_all), n_ranks, n_sg, _ptr(M), _ptr(F),
+                                 _stream(stream)), "dq_stats_reduce")
+
+
+def dq_workspace_bytes(n_sg: int) -> int:
+    return lib().dq_workspace_bytes(n_sg)
+
+
+def dq_allocate(F, n_sg, budget, b, T_dev, counts_dev, ws, ws_bytes, stream=None):
+    _check(lib().dq_allocate(_ptr(F), n_sg, budget, _ptr(b), _ptr(T_dev), _ptr(counts_dev), _ptr(ws),
+                             ws_bytes, _stream(stream)), "dq_allocate")
+
+
+def dq_reorder(b, n_sg, perm, ws, ws_bytes, stream=None):
+    _check(lib().dq_reorder(_ptr(b), n_sg, _ptr(perm), _ptr(ws), ws_bytes, _stream(stream)), "dq_reorder")
+
+
+def dq_chunk_cuts(n2, n4, n8, n_chunks):
+    out = (C.c_int64 * (n_chunks + 1))()
+    _check(lib().dq_chunk_cuts(n2, n4, n8, n_chunks, C.addressof(out)), "dq_chunk_cuts")
+    return list(out)
+
+
+def dq_compress(cfg, r, st, g, M, perm, msg_out, stream=None):
+    _check(lib().dq_compress(C.byref(cfg), r, st, _ptr(g), _ptr(M), _ptr(perm), _ptr(msg_out),
+                             _stream(stream)), "dq_compress")
+
+
+def dq_dar(cfg, r_in, st, msg_in, addend, addend_is_fp32, M, perm, send, msg_out, keep, keep_out,
+           stream=None):
+    _check(lib().dq_dar(C.byref(cfg), r_in, st, _ptr(msg_in), _ptr(addend), int(addend_is_fp32),
+                        _ptr(M), _ptr(perm), send, _ptr(msg_out), keep, _ptr(keep_out), _stream(stream)),
+           "dq_dar")
+
+
+def dq_decode(cfg, r, msg, M, perm, out, out_is_bf16=False, stream=None):
+    _check(lib().dq_decode(C.byref(cfg), r, _ptr(msg), _ptr(M), _ptr(perm), _ptr(out), int(out_is_bf16),
+                           _stream(stream)), "dq_decode")
+
+
+def dq_plan_workspace_bytes(n_ranks, n_sg) -> int:
+    return lib().dq_plan_workspace_bytes(n_ranks, n_sg)
+
+
+def dq_plan(cfg, grads, n_sg, M, perm, ws, ws_bytes, stream=None) -> dq_plan_info:
+    ptrs = (C.c_void_p * len(grads))(*[_ptr(g) for g in grads])
+    info = dq_plan_info()
+    _check(lib().dq_plan(C.byref(cfg), C.cast(ptrs, C.c_void_p), n_sg, _ptr(M), _ptr(perm), _ptr(ws),
+                         ws_bytes, C.byref(info), _stream(stream)), "dq_plan")
+    return info
+
+
+def dq_exchange_workspace_bytes(cfg, butterfly, n_sg, info) -> int:
+    return lib().dq_exchange_workspace_bytes(C.byref(cfg), int(butterfly), n_sg, C.byref(info))
+
+
+class LaunchLog:
+    """Host side of a dq_launch_log: caller-created CUDA events (from torch)."""
+
+    def __init__(self, capacity: int, stream=None):
+        import numpy as np
+        st = torch.cuda.current_stream() if stream is None else stream
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * capacity)]
+        for e in self.events:          # torch creates the CUDA event on first record
+            e.record(st)
+        self._ev = (C.c_void_p * (2 * capacity))(*[e.cuda_event for e in self.events])
+        self.kinds = np.zeros(capacity, np.int32)
+        self.sgs = np.zeros(capacity, np.int64)
+        self.c = dq_launch_log(C.cast(self._ev, C.c_void_p), self.kinds.ctypes.data, self.sgs.ctypes.data,
+                               capacity, 0)
+
+    def launches(self):
+        """[(kind, super-groups, milliseconds)] of the recorded launches (after a sync)."""
+        return [(int(self.kinds[i]), int(self.sgs[i]), self.events[2 * i].elapsed_time(self.events[2 * i + 1]))
+                for i in range(self.c.count)]
+
+
+def dq_exchange(cfg, butterfly, grads, n_sg, M, perm, info, ws, ws_bytes, outs, out_is_bf16=False,
+                log: LaunchLog = None, stream=None):
+    """Returns the N device addresses of the final chunk messages (inside ws)."""
+    n = len(grads)
+    gp = (C.c_void_p * n)(*[_ptr(g) for g in grads])
+    op = (C.c_void_p * n)(*[_ptr(o) for o in outs])
+    fin = (C.c_void_p * n)()
+    _check(lib().dq_exchange(C.byref(cfg), int(butterfly), C.cast(gp, C.c_void_p), n_sg, _ptr(M), _ptr(perm),
+                             C.byref(info), _ptr(ws), ws_bytes, C.cast(op, C.c_void_p), int(out_is_bf16),
+                             C.cast(fin, C.c_void_p), C.byref(log.c) if log is not None else None,
+                             _stream(stream)), "dq_exchange")
+    return [fin[i] for i in range(n)]

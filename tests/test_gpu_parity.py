@@ -1,0 +1,259 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle, on the GPU.
+
+Bar: codes, scales, bitwidth maps, permutations, thresholds and counts
+bit-exact; decoded fp32 values bit-exact as well (both sides perform the
+same correctly rounded fp32 steps), which is stricter than the 1e-6
+relative bound the decode is held to; vNMSE equal.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_hop_gradient_gb300 import build, dq, synth
+from quantized_hop_gradient_gb300.allreduce import DynamiQAllReduce
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    dq.lib()
+
+
+def dev_u16(a):
+    """numpy uint16 bf16 patterns -> device bf16 tensor."""
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(DEV).view(torch.bfloat16)
+
+
+def host(t):
+    return t.detach().cpu().numpy()
+
+
+def bits32(a):
+    return np.ascontiguousarray(a, np.float32).view(np.int32)
+
+
+def grads_for(name, n, N=None, seed=0):
+    w = synth.WORKLOADS[name].scaled(n)
+    if N is not None:
+        w = w.__class__(**{**w.__dict__, "n_ranks": N})
+    return w, [synth.as_u16(g) for g in synth.generate(w, "cpu", seed=seed)]
+
+
+# --------------------------------------------------------------------------- statistics
+@pytest.mark.parametrize("J", [1, 3, 37, 4096, 20001])
+def test_stats_bit_exact(J):
+    _, gr = grads_for("ring4_1m", J * 256, seed=J)
+    for g in gr[:2]:
+        m = torch.empty(J, device=DEV)
+        q = torch.empty(J, device=DEV)
+        dq.dq_stats(dev_u16(g), J, m, q)
+        em, eq = oracle.stats(g)
+        assert np.array_equal(bits32(host(m)), bits32(em))
+        assert np.array_equal(bits32(host(q)), bits32(eq))
+
+
+def test_stats_reduce_bit_exact():
+    rs = np.random.default_rng(0)
+    for N, J in [(1, 5), (4, 4096), (16, 777)]:
+        means = (rs.standard_normal((N, J)) * 10.0 ** rs.integers(-8, 8, (N, J))).astype(np.float32)
+        sqs = np.abs(rs.standard_normal((N, J)) * 10.0 ** rs.integers(-8, 8, (N, J))).astype(np.float32)
+        M = torch.empty(J, device=DEV)
+        F = torch.empty(J, device=DEV)
+        dq.dq_stats_reduce(torch.from_numpy(means).to(DEV), torch.from_numpy(sqs).to(DEV), N, J, M, F)
+        eM, eF = oracle.stats_reduce(means, sqs)
+        assert np.array_equal(bits32(host(M)), bits32(eM))
+        assert np.array_equal(bits32(host(F)), bits32(eF))
+
+
+# --------------------------------------------------------------------------- allocation and reorder
+def _F_cases(rs):
+    yield np.exp(rs.normal(0, 3, 4096))
+    yield rs.choice([0.0, 1.0, 30.117647, 30.12, 1e6], 5000)
+    yield np.full(17, 2.5)
+    yield np.array([7.0])
+    yield np.zeros(64)
+    yield rs.exponential(1.0, 100_000) * 1e-35
+    yield np.exp(rs.normal(0, 8, 250_000))
+
+
+def test_allocate_bit_exact():
+    rs = np.random.default_rng(1)
+    for F in _F_cases(rs):
+        F = F.astype(np.float32)
+        J = F.size
+        Fd = torch.from_numpy(F).to(DEV)
+        ws = torch.empty(dq.dq_workspace_bytes(J), dtype=torch.uint8, device=DEV)
+        for B in (2.0, 2.01, 3.3, 4.0, 5.0, 6.0, 7.99, 8.0, 12.0):
+            b = torch.empty(J, dtype=torch.uint8, device=DEV)
+            T = torch.empty(1, device=DEV)
+            counts = torch.empty(3, dtype=torch.int64, device=DEV)
+            dq.dq_allocate(Fd, J, B, b, T, counts, ws, ws.numel())
+            eb, eT, ec = oracle.allocate(F, B)
+            assert bits32(host(T))[0] == bits32(np.array([eT]))[0], (J, B)
+            assert np.array_equal(host(b), eb)
+            assert np.array_equal(host(counts), ec)
+    with pytest.raises(dq.BudgetInfeasible):
+        dq.dq_allocate(Fd, J, 1.9, b, T, counts, ws, ws.numel())
+
+
+@pytest.mark.parametrize("J", [1, 5, 2047, 2048, 2049, 100_003])
+def test_reorder_bit_exact(J):
+    rs = np.random.default_rng(J)
+    b = rs.choice([2, 4, 8], J, p=[0.25, 0.5, 0.25]).astype(np.uint8)
+    perm = torch.empty(J, dtype=torch.int32, device=DEV)
+    ws = torch.empty(dq.dq_workspace_bytes(J), dtype=torch.uint8, device=DEV)
+    dq.dq_reorder(torch.from_numpy(b).to(DEV), J, perm, ws, ws.numel())
+    assert np.array_equal(host(perm), oracle.reorder(b))
+
+
+# --------------------------------------------------------------------------- compress / DAR / decode
+def _plan(gr, N, B=5.0):
+    cfg = oracle.Config(N, B)
+    return oracle.plan(cfg, gr)
+
+
+def _ranges(p, N):
+    lo = p.chunk_lo
+    N2, N4 = int(p.counts[0]), int(p.counts[1])
+    J = p.b.size
+    cuts = sorted({0, J, N2, N2 + N4, max(0, N2 - 3), min(J, N2 + 5), (N2 + N4) // 2})
+    out = [(int(lo[c]), int(lo[c + 1])) for c in range(N)]
+    out += [(cuts[i], cuts[j]) for i in range(len(cuts)) for j in range(i + 1, len(cuts))][:12]
+    return out, N2, N4
+
+
+@pytest.mark.parametrize("eps", [1.0, math.inf, 0.3])
+@pytest.mark.parametrize("correlated", [False, True])
+def test_compress_dar_decode_bit_exact(eps, correlated):
+    N = 4
+    _, gr = grads_for("ring4_1m", 256 * 3000, N=N, seed=5)
+    p = _plan(gr, N)
+    M = torch.from_numpy(p.M).to(DEV)
+    perm = torch.from_numpy(p.perm).to(DEV)
+    gd = [dev_u16(g) for g in gr]
+    cfg_o = oracle.Config(N, 5.0, eps=eps, correlated=correlated, seed=11, round=3)
+    cfg = dq.config(N, 5.0, eps=eps, correlated=correlated, seed=11, round=3)
+    ranges, N2, N4 = _ranges(p, N)
+    E4 = N2 + N4
+    for (a, b) in ranges:
+        if b <= a:
+            continue
+        r = dq.rng(a, b, N2, E4)
+        nb = dq.dq_message_bytes(r)
+        # compress
+        st = (1, 0, 1, 2)
+        msg = torch.zeros(nb, dtype=torch.uint8, device=DEV)
+        dq.dq_compress(cfg, r, dq.stage(*st), gd[1], M, perm, msg)
+        exp = oracle.compress(cfg_o, a, b, N2, N4, st[0], st[1], gr[1], p.M, p.perm, slot=st[2], n_slots=st[3])
+        assert np.array_equal(host(msg), exp), ("compress", a, b)
+        # ring DAR (bf16 addend)
+        out = torch.zeros(nb, dtype=torch.uint8, device=DEV)
+        dq.dq_dar(cfg, r, dq.stage(2, 1), msg, gd[2], False, M, perm, r, out, dq.rng(b, b, N2, E4), None)
+        eo, _ = oracle.dar(cfg_o, a, b, N2, N4, 2, 1, exp, gr[2], p.M, p.perm, send=(a, b))
+        assert np.array_equal(host(out), eo), ("dar", a, b)
+        # butterfly DAR: fp32 addend, send the upper part, keep the lower part
+        mid = (a + b) // 2
+        addend = np.random.default_rng(a).standard_normal((b - a) * 256).astype(np.float32)
+        sr, kr = dq.rng(mid, b, N2, E4), dq.rng(a, mid, N2, E4)
+        out2 = torch.zeros(max(1, dq.dq_message_bytes(sr)), dtype=torch.uint8, device=DEV)
+        keep = torch.zeros(max(1, (mid - a) * 256), device=DEV)
+        dq.dq_dar(cfg, r, dq.stage(3, 2, 1, 2), msg, torch.from_numpy(addend).to(DEV), True, M, perm, sr, out2,
+                  kr, keep)
+        eo2, ek = oracle.dar(cfg_o, a, b, N2, N4, 3, 2, exp, addend, p.M, p.perm, send=(mid, b),
+                             keep=(a, mid), slot=1, n_slots=2)
+        assert np.array_equal(host(out2)[: eo2.size], eo2), ("split dar msg", a, b)
+        assert np.array_equal(bits32(host(keep)[: ek.size]), bits32(ek)), ("split dar keep", a, b)
+        # decode (fp32 and bf16)
+        o32 = torch.zeros(p.b.size * 256, device=DEV)
+        dq.dq_decode(cfg, r, out, M, perm, o32)
+        e32 = oracle.decode(cfg_o, a, b, N2, N4, eo, p.M, p.perm)
+        assert np.array_equal(bits32(host(o32)), bits32(e32)), ("decode", a, b)
+        o16 = torch.zeros(p.b.size * 256, dtype=torch.bfloat16, device=DEV)
+        dq.dq_decode(cfg, r, out, M, perm, o16, out_is_bf16=True)
+        assert torch.equal(o16.cpu(), torch.from_numpy(e32).to(torch.bfloat16))
+
+
+# --------------------------------------------------------------------------- whole all-reduce
+def _check_allreduce(name, n, N, butterfly, correlated, B=5.0, seed=0):
+    _, gr = grads_for(name, n, N=N, seed=seed)
+    J = gr[0].size // 256
+    ar = DynamiQAllReduce(N, J, budget=B, correlated=correlated, butterfly=butterfly, seed=seed)
+    outs = ar([dev_u16(g) for g in gr], round=7)
+    torch.cuda.synchronize()
+    cfg = oracle.Config(N, B, correlated=correlated, seed=seed, round=7)
+    p = oracle.plan(cfg, gr)
+    assert ar.info.n2 == p.counts[0] and ar.info.n4 == p.counts[1] and ar.info.n8 == p.counts[2]
+    assert bits32(np.array([ar.info.T]))[0] == bits32(np.array([p.T]))[0]
+    assert np.array_equal(host(ar.perm), p.perm)
+    assert np.array_equal(bits32(host(ar.M)), bits32(p.M))
+    sel = np.arange(J, dtype=np.int64)
+    rows, fin = oracle.allreduce_sg(cfg, butterfly, gr, p.M, p.perm, int(p.counts[0]), int(p.counts[1]),
+                                    p.chunk_lo, sel)
+    exp = np.zeros(J * 256, np.float32)
+    exp.reshape(J, 256)[p.perm] = rows
+    o0 = host(outs[0])
+    assert np.array_equal(bits32(o0), bits32(exp))
+    for o in outs[1:]:
+        assert np.array_equal(bits32(host(o)), bits32(o0))   # replicas identical
+    # final chunk messages: E, u and codes of every super-group
+    lo = ar.chunk_lo()
+    N2, N4 = ar.info.n2, ar.info.n4
+    for c in range(N):
+        a, b = lo[c], lo[c + 1]
+        if b == a:
+            continue
+        m = ar.final_message(c).numpy()
+        cnt = b - a
+        n2, n4, n8 = oracle.range_counts(a, b, N2, N4)
+        off_u = -(-cnt // 16) * 16
+        offs = [off_u + 16 * cnt, off_u + 16 * cnt + 64 * n2, off_u + 16 * cnt + 64 * n2 + 128 * n4]
+        for s in range(cnt):
+            j = a + s
+            f = fin[j]
+            assert m[s] == f[0]
+            assert np.array_equal(m[off_u + 16 * s: off_u + 16 * s + 16], f[1:17])
+            if s < n2:
+                blk = m[offs[0] + 64 * s: offs[0] + 64 * s + 64]
+            elif s < n2 + n4:
+                blk = m[offs[1] + 128 * (s - n2): offs[1] + 128 * (s - n2) + 128]
+            else:
+                blk = m[offs[2] + 256 * (s - n2 - n4): offs[2] + 256 * (s - n2 - n4) + 256]
+            assert np.array_equal(blk, f[17:17 + blk.size])
+    v_gpu = oracle.vnmse(o0, gr)
+    v_orc = oracle.vnmse(exp, gr)
+    assert v_gpu == pytest.approx(v_orc, rel=0.01)
+    return v_gpu
+
+
+@pytest.mark.parametrize("correlated", [False, True])
+def test_ring4_1m_full_size(correlated):
+    """The 4-worker ring on 1,048,576 coordinates per worker, in full."""
+    _check_allreduce("ring4_1m", 1_048_576, 4, False, correlated)
+
+
+@pytest.mark.parametrize("N", [2, 4, 8, 16])
+def test_butterfly(N):
+    _check_allreduce("llama1b_butterfly8", 256 * 1500 + 77, N, True, True)
+
+
+@pytest.mark.parametrize("N", [1, 3, 8])
+def test_ring_various_ranks(N):
+    _check_allreduce("bert_large_ring8", 256 * 999, N, False, True)
+
+
+@pytest.mark.parametrize("B", [2.0, 4.0, 6.0, 8.0])
+def test_budget_sweep(B):
+    _check_allreduce("gemma1b_ring16", 256 * 2000, 16, False, True, B=B)
+
+
+def test_fewer_supergroups_than_ranks():
+    """Empty chunks: 3 super-groups over 8 ranks (ring and butterfly), 1 over 4."""
+    _check_allreduce("ring4_1m", 3 * 256, 8, False, False)
+    _check_allreduce("ring4_1m", 3 * 256, 8, True, True)
+    _check_allreduce("ring4_1m", 200, 4, False, True)
