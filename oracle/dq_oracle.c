@@ -457,7 +457,8 @@ void or_quantize_sg(const float *x, int bits, const float *q, const float *G,
 }
 
 /* Decode one super-group: sigma_g = u_g * 2^(E-127) (0 when E = 0), exact in
- * fp32; value = fl(sigma_g * q_code). */
+ * fp32; value = fl(sigma_g * q_code).  (Used on its own only by tests; the
+ * path adds every decoded value to something, see or_decode_add_sg.) */
 void or_dequantize_sg(uint8_t E, const uint8_t *u, const uint8_t *codes, int bits,
                       const float *q, float *out)
 {
@@ -467,6 +468,24 @@ void or_dequantize_sg(uint8_t E, const uint8_t *u, const uint8_t *codes, int bit
         for (int i = 0; i < OR_GROUP; ++i) {
             int ci = grp * OR_GROUP + i;
             out[ci] = sigma * q[get_code(codes, bits, ci)];
+        }
+    }
+}
+
+/* Decode one super-group and add: out_i = fl(sigma_g * q_code + add_i) with
+ * ONE rounding (a fused multiply-add, C99 fmaf).
+ * Reading: the pages do not fix how the decoded partial sum and the local
+ * gradient are combined; a single rounding is the more accurate choice and
+ * is what the GPU's packed fp32 arithmetic performs. */
+void or_decode_add_sg(uint8_t E, const uint8_t *u, const uint8_t *codes, int bits, const float *q,
+                      const float *add, float *out)
+{
+    for (int grp = 0; grp < OR_NGROUP; ++grp) {
+        float sigma = 0.0f;
+        if (E != 0) sigma = (float)u[grp] * ldexpf(1.0f, (int)E - 127);
+        for (int i = 0; i < OR_GROUP; ++i) {
+            int ci = grp * OR_GROUP + i;
+            out[ci] = fmaf(sigma, q[get_code(codes, bits, ci)], add[ci]);
         }
     }
 }
@@ -553,7 +572,7 @@ int or_compress(const or_cfg *cfg, int64_t lo, int64_t hi, int64_t N2, int64_t N
 /* One hop: decompress - accumulate - recompress [S "Key idea and           */
 /* contribution": decompress the incoming partial sum, accumulate the local */
 /* gradient, recompress and forward; P "The pith"].                         */
-/*   x = fl(dec(msg_in) + addend),                                           */
+/*   x = fl(sigma * q_code + addend) (one rounding, or_decode_add_sg),       */
 /*   addend = fl(float(g_local) - mu_j) (bf16 local gradient, via perm) or   */
 /*            the fp32 partial sum held for [in_lo, in_hi) (row j - in_lo).  */
 /* Super-groups in [send_lo, send_hi) are requantized into msg_out (stage   */
@@ -578,15 +597,13 @@ int or_dar(const or_cfg *cfg, int64_t in_lo, int64_t in_hi, int64_t N2, int64_t 
     for (int64_t j = in_lo; j < in_hi; ++j) {
         int64_t s = j - in_lo, old = perm[j];
         int bits = sg_bits(&Lin, s);
-        float dec[OR_SG], x[OR_SG];
-        or_dequantize_sg(Lin.E[s], &Lin.u[16 * s], sg_codes(&Lin, s), bits, tq(&t, bits), dec);
+        float a[OR_SG], x[OR_SG];
         float mu = mean_of(M, old, cfg->n_ranks);
         for (int i = 0; i < OR_SG; ++i) {
-            float a;
-            if (addend_is_fp32) a = ((const float *)addend)[s * OR_SG + i];
-            else a = bf16_to_f32(((const uint16_t *)addend)[old * OR_SG + i]) - mu;
-            x[i] = dec[i] + a;
+            if (addend_is_fp32) a[i] = ((const float *)addend)[s * OR_SG + i];
+            else a[i] = bf16_to_f32(((const uint16_t *)addend)[old * OR_SG + i]) - mu;
         }
+        or_decode_add_sg(Lin.E[s], &Lin.u[16 * s], sg_codes(&Lin, s), bits, tq(&t, bits), a, x);
         if (j >= send_lo && j < send_hi) {
             int64_t so = j - send_lo;
             or_quantize_sg(x, bits, tq(&t, bits), tG(&t, bits), &r, old * OR_SG,
@@ -603,7 +620,7 @@ int or_dar(const or_cfg *cfg, int64_t in_lo, int64_t in_hi, int64_t N2, int64_t 
 /* super-group order and add back the previously subtracted mean;           */
 /* P Referee Report summary: the receiver reconstructs by unnormalising].   */
 /* Reading: the all-reduce returns the SUM; each of the N workers subtracted */
-/* mu_j, so out[perm[j]*256 + i] = fl(dec + fl(mu_j * N)).                    */
+/* mu_j, so out[perm[j]*256 + i] = fl(sigma * q_code + fl(mu_j * N)).        */
 /* ------------------------------------------------------------------------ */
 int or_decode(const or_cfg *cfg, int64_t lo, int64_t hi, int64_t N2, int64_t N4,
               const uint8_t *msg, const float *M, const int32_t *perm, float *out)
@@ -615,11 +632,11 @@ int or_decode(const or_cfg *cfg, int64_t lo, int64_t hi, int64_t N2, int64_t N4,
     for (int64_t j = lo; j < hi; ++j) {
         int64_t s = j - lo, old = perm[j];
         int bits = sg_bits(&L, s);
-        float dec[OR_SG];
-        or_dequantize_sg(L.E[s], &L.u[16 * s], sg_codes(&L, s), bits, tq(&t, bits), dec);
+        float back[OR_SG], x[OR_SG];
         float mu = mean_of(M, old, cfg->n_ranks);
-        float back = mu * (float)cfg->n_ranks;
-        for (int i = 0; i < OR_SG; ++i) out[old * OR_SG + i] = dec[i] + back;
+        for (int i = 0; i < OR_SG; ++i) back[i] = mu * (float)cfg->n_ranks;
+        or_decode_add_sg(L.E[s], &L.u[16 * s], sg_codes(&L, s), bits, tq(&t, bits), back, x);
+        for (int i = 0; i < OR_SG; ++i) out[old * OR_SG + i] = x[i];
     }
     return 0;
 }
@@ -679,21 +696,18 @@ int or_allreduce_sg(const or_cfg *cfg, int32_t butterfly, const uint16_t *const 
         int bits = j < N2 ? 2 : (j < N2 + N4 ? 4 : 8);
         const float *q = tq(&t, bits), *G = tG(&t, bits);
         float mu = mean_of(M, old, N);
-        uint8_t E, u[16], codes[OR_SG];
-        float dec[OR_SG];
+        uint8_t E = 0, u[16], codes[OR_SG];
         or_rng r = {cfg->seed, cfg->round, N, cfg->correlated, 0, 0, 0, 1};
         if (!butterfly) {
-            float x[OR_SG];
+            float a[OR_SG], x[OR_SG];
             for (int32_t st = 0; st < N; ++st) {
                 int32_t rk = (c + 1 + st) % N;
                 const uint16_t *g = grads[rk] + old * OR_SG;
-                for (int i = 0; i < OR_SG; ++i) {
-                    float a = bf16_to_f32(g[i]) - mu;
-                    x[i] = st == 0 ? a : dec[i] + a;
-                }
+                for (int i = 0; i < OR_SG; ++i) a[i] = bf16_to_f32(g[i]) - mu;
+                if (st == 0) memcpy(x, a, sizeof(x));
+                else or_decode_add_sg(E, u, codes, bits, q, a, x);
                 r.hop = st; r.rank = rk; r.slot = 0; r.n_slots = 1;
                 or_quantize_sg(x, bits, q, G, &r, old * OR_SG, &E, u, codes);
-                or_dequantize_sg(E, u, codes, bits, q, dec);
             }
         } else {
             float *part = (float *)malloc(sizeof(float) * OR_SG * (size_t)N);
@@ -712,20 +726,18 @@ int or_allreduce_sg(const or_cfg *cfg, int32_t butterfly, const uint16_t *const 
                     r.n_slots = bit;                  /* senders of this stage: 2^(L-1-s) */
                     r.slot = rk & (bit - 1);
                     or_quantize_sg(&part[rk * OR_SG], bits, q, G, &r, old * OR_SG, &E, u, codes);
-                    or_dequantize_sg(E, u, codes, bits, q, dec);
-                    for (int i = 0; i < OR_SG; ++i)
-                        part[partner * OR_SG + i] = dec[i] + part[partner * OR_SG + i];
+                    or_decode_add_sg(E, u, codes, bits, q, &part[partner * OR_SG], &part[partner * OR_SG]);
                     holder[rk] = 0;
                 }
             }
             r.hop = levels; r.rank = c; r.slot = 0; r.n_slots = 1;
             or_quantize_sg(&part[c * OR_SG], bits, q, G, &r, old * OR_SG, &E, u, codes);
-            or_dequantize_sg(E, u, codes, bits, q, dec);
             free(part);
             free(holder);
         }
-        float back = mu * (float)N;
-        for (int i = 0; i < OR_SG; ++i) out[k * OR_SG + i] = dec[i] + back;
+        float back[OR_SG];
+        for (int i = 0; i < OR_SG; ++i) back[i] = mu * (float)N;
+        or_decode_add_sg(E, u, codes, bits, q, back, &out[k * OR_SG]);
         if (final_sg) {
             uint8_t *f = final_sg + k * (1 + 16 + OR_SG);
             f[0] = E;
