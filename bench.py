@@ -1,0 +1,438 @@
+#!/usr/bin/env python3
+"""Benchmark of the DynamiQ hot path on one GB300: one step = one full
+simulated all-reduce round of N workers (statistics, metadata all-reduce,
+allocation, reordering, compress, N-1 decompress-accumulate-recompress hops
+or the butterfly steps, and every rank's final decode) over synthetic bf16
+gradients already resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Prints one JSON line (rank 0).  Under torchrun each GPU runs an independent
+replica of the whole simulation (the path does not shard across GPUs: all N
+simulated workers live in one GPU's memory), timed between barriers, and the
+slowest rank's time is reported ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "DAR Gcoords/s/hop and % of HBM peak; simulated all-reduce ms per GB of grad"
+UNIT = "ms/GB"
+DEFAULT_WORKLOAD = "bert_large_ring8"
+SG = 256
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=60)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["dq", "reference"], default="dq")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--coords", type=int, default=0,
+                   help="coordinates per worker (0: the workload's own size; smaller for profiling)")
+    p.add_argument("--e2e-steps", type=int, default=0, help="steps of the end-to-end timing (0: auto)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    return p.parse_args(argv)
+
+
+# --------------------------------------------------------------------------- distributed helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as td
+    if world > 1 and not td.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        td.init_process_group(backend=backend)
+    return td
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as td
+        if device is not None and td.get_backend() == "nccl":
+            td.barrier(device_ids=[device.index])
+        else:
+            td.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Maximum of a float over all ranks (works with nccl and gloo)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as td
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if td.get_backend() == "nccl" else "cpu")
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="dq_clocks_", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    @staticmethod
+    def _epoch(ts: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(ts.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def stop(self, t0: float = None, t1: float = None):
+        """Summary of the samples taken between wall-clock times t0 and t1."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 10:
+                    t = self._epoch(parts[0])
+                    if t0 is not None and t is not None and not (t0 - 0.05 <= t <= t1 + 0.05):
+                        continue
+                    rows.append(parts[1:])
+        os.unlink(self.path)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_hop_gradient_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    want = kernel_source_hash()
+    with open(p) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload \
+                    and parts[3] == want:
+                return float(parts[2])
+    return None
+
+
+# --------------------------------------------------------------------------- algorithmic bytes
+def stream_message_bytes(dq, info, N):
+    lo = dq.dq_chunk_cuts(info.n2, info.n4, info.n8, N)
+    e2, e4 = info.n2, info.n2 + info.n4
+    return sum(dq.dq_message_bytes(dq.rng(lo[c], lo[c + 1], e2, e4)) for c in range(N))
+
+
+def launch_bytes(kind: int, sgs: int, msg_per_sg: float, fp32_addend: bool = False) -> float:
+    """Algorithmic HBM bytes of one launch over `sgs` super-groups: every
+    input byte read once and every output byte written once, nothing else.
+    compress: bf16 gradient 512 B/SG + message out + mean and perm 8 B/SG;
+    DAR: message in + addend (512 B/SG bf16, 1 KiB fp32) + message out + 8 B/SG;
+    decode: message in + fp32 output 1 KiB/SG + 8 B/SG."""
+    if kind == 0:
+        return sgs * (512 + msg_per_sg + 8)
+    if kind == 1:
+        return sgs * (2 * msg_per_sg + (1024 if fp32_addend else 512) + 8)
+    return sgs * (msg_per_sg + 1024 + 8)
+
+
+# --------------------------------------------------------------------------- oracle on the host
+def oracle_allreduce_seconds(w, gu, round_=0):
+    import oracle
+    cfg = oracle.Config(w.n_ranks, w.budget, correlated=w.correlated, seed=0, round=round_)
+    t = time.perf_counter()
+    oracle.allreduce(cfg, gu, butterfly=w.topology == "butterfly")
+    return time.perf_counter() - t
+
+
+def oracle_threads() -> int:
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def calibrated_sample(w, host_slices, target_s: float):
+    """Coordinates per worker for a run of about target_s seconds."""
+    probe = min(w.n_pad, 1 << 18)
+    t = oracle_allreduce_seconds(w, [h[:probe] for h in host_slices(probe)])
+    n = int(probe * target_s / max(t, 1e-3))
+    n = max(probe, min(w.n_pad, n)) // SG * SG
+    return n
+
+
+def cpu_baseline(w, grads_dev, target_s: float):
+    """The oracle, as it stands, on the first coordinates of every worker of
+    the same workload (its own all-reduce over that sample)."""
+    from quantized_hop_gradient_gb300 import synth
+
+    def slices(n):
+        return [synth.as_u16(g[:n]) for g in grads_dev]
+
+    n = calibrated_sample(w, slices, target_s)
+    gu = slices(n)
+    secs = oracle_allreduce_seconds(w, gu)
+    gb = n * 2 / 1e9
+    return {"value": secs * 1e3 / gb, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"first {n} of {w.n_pad} coordinates of each of the {w.n_ranks} workers "
+                      f"({n // SG} super-groups): statistics, allocation, reordering, the "
+                      f"{w.topology} all-reduce and one decode, {secs:.1f} s"}
+
+
+# --------------------------------------------------------------------------- the GPU arm
+def run_gpu(args, rank, world, local):
+    import torch
+
+    from quantized_hop_gradient_gb300 import dq, synth
+    from quantized_hop_gradient_gb300.allreduce import DynamiQAllReduce
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the CUDA path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    dq.lib(build=True)
+    w = synth.WORKLOADS[args.workload]
+    if args.coords:
+        w = w.scaled(args.coords)
+    if w.bucket:
+        raise SystemExit("streamed (bucketed) workloads are not a bench line; use a single-round workload")
+    N, J = w.n_ranks, w.n_sg
+    butterfly = w.topology == "butterfly"
+    grads = synth.generate(w, dev, seed=0)
+    ar = DynamiQAllReduce(N, J, budget=w.budget, correlated=w.correlated, butterfly=butterfly, seed=0)
+    outs = ar.new_outputs()
+    K, W = args.steps, max(args.warmup, 0)
+
+    def step(i, log=None):
+        ar.plan(grads, round=i)
+        ar.exchange(grads, outs, round=i, log=log)
+
+    clocks = ClockSampler(local).start()
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize()
+    log = dq.LaunchLog(K * (4 * N + 8))
+    log.c.count = 0
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    n_launch0 = dq.dq_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record()
+    for i in range(K):
+        step(W + i, log)
+    e1.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world, dev)
+    n_launch = dq.dq_launch_count() - n_launch0
+    clk = clocks.stop(t0, t1)
+    ms = e0.elapsed_time(e1) / K
+    ms_max = max_over_ranks(ms, world, dev)
+
+    # per-launch times of the recorded kernels
+    msg_total = stream_message_bytes(dq, ar.info, N)
+    msg_per_sg = msg_total / J
+    per_kind = {}
+    for kind, sgs, t in log.launches():
+        d = per_kind.setdefault(kind, {"launches": 0, "ms": 0.0, "sgs": 0, "bytes": 0.0})
+        d["launches"] += 1
+        d["ms"] += t
+        d["sgs"] += sgs
+        d["bytes"] += launch_bytes(kind, sgs, msg_per_sg, fp32_addend=False)
+    names = {0: "compress", 1: "dar", 2: "decode"}
+    peak, peak_kind = measured_peaks()
+    kernels = {}
+    for kind, d in per_kind.items():
+        avg_ms = d["ms"] / d["launches"]
+        gbs = d["bytes"] / d["launches"] / (avg_ms * 1e-3) / 1e9
+        kernels[names[kind]] = {"launches_per_step": d["launches"] / K, "avg_launch_ms": avg_ms,
+                                "share_of_step": d["ms"] / K / ms, "alg_bytes_per_launch": d["bytes"] / d["launches"],
+                                "achieved_gbs": gbs,
+                                "gcoords_per_s": d["sgs"] / d["launches"] * SG / (avg_ms * 1e-3) / 1e9}
+    dominant = max(kernels, key=lambda k: kernels[k]["share_of_step"])
+    dk = kernels[dominant]
+    kname = {"compress": "hop_kernel<false,false>", "dar": "hop_kernel<true,false>", "decode": "decode_kernel"}
+    roofline = {"bound": "hbm", "kernel": kname[dominant], "achieved": dk["achieved_gbs"], "peak": peak,
+                "unit": "GB/s", "frac": dk["achieved_gbs"] / peak, "peak_source": peak_kind,
+                "traffic": ncu_traffic(kname[dominant], w.name),
+                "alg_bytes_per_launch": dk["alg_bytes_per_launch"]}
+    dar = kernels.get("dar", {})
+    gb = J * SG * 2 / 1e9
+
+    # end to end: host gradients in pinned memory, copies inside the timed region
+    KE = args.e2e_steps or max(3, min(K, 10))
+    hosts = [torch.empty(g.numel(), dtype=torch.bfloat16, pin_memory=True) for g in grads]
+    for h, g in zip(hosts, grads):
+        h.copy_(g)
+    out_host = torch.empty(J * SG, dtype=torch.float32, pin_memory=True)
+
+    def e2e_step(i):
+        for g, h in zip(grads, hosts):
+            g.copy_(h, non_blocking=True)
+        ar(grads, round=i, outs=outs)
+        out_host.copy_(outs[0], non_blocking=True)
+
+    e2e_step(0)
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record()
+    for i in range(KE):
+        e2e_step(1 + i)
+    f1.record()
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    ms_e2e = max_over_ranks(f0.elapsed_time(f1) / KE, world, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, grads, args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": ms_max / (world * gb), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms_max, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 in, fp32 codec, 2/4/8-bit codes", "data": "synthetic (seeded; see DESIGN.md)",
+        "config": {"workload": w.name, "simulated_workers": N, "topology": w.topology,
+                   "coords_per_worker": w.n, "super_groups": J, "budget_bits": w.budget,
+                   "correlated_rounding": w.correlated, "grad_gb_per_worker": gb,
+                   "parallelism": f"replicas x{world} (all simulated workers on each GPU)",
+                   "l2": "inputs larger than L2 (no flush needed)",
+                   "allocation": {"T": ar.info.T, "n2": ar.info.n2, "n4": ar.info.n4, "n8": ar.info.n8}},
+        "dar": {"gcoords_per_s_per_hop": dar.get("gcoords_per_s"), "achieved_gbs": dar.get("achieved_gbs"),
+                "hbm_frac": (dar["achieved_gbs"] / peak) if dar else None, "avg_launch_ms": dar.get("avg_launch_ms")},
+        "kernels": kernels,
+        "roofline": roofline,
+        "e2e": {"value": ms_e2e / (world * gb), "unit": UNIT, "h2d_bytes_per_step": N * J * SG * 2,
+                "d2h_bytes_per_step": J * SG * 4, "ms_per_step": ms_e2e},
+        "gpu_launches": n_launch,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- the reference arm (oracle)
+def run_reference(args, rank, world):
+    """The oracle, as it stands, on the host cores: each step is the oracle's
+    whole all-reduce over a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    from quantized_hop_gradient_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.coords:
+        w = w.scaled(args.coords)
+    K, W = args.steps, max(args.warmup, 0)
+    per_step = max(0.5, min(8.0, 150.0 / max(1, K + W)))
+    full = None
+
+    def slices(n):
+        nonlocal full
+        if full is None or full[0].size < n:
+            full = [synth.as_u16(g) for g in synth.generate(w.scaled(max(n, 1 << 18)), "cpu", seed=0)]
+        return [f[:n] for f in full]
+
+    n = calibrated_sample(w, slices, per_step)
+    gu = slices(n)
+    for i in range(W):
+        oracle_allreduce_seconds(w, gu, round_=i)
+    t = time.perf_counter()
+    for i in range(K):
+        oracle_allreduce_seconds(w, gu, round_=W + i)
+    secs = (time.perf_counter() - t) / K
+    gb = n * 2 / 1e9
+    value = secs * 1e3 / gb
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": secs * 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 in, fp32 codec, 2/4/8-bit codes", "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "simulated_workers": w.n_ranks, "topology": w.topology,
+                   "coords_per_worker": w.n, "budget_bits": w.budget, "correlated_rounding": w.correlated},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+                         "sample": f"first {n} of {w.n_pad} coordinates of each of the {w.n_ranks} workers "
+                                   f"per step, whole oracle all-reduce"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_gpu(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as td
+        td.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -122,9 +122,10 @@ dq_status dq_stats(const void *g_bf16, int64_t n_sg, float *mean, float *sq, voi
  * lightweight all-reduce of the statistics; P Fig. 2(b)].
  *   mean_all, sq_all: device, N x J row-major (row r = rank r's dq_stats).
  *   M, F: device, J floats: M_j = sum of means, F_j = sum of squared norms,
- *   each added in rank order 0..N-1 in fp32. */
+ *   each added in rank order 0..N-1 in fp32 (M may be NULL).
+ *   mu: device, J floats: the mean every worker subtracts, fl(M_j / N). */
 dq_status dq_stats_reduce(const float *mean_all, const float *sq_all, int32_t n_ranks,
-                          int64_t n_sg, float *M, float *F, void *stream);
+                          int64_t n_sg, float *M, float *F, float *mu, void *stream);
 
 /* Device scratch needed by dq_allocate and dq_reorder for J super-groups. */
 size_t dq_workspace_bytes(int64_t n_sg);
@@ -157,11 +158,12 @@ dq_status dq_chunk_cuts(int64_t n2, int64_t n4, int64_t n8, int32_t n_chunks,
 /* First hop: quantize one worker's normalised gradient over range r
  * [S "Key idea and contribution": each worker normalises by the global mean
  * and quantizes; non-uniform levels, UINT8 second-level scales, correlated
- * rounding].  x = fl(float(g[perm[j]*256 + i]) - M[perm[j]] / N).
+ * rounding].  x = fl(float(g[perm[j]*256 + i]) - mu[perm[j]]), mu as written
+ * by dq_stats_reduce.
  *   hop: quantization stage index; rank: the quantizing rank (generator
  *   counter and correlated offset).  msg_out: device, dq_message_bytes(r). */
 dq_status dq_compress(const dq_config *cfg, dq_range r, dq_stage stage, const void *g_bf16,
-                      const float *M, const int32_t *perm, uint8_t *msg_out, void *stream);
+                      const float *mu, const int32_t *perm, uint8_t *msg_out, void *stream);
 
 /* One hop: decompress - accumulate - recompress, fused [S "Key idea and
  * contribution": decompress the incoming partial sum, accumulate the local
@@ -175,14 +177,14 @@ dq_status dq_compress(const dq_config *cfg, dq_range r, dq_stage stage, const vo
  *   empty): a ring hop sends everything, a butterfly step sends one half and
  *   keeps the other. */
 dq_status dq_dar(const dq_config *cfg, dq_range in, dq_stage stage, const uint8_t *msg_in,
-                 const void *addend, int32_t addend_is_fp32, const float *M, const int32_t *perm, dq_range send, uint8_t *msg_out,
+                 const void *addend, int32_t addend_is_fp32, const float *mu, const int32_t *perm, dq_range send, uint8_t *msg_out,
                  dq_range keep, float *keep_out, void *stream);
 
 /* Final decode [S "Key idea and contribution": restore the original
  * super-group order and add back the subtracted mean; P Referee Report
  * summary: the receiver unnormalises].  out[perm[j]*256 + i] =
- * fl(dec + fl(fl(M/N) * N)), fp32 (out_is_bf16 = 0) or rounded to bf16. */
-dq_status dq_decode(const dq_config *cfg, dq_range r, const uint8_t *msg, const float *M,
+ * fl(dec + fl(mu_j * N)), fp32 (out_is_bf16 = 0) or rounded to bf16. */
+dq_status dq_decode(const dq_config *cfg, dq_range r, const uint8_t *msg, const float *mu,
                     const int32_t *perm, void *out, int32_t out_is_bf16, void *stream);
 
 /* ---- the whole round: statistics to decode, N simulated ranks ---------- */
@@ -200,11 +202,11 @@ size_t dq_plan_workspace_bytes(int32_t n_ranks, int64_t n_sg);
  * contribution", statistics collection phase; P Fig. 2(a)-(c)]: per-rank
  * statistics, metadata all-reduce, allocation and reordering.
  *   grads_host: host array of N device pointers (J*256 bf16 each).
- *   M, perm: device outputs (J floats, J int32) used by dq_exchange.
+ *   mu, perm: device outputs (J floats, J int32) used by dq_exchange.
  *   info_host: host output.  Synchronises `stream` once to read the counts.
  *   plan_ws: device scratch of dq_plan_workspace_bytes(N, J). */
 dq_status dq_plan(const dq_config *cfg, const void *const *grads_host, int64_t n_sg,
-                  float *M, int32_t *perm, void *plan_ws, size_t plan_ws_bytes,
+                  float *mu, int32_t *perm, void *plan_ws, size_t plan_ws_bytes,
                   dq_plan_info *info_host, void *stream);
 
 /* Optional record of the kernel launches of dq_exchange, for timing them on
@@ -240,7 +242,7 @@ size_t dq_exchange_workspace_bytes(const dq_config *cfg, int32_t butterfly, int6
  * N device pointers (inside ws) of the final chunk messages.  log: NULL or
  * a dq_launch_log to fill.  No sync. */
 dq_status dq_exchange(const dq_config *cfg, int32_t butterfly, const void *const *grads_host,
-                      int64_t n_sg, const float *M, const int32_t *perm,
+                      int64_t n_sg, const float *mu, const int32_t *perm,
                       const dq_plan_info *info, void *ws, size_t ws_bytes,
                       void *const *outs_host, int32_t out_is_bf16,
                       const uint8_t **final_msgs_host, dq_launch_log *log, void *stream);

@@ -24,7 +24,7 @@ class DynamiQAllReduce:
         self.out_dtype = out_dtype
         self.device = torch.device(device)
         dq.lib()
-        self.M = torch.empty(n_sg, dtype=torch.float32, device=self.device)
+        self.mu = torch.empty(n_sg, dtype=torch.float32, device=self.device)
         self.perm = torch.empty(n_sg, dtype=torch.int32, device=self.device)
         nb = dq.dq_plan_workspace_bytes(n_ranks, n_sg)
         self.plan_ws = torch.empty(nb, dtype=torch.uint8, device=self.device)
@@ -37,7 +37,7 @@ class DynamiQAllReduce:
 
     def plan(self, grads, round: int = 0, stream=None):
         cfg = self.config(round)
-        self.info = dq.dq_plan(cfg, grads, self.n_sg, self.M, self.perm, self.plan_ws, self.plan_ws.numel(),
+        self.info = dq.dq_plan(cfg, grads, self.n_sg, self.mu, self.perm, self.plan_ws, self.plan_ws.numel(),
                                stream)
         return self.info
 
@@ -51,7 +51,7 @@ class DynamiQAllReduce:
         if need == 0:
             raise dq.DQError(dq.DQ_ERR_INVALID_ARG, "dq_exchange_workspace_bytes")
         self.reserve(need)
-        self.final = dq.dq_exchange(cfg, self.butterfly, grads, self.n_sg, self.M, self.perm, self.info,
+        self.final = dq.dq_exchange(cfg, self.butterfly, grads, self.n_sg, self.mu, self.perm, self.info,
                                     self.ws, self.ws.numel(), outs, self.out_dtype == torch.bfloat16, log,
                                     stream)
         return outs

@@ -1,11 +1,14 @@
 // dq_common.cuh -- shared definitions of the libdq CUDA kernels (sm_103a).
 //
 // Floating point: all codec arithmetic uses explicitly rounded fp32
-// intrinsics (__fadd_rn, __fsub_rn, __fmul_rn, __fdiv_rn, __frcp_rn) and the
-// library is built with -fmad=false, so no multiply-add is contracted and
-// every result is the correctly rounded binary32 of each step.  That makes
-// codes, scales and decoded values reproducible bit for bit by any IEEE
-// implementation that performs the same steps.
+// operations: scalar __fmul_rn-style intrinsics (never contracted) and the
+// packed .f32x2 instructions with .rn rounding; the library is built with
+// -fmad=false.  ptxas does contract a packed multiply that feeds a packed
+// add into one fused multiply-add even under .rn, so the kernels use a
+// packed multiply only where its result feeds a compare or a multiply, and
+// write every intended fused multiply-add explicitly.  Each result is then
+// the correctly rounded binary32 of each step as written, reproducible bit
+// for bit by any IEEE implementation that performs the same steps.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -18,30 +21,44 @@ namespace dq {
 
 constexpr int kSG = 256;        // coordinates per super-group
 constexpr int kGroup = 16;      // coordinates per group (one UINT8 scale each)
-constexpr int kLaneCoords = 8;  // one warp per super-group: 8 coordinates per lane
+constexpr int kUnit = 32;       // super-groups per work unit of a warp
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
-// Bucket tables for the level search: bucket t of bitwidth b covers
-// y in [t/H - 1, (t+1)/H - 1); kb is the largest level index with
-// q_kb <= t/H - 1 and boundary = q_{kb+1} (+inf for the top level).
-constexpr int kMaxH2 = 64, kMaxH4 = 128, kMaxH8 = 512;
+// ---------------------------------------------------------------------------
+// Level tables for one eps, built on the host and copied to shared memory.
+//
+// q*[k]   : the levels (decode).
+// qg*[k]  : {q_k, G16_k}, G16_k = fl(1/fl(q_{k+1} - q_k)) * 2^16 (exact
+//           scaling), G16 of the top level 0, then a sentinel {+inf, 0}.
+// bk*[i]  : level-search buckets.  For y in [-1, 1] and H a power of two,
+//           r = rint(y*H) (ties to even) is read from the bit pattern of
+//           fl(y*H + 1.5*2^23); bucket r covers [(r-1/2)/H, (r+1/2)/H].  The
+//           entry sits at index r & MASK (negative r wrap to the top of the
+//           table), so any bit pattern indexes inside the table.  It holds
+//           the next level above the bucket's lower edge (boundary) and 8x
+//           the index kb of the largest level at or below that edge.
+// rcp[u]  : fl(1/u) for the UINT8 scales, rcp[0] = 0.
+// ---------------------------------------------------------------------------
+constexpr int kMask2 = 63, kMask4 = 255, kMask8 = 1023;   // tables of MASK+1 entries
+// H is a power of two with 2H + 1 <= MASK + 1: at most 16, 64 and 256.
+constexpr uint32_t kMagicBits = 0x4B400000u;              // bits of 1.5 * 2^23
+constexpr float kMagic = 12582912.0f;
 
 struct BucketEntry {
-    int32_t kb;
     float boundary;
+    int32_t kb8;
 };
 
-// Level tables for one eps, built on the host.
-// qg*[k] = {q_k, G_k}: the level and the reciprocal gap fl(1/fl(q_{k+1}-q_k));
-// G of the top level is 0, and one sentinel entry {+inf, 0} follows it.
 struct Tables {
-    float2 qg2[5];
-    float2 qg4[17];
-    float2 qg8[257];
-    int32_t H2, H4, H8, pad_;
-    BucketEntry bk2[2 * kMaxH2 + 1];
-    BucketEntry bk4[2 * kMaxH4 + 1];
-    BucketEntry bk8[2 * kMaxH8 + 1];
+    float q2[4], q4[16], q8[256];
+    float2 qg2[5], qg4[17], qg8[257];
+    float2 pad0_;
+    BucketEntry bk2[kMask2 + 1];
+    BucketEntry bk4[kMask4 + 1];
+    BucketEntry bk8[kMask8 + 1];
+    float rcp[256];
+    float H2, H4, H8;
+    int32_t one_level;   // every bucket holds at most one level above its lower edge
 };
 
 // One message (the bytes that carry a range of reordered super-groups).
@@ -52,6 +69,8 @@ struct MsgView {
 };
 
 // One fused hop (one rank's dq_compress or dq_dar) inside a batched launch.
+// Its super-groups [in_lo, in_hi) are cut into three bitwidth-pure segments,
+// each split into work units of up to kUnit consecutive super-groups.
 struct HopTask {
     MsgView in;                 // incoming message (unused for compress)
     MsgView out;                // message for the send range
@@ -59,9 +78,10 @@ struct HopTask {
     float *keep_out;            // fp32 rows (j - keep_lo)
     int64_t in_lo;
     int64_t send_lo, send_hi, keep_lo, keep_hi;
-    int64_t sg_begin;           // first batched super-group index of this task
-    uint32_t stage_word;        // generator counter word 1: hop | rank << 16, 0 if correlated
-    uint32_t corr_off;          // floor(rank * 2^16 / N) if correlated, else 0
+    int64_t seg_lo[3], seg_hi[3];
+    int64_t unit_begin[4];      // first global unit of each segment; [3] = end
+    uint32_t stage_word;        // generator counter word 1
+    uint32_t corr2;             // correlated offset in both 16-bit halves
 };
 
 constexpr int kMaxTasks = 32;
@@ -71,19 +91,19 @@ struct HopParams {
     HopTask task[kMaxTasks];
     int32_t n_tasks;
     int32_t n_ranks;
-    int64_t total_sg;
-    int64_t end2, end4;
-    const float *M;
+    int64_t total_units;
+    const float *mu;
     const int32_t *perm;
     uint32_t key0, key1;        // seed
     uint32_t round0, round1;    // round
 };
 
-// One chunk decoded by the final decode.
+// One chunk decoded by the final decode (same unit structure).
 struct DecodeTask {
     MsgView msg;
     int64_t lo;
-    int64_t sg_begin;
+    int64_t seg_lo[3], seg_hi[3];
+    int64_t unit_begin[4];
 };
 
 struct DecodeParams {
@@ -91,9 +111,8 @@ struct DecodeParams {
     DecodeTask task[kMaxTasks];
     int32_t n_tasks;
     int32_t n_ranks;
-    int64_t total_sg;
-    int64_t end2, end4;
-    const float *M;
+    int64_t total_units;
+    const float *mu;
     const int32_t *perm;
     void *out;
     int32_t out_is_bf16;
@@ -124,6 +143,56 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// ---------------------------------------------------------------------------
+// Packed fp32 pairs (Blackwell .f32x2): two IEEE binary32 operations with the
+// given rounding in one instruction.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b)
+{
+    float2 r;
+    asm("{ .reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d; }"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 f2_sub(float2 a, float2 b)
+{
+    float2 r;
+    asm("{ .reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d; }"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+// a * b + c with ONE rounding.
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c)
+{
+    float2 r;
+    asm("{ .reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mov.b64 c, {%6, %7};\n\tfma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d; }"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// cp.async staging (16-byte global -> shared copies, L2 only)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst_smem), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
 // Copy a POD struct from parameter space to shared memory with the whole block.
 template <typename T>
 __device__ __forceinline__ void block_copy(T *dst, const T *src)
@@ -132,6 +201,16 @@ __device__ __forceinline__ void block_copy(T *dst, const T *src)
     const int4 *s = reinterpret_cast<const int4 *>(src);
     int4 *d = reinterpret_cast<int4 *>(dst);
     for (int i = threadIdx.x; i < (int)(sizeof(T) / 16); i += blockDim.x) d[i] = s[i];
+}
+
+// Which task and bitwidth segment a work unit belongs to.
+template <typename Task>
+__device__ __forceinline__ void locate_unit(const Task *tasks, int n_tasks, int64_t u, int &ti, int &seg)
+{
+    ti = 0;
+    while (ti + 1 < n_tasks && u >= tasks[ti + 1].unit_begin[0]) ++ti;
+    seg = 0;
+    while (seg < 2 && u >= tasks[ti].unit_begin[seg + 1]) ++seg;
 }
 
 }  // namespace dq

@@ -1,0 +1,458 @@
+// dq_hop.cu -- fused hop (compress / decompress-accumulate-recompress) and
+// final decode kernels.
+//
+// Work mapping.  A warp takes a work unit of up to 32 consecutive reordered
+// super-groups of one task and one bitwidth, and processes them two at a
+// time: lanes 0-15 one super-group, lanes 16-31 the next.  Lane l of a half
+// owns group l (coordinates 16l .. 16l+15), so a group maximum needs no
+// shuffle, a super-group maximum four, and each lane draws two Philox calls
+// (eight 16-bit uniforms each) for its sixteen coordinates.  The unit's
+// permutation entries, means and exponent bytes are loaded once, coalesced,
+// and broadcast by shuffles.  The gradient (or fp32 partial), the incoming
+// codes and the incoming UINT8 scales of a pair of super-groups are staged
+// in shared memory by cp.async, three pairs ahead of the computation.
+#include "dq_common.cuh"
+#include "dq_internal.h"
+
+namespace dq {
+
+namespace {
+
+constexpr int kWarps = 4;       // warps per block
+constexpr int kStages = 3;      // pairs of super-groups in flight per warp
+
+__shared__ __align__(16) Tables g_tab;
+
+// e for S > 0: with S = (1 + f) 2^(eb-127), 255 * 2^e >= S holds first at
+// e = eb - 134 when (1 + f) <= 510/256 (mantissa field <= 0x7F0000), else at
+// eb - 133; subnormal S (eb = 0) and tiny S clamp to -126.  Byte E = e + 127,
+// E = 0 when S = 0.
+__device__ __forceinline__ uint32_t exponent_byte(float S)
+{
+    if (!(S > 0.0f)) return 0u;
+    const uint32_t bits = __float_as_uint(S);
+    const int eb = (int)(bits >> 23);
+    int e = eb - 134 + ((bits & 0x7FFFFFu) > 0x7F0000u ? 1 : 0);
+    if (eb == 0 || e < -126) e = -126;
+    return (uint32_t)(e + 127);
+}
+
+template <int BITS> struct Lvl;
+template <> struct Lvl<2> {
+    static constexpr int kMask = kMask2;
+    __device__ static const float *q() { return g_tab.q2; }
+    __device__ static const float2 *qg() { return g_tab.qg2; }
+    __device__ static const BucketEntry *bk() { return g_tab.bk2; }
+    __device__ static float H() { return g_tab.H2; }
+};
+template <> struct Lvl<4> {
+    static constexpr int kMask = kMask4;
+    __device__ static const float *q() { return g_tab.q4; }
+    __device__ static const float2 *qg() { return g_tab.qg4; }
+    __device__ static const BucketEntry *bk() { return g_tab.bk4; }
+    __device__ static float H() { return g_tab.H4; }
+};
+template <> struct Lvl<8> {
+    static constexpr int kMask = kMask8;
+    __device__ static const float *q() { return g_tab.q8; }
+    __device__ static const float2 *qg() { return g_tab.qg8; }
+    __device__ static const BucketEntry *bk() { return g_tab.bk8; }
+    __device__ static float H() { return g_tab.H8; }
+};
+
+// Codes of one lane: 16 coordinates of BITS bits, coordinate i at bit BITS*i.
+template <int BITS> struct LaneCodes { uint32_t w[BITS / 2]; };
+
+template <int BITS>
+__device__ __forceinline__ uint32_t code_of(const LaneCodes<BITS> &c, int i)
+{
+    return (c.w[(BITS * i) >> 5] >> ((BITS * i) & 31)) & ((1u << BITS) - 1u);
+}
+
+template <int BITS>
+__device__ __forceinline__ const uint8_t *code_block(const MsgView &m, int64_t s)
+{
+    if (BITS == 2) return m.base + m.off_c2 + 64 * s;
+    if (BITS == 4) return m.base + m.off_c4 + 128 * (s - m.n2);
+    return m.base + m.off_c8 + 256 * (s - m.n2 - m.n4);
+}
+
+template <int BITS>
+__device__ __forceinline__ LaneCodes<BITS> lds_codes(const uint8_t *p)
+{
+    LaneCodes<BITS> c;
+    if (BITS == 2) {
+        c.w[0] = *reinterpret_cast<const uint32_t *>(p);
+    } else if (BITS == 4) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        c.w[0] = v.x; c.w[1] = v.y;
+    } else {
+        const uint4 v = *reinterpret_cast<const uint4 *>(p);
+        c.w[0] = v.x; c.w[1] = v.y; c.w[2] = v.z; c.w[3] = v.w;
+    }
+    return c;
+}
+
+template <int BITS>
+__device__ __forceinline__ void stg_codes(uint8_t *p, const LaneCodes<BITS> &c)
+{
+    if (BITS == 2) *reinterpret_cast<uint32_t *>(p) = c.w[0];
+    else if (BITS == 4) *reinterpret_cast<uint2 *>(p) = make_uint2(c.w[0], c.w[1]);
+    else *reinterpret_cast<uint4 *>(p) = make_uint4(c.w[0], c.w[1], c.w[2], c.w[3]);
+}
+
+// x = fl(sigma * q_code + x) with one rounding (fused multiply-add),
+// sigma = u * 2^(E-127) (0 when E = 0).
+template <int BITS>
+__device__ __forceinline__ void decode_add(float2 (&x)[8], uint32_t E, uint32_t u, const LaneCodes<BITS> &c)
+{
+    const float sigma = __fmul_rn((float)u, __uint_as_float(E << 23));
+    const float2 s2 = make_float2(sigma, sigma);
+    const float *q = Lvl<BITS>::q();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float2 lv = make_float2(q[code_of<BITS>(c, 2 * k)], q[code_of<BITS>(c, 2 * k + 1)]);
+        x[k] = f2_fma(s2, lv, x[k]);
+    }
+}
+
+// Quantization of one lane's group (16 values).  Scale hierarchy: s = group
+// max |x|; S = super-group max (half-warp); E from S; u = smallest integer
+// with u * 2^e >= s; m = fl(fl(1/u) * 2^-e).  Per coordinate: y = fl(x * m);
+// k = largest level <= y (bucket table, then exact compares); p16 =
+// fl(fl(y - q_k) * G16_k) = p * 2^16; code = k + (U < p16).
+// Packed multiplies are only followed by compares here: ptxas contracts a
+// packed multiply feeding a packed add into one fused operation even with
+// explicit .rn rounding, so y is formed by scalar __fmul_rn (which is never
+// contracted) and U < p16 is a float compare of U (exact) with p16.
+template <int BITS, bool ONE_LEVEL>
+__device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], uint32_t ctr0, uint32_t stage_word,
+                                                          uint32_t corr2, uint32_t key0, uint32_t key1,
+                                                          uint32_t round0, uint32_t round1, uint32_t &E_out,
+                                                          uint32_t &u_out)
+{
+    float s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s = fmaxf(s, fmaxf(fabsf(x[k].x), fabsf(x[k].y)));
+    float S = s;
+#pragma unroll
+    for (int m = 1; m <= 8; m <<= 1) S = fmaxf(S, __shfl_xor_sync(kFull, S, m));
+    const uint32_t E = exponent_byte(S);
+    const float inv2e = __uint_as_float((254u - E) << 23);   // 2^-e (any E: finite)
+    uint32_t u = __float2uint_ru(__fmul_rn(s, inv2e));
+    u = max(u, s > 0.0f ? 1u : 0u);
+    u = min(u, 255u);
+    const float m = __fmul_rn(g_tab.rcp[u], inv2e);
+    E_out = E;
+    u_out = u;
+
+    uint32_t r0[4] = {ctr0, stage_word, round0, round1};
+    uint32_t r1[4] = {ctr0 + 1u, stage_word, round0, round1};
+    philox4x32_10(r0, key0, key1);
+    philox4x32_10(r1, key0, key1);
+    const uint32_t rw[8] = {__vadd2(r0[0], corr2), __vadd2(r0[1], corr2), __vadd2(r0[2], corr2),
+                            __vadd2(r0[3], corr2), __vadd2(r1[0], corr2), __vadd2(r1[1], corr2),
+                            __vadd2(r1[2], corr2), __vadd2(r1[3], corr2)};
+
+    const float2 *qg = Lvl<BITS>::qg();
+    const BucketEntry *bk = Lvl<BITS>::bk();
+    const float H = Lvl<BITS>::H();
+    const float2 H2 = make_float2(H, H), M2 = make_float2(kMagic, kMagic);
+    const float2 C2 = make_float2(8388608.0f, 8388608.0f);   // 2^23
+    LaneCodes<BITS> out;
+#pragma unroll
+    for (int w = 0; w < BITS / 2; ++w) out.w[w] = 0u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float2 y = make_float2(__fmul_rn(x[k].x, m), __fmul_rn(x[k].y, m));
+        const float2 tf = f2_fma(y, H2, M2);                  // y*H is exact: one rounding = rint
+        const BucketEntry b0 = bk[__float_as_uint(tf.x) & Lvl<BITS>::kMask];
+        const BucketEntry b1 = bk[__float_as_uint(tf.y) & Lvl<BITS>::kMask];
+        int k80 = b0.kb8 + (y.x >= b0.boundary ? 8 : 0);
+        int k81 = b1.kb8 + (y.y >= b1.boundary ? 8 : 0);
+        if (!ONE_LEVEL) {  // buckets wider than a gap: walk up (bounded by the top level)
+            constexpr int kTop8 = 8 * ((1 << BITS) - 1);
+            while (k80 < kTop8 && y.x >= qg[(k80 >> 3) + 1].x) k80 += 8;
+            while (k81 < kTop8 && y.y >= qg[(k81 >> 3) + 1].x) k81 += 8;
+        }
+        const float2 l0 = *reinterpret_cast<const float2 *>(reinterpret_cast<const char *>(qg) + k80);
+        const float2 l1 = *reinterpret_cast<const float2 *>(reinterpret_cast<const char *>(qg) + k81);
+        const float2 p16 = f2_mul(f2_sub(y, make_float2(l0.x, l1.x)), make_float2(l0.y, l1.y));
+        const float2 Ub = make_float2(__uint_as_float(__byte_perm(rw[k], 0x4B00u, 0x5410u)),   // 2^23 + U
+                                      __uint_as_float(__byte_perm(rw[k], 0x4B00u, 0x5432u)));
+        const float2 Uf = f2_sub(Ub, C2);                      // U, exactly
+        const uint32_t c0 = (uint32_t)(k80 >> 3) + (Uf.x < p16.x ? 1u : 0u);
+        const uint32_t c1 = (uint32_t)(k81 >> 3) + (Uf.y < p16.y ? 1u : 0u);
+        const int i0 = 2 * k, i1 = 2 * k + 1;
+        out.w[(BITS * i0) >> 5] |= c0 << ((BITS * i0) & 31);
+        out.w[(BITS * i1) >> 5] |= c1 << ((BITS * i1) & 31);
+    }
+    return out;
+}
+
+// One work unit: super-groups j0 .. j0+cnt-1 (one task, one bitwidth).
+template <int BITS, bool HAS_IN, bool ADD_F32, bool ONE_LEVEL>
+__device__ __forceinline__ void hop_unit(const HopParams &P, const HopTask &t, uint8_t *stg, int64_t j0, int cnt,
+                                         int lane)
+{
+    constexpr int A_BYTES = ADD_F32 ? 2048 : 1024;
+    constexpr int C_OFF = A_BYTES, U_OFF = A_BYTES + 512, STAGE = A_BYTES + 544;
+    const int half = lane >> 4, hl = lane & 15;
+    const uint32_t stg_s = smem_addr(stg);
+
+    int32_t old_i = 0;
+    float mu_i = 0.0f;
+    uint32_t ein_i = 0;
+    if (lane < cnt) {
+        old_i = __ldg(P.perm + j0 + lane);
+        if (!ADD_F32) mu_i = __ldg(P.mu + old_i);
+        if (HAS_IN) ein_i = __ldg(t.in.base + (j0 + lane - t.in_lo));
+    }
+    const int npairs = (cnt + 1) >> 1;
+
+    auto issue = [&](int pp) {
+        const int s = 2 * pp + half;
+        const int32_t old = __shfl_sync(kFull, old_i, s & 31);
+        if (pp < npairs && s < cnt) {
+            const uint32_t st = stg_s + (uint32_t)((pp % kStages) * STAGE);
+            const int64_t sl = j0 + s - t.in_lo;
+            if (ADD_F32) {
+                const float *src = static_cast<const float *>(t.addend) + sl * kSG + hl * 16;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) cp_async16(st + half * 1024 + k * 256 + hl * 16, src + 4 * k);
+            } else {
+                const uint16_t *src = static_cast<const uint16_t *>(t.addend) + (int64_t)old * kSG + hl * 16;
+                cp_async16(st + half * 512 + hl * 16, src);
+                cp_async16(st + half * 512 + 256 + hl * 16, src + 8);
+            }
+            if (HAS_IN) {
+                if (hl < 2 * BITS) cp_async16(st + C_OFF + half * 256 + hl * 16, code_block<BITS>(t.in, sl) + hl * 16);
+                if (hl == 15) cp_async16(st + U_OFF + half * 16, t.in.base + t.in.off_u + sl * 16);
+            }
+        }
+        cp_async_commit();
+    };
+
+#pragma unroll
+    for (int pp = 0; pp < kStages - 1; ++pp) issue(pp);
+    uint32_t e_out = 0;
+    for (int p = 0; p < npairs; ++p) {
+        issue(p + kStages - 1);
+        cp_async_wait<kStages - 1>();
+        __syncwarp();
+        const uint8_t *st = stg + (p % kStages) * STAGE;
+        const int s = 2 * p + half;
+        const bool valid = s < cnt;
+        const int64_t j = j0 + s;
+        const int32_t old = __shfl_sync(kFull, old_i, s & 31);
+        const float mu = __shfl_sync(kFull, mu_i, s & 31);
+        const uint32_t ein = __shfl_sync(kFull, ein_i, s & 31);
+
+        float2 x[8];
+        if (ADD_F32) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 v = *reinterpret_cast<const float4 *>(st + half * 1024 + k * 256 + hl * 16);
+                x[2 * k] = make_float2(v.x, v.y);
+                x[2 * k + 1] = make_float2(v.z, v.w);
+            }
+        } else {
+            const uint4 a = *reinterpret_cast<const uint4 *>(st + half * 512 + hl * 16);
+            const uint4 b = *reinterpret_cast<const uint4 *>(st + half * 512 + 256 + hl * 16);
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            const float2 mu2 = make_float2(mu, mu);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) x[k] = f2_sub(make_float2(bf16_lo(w[k]), bf16_hi(w[k])), mu2);
+        }
+        if (HAS_IN) {
+            const uint32_t u = st[U_OFF + half * 16 + hl];
+            const LaneCodes<BITS> c = lds_codes<BITS>(st + C_OFF + half * 256 + hl * 2 * BITS);
+            decode_add<BITS>(x, ein, u, c);
+        }
+        if (!valid) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) x[k] = make_float2(0.0f, 0.0f);
+        }
+        const bool send = valid && j >= t.send_lo && j < t.send_hi;
+        const bool keep = valid && j >= t.keep_lo && j < t.keep_hi;
+        uint32_t E, u;
+        const uint32_t ctr0 = (uint32_t)old * 32u + 2u * (uint32_t)hl;
+        const LaneCodes<BITS> q = quantize_group<BITS, ONE_LEVEL>(x, ctr0, t.stage_word, t.corr2, P.key0, P.key1,
+                                                                  P.round0, P.round1, E, u);
+        if (send) {
+            const int64_t so = j - t.send_lo;
+            stg_codes<BITS>(const_cast<uint8_t *>(code_block<BITS>(t.out, so)) + hl * 2 * BITS, q);
+            t.out.base[t.out.off_u + so * 16 + hl] = (uint8_t)u;
+        } else if (keep) {
+            float4 *o = reinterpret_cast<float4 *>(t.keep_out + (j - t.keep_lo) * kSG + hl * 16);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[k] = make_float4(x[2 * k].x, x[2 * k].y, x[2 * k + 1].x, x[2 * k + 1].y);
+        }
+        const uint32_t e_pair = __shfl_sync(kFull, E, (lane & 1) << 4);
+        if ((lane >> 1) == p) e_out = e_pair;
+        __syncwarp();
+    }
+    if (lane < cnt) {
+        const int64_t j = j0 + lane;
+        if (j >= t.send_lo && j < t.send_hi) t.out.base[j - t.send_lo] = (uint8_t)e_out;
+    }
+}
+
+template <bool HAS_IN, bool ADD_F32, bool ONE_LEVEL>
+__global__ void __launch_bounds__(kWarps * 32) hop_kernel(const __grid_constant__ HopParams P)
+{
+    extern __shared__ __align__(16) uint8_t dyn[];
+    block_copy(&g_tab, &P.tab);
+    __syncthreads();
+    constexpr int STAGE = (ADD_F32 ? 2048 : 1024) + 544;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t *stg = dyn + warp * kStages * STAGE;
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < P.total_units; u += nw) {
+        int ti, seg;
+        locate_unit(P.task, P.n_tasks, u, ti, seg);
+        const HopTask &t = P.task[ti];
+        const int64_t j0 = t.seg_lo[seg] + (u - t.unit_begin[seg]) * kUnit;
+        const int64_t rem = t.seg_hi[seg] - j0;
+        const int cnt = (int)(rem < kUnit ? rem : kUnit);
+        if (seg == 0) hop_unit<2, HAS_IN, ADD_F32, ONE_LEVEL>(P, t, stg, j0, cnt, lane);
+        else if (seg == 1) hop_unit<4, HAS_IN, ADD_F32, ONE_LEVEL>(P, t, stg, j0, cnt, lane);
+        else hop_unit<8, HAS_IN, ADD_F32, ONE_LEVEL>(P, t, stg, j0, cnt, lane);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Final decode: out[perm[j]*256 + i] = fl(sigma * q_code + fl(mu_j * N)) (one
+// rounding), fp32 or bf16.
+// ---------------------------------------------------------------------------
+template <int BITS>
+__device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeTask &t, uint8_t *stg, int64_t j0,
+                                            int cnt, int lane)
+{
+    constexpr int U_OFF = 512, STAGE = 544;
+    const int half = lane >> 4, hl = lane & 15;
+    const uint32_t stg_s = smem_addr(stg);
+    int32_t old_i = 0;
+    float mu_i = 0.0f;
+    uint32_t ein_i = 0;
+    if (lane < cnt) {
+        old_i = __ldg(P.perm + j0 + lane);
+        mu_i = __ldg(P.mu + old_i);
+        ein_i = __ldg(t.msg.base + (j0 + lane - t.lo));
+    }
+    const int npairs = (cnt + 1) >> 1;
+    auto issue = [&](int pp) {
+        const int s = 2 * pp + half;
+        if (pp < npairs && s < cnt) {
+            const uint32_t st = stg_s + (uint32_t)((pp % kStages) * STAGE);
+            const int64_t sl = j0 + s - t.lo;
+            if (hl < 2 * BITS) cp_async16(st + half * 256 + hl * 16, code_block<BITS>(t.msg, sl) + hl * 16);
+            if (hl == 15) cp_async16(st + U_OFF + half * 16, t.msg.base + t.msg.off_u + sl * 16);
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int pp = 0; pp < kStages - 1; ++pp) issue(pp);
+    const float nr = (float)P.n_ranks;
+    for (int p = 0; p < npairs; ++p) {
+        issue(p + kStages - 1);
+        cp_async_wait<kStages - 1>();
+        __syncwarp();
+        const uint8_t *st = stg + (p % kStages) * STAGE;
+        const int s = 2 * p + half;
+        const int32_t old = __shfl_sync(kFull, old_i, s & 31);
+        const float mu = __shfl_sync(kFull, mu_i, s & 31);
+        const uint32_t ein = __shfl_sync(kFull, ein_i, s & 31);
+        if (s < cnt) {
+            const float back = __fmul_rn(mu, nr);
+            float2 x[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) x[k] = make_float2(back, back);
+            const uint32_t u = st[U_OFF + half * 16 + hl];
+            const LaneCodes<BITS> c = lds_codes<BITS>(st + half * 256 + hl * 2 * BITS);
+            decode_add<BITS>(x, ein, u, c);   // fl(sigma * q + back)
+            if (P.out_is_bf16) {
+                uint32_t w[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    w[k] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[k].x)) |
+                           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[k].y)) << 16);
+                uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(P.out) + (int64_t)old * kSG + hl * 16);
+                __stcs(o, make_uint4(w[0], w[1], w[2], w[3]));
+                __stcs(o + 1, make_uint4(w[4], w[5], w[6], w[7]));
+            } else {
+                float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(P.out) + (int64_t)old * kSG + hl * 16);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    __stcs(o + k, make_float4(x[2 * k].x, x[2 * k].y, x[2 * k + 1].x, x[2 * k + 1].y));
+            }
+        }
+        __syncwarp();
+    }
+}
+
+__global__ void __launch_bounds__(kWarps * 32) decode_kernel(const __grid_constant__ DecodeParams P)
+{
+    extern __shared__ __align__(16) uint8_t dyn[];
+    block_copy(&g_tab, &P.tab);
+    __syncthreads();
+    constexpr int STAGE = 544;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t *stg = dyn + warp * kStages * STAGE;
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < P.total_units; u += nw) {
+        int ti, seg;
+        locate_unit(P.task, P.n_tasks, u, ti, seg);
+        const DecodeTask &t = P.task[ti];
+        const int64_t j0 = t.seg_lo[seg] + (u - t.unit_begin[seg]) * kUnit;
+        const int64_t rem = t.seg_hi[seg] - j0;
+        const int cnt = (int)(rem < kUnit ? rem : kUnit);
+        if (seg == 0) decode_unit<2>(P, t, stg, j0, cnt, lane);
+        else if (seg == 1) decode_unit<4>(P, t, stg, j0, cnt, lane);
+        else decode_unit<8>(P, t, stg, j0, cnt, lane);
+    }
+}
+
+template <typename K>
+int grid_for(K kernel, size_t dyn_smem, int64_t units)
+{
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kWarps * 32, dyn_smem) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    const int64_t need = (units + kWarps - 1) / kWarps;
+    return (int)(need < cap ? (need < 1 ? 1 : need) : cap);
+}
+
+template <bool HAS_IN, bool ADD_F32, bool ONE_LEVEL>
+cudaError_t launch_hop_t(const HopParams &P, cudaStream_t st)
+{
+    const size_t dyn = (size_t)kWarps * kStages * ((ADD_F32 ? 2048 : 1024) + 544);
+    auto k = hop_kernel<HAS_IN, ADD_F32, ONE_LEVEL>;
+    k<<<grid_for(k, dyn, P.total_units), kWarps * 32, dyn, st>>>(P);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_hop(const HopParams &P, bool has_in, bool add_f32, cudaStream_t st)
+{
+    if (P.total_units <= 0) return cudaSuccess;
+    const bool one = P.tab.one_level != 0;
+    if (!has_in) return one ? launch_hop_t<false, false, true>(P, st) : launch_hop_t<false, false, false>(P, st);
+    if (add_f32) return one ? launch_hop_t<true, true, true>(P, st) : launch_hop_t<true, true, false>(P, st);
+    return one ? launch_hop_t<true, false, true>(P, st) : launch_hop_t<true, false, false>(P, st);
+}
+
+cudaError_t launch_decode(const DecodeParams &P, cudaStream_t st)
+{
+    if (P.total_units <= 0) return cudaSuccess;
+    const size_t dyn = (size_t)kWarps * kStages * 544;
+    decode_kernel<<<grid_for(decode_kernel, dyn, P.total_units), kWarps * 32, dyn, st>>>(P);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace dq

@@ -68,7 +68,7 @@ _SIGS = {
     "dq_level_table": ([C.c_int32, C.c_double, C.c_void_p], C.c_int),
     "dq_stats": ([C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "dq_stats_reduce": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_int64, C.c_void_p, C.c_void_p,
-                         C.c_void_p], C.c_int),
+                         C.c_void_p, C.c_void_p], C.c_int),
     "dq_workspace_bytes": ([C.c_int64], C.c_size_t),
     "dq_allocate": ([C.c_void_p, C.c_int64, C.c_float, C.c_void_p, C.c_void_p, C.c_void_p,
                      C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
@@ -181,8 +181,8 @@ def dq_stats(g, n_sg, mean, sq, stream=None):
     _check(lib().dq_stats(_ptr(g), n_sg, _ptr(mean), _ptr(sq), _stream(stream)), "dq_stats")
 
 
-def dq_stats_reduce(mean_all, sq_all, n_ranks, n_sg, M, F, stream=None):
-    _check(lib().dq_stats_reduce(_ptr(mean_all), _ptr(sq_all), n_ranks, n_sg, _ptr(M), _ptr(F),
+def dq_stats_reduce(mean_all, sq_all, n_ranks, n_sg, M, F, mu, stream=None):
+    _check(lib().dq_stats_reduce(_ptr(mean_all), _ptr(sq_all), n_ranks, n_sg, _ptr(M), _ptr(F), _ptr(mu),
                                  _stream(stream)), "dq_stats_reduce")
 
 
@@ -205,20 +205,20 @@ def dq_chunk_cuts(n2, n4, n8, n_chunks):
     return list(out)
 
 
-def dq_compress(cfg, r, st, g, M, perm, msg_out, stream=None):
-    _check(lib().dq_compress(C.byref(cfg), r, st, _ptr(g), _ptr(M), _ptr(perm), _ptr(msg_out),
+def dq_compress(cfg, r, st, g, mu, perm, msg_out, stream=None):
+    _check(lib().dq_compress(C.byref(cfg), r, st, _ptr(g), _ptr(mu), _ptr(perm), _ptr(msg_out),
                              _stream(stream)), "dq_compress")
 
 
-def dq_dar(cfg, r_in, st, msg_in, addend, addend_is_fp32, M, perm, send, msg_out, keep, keep_out,
+def dq_dar(cfg, r_in, st, msg_in, addend, addend_is_fp32, mu, perm, send, msg_out, keep, keep_out,
            stream=None):
     _check(lib().dq_dar(C.byref(cfg), r_in, st, _ptr(msg_in), _ptr(addend), int(addend_is_fp32),
-                        _ptr(M), _ptr(perm), send, _ptr(msg_out), keep, _ptr(keep_out), _stream(stream)),
+                        _ptr(mu), _ptr(perm), send, _ptr(msg_out), keep, _ptr(keep_out), _stream(stream)),
            "dq_dar")
 
 
-def dq_decode(cfg, r, msg, M, perm, out, out_is_bf16=False, stream=None):
-    _check(lib().dq_decode(C.byref(cfg), r, _ptr(msg), _ptr(M), _ptr(perm), _ptr(out), int(out_is_bf16),
+def dq_decode(cfg, r, msg, mu, perm, out, out_is_bf16=False, stream=None):
+    _check(lib().dq_decode(C.byref(cfg), r, _ptr(msg), _ptr(mu), _ptr(perm), _ptr(out), int(out_is_bf16),
                            _stream(stream)), "dq_decode")
 
 
@@ -226,10 +226,10 @@ def dq_plan_workspace_bytes(n_ranks, n_sg) -> int:
     return lib().dq_plan_workspace_bytes(n_ranks, n_sg)
 
 
-def dq_plan(cfg, grads, n_sg, M, perm, ws, ws_bytes, stream=None) -> dq_plan_info:
+def dq_plan(cfg, grads, n_sg, mu, perm, ws, ws_bytes, stream=None) -> dq_plan_info:
     ptrs = (C.c_void_p * len(grads))(*[_ptr(g) for g in grads])
     info = dq_plan_info()
-    _check(lib().dq_plan(C.byref(cfg), C.cast(ptrs, C.c_void_p), n_sg, _ptr(M), _ptr(perm), _ptr(ws),
+    _check(lib().dq_plan(C.byref(cfg), C.cast(ptrs, C.c_void_p), n_sg, _ptr(mu), _ptr(perm), _ptr(ws),
                          ws_bytes, C.byref(info), _stream(stream)), "dq_plan")
     return info
 
@@ -259,14 +259,14 @@ class LaunchLog:
                 for i in range(self.c.count)]
 
 
-def dq_exchange(cfg, butterfly, grads, n_sg, M, perm, info, ws, ws_bytes, outs, out_is_bf16=False,
+def dq_exchange(cfg, butterfly, grads, n_sg, mu, perm, info, ws, ws_bytes, outs, out_is_bf16=False,
                 log: LaunchLog = None, stream=None):
     """Returns the N device addresses of the final chunk messages (inside ws)."""
     n = len(grads)
     gp = (C.c_void_p * n)(*[_ptr(g) for g in grads])
     op = (C.c_void_p * n)(*[_ptr(o) for o in outs])
     fin = (C.c_void_p * n)()
-    _check(lib().dq_exchange(C.byref(cfg), int(butterfly), C.cast(gp, C.c_void_p), n_sg, _ptr(M), _ptr(perm),
+    _check(lib().dq_exchange(C.byref(cfg), int(butterfly), C.cast(gp, C.c_void_p), n_sg, _ptr(mu), _ptr(perm),
                              C.byref(info), _ptr(ws), ws_bytes, C.cast(op, C.c_void_p), int(out_is_bf16),
                              C.cast(fin, C.c_void_p), C.byref(log.c) if log is not None else None,
                              _stream(stream)), "dq_exchange")

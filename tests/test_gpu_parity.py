@@ -65,10 +65,12 @@ def test_stats_reduce_bit_exact():
         sqs = np.abs(rs.standard_normal((N, J)) * 10.0 ** rs.integers(-8, 8, (N, J))).astype(np.float32)
         M = torch.empty(J, device=DEV)
         F = torch.empty(J, device=DEV)
-        dq.dq_stats_reduce(torch.from_numpy(means).to(DEV), torch.from_numpy(sqs).to(DEV), N, J, M, F)
+        mu = torch.empty(J, device=DEV)
+        dq.dq_stats_reduce(torch.from_numpy(means).to(DEV), torch.from_numpy(sqs).to(DEV), N, J, M, F, mu)
         eM, eF = oracle.stats_reduce(means, sqs)
         assert np.array_equal(bits32(host(M)), bits32(eM))
         assert np.array_equal(bits32(host(F)), bits32(eF))
+        assert np.array_equal(bits32(host(mu)), bits32(eM / np.float32(N)))   # fl(M / N)
 
 
 # --------------------------------------------------------------------------- allocation and reorder
@@ -134,7 +136,7 @@ def test_compress_dar_decode_bit_exact(eps, correlated):
     N = 4
     _, gr = grads_for("ring4_1m", 256 * 3000, N=N, seed=5)
     p = _plan(gr, N)
-    M = torch.from_numpy(p.M).to(DEV)
+    M = torch.from_numpy(p.M / np.float32(N)).to(DEV)   # mu = fl(M / N)
     perm = torch.from_numpy(p.perm).to(DEV)
     gd = [dev_u16(g) for g in gr]
     cfg_o = oracle.Config(N, 5.0, eps=eps, correlated=correlated, seed=11, round=3)
@@ -191,7 +193,7 @@ def _check_allreduce(name, n, N, butterfly, correlated, B=5.0, seed=0):
     assert ar.info.n2 == p.counts[0] and ar.info.n4 == p.counts[1] and ar.info.n8 == p.counts[2]
     assert bits32(np.array([ar.info.T]))[0] == bits32(np.array([p.T]))[0]
     assert np.array_equal(host(ar.perm), p.perm)
-    assert np.array_equal(bits32(host(ar.M)), bits32(p.M))
+    assert np.array_equal(bits32(host(ar.mu)), bits32(p.M / np.float32(N)))
     sel = np.arange(J, dtype=np.int64)
     rows, fin = oracle.allreduce_sg(cfg, butterfly, gr, p.M, p.perm, int(p.counts[0]), int(p.counts[1]),
                                     p.chunk_lo, sel)
@@ -237,12 +239,12 @@ def test_ring4_1m_full_size(correlated):
     _check_allreduce("ring4_1m", 1_048_576, 4, False, correlated)
 
 
-@pytest.mark.parametrize("N", [2, 4, 8, 16])
+@pytest.mark.parametrize("N", [2, 4, 8, 16, 64])
 def test_butterfly(N):
     _check_allreduce("llama1b_butterfly8", 256 * 1500 + 77, N, True, True)
 
 
-@pytest.mark.parametrize("N", [1, 3, 8])
+@pytest.mark.parametrize("N", [1, 3, 8, 33])
 def test_ring_various_ranks(N):
     _check_allreduce("bert_large_ring8", 256 * 999, N, False, True)
 
