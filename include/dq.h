@@ -148,6 +148,25 @@ dq_status dq_allocate(const float *F, int64_t n_sg, float budget, uint8_t *b, fl
 dq_status dq_reorder(const uint8_t *b, int64_t n_sg, int32_t *perm, void *ws, size_t ws_bytes,
                      void *stream);
 
+/* dq_reorder for callers that cannot allocate device memory.  No passage of
+ * the paper corresponds to it: it exists for code that must not, or cannot,
+ * call cudaMalloc when it reorders -- e.g. an application that reserved all
+ * device memory for its own pool at start-up, a loop that forbids allocation
+ * while it runs, or a caller that holds the input and output buffers but no
+ * handle to the allocator that owns them.  Same result as dq_reorder; the
+ * scratch is a 128 KiB array inside the library, resident on every GPU that
+ * loads it until the process exits, so the call allocates nothing.
+ *   b: device, n_sg bytes; perm: device, n_sg int32 (caller-owned).
+ *   n_sg must be 1 .. DQ_REORDER_STATIC_MAX_SG; larger sizes return
+ *   DQ_ERR_INVALID_ARG without touching the GPU (use dq_reorder then).
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.  All calls share the one array: calls that
+ *   overlap on the GPU (different streams, or different host threads without
+ *   ordering) race and must not be made. */
+#define DQ_REORDER_STATIC_MAX_SG 8388608
+dq_status dq_reorder_static(const uint8_t *b, int64_t n_sg, int32_t *perm, void *stream);
+
 /* Chunk cuts of the reordered stream among n_chunks workers (host, pure):
  * chunk_lo_host[c] = the smallest reordered index whose prefix of code bits
  * reaches ceil(c * total / n_chunks); chunk_lo_host[n_chunks] = J.  Chunks

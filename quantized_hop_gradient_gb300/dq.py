@@ -73,6 +73,7 @@ _SIGS = {
     "dq_allocate": ([C.c_void_p, C.c_int64, C.c_float, C.c_void_p, C.c_void_p, C.c_void_p,
                      C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
     "dq_reorder": ([C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
+    "dq_reorder_static": ([C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p], C.c_int),
     "dq_chunk_cuts": ([C.c_int64, C.c_int64, C.c_int64, C.c_int32, C.c_void_p], C.c_int),
     "dq_compress": ([C.POINTER(dq_config), dq_range, dq_stage, C.c_void_p, C.c_void_p,
                      C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
@@ -197,6 +198,15 @@ def dq_allocate(F, n_sg, budget, b, T_dev, counts_dev, ws, ws_bytes, stream=None
 
 def dq_reorder(b, n_sg, perm, ws, ws_bytes, stream=None):
     _check(lib().dq_reorder(_ptr(b), n_sg, _ptr(perm), _ptr(ws), ws_bytes, _stream(stream)), "dq_reorder")
+
+
+REORDER_STATIC_MAX_SG = 8388608
+
+
+def dq_reorder_static(b, n_sg, perm, stream=None):
+    """dq_reorder without a workspace (scratch inside the library); for
+    callers that cannot allocate device memory."""
+    _check(lib().dq_reorder_static(_ptr(b), n_sg, _ptr(perm), _stream(stream)), "dq_reorder_static")
 
 
 def dq_chunk_cuts(n2, n4, n8, n_chunks):
