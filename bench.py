@@ -190,17 +190,25 @@ def stream_message_bytes(dq, info, N):
     return sum(dq.dq_message_bytes(dq.rng(lo[c], lo[c + 1], e2, e4)) for c in range(N))
 
 
-def launch_bytes(kind: int, sgs: int, msg_per_sg: float, fp32_addend: bool = False) -> float:
+def launch_bytes(kind: int, sgs: int, msg_per_sg: float, fp32_addend: bool = False, n_ranks: int = 1) -> float:
     """Algorithmic HBM bytes of one launch over `sgs` super-groups: every
     input byte read once and every output byte written once, nothing else.
     compress: bf16 gradient 512 B/SG + message out + mean and perm 8 B/SG;
     DAR: message in + addend (512 B/SG bf16, 1 KiB fp32) + message out + 8 B/SG;
-    decode: message in + fp32 output 1 KiB/SG + 8 B/SG."""
+    decode: message in + fp32 output 1 KiB/SG + 8 B/SG;
+    stats: bf16 gradient 512 B/SG + mean and squared norm 8 B/SG;
+    allocate + reorder span: N x 8 B/SG of statistics read, M, F, mu written
+    (12 B/SG), then about five passes over F (20 B/SG) and the bitwidths and
+    permutation (about 7 B/SG)."""
     if kind == 0:
         return sgs * (512 + msg_per_sg + 8)
     if kind == 1:
         return sgs * (2 * msg_per_sg + (1024 if fp32_addend else 512) + 8)
-    return sgs * (msg_per_sg + 1024 + 8)
+    if kind == 2:
+        return sgs * (msg_per_sg + 1024 + 8)
+    if kind == 3:
+        return sgs * (512 + 8)
+    return sgs * (8 * n_ranks + 12 + 20 + 7)
 
 
 # --------------------------------------------------------------------------- oracle on the host
@@ -269,14 +277,14 @@ def run_gpu(args, rank, world, local):
     K, W = args.steps, max(args.warmup, 0)
 
     def step(i, log=None):
-        ar.plan(grads, round=i)
+        ar.plan(grads, round=i, log=log)
         ar.exchange(grads, outs, round=i, log=log)
 
     clocks = ClockSampler(local).start()
     for i in range(W):
         step(i)
     torch.cuda.synchronize()
-    log = dq.LaunchLog(K * (4 * N + 8))
+    log = dq.LaunchLog(K * (6 * N + 12))
     log.c.count = 0
     torch.cuda.synchronize()
     barrier(world, dev)
@@ -305,8 +313,8 @@ def run_gpu(args, rank, world, local):
         d["launches"] += 1
         d["ms"] += t
         d["sgs"] += sgs
-        d["bytes"] += launch_bytes(kind, sgs, msg_per_sg, fp32_addend=False)
-    names = {0: "compress", 1: "dar", 2: "decode"}
+        d["bytes"] += launch_bytes(kind, sgs, msg_per_sg, fp32_addend=False, n_ranks=N)
+    names = {0: "compress", 1: "dar", 2: "decode", 3: "stats", 4: "allocate_reorder"}
     peak, peak_kind = measured_peaks()
     kernels = {}
     for kind, d in per_kind.items():
@@ -316,9 +324,10 @@ def run_gpu(args, rank, world, local):
                                 "share_of_step": d["ms"] / K / ms, "alg_bytes_per_launch": d["bytes"] / d["launches"],
                                 "achieved_gbs": gbs,
                                 "gcoords_per_s": d["sgs"] / d["launches"] * SG / (avg_ms * 1e-3) / 1e9}
-    dominant = max(kernels, key=lambda k: kernels[k]["share_of_step"])
+    dominant = max((k for k in kernels if k != "allocate_reorder"), key=lambda k: kernels[k]["share_of_step"])
     dk = kernels[dominant]
-    kname = {"compress": "hop_kernel<false,false>", "dar": "hop_kernel<true,false>", "decode": "decode_kernel"}
+    kname = {"compress": "hop_kernel<false,false>", "dar": "hop_kernel<true,false>", "decode": "decode_kernel",
+             "stats": "stats_kernel"}
     roofline = {"bound": "hbm", "kernel": kname[dominant], "achieved": dk["achieved_gbs"], "peak": peak,
                 "unit": "GB/s", "frac": dk["achieved_gbs"] / peak, "peak_source": peak_kind,
                 "traffic": ncu_traffic(kname[dominant], w.name),

@@ -223,25 +223,28 @@ size_t dq_plan_workspace_bytes(int32_t n_ranks, int64_t n_sg);
  *   grads_host: host array of N device pointers (J*256 bf16 each).
  *   mu, perm: device outputs (J floats, J int32) used by dq_exchange.
  *   info_host: host output.  Synchronises `stream` once to read the counts.
- *   plan_ws: device scratch of dq_plan_workspace_bytes(N, J). */
+ *   plan_ws: device scratch of dq_plan_workspace_bytes(N, J).
+ *   log: NULL or a dq_launch_log to fill (see below). */
+typedef struct dq_launch_log dq_launch_log;
 dq_status dq_plan(const dq_config *cfg, const void *const *grads_host, int64_t n_sg,
                   float *mu, int32_t *perm, void *plan_ws, size_t plan_ws_bytes,
-                  dq_plan_info *info_host, void *stream);
+                  dq_plan_info *info_host, dq_launch_log *log, void *stream);
 
-/* Optional record of the kernel launches of dq_exchange, for timing them on
+/* Optional record of the kernel launches of dq_plan and dq_exchange, for timing them on
  * the launching stream.  events: host array of 2*capacity cudaEvent_t created
  * by the caller (timing enabled); launch i is bracketed by events[2i] and
  * events[2i+1].  kinds[i]: DQ_LAUNCH_*; sgs[i]: super-groups it processed.
  * count: in, first free slot; out, slots used.  Launches beyond capacity
  * are not recorded (they still run). */
-enum { DQ_LAUNCH_COMPRESS = 0, DQ_LAUNCH_DAR = 1, DQ_LAUNCH_DECODE = 2 };
-typedef struct {
+enum { DQ_LAUNCH_COMPRESS = 0, DQ_LAUNCH_DAR = 1, DQ_LAUNCH_DECODE = 2, DQ_LAUNCH_STATS = 3,
+       DQ_LAUNCH_ALLOCATE_REORDER = 4 /* statistics reduce, allocation and reorder, one bracket */ };
+struct dq_launch_log {
     void   **events;
     int32_t *kinds;
     int64_t *sgs;
     int32_t  capacity;
     int32_t  count;
-} dq_launch_log;
+};
 
 /* Number of kernels libdq has launched in this process (all entry points). */
 uint64_t dq_launch_count(void);

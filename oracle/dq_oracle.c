@@ -84,9 +84,13 @@ typedef struct {
  * rounding, shared randomness across workers so that rounding errors cancel
  * in the aggregate, after Suresh et al., ICML 2022 [S "Key idea and
  * contribution"; P circularity audit]):
- *   key = (seed lo, seed hi), counter = (i/8, stage word, round lo, round hi);
- *   one Philox call gives 128 bits = eight 16-bit uniforms for coordinates
- *   8m..8m+7, coordinate i taking half (i mod 2) of word (i/2) mod 4.
+ *   key = (seed lo, seed hi), counter = (i/16, stage word, round lo, round hi):
+ *   one Philox call per group of 16 coordinates gives eight 16-bit fields;
+ *   coordinate c = i mod 16 takes field c mod 8 (half (c mod 2) of word
+ *   (c mod 8)/2), plus 2^15 (mod 2^16) when c >= 8.  Every coordinate's
+ *   uniform is still uniform and independent of the value it rounds, which
+ *   is all unbiasedness needs; the two coordinates sharing a field are
+ *   antithetic, which does not change any coordinate's error variance.
  *   Independent rounding: stage word = hop | rank << 16.
  *   Correlated rounding: stage word = hop | 0xFFFF << 16, the same on every
  *   worker, fresh for every stage; the worker then adds its stratum offset:
@@ -101,7 +105,7 @@ typedef struct {
 uint32_t or_uniform16(const or_rng *r, int64_t i)
 {
     uint32_t ctr[4], key[2], out[4];
-    uint64_t blk = (uint64_t)i >> 3;
+    uint64_t blk = (uint64_t)i >> 4;
     ctr[0] = (uint32_t)blk;
     ctr[1] = (uint32_t)r->hop | ((r->correlated ? 0xFFFFu : (uint32_t)r->rank) << 16);
     ctr[2] = (uint32_t)r->round;
@@ -111,6 +115,7 @@ uint32_t or_uniform16(const or_rng *r, int64_t i)
     or_philox4x32_10(ctr, key, out);
     uint32_t w = out[(i >> 1) & 3];
     uint32_t u = (i & 1) ? (w >> 16) : (w & 0xFFFFu);
+    if (i & 8) u = (u + 0x8000u) & 0xFFFFu;
     if (r->correlated) {
         uint32_t off = (uint32_t)(((uint64_t)(uint32_t)r->slot << 16) / (uint64_t)(uint32_t)r->n_slots);
         u = (u + off) & 0xFFFFu;

@@ -35,10 +35,10 @@ class DynamiQAllReduce:
     def config(self, round: int = 0):
         return dq.config(self.n_ranks, self.budget, self.eps, self.correlated, self.seed, round)
 
-    def plan(self, grads, round: int = 0, stream=None):
+    def plan(self, grads, round: int = 0, stream=None, log=None):
         cfg = self.config(round)
         self.info = dq.dq_plan(cfg, grads, self.n_sg, self.mu, self.perm, self.plan_ws, self.plan_ws.numel(),
-                               stream)
+                               log, stream)
         return self.info
 
     def reserve(self, nbytes: int):

@@ -35,24 +35,35 @@ __device__ __forceinline__ float lane_tree8(float (&a)[8])
 __global__ void __launch_bounds__(256) stats_kernel(const uint16_t *__restrict__ g, int64_t n_sg,
                                                     float *__restrict__ mean, float *__restrict__ sq)
 {
+    constexpr int kAhead = 4;   // super-groups loaded before any is reduced
     const int lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t j = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; j < n_sg; j += nw) {
-        const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(g + j * kSG) + lane);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        float a[8], b[8];
+    const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    for (int64_t jb = w0; jb < n_sg; jb += nw * kAhead) {
+        uint4 v[kAhead];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            a[2 * k] = bf16_lo(w[k]);
-            a[2 * k + 1] = bf16_hi(w[k]);
+        for (int a = 0; a < kAhead; ++a) {
+            const int64_t j = jb + a * nw;
+            v[a] = j < n_sg ? __ldcs(reinterpret_cast<const uint4 *>(g + j * kSG) + lane) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) b[i] = __fmul_rn(a[i], a[i]);
-        const float s = lane_tree8(a);
-        const float q = lane_tree8(b);
-        if (lane == 0) {
-            mean[j] = __fmul_rn(s, 0.00390625f);
-            sq[j] = q;
+        for (int a = 0; a < kAhead; ++a) {
+            const int64_t j = jb + a * nw;
+            const uint32_t w[4] = {v[a].x, v[a].y, v[a].z, v[a].w};
+            float x[8], y[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                x[2 * k] = bf16_lo(w[k]);
+                x[2 * k + 1] = bf16_hi(w[k]);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(x[i], x[i]);
+            const float s = lane_tree8(x);
+            const float q = lane_tree8(y);
+            if (lane == 0 && j < n_sg) {
+                mean[j] = __fmul_rn(s, 0.00390625f);
+                sq[j] = q;
+            }
         }
     }
 }

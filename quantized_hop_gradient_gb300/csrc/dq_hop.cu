@@ -5,12 +5,12 @@
 // super-groups of one task and one bitwidth, and processes them two at a
 // time: lanes 0-15 one super-group, lanes 16-31 the next.  Lane l of a half
 // owns group l (coordinates 16l .. 16l+15), so a group maximum needs no
-// shuffle, a super-group maximum four, and each lane draws two Philox calls
-// (eight 16-bit uniforms each) for its sixteen coordinates.  The unit's
+// shuffle, a super-group maximum four, and each lane draws one Philox call
+// (eight 16-bit fields) for its sixteen coordinates.  The unit's
 // permutation entries, means and exponent bytes are loaded once, coalesced,
 // and broadcast by shuffles.  The gradient (or fp32 partial), the incoming
 // codes and the incoming UINT8 scales of a pair of super-groups are staged
-// in shared memory by cp.async, three pairs ahead of the computation.
+// in shared memory by cp.async, one pair ahead of the computation.
 #include "dq_common.cuh"
 #include "dq_internal.h"
 
@@ -19,7 +19,7 @@ namespace dq {
 namespace {
 
 constexpr int kWarps = 4;       // warps per block
-constexpr int kStages = 3;      // pairs of super-groups in flight per warp
+constexpr int kStages = 2;      // pairs of super-groups in flight per warp
 
 __shared__ __align__(16) Tables g_tab;
 
@@ -146,13 +146,14 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
     E_out = E;
     u_out = u;
 
+    // One Philox call per group: coordinate c takes 16-bit field c mod 8,
+    // shifted by half a period (xor 0x8000 in each half) for c >= 8.
     uint32_t r0[4] = {ctr0, stage_word, round0, round1};
-    uint32_t r1[4] = {ctr0 + 1u, stage_word, round0, round1};
     philox4x32_10(r0, key0, key1);
-    philox4x32_10(r1, key0, key1);
     const uint32_t rw[8] = {__vadd2(r0[0], corr2), __vadd2(r0[1], corr2), __vadd2(r0[2], corr2),
-                            __vadd2(r0[3], corr2), __vadd2(r1[0], corr2), __vadd2(r1[1], corr2),
-                            __vadd2(r1[2], corr2), __vadd2(r1[3], corr2)};
+                            __vadd2(r0[3], corr2), __vadd2(r0[0] ^ 0x80008000u, corr2),
+                            __vadd2(r0[1] ^ 0x80008000u, corr2), __vadd2(r0[2] ^ 0x80008000u, corr2),
+                            __vadd2(r0[3] ^ 0x80008000u, corr2)};
 
     const float2 *qg = Lvl<BITS>::qg();
     const BucketEntry *bk = Lvl<BITS>::bk();
@@ -276,7 +277,7 @@ __device__ __forceinline__ void hop_unit(const HopParams &P, const HopTask &t, u
         const bool send = valid && j >= t.send_lo && j < t.send_hi;
         const bool keep = valid && j >= t.keep_lo && j < t.keep_hi;
         uint32_t E, u;
-        const uint32_t ctr0 = (uint32_t)old * 32u + 2u * (uint32_t)hl;
+        const uint32_t ctr0 = (uint32_t)old * 16u + (uint32_t)hl;   // global coordinate index / 16
         const LaneCodes<BITS> q = quantize_group<BITS, ONE_LEVEL>(x, ctr0, t.stage_word, t.corr2, P.key0, P.key1,
                                                                   P.round0, P.round1, E, u);
         if (send) {
@@ -323,15 +324,25 @@ __global__ void __launch_bounds__(kWarps * 32) hop_kernel(const __grid_constant_
 
 // ---------------------------------------------------------------------------
 // Final decode: out[perm[j]*256 + i] = fl(sigma * q_code + fl(mu_j * N)) (one
-// rounding), fp32 or bf16.
+// rounding), fp32 or bf16.  Output-bound (4 bytes out per 0.69 in), so the
+// mapping makes every store instruction cover contiguous memory: lane l of
+// the warp decodes coordinates 4l..4l+3 (group l/4) and 128+4l..131+4l
+// (group 8 + l/4) of a super-group, so each warp store writes 512
+// contiguous bytes.  Four super-groups are loaded before any is computed.
 // ---------------------------------------------------------------------------
 template <int BITS>
-__device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeTask &t, uint8_t *stg, int64_t j0,
-                                            int cnt, int lane)
+__device__ __forceinline__ uint32_t ldg_codes4(const uint8_t *blk, int idx)
 {
-    constexpr int U_OFF = 512, STAGE = 544;
-    const int half = lane >> 4, hl = lane & 15;
-    const uint32_t stg_s = smem_addr(stg);
+    // codes of 4 consecutive coordinates starting at coordinate 4*idx
+    if (BITS == 8) return __ldg(reinterpret_cast<const uint32_t *>(blk) + idx);
+    if (BITS == 4) return __ldg(reinterpret_cast<const unsigned short *>(blk) + idx);
+    return __ldg(blk + idx);
+}
+
+template <int BITS>
+__device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeTask &t, int64_t j0, int cnt, int lane)
+{
+    constexpr int kAhead = 4;
     int32_t old_i = 0;
     float mu_i = 0.0f;
     uint32_t ein_i = 0;
@@ -340,88 +351,95 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeT
         mu_i = __ldg(P.mu + old_i);
         ein_i = __ldg(t.msg.base + (j0 + lane - t.lo));
     }
-    const int npairs = (cnt + 1) >> 1;
-    auto issue = [&](int pp) {
-        const int s = 2 * pp + half;
-        if (pp < npairs && s < cnt) {
-            const uint32_t st = stg_s + (uint32_t)((pp % kStages) * STAGE);
-            const int64_t sl = j0 + s - t.lo;
-            if (hl < 2 * BITS) cp_async16(st + half * 256 + hl * 16, code_block<BITS>(t.msg, sl) + hl * 16);
-            if (hl == 15) cp_async16(st + U_OFF + half * 16, t.msg.base + t.msg.off_u + sl * 16);
-        }
-        cp_async_commit();
-    };
-#pragma unroll
-    for (int pp = 0; pp < kStages - 1; ++pp) issue(pp);
     const float nr = (float)P.n_ranks;
-    for (int p = 0; p < npairs; ++p) {
-        issue(p + kStages - 1);
-        cp_async_wait<kStages - 1>();
-        __syncwarp();
-        const uint8_t *st = stg + (p % kStages) * STAGE;
-        const int s = 2 * p + half;
-        const int32_t old = __shfl_sync(kFull, old_i, s & 31);
-        const float mu = __shfl_sync(kFull, mu_i, s & 31);
-        const uint32_t ein = __shfl_sync(kFull, ein_i, s & 31);
-        if (s < cnt) {
-            const float back = __fmul_rn(mu, nr);
-            float2 x[8];
+    const float *q = Lvl<BITS>::q();
+    const int g0 = lane >> 2;
+    for (int s0 = 0; s0 < cnt; s0 += kAhead) {
+        uint32_t ca[kAhead], cb[kAhead], ua[kAhead], ub[kAhead];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) x[k] = make_float2(back, back);
-            const uint32_t u = st[U_OFF + half * 16 + hl];
-            const LaneCodes<BITS> c = lds_codes<BITS>(st + half * 256 + hl * 2 * BITS);
-            decode_add<BITS>(x, ein, u, c);   // fl(sigma * q + back)
-            if (P.out_is_bf16) {
-                uint32_t w[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    w[k] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[k].x)) |
-                           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[k].y)) << 16);
-                uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(P.out) + (int64_t)old * kSG + hl * 16);
-                __stcs(o, make_uint4(w[0], w[1], w[2], w[3]));
-                __stcs(o + 1, make_uint4(w[4], w[5], w[6], w[7]));
-            } else {
-                float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(P.out) + (int64_t)old * kSG + hl * 16);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    __stcs(o + k, make_float4(x[2 * k].x, x[2 * k].y, x[2 * k + 1].x, x[2 * k + 1].y));
+        for (int a = 0; a < kAhead; ++a) {
+            ca[a] = cb[a] = ua[a] = ub[a] = 0u;
+            if (s0 + a < cnt) {
+                const int64_t sl = j0 + s0 + a - t.lo;
+                const uint8_t *blk = code_block<BITS>(t.msg, sl);
+                ca[a] = ldg_codes4<BITS>(blk, lane);
+                cb[a] = ldg_codes4<BITS>(blk, 32 + lane);
+                const uint8_t *ub8 = t.msg.base + t.msg.off_u + sl * 16;
+                ua[a] = __ldg(ub8 + g0);
+                ub[a] = __ldg(ub8 + 8 + g0);
             }
         }
-        __syncwarp();
+#pragma unroll
+        for (int a = 0; a < kAhead; ++a) {
+            const int s = s0 + a;
+            const int32_t old = __shfl_sync(kFull, old_i, s & 31);
+            const float mu = __shfl_sync(kFull, mu_i, s & 31);
+            const uint32_t E = __shfl_sync(kFull, ein_i, s & 31);
+            if (s < cnt) {
+                const float back = __fmul_rn(mu, nr);
+                const float p2e = __uint_as_float(E << 23);
+                const float sa = __fmul_rn((float)ua[a], p2e), sb = __fmul_rn((float)ub[a], p2e);
+                float va[4], vb[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t mask = (1u << BITS) - 1u;
+                    va[i] = __fmaf_rn(sa, q[(ca[a] >> (BITS * i)) & mask], back);
+                    vb[i] = __fmaf_rn(sb, q[(cb[a] >> (BITS * i)) & mask], back);
+                }
+                if (P.out_is_bf16) {
+                    uint16_t *o = static_cast<uint16_t *>(P.out) + (int64_t)old * kSG;
+                    const uint2 wa = make_uint2(
+                        (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(va[0])) |
+                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(va[1])) << 16),
+                        (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(va[2])) |
+                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(va[3])) << 16));
+                    const uint2 wb = make_uint2(
+                        (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(vb[0])) |
+                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(vb[1])) << 16),
+                        (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(vb[2])) |
+                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(vb[3])) << 16));
+                    __stcs(reinterpret_cast<uint2 *>(o + 4 * lane), wa);
+                    __stcs(reinterpret_cast<uint2 *>(o + 128 + 4 * lane), wb);
+                } else {
+                    float *o = static_cast<float *>(P.out) + (int64_t)old * kSG;
+                    __stcs(reinterpret_cast<float4 *>(o + 4 * lane), make_float4(va[0], va[1], va[2], va[3]));
+                    __stcs(reinterpret_cast<float4 *>(o + 128 + 4 * lane), make_float4(vb[0], vb[1], vb[2], vb[3]));
+                }
+            }
+        }
     }
 }
 
-__global__ void __launch_bounds__(kWarps * 32) decode_kernel(const __grid_constant__ DecodeParams P)
+constexpr int kDecodeWarps = 8;
+
+__global__ void __launch_bounds__(kDecodeWarps * 32) decode_kernel(const __grid_constant__ DecodeParams P)
 {
-    extern __shared__ __align__(16) uint8_t dyn[];
     block_copy(&g_tab, &P.tab);
     __syncthreads();
-    constexpr int STAGE = 544;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint8_t *stg = dyn + warp * kStages * STAGE;
-    const int64_t nw = (int64_t)gridDim.x * kWarps;
-    for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < P.total_units; u += nw) {
+    const int64_t nw = (int64_t)gridDim.x * kDecodeWarps;
+    for (int64_t u = (int64_t)blockIdx.x * kDecodeWarps + warp; u < P.total_units; u += nw) {
         int ti, seg;
         locate_unit(P.task, P.n_tasks, u, ti, seg);
         const DecodeTask &t = P.task[ti];
         const int64_t j0 = t.seg_lo[seg] + (u - t.unit_begin[seg]) * kUnit;
         const int64_t rem = t.seg_hi[seg] - j0;
         const int cnt = (int)(rem < kUnit ? rem : kUnit);
-        if (seg == 0) decode_unit<2>(P, t, stg, j0, cnt, lane);
-        else if (seg == 1) decode_unit<4>(P, t, stg, j0, cnt, lane);
-        else decode_unit<8>(P, t, stg, j0, cnt, lane);
+        if (seg == 0) decode_unit<2>(P, t, j0, cnt, lane);
+        else if (seg == 1) decode_unit<4>(P, t, j0, cnt, lane);
+        else decode_unit<8>(P, t, j0, cnt, lane);
     }
 }
 
 template <typename K>
-int grid_for(K kernel, size_t dyn_smem, int64_t units)
+int grid_for(K kernel, int warps, size_t dyn_smem, int64_t units)
 {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kWarps * 32, dyn_smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, warps * 32, dyn_smem) != cudaSuccess ||
         per_sm < 1)
         per_sm = 1;
     const int64_t cap = (int64_t)sm_count() * per_sm;
-    const int64_t need = (units + kWarps - 1) / kWarps;
+    const int64_t need = (units + warps - 1) / warps;
     return (int)(need < cap ? (need < 1 ? 1 : need) : cap);
 }
 
@@ -430,7 +448,7 @@ cudaError_t launch_hop_t(const HopParams &P, cudaStream_t st)
 {
     const size_t dyn = (size_t)kWarps * kStages * ((ADD_F32 ? 2048 : 1024) + 544);
     auto k = hop_kernel<HAS_IN, ADD_F32, ONE_LEVEL>;
-    k<<<grid_for(k, dyn, P.total_units), kWarps * 32, dyn, st>>>(P);
+    k<<<grid_for(k, kWarps, dyn, P.total_units), kWarps * 32, dyn, st>>>(P);
     note_launches(1);
     return cudaGetLastError();
 }
@@ -449,8 +467,7 @@ cudaError_t launch_hop(const HopParams &P, bool has_in, bool add_f32, cudaStream
 cudaError_t launch_decode(const DecodeParams &P, cudaStream_t st)
 {
     if (P.total_units <= 0) return cudaSuccess;
-    const size_t dyn = (size_t)kWarps * kStages * 544;
-    decode_kernel<<<grid_for(decode_kernel, dyn, P.total_units), kWarps * 32, dyn, st>>>(P);
+    decode_kernel<<<grid_for(decode_kernel, kDecodeWarps, 0, P.total_units), kDecodeWarps * 32, 0, st>>>(P);
     note_launches(1);
     return cudaGetLastError();
 }

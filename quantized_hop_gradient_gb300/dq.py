@@ -53,7 +53,7 @@ class dq_launch_log(C.Structure):
                 ("capacity", C.c_int32), ("count", C.c_int32)]
 
 
-DQ_LAUNCH_COMPRESS, DQ_LAUNCH_DAR, DQ_LAUNCH_DECODE = 0, 1, 2
+DQ_LAUNCH_COMPRESS, DQ_LAUNCH_DAR, DQ_LAUNCH_DECODE, DQ_LAUNCH_STATS, DQ_LAUNCH_ALLOCATE_REORDER = 0, 1, 2, 3, 4
 
 
 class dq_plan_info(C.Structure):
@@ -84,7 +84,7 @@ _SIGS = {
                    C.c_int32, C.c_void_p], C.c_int),
     "dq_plan_workspace_bytes": ([C.c_int32, C.c_int64], C.c_size_t),
     "dq_plan": ([C.POINTER(dq_config), C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p,
-                 C.c_size_t, C.POINTER(dq_plan_info), C.c_void_p], C.c_int),
+                 C.c_size_t, C.POINTER(dq_plan_info), C.c_void_p, C.c_void_p], C.c_int),
     "dq_exchange_workspace_bytes": ([C.POINTER(dq_config), C.c_int32, C.c_int64,
                                      C.POINTER(dq_plan_info)], C.c_size_t),
     "dq_exchange": ([C.POINTER(dq_config), C.c_int32, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
@@ -236,11 +236,12 @@ def dq_plan_workspace_bytes(n_ranks, n_sg) -> int:
     return lib().dq_plan_workspace_bytes(n_ranks, n_sg)
 
 
-def dq_plan(cfg, grads, n_sg, mu, perm, ws, ws_bytes, stream=None) -> dq_plan_info:
+def dq_plan(cfg, grads, n_sg, mu, perm, ws, ws_bytes, log=None, stream=None) -> dq_plan_info:
     ptrs = (C.c_void_p * len(grads))(*[_ptr(g) for g in grads])
     info = dq_plan_info()
     _check(lib().dq_plan(C.byref(cfg), C.cast(ptrs, C.c_void_p), n_sg, _ptr(mu), _ptr(perm), _ptr(ws),
-                         ws_bytes, C.byref(info), _stream(stream)), "dq_plan")
+                         ws_bytes, C.byref(info), C.byref(log.c) if log is not None else None,
+                         _stream(stream)), "dq_plan")
     return info
 
 

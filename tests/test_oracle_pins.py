@@ -98,6 +98,22 @@ def test_uniform16_is_uniform_and_streams_differ():
     assert np.array_equal(u, oracle.uniform16(idx, seed=7, round=3, n_ranks=8, hop=1, rank=2))
 
 
+def test_uniform_mapping_one_draw_per_group():
+    """One Philox call per group of 16 coordinates: coordinate c takes the
+    16-bit field c mod 8 of the call with counter i/16, shifted by half a
+    period for c >= 8 (read here straight from the generator's words)."""
+    seed, rnd, hop, rank = 0x1234_5678_9ABC, 5, 3, 2
+    idx = np.arange(16 * 6) + 16 * 1000
+    u = oracle.uniform16(idx, seed=seed, round=rnd, n_ranks=4, hop=hop, rank=rank)
+    for i, ui in zip(idx, u):
+        w = oracle.philox4x32_10([i >> 4, hop | (rank << 16), rnd, 0], [seed & 0xFFFFFFFF, seed >> 32])
+        f = i & 7
+        v = (int(w[f >> 1]) >> (16 * (f & 1))) & 0xFFFF
+        if i & 8:
+            v = (v + 0x8000) & 0xFFFF
+        assert ui == v
+
+
 def test_correlated_uniforms_are_stratified_within_a_stage():
     """Correlated rounding: the n workers quantizing one coordinate at one
     stage draw one uniform per stratum [k/n, (k+1)/n); each is uniform, and
