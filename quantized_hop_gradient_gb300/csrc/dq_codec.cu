@@ -1,9 +1,8 @@
 // dq_codec.cu -- per-super-group statistics and the simulated metadata
 // all-reduce.
 //
-// Work mapping: one warp per super-group, lane l owning coordinates
-// 8l .. 8l+7 (16 bytes of bf16, one 128-bit load); lanes 2g and 2g+1 hold
-// group g.
+// Work mapping of the statistics: half a warp per super-group, one group of
+// 16 coordinates per lane.
 #include "dq_common.cuh"
 #include "dq_internal.h"
 
@@ -12,55 +11,67 @@ namespace dq {
 // ---------------------------------------------------------------------------
 // Statistics: per super-group sum and sum of squares over the raw bf16
 // values, fp32, fixed tree.  Tree within a group: a[i] += a[i+h] for
-// h = 8, 4, 2, 1 (h = 8 pairs the two lanes of a group: one xor-1 shuffle;
-// h = 4, 2, 1 stay in the lane).  Then the 16 group partials by the same
-// tree: h = 8, 4, 2, 1 groups apart = lanes xor 16, 8, 4, 2.  fp32 addition
-// is commutative, so the lane on either side of a shuffle computes the same
-// value.  mean = sum * 2^-8.
+// h = 8, 4, 2, 1; then the 16 group partials by the same tree.  Mapping:
+// half a warp per super-group, lane l of the half owning group l (two
+// 128-bit loads of 8 bf16), so the group tree stays in the lane and the tree
+// over groups is four xor shuffles (h = 8, 4, 2, 1 lanes apart) per sum.
+// fp32 addition is commutative, so the lanes on both sides of a shuffle
+// compute the same value.  mean = sum * 2^-8.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float lane_tree8(float (&a)[8])
+__device__ __forceinline__ float group_tree16(float (&a)[16])
 {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = __fadd_rn(a[i], __shfl_xor_sync(kFull, a[i], 1));
-#pragma unroll
-    for (int h = 4; h >= 1; h >>= 1)
+    for (int h = 8; h >= 1; h >>= 1)
 #pragma unroll
         for (int i = 0; i < h; ++i) a[i] = __fadd_rn(a[i], a[i + h]);
-    float v = a[0];
+    return a[0];
+}
+
+__device__ __forceinline__ float half_tree16(float v)
+{
 #pragma unroll
-    for (int m = 16; m >= 2; m >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, m));
+    for (int h = 8; h >= 1; h >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, h));
     return v;
 }
 
 __global__ void __launch_bounds__(256) stats_kernel(const uint16_t *__restrict__ g, int64_t n_sg,
                                                     float *__restrict__ mean, float *__restrict__ sq)
 {
-    constexpr int kAhead = 4;   // super-groups loaded before any is reduced
-    const int lane = threadIdx.x & 31;
+    constexpr int kAhead = 2;   // pairs of super-groups loaded before any is reduced
+    const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
     const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    for (int64_t jb = w0; jb < n_sg; jb += nw * kAhead) {
-        uint4 v[kAhead];
+    // warp w handles super-group pairs w, w + nw, ...; pair p = super-groups 2p, 2p+1
+    const int64_t n_pairs = (n_sg + 1) >> 1;
+    for (int64_t pb = w0; pb < n_pairs; pb += nw * kAhead) {
+        uint4 v[kAhead][2];
 #pragma unroll
         for (int a = 0; a < kAhead; ++a) {
-            const int64_t j = jb + a * nw;
-            v[a] = j < n_sg ? __ldcs(reinterpret_cast<const uint4 *>(g + j * kSG) + lane) : make_uint4(0, 0, 0, 0);
+            const int64_t j = 2 * (pb + a * nw) + half;
+            if (j < n_sg) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(g + j * kSG + hl * 16);
+                v[a][0] = __ldg(src);
+                v[a][1] = __ldg(src + 1);
+            } else {
+                v[a][0] = v[a][1] = make_uint4(0, 0, 0, 0);
+            }
         }
 #pragma unroll
         for (int a = 0; a < kAhead; ++a) {
-            const int64_t j = jb + a * nw;
-            const uint32_t w[4] = {v[a].x, v[a].y, v[a].z, v[a].w};
-            float x[8], y[8];
+            const int64_t j = 2 * (pb + a * nw) + half;
+            const uint32_t w[8] = {v[a][0].x, v[a][0].y, v[a][0].z, v[a][0].w,
+                                   v[a][1].x, v[a][1].y, v[a][1].z, v[a][1].w};
+            float x[16], y[16];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < 8; ++k) {
                 x[2 * k] = bf16_lo(w[k]);
                 x[2 * k + 1] = bf16_hi(w[k]);
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(x[i], x[i]);
-            const float s = lane_tree8(x);
-            const float q = lane_tree8(y);
-            if (lane == 0 && j < n_sg) {
+            for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(x[i], x[i]);
+            const float s = half_tree16(group_tree16(x));
+            const float q = half_tree16(group_tree16(y));
+            if (hl == 0 && j < n_sg) {
                 mean[j] = __fmul_rn(s, 0.00390625f);
                 sq[j] = q;
             }
@@ -101,7 +112,7 @@ static int grid_for(int64_t work_warps)
 
 cudaError_t launch_stats(const uint16_t *g, int64_t n_sg, float *mean, float *sq, cudaStream_t st)
 {
-    stats_kernel<<<grid_for(n_sg), 256, 0, st>>>(g, n_sg, mean, sq);
+    stats_kernel<<<grid_for((n_sg + 1) / 2), 256, 0, st>>>(g, n_sg, mean, sq);
     note_launches(1);
     return cudaGetLastError();
 }

@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kWarps * 32) hop_kernel(const __grid_constant_
 // mapping makes every store instruction cover contiguous memory: lane l of
 // the warp decodes coordinates 4l..4l+3 (group l/4) and 128+4l..131+4l
 // (group 8 + l/4) of a super-group, so each warp store writes 512
-// contiguous bytes.  Four super-groups are loaded before any is computed.
+// contiguous bytes.  Eight super-groups are loaded before any is computed.
 // ---------------------------------------------------------------------------
 template <int BITS>
 __device__ __forceinline__ uint32_t ldg_codes4(const uint8_t *blk, int idx)
@@ -342,7 +342,7 @@ __device__ __forceinline__ uint32_t ldg_codes4(const uint8_t *blk, int idx)
 template <int BITS>
 __device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeTask &t, int64_t j0, int cnt, int lane)
 {
-    constexpr int kAhead = 4;
+    constexpr int kAhead = 8;
     int32_t old_i = 0;
     float mu_i = 0.0f;
     uint32_t ein_i = 0;
@@ -410,7 +410,7 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeT
     }
 }
 
-constexpr int kDecodeWarps = 8;
+constexpr int kDecodeWarps = 16;
 
 __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kernel(const __grid_constant__ DecodeParams P)
 {
