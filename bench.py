@@ -167,20 +167,21 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:12]
 
 
-def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+def ncu_counters(kernel: str, workload: str):
+    """(DRAM bytes per launch, warp-instructions per super-group) from the
+    committed ncu summary, if it was taken on the current kernel sources
+    (else (None, None))."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
-        return None
+        return None, None
     want = kernel_source_hash()
     with open(p) as f:
         for line in f:
             parts = line.split()
             if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload \
                     and parts[3] == want:
-                return float(parts[2])
-    return None
+                return float(parts[2]), (float(parts[4]) if len(parts) > 4 else None)
+    return None, None
 
 
 # --------------------------------------------------------------------------- algorithmic bytes
@@ -328,11 +329,30 @@ def run_gpu(args, rank, world, local):
     dk = kernels[dominant]
     kname = {"compress": "hop_kernel<false,false>", "dar": "hop_kernel<true,false>", "decode": "decode_kernel",
              "stats": "stats_kernel"}
+    traffic, _ = ncu_counters(kname[dominant], w.name)
     roofline = {"bound": "hbm", "kernel": kname[dominant], "achieved": dk["achieved_gbs"], "peak": peak,
                 "unit": "GB/s", "frac": dk["achieved_gbs"] / peak, "peak_source": peak_kind,
-                "traffic": ncu_traffic(kname[dominant], w.name),
-                "alg_bytes_per_launch": dk["alg_bytes_per_launch"]}
+                "traffic": traffic, "alg_bytes_per_launch": dk["alg_bytes_per_launch"]}
     dar = kernels.get("dar", {})
+    # The DAR hop is bound by instruction issue, not HBM: its issue roofline
+    # (warp-instructions per super-group from the committed ncu capture,
+    # times super-groups per launch, over the measured launch time) against
+    # 4 issue slots per SM per cycle at the maximum SM clock.
+    dar_issue = None
+    _, inst_per_sg = ncu_counters("hop_kernel<true,false>", w.name)
+    if dar and inst_per_sg:
+        sm_mhz = 2070.0
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                sm_mhz = float(json.load(f).get("sm_max_mhz", sm_mhz))
+        except Exception:
+            pass
+        issue_peak = 4 * torch.cuda.get_device_properties(dev).multi_processor_count * sm_mhz * 1e6
+        sgs = dar["gcoords_per_s"] * 1e9 / SG * dar["avg_launch_ms"] * 1e-3
+        achieved = inst_per_sg * sgs / (dar["avg_launch_ms"] * 1e-3)
+        dar_issue = {"bound": "alu", "achieved": achieved / 1e12, "peak": issue_peak / 1e12,
+                     "unit": "T warp-instructions/s", "frac": achieved / issue_peak,
+                     "warp_instructions_per_super_group": inst_per_sg}
     gb = J * SG * 2 / 1e9
 
     # end to end: host gradients in pinned memory, copies inside the timed region
@@ -374,7 +394,8 @@ def run_gpu(args, rank, world, local):
                    "l2": "inputs larger than L2 (no flush needed)",
                    "allocation": {"T": ar.info.T, "n2": ar.info.n2, "n4": ar.info.n4, "n8": ar.info.n8}},
         "dar": {"gcoords_per_s_per_hop": dar.get("gcoords_per_s"), "achieved_gbs": dar.get("achieved_gbs"),
-                "hbm_frac": (dar["achieved_gbs"] / peak) if dar else None, "avg_launch_ms": dar.get("avg_launch_ms")},
+                "hbm_frac": (dar["achieved_gbs"] / peak) if dar else None, "avg_launch_ms": dar.get("avg_launch_ms"),
+                "issue_roofline": dar_issue},
         "kernels": kernels,
         "roofline": roofline,
         "e2e": {"value": ms_e2e / (world * gb), "unit": UNIT, "h2d_bytes_per_step": N * J * SG * 2,

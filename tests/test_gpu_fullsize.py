@@ -1,0 +1,82 @@
+"""Parity at full workload sizes, in the launch configuration bench.py times.
+
+The GPU runs the whole all-reduce exactly as the benchmark does (gradients
+drawn on the device, DynamiQAllReduce).  The oracle recomputes the plan for
+the whole gradient (statistics, allocation, reordering: compared in full,
+bit for bit) and then follows a sample of super-groups one by one through
+the topology (random ones plus the first and last of every chunk and of
+every bitwidth stream); their outputs and final message bytes must match
+bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_hop_gradient_gb300 import build, dq, synth
+from quantized_hop_gradient_gb300.allreduce import DynamiQAllReduce
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample(J, chunk_lo, n2, n4, rs, k=1500):
+    pts = set(rs.integers(0, J, k).tolist())
+    for c in chunk_lo:
+        for d in (-2, -1, 0, 1):
+            if 0 <= c + d < J:
+                pts.add(int(c + d))
+    for e in (n2, n2 + n4):
+        for d in (-2, -1, 0, 1):
+            if 0 <= e + d < J:
+                pts.add(int(e + d))
+    return np.array(sorted(pts), dtype=np.int64)
+
+
+def _full_size(name, butterfly):
+    build.build()
+    w = synth.WORKLOADS[name]
+    N, J = w.n_ranks, w.n_sg
+    grads = synth.generate(w, "cuda", seed=0)
+    ar = DynamiQAllReduce(N, J, budget=w.budget, correlated=w.correlated, butterfly=butterfly, seed=0)
+    outs = ar(grads, round=3)
+    torch.cuda.synchronize()
+    gu = [synth.as_u16(g) for g in grads]
+    del grads
+    cfg = oracle.Config(N, w.budget, correlated=w.correlated, seed=0, round=3)
+    p = oracle.plan(cfg, gu)
+    info = ar.info
+    assert [info.n2, info.n4, info.n8] == p.counts.tolist()
+    assert np.float32(info.T).view(np.int32) == np.float32(p.T).view(np.int32)
+    assert np.array_equal(ar.perm.cpu().numpy(), p.perm)
+    assert np.array_equal(ar.mu.cpu().numpy().view(np.int32), (p.M / np.float32(N)).view(np.int32))
+    lo = ar.chunk_lo()
+    assert lo == p.chunk_lo.tolist()
+    sel = _sample(J, lo, info.n2, info.n4, np.random.default_rng(7))
+    rows, fin = oracle.allreduce_sg(cfg, butterfly, gu, p.M, p.perm, int(info.n2), int(info.n4), p.chunk_lo, sel)
+    old = torch.from_numpy(p.perm[sel].astype(np.int64)).cuda()
+    idx = (old[:, None] * 256 + torch.arange(256, device="cuda")[None, :]).reshape(-1)
+    for r in (0, N - 1):
+        got = outs[r][idx].cpu().numpy().reshape(-1, 256)
+        assert np.array_equal(got.view(np.int32), rows.view(np.int32)), f"rank {r}: outputs differ"
+    # E bytes and UINT8 scales of the sampled super-groups in the final chunk messages
+    for c in range(N):
+        a, b = lo[c], lo[c + 1]
+        inside = sel[(sel >= a) & (sel < b)]
+        if inside.size == 0:
+            continue
+        m = ar.final_message(c).numpy()
+        cnt = b - a
+        off_u = -(-cnt // 16) * 16
+        for j in inside:
+            s = int(j - a)
+            f = fin[np.searchsorted(sel, j)]
+            assert m[s] == f[0]
+            assert np.array_equal(m[off_u + 16 * s: off_u + 16 * s + 16], f[1:17])
+
+
+def test_bert_large_ring8_full_size_sampled():
+    _full_size("bert_large_ring8", butterfly=False)
+
+
+def test_llama1b_butterfly8_full_size_sampled():
+    _full_size("llama1b_butterfly8", butterfly=True)
