@@ -224,11 +224,16 @@ size_t dq_plan_workspace_bytes(int32_t n_ranks, int64_t n_sg);
  *   mu, perm: device outputs (J floats, J int32) used by dq_exchange.
  *   info_host: host output.  Synchronises `stream` once to read the counts.
  *   plan_ws: device scratch of dq_plan_workspace_bytes(N, J).
+ *   rank_ready_host: NULL, or a host array of N cudaEvent_t (entries may
+ *   be NULL): the statistics of rank r wait on event r, so a rank's
+ *   statistics start as soon as its gradient is ready (e.g. its upload or
+ *   its backward pass finished) while other ranks' are still in flight.
  *   log: NULL or a dq_launch_log to fill (see below). */
 typedef struct dq_launch_log dq_launch_log;
 dq_status dq_plan(const dq_config *cfg, const void *const *grads_host, int64_t n_sg,
                   float *mu, int32_t *perm, void *plan_ws, size_t plan_ws_bytes,
-                  dq_plan_info *info_host, dq_launch_log *log, void *stream);
+                  dq_plan_info *info_host, void *const *rank_ready_host, dq_launch_log *log,
+                  void *stream);
 
 /* Optional record of the kernel launches of dq_plan and dq_exchange, for timing them on
  * the launching stream.  events: host array of 2*capacity cudaEvent_t created

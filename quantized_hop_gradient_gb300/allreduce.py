@@ -35,10 +35,16 @@ class DynamiQAllReduce:
     def config(self, round: int = 0):
         return dq.config(self.n_ranks, self.budget, self.eps, self.correlated, self.seed, round)
 
-    def plan(self, grads, round: int = 0, stream=None, log=None):
+    def plan(self, grads, round: int = 0, stream=None, log=None, ready=None, n_sg=None):
+        """Statistics, allocation and reordering.  ``ready``: optional
+        per-rank events the statistics of each rank wait on.  ``n_sg``: a
+        smaller super-group count than the buffers were sized for."""
         cfg = self.config(round)
-        self.info = dq.dq_plan(cfg, grads, self.n_sg, self.mu, self.perm, self.plan_ws, self.plan_ws.numel(),
-                               log, stream)
+        self.cur_sg = n_sg or self.n_sg
+        if self.cur_sg > self.n_sg:
+            raise ValueError("more super-groups than the buffers hold")
+        self.info = dq.dq_plan(cfg, grads, self.cur_sg, self.mu, self.perm, self.plan_ws, self.plan_ws.numel(),
+                               log, stream, ready)
         return self.info
 
     def reserve(self, nbytes: int):
@@ -47,11 +53,12 @@ class DynamiQAllReduce:
 
     def exchange(self, grads, outs, round: int = 0, stream=None, log=None):
         cfg = self.config(round)
-        need = dq.dq_exchange_workspace_bytes(cfg, self.butterfly, self.n_sg, self.info)
+        n_sg = getattr(self, "cur_sg", self.n_sg)
+        need = dq.dq_exchange_workspace_bytes(cfg, self.butterfly, n_sg, self.info)
         if need == 0:
             raise dq.DQError(dq.DQ_ERR_INVALID_ARG, "dq_exchange_workspace_bytes")
         self.reserve(need)
-        self.final = dq.dq_exchange(cfg, self.butterfly, grads, self.n_sg, self.mu, self.perm, self.info,
+        self.final = dq.dq_exchange(cfg, self.butterfly, grads, n_sg, self.mu, self.perm, self.info,
                                     self.ws, self.ws.numel(), outs, self.out_dtype == torch.bfloat16, log,
                                     stream)
         return outs

@@ -603,7 +603,7 @@ size_t dq_plan_workspace_bytes(int32_t n_ranks, int64_t n_sg)
 }
 
 dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, float *mu, int32_t *perm, void *ws,
-                  size_t ws_bytes, dq_plan_info *info, dq_launch_log *log, void *stream)
+                  size_t ws_bytes, dq_plan_info *info, void *const *rank_ready, dq_launch_log *log, void *stream)
 {
     if (!cfg_ok(cfg) || !grads || !mu || !perm || !ws || !info || n_sg < 1 || n_sg >= kMaxSG)
         return DQ_ERR_INVALID_ARG;
@@ -627,6 +627,9 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
     int64_t *counts = reinterpret_cast<int64_t *>(w + L.counts);
     void *scratch = w + L.scratch;
     for (int32_t r = 0; r < N; ++r) {
+        if (rank_ready && rank_ready[r] &&
+            cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(rank_ready[r]), 0) != cudaSuccess)
+            return DQ_ERR_CUDA;
         const LogSlot slot = log_begin(log, DQ_LAUNCH_STATS, n_sg, st);
         const cudaError_t e = launch_stats(static_cast<const uint16_t *>(grads[r]), n_sg,
                                            mean_all + (size_t)r * n_sg, sq_all + (size_t)r * n_sg, st);

@@ -84,7 +84,7 @@ _SIGS = {
                    C.c_int32, C.c_void_p], C.c_int),
     "dq_plan_workspace_bytes": ([C.c_int32, C.c_int64], C.c_size_t),
     "dq_plan": ([C.POINTER(dq_config), C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p,
-                 C.c_size_t, C.POINTER(dq_plan_info), C.c_void_p, C.c_void_p], C.c_int),
+                 C.c_size_t, C.POINTER(dq_plan_info), C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "dq_exchange_workspace_bytes": ([C.POINTER(dq_config), C.c_int32, C.c_int64,
                                      C.POINTER(dq_plan_info)], C.c_size_t),
     "dq_exchange": ([C.POINTER(dq_config), C.c_int32, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
@@ -236,12 +236,16 @@ def dq_plan_workspace_bytes(n_ranks, n_sg) -> int:
     return lib().dq_plan_workspace_bytes(n_ranks, n_sg)
 
 
-def dq_plan(cfg, grads, n_sg, mu, perm, ws, ws_bytes, log=None, stream=None) -> dq_plan_info:
+def dq_plan(cfg, grads, n_sg, mu, perm, ws, ws_bytes, log=None, stream=None, ready=None) -> dq_plan_info:
+    """``ready``: optional list of torch.cuda.Event, one per rank (or None)."""
     ptrs = (C.c_void_p * len(grads))(*[_ptr(g) for g in grads])
+    ev = None
+    if ready is not None:
+        ev = (C.c_void_p * len(grads))(*[(e.cuda_event if e is not None else None) for e in ready])
     info = dq_plan_info()
     _check(lib().dq_plan(C.byref(cfg), C.cast(ptrs, C.c_void_p), n_sg, _ptr(mu), _ptr(perm), _ptr(ws),
-                         ws_bytes, C.byref(info), C.byref(log.c) if log is not None else None,
-                         _stream(stream)), "dq_plan")
+                         ws_bytes, C.byref(info), C.cast(ev, C.c_void_p) if ev is not None else None,
+                         C.byref(log.c) if log is not None else None, _stream(stream)), "dq_plan")
     return info
 
 

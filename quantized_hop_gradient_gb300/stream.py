@@ -1,0 +1,50 @@
+"""Bucketed (DDP-style) all-reduce of a large gradient on one GPU.
+
+The gradient of every simulated worker is cut into buckets of a fixed number
+of super-groups, as DDP cuts it into communication buckets; each bucket is
+one DynamiQ round with its own statistics, allocation, reordering, hops and
+decode.  Bucket k+1's planning runs on a second CUDA stream while bucket k's
+hops and decode run on the first; two buffer sets alternate between buckets,
+ordered by events.
+"""
+from __future__ import annotations
+
+import torch
+
+from .allreduce import DynamiQAllReduce
+
+
+class BucketedAllReduce:
+    def __init__(self, n_ranks: int, bucket_sg: int, *, overlap: bool = True, **kw):
+        self.n_ranks, self.bucket_sg, self.overlap = n_ranks, bucket_sg, overlap
+        self.sets = [DynamiQAllReduce(n_ranks, bucket_sg, **kw) for _ in range(2)]
+        self.plan_stream = torch.cuda.Stream() if overlap else None
+        self.ev_plan = [torch.cuda.Event(), torch.cuda.Event()]
+        self.ev_done = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def run(self, buckets, outs, round0: int = 0):
+        """buckets[k][r]: rank r's bf16 gradient of bucket k (device, a multiple
+        of 256 coordinates, at most bucket_sg super-groups); outs[k][r]: where
+        rank r's fp32 (or bf16) result of bucket k goes.  Returns the plan
+        infos of the buckets."""
+        main = torch.cuda.current_stream()
+        side = self.plan_stream if self.overlap else main
+        infos = []
+
+        def plan(k):
+            s = k & 1
+            n_sg = buckets[k][0].numel() // 256
+            side.wait_event(self.ev_done[s])           # the set's previous bucket has finished
+            with torch.cuda.stream(side):
+                infos.append(self.sets[s].plan(buckets[k], round=round0 + k, n_sg=n_sg))
+                self.ev_plan[s].record(side)
+
+        plan(0)
+        for k in range(len(buckets)):
+            s = k & 1
+            main.wait_event(self.ev_plan[s])
+            self.sets[s].exchange(buckets[k], outs[k], round=round0 + k)
+            self.ev_done[s].record(main)
+            if k + 1 < len(buckets):
+                plan(k + 1)
+        return infos
