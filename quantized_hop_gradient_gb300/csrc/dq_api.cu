@@ -279,10 +279,11 @@ cudaError_t run_hops(HopParams &P, const std::vector<PendingHop> &tasks, int64_t
     return cudaSuccess;
 }
 
-// A chunk to decode: its message and reordered range.
+// A chunk to decode: its message, reordered range and output.
 struct PendingDecode {
     const uint8_t *msg;
     int64_t lo, hi;
+    void *out;
 };
 
 cudaError_t run_decodes(DecodeParams &D, const std::vector<PendingDecode> &chunks, int64_t end2, int64_t end4,
@@ -298,6 +299,7 @@ cudaError_t run_decodes(DecodeParams &D, const std::vector<PendingDecode> &chunk
             DecodeTask &t = D.task[n++];
             memset(&t, 0, sizeof(t));
             t.msg = msg_view(const_cast<uint8_t *>(c.msg), c.lo, c.hi, end2, end4);
+            t.out = c.out;
             t.lo = c.lo;
             units += set_units(t, c.lo, c.hi, end2, end4, units);
             sgs += c.hi - c.lo;
@@ -314,7 +316,7 @@ cudaError_t run_decodes(DecodeParams &D, const std::vector<PendingDecode> &chunk
     return cudaSuccess;
 }
 
-std::unique_ptr<DecodeParams> decode_params(const dq_config *cfg, const float *mu, const int32_t *perm, void *out,
+std::unique_ptr<DecodeParams> decode_params(const dq_config *cfg, const float *mu, const int32_t *perm,
                                             int32_t out_is_bf16, const Tables &tab)
 {
     std::unique_ptr<DecodeParams> D(new DecodeParams());
@@ -323,7 +325,6 @@ std::unique_ptr<DecodeParams> decode_params(const dq_config *cfg, const float *m
     D->n_ranks = cfg->n_ranks;
     D->mu = mu;
     D->perm = perm;
-    D->out = out;
     D->out_is_bf16 = out_is_bf16 ? 1 : 0;
     return D;
 }
@@ -500,8 +501,8 @@ dq_status dq_decode(const dq_config *cfg, dq_range r, const uint8_t *msg, const 
     if (!aligned16(msg) || !aligned16(out)) return DQ_ERR_ALIGNMENT;
     Tables tab;
     if (!build_tables(cfg->eps, &tab)) return DQ_ERR_INVALID_ARG;
-    std::unique_ptr<DecodeParams> D = decode_params(cfg, mu, perm, out, out_is_bf16, tab);
-    return cuda_status(run_decodes(*D, {PendingDecode{msg, r.lo, r.hi}}, r.end2, r.end4,
+    std::unique_ptr<DecodeParams> D = decode_params(cfg, mu, perm, out_is_bf16, tab);
+    return cuda_status(run_decodes(*D, {PendingDecode{msg, r.lo, r.hi, out}}, r.end2, r.end4,
                                    static_cast<cudaStream_t>(stream), nullptr));
 }
 
@@ -626,15 +627,30 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
     float *T = reinterpret_cast<float *>(w + L.T);
     int64_t *counts = reinterpret_cast<int64_t *>(w + L.counts);
     void *scratch = w + L.scratch;
-    for (int32_t r = 0; r < N; ++r) {
-        if (rank_ready && rank_ready[r] &&
-            cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(rank_ready[r]), 0) != cudaSuccess)
-            return DQ_ERR_CUDA;
-        const LogSlot slot = log_begin(log, DQ_LAUNCH_STATS, n_sg, st);
-        const cudaError_t e = launch_stats(static_cast<const uint16_t *>(grads[r]), n_sg,
-                                           mean_all + (size_t)r * n_sg, sq_all + (size_t)r * n_sg, st);
-        log_end(slot, st);
-        if (e != cudaSuccess) return DQ_ERR_CUDA;
+    if (rank_ready) {  // one launch per rank, each after its rank's event
+        for (int32_t r = 0; r < N; ++r) {
+            if (rank_ready[r] && cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(rank_ready[r]), 0) != cudaSuccess)
+                return DQ_ERR_CUDA;
+            const LogSlot slot = log_begin(log, DQ_LAUNCH_STATS, n_sg, st);
+            const cudaError_t e = launch_stats(static_cast<const uint16_t *>(grads[r]), n_sg,
+                                               mean_all + (size_t)r * n_sg, sq_all + (size_t)r * n_sg, st);
+            log_end(slot, st);
+            if (e != cudaSuccess) return DQ_ERR_CUDA;
+        }
+    } else {           // all ranks in launches of up to kMaxStatsRanks
+        for (int32_t r0 = 0; r0 < N; r0 += kMaxStatsRanks) {
+            StatsParams S;
+            memset(&S, 0, sizeof(S));
+            S.n_ranks = std::min(N - r0, kMaxStatsRanks);
+            for (int32_t r = 0; r < S.n_ranks; ++r) S.g[r] = static_cast<const uint16_t *>(grads[r0 + r]);
+            S.n_sg = n_sg;
+            S.mean_all = mean_all + (size_t)r0 * n_sg;
+            S.sq_all = sq_all + (size_t)r0 * n_sg;
+            const LogSlot slot = log_begin(log, DQ_LAUNCH_STATS, n_sg * S.n_ranks, st);
+            const cudaError_t e = launch_stats_batched(S, st);
+            log_end(slot, st);
+            if (e != cudaSuccess) return DQ_ERR_CUDA;
+        }
     }
     const LogSlot slot = log_begin(log, DQ_LAUNCH_ALLOCATE_REORDER, n_sg, st);
     if (launch_stats_reduce(mean_all, sq_all, N, n_sg, M, F, mu, st) != cudaSuccess) return DQ_ERR_CUDA;
@@ -777,13 +793,12 @@ dq_status dq_exchange(const dq_config *cfg, int32_t butterfly, const void *const
 
     // All-gather hands the final chunks to every rank unchanged; each rank
     // decodes all of them into its own output.
+    // (rank, chunk) pairs in launches of up to kMaxTasks tasks.
     std::vector<PendingDecode> chunks;
-    for (int32_t c = 0; c < N; ++c) chunks.push_back(PendingDecode{fin[c], lo[c], lo[c + 1]});
-    std::unique_ptr<DecodeParams> D = decode_params(cfg, mu, perm, nullptr, out_is_bf16, P->tab);
-    for (int32_t r = 0; r < N; ++r) {
-        D->out = outs[r];
-        if (run_decodes(*D, chunks, end2, end4, st, log) != cudaSuccess) return DQ_ERR_CUDA;
-    }
+    for (int32_t r = 0; r < N; ++r)
+        for (int32_t c = 0; c < N; ++c) chunks.push_back(PendingDecode{fin[c], lo[c], lo[c + 1], outs[r]});
+    std::unique_ptr<DecodeParams> D = decode_params(cfg, mu, perm, out_is_bf16, P->tab);
+    if (run_decodes(*D, chunks, end2, end4, st, log) != cudaSuccess) return DQ_ERR_CUDA;
     if (final_msgs)
         for (int32_t c = 0; c < N; ++c) final_msgs[c] = fin[c];
     return DQ_OK;

@@ -34,48 +34,68 @@ __device__ __forceinline__ float half_tree16(float v)
     return v;
 }
 
+// Pairs of super-groups of one rank: super-groups 2p, 2p+1 of gradient g.
+__device__ __forceinline__ void stats_pairs(const uint16_t *__restrict__ g, int64_t n_sg, float *__restrict__ mean,
+                                            float *__restrict__ sq, int64_t pb, int64_t stride, int lane)
+{
+    constexpr int kAhead = 2;   // pairs of super-groups loaded before any is reduced
+    const int half = lane >> 4, hl = lane & 15;
+    uint4 v[kAhead][2];
+#pragma unroll
+    for (int a = 0; a < kAhead; ++a) {
+        const int64_t j = 2 * (pb + a * stride) + half;
+        if (j < n_sg) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(g + j * kSG + hl * 16);
+            v[a][0] = __ldg(src);
+            v[a][1] = __ldg(src + 1);
+        } else {
+            v[a][0] = v[a][1] = make_uint4(0, 0, 0, 0);
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < kAhead; ++a) {
+        const int64_t j = 2 * (pb + a * stride) + half;
+        const uint32_t w[8] = {v[a][0].x, v[a][0].y, v[a][0].z, v[a][0].w,
+                               v[a][1].x, v[a][1].y, v[a][1].z, v[a][1].w};
+        float x[16], y[16];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            x[2 * k] = bf16_lo(w[k]);
+            x[2 * k + 1] = bf16_hi(w[k]);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(x[i], x[i]);
+        const float s = half_tree16(group_tree16(x));
+        const float q = half_tree16(group_tree16(y));
+        if (hl == 0 && j < n_sg) {
+            mean[j] = __fmul_rn(s, 0.00390625f);
+            sq[j] = q;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(256) stats_kernel(const uint16_t *__restrict__ g, int64_t n_sg,
                                                     float *__restrict__ mean, float *__restrict__ sq)
 {
-    constexpr int kAhead = 2;   // pairs of super-groups loaded before any is reduced
-    const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
+    const int lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    // warp w handles super-group pairs w, w + nw, ...; pair p = super-groups 2p, 2p+1
     const int64_t n_pairs = (n_sg + 1) >> 1;
-    for (int64_t pb = w0; pb < n_pairs; pb += nw * kAhead) {
-        uint4 v[kAhead][2];
-#pragma unroll
-        for (int a = 0; a < kAhead; ++a) {
-            const int64_t j = 2 * (pb + a * nw) + half;
-            if (j < n_sg) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(g + j * kSG + hl * 16);
-                v[a][0] = __ldg(src);
-                v[a][1] = __ldg(src + 1);
-            } else {
-                v[a][0] = v[a][1] = make_uint4(0, 0, 0, 0);
-            }
-        }
-#pragma unroll
-        for (int a = 0; a < kAhead; ++a) {
-            const int64_t j = 2 * (pb + a * nw) + half;
-            const uint32_t w[8] = {v[a][0].x, v[a][0].y, v[a][0].z, v[a][0].w,
-                                   v[a][1].x, v[a][1].y, v[a][1].z, v[a][1].w};
-            float x[16], y[16];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                x[2 * k] = bf16_lo(w[k]);
-                x[2 * k + 1] = bf16_hi(w[k]);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(x[i], x[i]);
-            const float s = half_tree16(group_tree16(x));
-            const float q = half_tree16(group_tree16(y));
-            if (hl == 0 && j < n_sg) {
-                mean[j] = __fmul_rn(s, 0.00390625f);
-                sq[j] = q;
-            }
-        }
+    for (int64_t pb = w0; pb < n_pairs; pb += nw * 2) stats_pairs(g, n_sg, mean, sq, pb, nw, lane);
+}
+
+// Several ranks: warp-blocks of pairs are numbered rank by rank.
+__global__ void __launch_bounds__(256) stats_batched_kernel(const __grid_constant__ StatsParams S)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_pairs = (S.n_sg + 1) >> 1;
+    const int64_t per_rank = (n_pairs + 1) >> 1;   // blocks of two pairs (kAhead) per rank
+    for (int64_t b = w0; b < per_rank * S.n_ranks; b += nw) {
+        const int r = (int)(b / per_rank);
+        const int64_t pb = (b - (int64_t)r * per_rank) * 2;
+        stats_pairs(S.g[r], S.n_sg, S.mean_all + (int64_t)r * S.n_sg, S.sq_all + (int64_t)r * S.n_sg, pb, 1, lane);
     }
 }
 
@@ -113,6 +133,14 @@ static int grid_for(int64_t work_warps)
 cudaError_t launch_stats(const uint16_t *g, int64_t n_sg, float *mean, float *sq, cudaStream_t st)
 {
     stats_kernel<<<grid_for((n_sg + 1) / 2), 256, 0, st>>>(g, n_sg, mean, sq);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stats_batched(const StatsParams &S, cudaStream_t st)
+{
+    const int64_t n_pairs = (S.n_sg + 1) >> 1;
+    stats_batched_kernel<<<grid_for(((n_pairs + 1) >> 1) * S.n_ranks), 256, 0, st>>>(S);
     note_launches(1);
     return cudaGetLastError();
 }

@@ -101,6 +101,7 @@ struct HopParams {
 // One chunk decoded by the final decode (same unit structure).
 struct DecodeTask {
     MsgView msg;
+    void *out;                  // this task's output (a rank's full gradient buffer)
     int64_t lo;
     int64_t seg_lo[3], seg_hi[3];
     int64_t unit_begin[4];
@@ -114,8 +115,17 @@ struct DecodeParams {
     int64_t total_units;
     const float *mu;
     const int32_t *perm;
-    void *out;
     int32_t out_is_bf16;
+};
+
+// Statistics of several ranks in one launch.
+constexpr int kMaxStatsRanks = 64;
+struct StatsParams {
+    const uint16_t *g[kMaxStatsRanks];
+    int32_t n_ranks;
+    int64_t n_sg;
+    float *mean_all;   // n_ranks x n_sg
+    float *sq_all;
 };
 
 // ---------------------------------------------------------------------------

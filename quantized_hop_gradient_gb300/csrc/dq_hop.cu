@@ -387,7 +387,7 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeT
                     vb[i] = __fmaf_rn(sb, q[(cb[a] >> (BITS * i)) & mask], back);
                 }
                 if (P.out_is_bf16) {
-                    uint16_t *o = static_cast<uint16_t *>(P.out) + (int64_t)old * kSG;
+                    uint16_t *o = static_cast<uint16_t *>(t.out) + (int64_t)old * kSG;
                     const uint2 wa = make_uint2(
                         (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(va[0])) |
                             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(va[1])) << 16),
@@ -401,7 +401,7 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeT
                     __stcs(reinterpret_cast<uint2 *>(o + 4 * lane), wa);
                     __stcs(reinterpret_cast<uint2 *>(o + 128 + 4 * lane), wb);
                 } else {
-                    float *o = static_cast<float *>(P.out) + (int64_t)old * kSG;
+                    float *o = static_cast<float *>(t.out) + (int64_t)old * kSG;
                     __stcs(reinterpret_cast<float4 *>(o + 4 * lane), make_float4(va[0], va[1], va[2], va[3]));
                     __stcs(reinterpret_cast<float4 *>(o + 128 + 4 * lane), make_float4(vb[0], vb[1], vb[2], vb[3]));
                 }
