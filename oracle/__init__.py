@@ -64,10 +64,23 @@ def lib():
             L.or_allocate.argtypes = [P, i64, C.c_float, P, P, P]
             L.or_reorder.argtypes = [P, i64, P]
             L.or_chunk_cuts.argtypes = [P, P, i64, i32, P]
-            L.or_message_bytes.argtypes = [i64, i64, i64]
+            L.or_message_bytes.argtypes = [i64, i64, i64, i32]
             L.or_message_bytes.restype = i64
             L.or_quantize_sg.argtypes = [P, C.c_int, P, P, P, i64, P, P, P]
+            L.or_quantize_sg_f32.argtypes = [P, C.c_int, P, P, P, i64, P, P]
             L.or_dequantize_sg.argtypes = [C.c_uint8, P, P, C.c_int, P, P]
+            L.or_decode_add_sg_f32.argtypes = [P, P, C.c_int, P, P, P]
+            L.or_e4m3_value.argtypes = [C.c_uint8]
+            L.or_e4m3_value.restype = C.c_double
+            L.or_e4m3_encode.argtypes = [C.c_double]
+            L.or_e4m3_encode.restype = C.c_uint8
+            L.or_mx_encode_block.argtypes = [P, P, P]
+            L.or_mx_decode_add_block.argtypes = [C.c_uint8, P, P, P]
+            L.or_mx_message_bytes.argtypes = [i64]
+            L.or_mx_message_bytes.restype = i64
+            L.or_mx_quantize.argtypes = [P, i64, P]
+            L.or_mx_dequantize.argtypes = [P, i64, P]
+            L.or_mx_allreduce_blk.argtypes = [i32, i32, P, i64, P, i64, P, P]
             L.or_compress.argtypes = [P, i64, i64, i64, i64, i32, i32, i32, i32, P, P, P, P]
             L.or_dar.argtypes = [P, i64, i64, i64, i64, i32, i32, i32, i32, P, P, i32, P, P,
                                  i64, i64, P, i64, i64, P]
@@ -79,7 +92,8 @@ def lib():
 
 class _Cfg(C.Structure):
     _fields_ = [("n_ranks", C.c_int32), ("budget", C.c_float), ("eps", C.c_double),
-                ("correlated", C.c_int32), ("seed", C.c_uint64), ("round", C.c_uint64)]
+                ("correlated", C.c_int32), ("seed", C.c_uint64), ("round", C.c_uint64),
+                ("fixed_bits", C.c_int32), ("scale_fp32", C.c_int32)]
 
 
 class _Rng(C.Structure):
@@ -90,15 +104,21 @@ class _Rng(C.Structure):
 
 @dataclass
 class Config:
+    """One all-reduce round.  Ablation switches: ``eps=inf`` (uniform levels),
+    ``correlated=False``, ``fixed_bits`` in {2, 4, 8} (uniform bitwidth, no
+    allocation) and ``scale_fp32`` (group scales in fp32, no UINT8 level)."""
     n_ranks: int
     budget: float = 5.0
     eps: float = 1.0
     correlated: bool = False
     seed: int = 0
     round: int = 0
+    fixed_bits: int = 0
+    scale_fp32: bool = False
 
     def c(self) -> _Cfg:
-        return _Cfg(self.n_ranks, self.budget, self.eps, int(self.correlated), self.seed, self.round)
+        return _Cfg(self.n_ranks, self.budget, self.eps, int(self.correlated), self.seed, self.round,
+                    int(self.fixed_bits), int(self.scale_fp32))
 
 
 def _addr(a: np.ndarray) -> int:
@@ -194,8 +214,8 @@ def chunk_cuts(b, perm, n_chunks: int) -> np.ndarray:
     return lo
 
 
-def message_bytes(n2: int, n4: int, n8: int) -> int:
-    return lib().or_message_bytes(n2, n4, n8)
+def message_bytes(n2: int, n4: int, n8: int, scale_fp32: bool = False) -> int:
+    return lib().or_message_bytes(n2, n4, n8, int(scale_fp32))
 
 
 def range_counts(lo: int, hi: int, N2: int, N4: int):
@@ -204,8 +224,8 @@ def range_counts(lo: int, hi: int, N2: int, N4: int):
     return ov(lo, hi, 0, N2), ov(lo, hi, N2, N2 + N4), ov(lo, hi, N2 + N4, 1 << 62)
 
 
-def range_message_bytes(lo, hi, N2, N4) -> int:
-    return message_bytes(*range_counts(lo, hi, N2, N4))
+def range_message_bytes(lo, hi, N2, N4, scale_fp32: bool = False) -> int:
+    return message_bytes(*range_counts(lo, hi, N2, N4), scale_fp32)
 
 
 def quantize_sg(x, bits: int, *, eps=1.0, seed=0, round=0, n_ranks=1, correlated=False,
@@ -221,6 +241,30 @@ def quantize_sg(x, bits: int, *, eps=1.0, seed=0, round=0, n_ranks=1, correlated
     lib().or_quantize_sg(_addr(x), bits, _addr(q), _addr(G), C.addressof(r), idx0,
                          _addr(E), _addr(u), _addr(codes))
     return int(E[0]), u, codes
+
+
+def quantize_sg_f32(x, bits: int, *, eps=1.0, seed=0, round=0, n_ranks=1, correlated=False,
+                    hop=0, rank=0, slot=0, n_slots=1, idx0=0):
+    """Quantization with fp32 group scales: returns (sigma[16] fp32, codes)."""
+    x = _c(x, np.float32)
+    assert x.size == SG
+    q = level_table(bits, eps)
+    G = gap_table(bits, q)
+    r = _Rng(seed, round, n_ranks, int(correlated), hop, rank, slot, n_slots)
+    sig = np.zeros(16, np.float32)
+    codes = np.zeros(SG * bits // 8, np.uint8)
+    lib().or_quantize_sg_f32(_addr(x), bits, _addr(q), _addr(G), C.addressof(r), idx0, _addr(sig), _addr(codes))
+    return sig, codes
+
+
+def decode_add_sg_f32(sig, codes, bits: int, add, *, eps=1.0) -> np.ndarray:
+    sig = _c(sig, np.float32)
+    codes = _c(codes, np.uint8)
+    add = _c(add, np.float32)
+    q = level_table(bits, eps)
+    out = np.zeros(SG, np.float32)
+    lib().or_decode_add_sg_f32(_addr(sig), _addr(codes), bits, _addr(q), _addr(add), _addr(out))
+    return out
 
 
 def dequantize_sg(E: int, u, codes, bits: int, *, eps=1.0) -> np.ndarray:
@@ -247,7 +291,7 @@ def compress(cfg: Config, lo, hi, N2, N4, rank, hop, g_u16, M, perm, slot=0, n_s
     g = _c(g_u16, np.uint16)
     M = _c(M, np.float32)
     perm = _c(perm, np.int32)
-    msg = np.zeros(range_message_bytes(lo, hi, N2, N4), np.uint8)
+    msg = np.zeros(range_message_bytes(lo, hi, N2, N4, cfg.scale_fp32), np.uint8)
     c = cfg.c()
     lib().or_compress(C.addressof(c), lo, hi, N2, N4, rank, hop, slot, n_slots, _addr(g), _addr(M),
                       _addr(perm), _addr(msg))
@@ -263,14 +307,14 @@ def dar(cfg: Config, in_lo, in_hi, N2, N4, rank, hop, msg_in, addend, M, perm,
     perm = _c(perm, np.int32)
     is32 = addend.dtype == np.float32
     addend = _c(addend, np.float32 if is32 else np.uint16)
-    msg_out = np.zeros(max(1, range_message_bytes(send[0], send[1], N2, N4)), np.uint8)
+    nb = range_message_bytes(send[0], send[1], N2, N4, cfg.scale_fp32)
+    msg_out = np.zeros(max(1, nb), np.uint8)
     keep_out = np.zeros(max(1, (keep[1] - keep[0]) * SG), np.float32)
     c = cfg.c()
     lib().or_dar(C.addressof(c), in_lo, in_hi, N2, N4, rank, hop, slot, n_slots, _addr(msg_in), _addr(addend),
                  int(is32), _addr(M), _addr(perm), send[0], send[1], _addr(msg_out),
                  keep[0], keep[1], _addr(keep_out))
-    return (msg_out[: range_message_bytes(send[0], send[1], N2, N4)],
-            keep_out[: (keep[1] - keep[0]) * SG])
+    return msg_out[:nb], keep_out[: (keep[1] - keep[0]) * SG]
 
 
 def decode(cfg: Config, lo, hi, N2, N4, msg, M, perm, out=None) -> np.ndarray:
@@ -287,8 +331,10 @@ def decode(cfg: Config, lo, hi, N2, N4, msg, M, perm, out=None) -> np.ndarray:
 # --------------------------------------------------------------------------- whole all-reduce
 def allreduce_sg(cfg: Config, butterfly: bool, grads, M, perm, N2, N4, chunk_lo, sel):
     """Per-super-group simulation of the all-reduce for reordered super-groups
-    ``sel``.  Returns (out[len(sel), 256] fp32, final[len(sel), 273] uint8 =
-    E byte, 16 u bytes, 256 code bytes (zero-padded))."""
+    ``sel``.  Returns (out[len(sel), 256] fp32, final[len(sel), 321] uint8):
+    65 metadata bytes (UINT8 scales: E byte, 16 u bytes, zeros; fp32 scales:
+    a zero byte, then the 16 fp32 scales), then 256 code bytes
+    (zero-padded)."""
     gs = [_c(g, np.uint16) for g in grads]
     assert len(gs) == cfg.n_ranks
     ptrs = (C.c_void_p * len(gs))(*[_addr(g) for g in gs])
@@ -297,7 +343,7 @@ def allreduce_sg(cfg: Config, butterfly: bool, grads, M, perm, N2, N4, chunk_lo,
     chunk_lo = _c(chunk_lo, np.int64)
     sel = _c(sel, np.int64)
     out = np.zeros((sel.size, SG), np.float32)
-    fin = np.zeros((sel.size, 1 + 16 + SG), np.uint8)
+    fin = np.zeros((sel.size, 65 + SG), np.uint8)
     c = cfg.c()
     rc = lib().or_allreduce_sg(C.addressof(c), int(butterfly), C.cast(ptrs, C.c_void_p), _addr(M),
                                _addr(perm), N2, N4, _addr(chunk_lo), _addr(sel), sel.size,
@@ -322,7 +368,16 @@ def plan(cfg: Config, grads) -> Plan:
     """Statistics, metadata all-reduce, allocation, reordering and chunking."""
     ms, qs = zip(*[stats(g) for g in grads])
     M, F = stats_reduce(np.stack(ms), np.stack(qs))
-    b, T, counts = allocate(F, cfg.budget)
+    if cfg.fixed_bits:
+        # uniform-bitwidth ablation: every super-group gets fixed_bits; no
+        # threshold applies (T is reported as NaN)
+        if cfg.fixed_bits not in (2, 4, 8):
+            raise ValueError("fixed_bits must be 2, 4 or 8")
+        b = np.full(F.size, cfg.fixed_bits, np.uint8)
+        T = np.float32(np.nan)
+        counts = np.array([F.size * (cfg.fixed_bits == k) for k in (2, 4, 8)], np.int64)
+    else:
+        b, T, counts = allocate(F, cfg.budget)
     perm = reorder(b)
     lo = chunk_cuts(b, perm, cfg.n_ranks)
     return Plan(M, F, b, float(T), counts, perm, lo)
@@ -362,3 +417,72 @@ def vnmse(out, grads) -> float:
     d = np.asarray(out, np.float64) - s
     den = float(np.dot(s, s))
     return float(np.dot(d, d)) / den if den > 0 else float(np.dot(d, d))
+
+
+# --------------------------------------------------------------------------- MXFP8 baseline
+MXB = 32
+
+
+def e4m3_value(code: int) -> float:
+    return lib().or_e4m3_value(int(code))
+
+
+def e4m3_encode(v: float) -> int:
+    return int(lib().or_e4m3_encode(float(v)))
+
+
+def mx_encode_block(v):
+    v = _c(v, np.float32)
+    assert v.size == MXB
+    X = np.zeros(1, np.uint8)
+    P = np.zeros(MXB, np.uint8)
+    lib().or_mx_encode_block(_addr(v), _addr(X), _addr(P))
+    return int(X[0]), P
+
+
+def mx_message_bytes(n_blk: int) -> int:
+    return lib().or_mx_message_bytes(n_blk)
+
+
+def mx_quantize(x) -> np.ndarray:
+    x = _c(x, np.float32)
+    assert x.size % MXB == 0
+    msg = np.zeros(mx_message_bytes(x.size // MXB), np.uint8)
+    lib().or_mx_quantize(_addr(x), x.size // MXB, _addr(msg))
+    return msg
+
+
+def mx_dequantize(msg, n_blk: int) -> np.ndarray:
+    msg = _c(msg, np.uint8)
+    out = np.zeros(n_blk * MXB, np.float32)
+    lib().or_mx_dequantize(_addr(msg), n_blk, _addr(out))
+    return out
+
+
+def mx_chunk_lo(n_blk: int, n_ranks: int) -> list:
+    """Equal runs of blocks: chunk c = [floor(c B / N), floor((c+1) B / N))."""
+    return [c * n_blk // n_ranks for c in range(n_ranks + 1)]
+
+
+def mx_allreduce_blk(n_ranks: int, butterfly: bool, grads, sel):
+    """MXFP8 all-reduce of blocks ``sel`` (32 coords each).  Returns
+    (out[len(sel), 32] fp32, final[len(sel), 33] = scale byte + 32 codes)."""
+    gs = [_c(g, np.uint16) for g in grads]
+    assert len(gs) == n_ranks
+    n_blk = gs[0].size // MXB
+    ptrs = (C.c_void_p * len(gs))(*[_addr(g) for g in gs])
+    sel = _c(sel, np.int64)
+    out = np.zeros((sel.size, MXB), np.float32)
+    fin = np.zeros((sel.size, 33), np.uint8)
+    rc = lib().or_mx_allreduce_blk(n_ranks, int(butterfly), C.cast(ptrs, C.c_void_p), n_blk, _addr(sel),
+                                   sel.size, _addr(out), _addr(fin))
+    if rc:
+        raise ValueError("butterfly needs a power-of-two number of ranks (or a block index is out of range)")
+    return out, fin
+
+
+def mx_allreduce(n_ranks: int, grads, butterfly: bool = False) -> np.ndarray:
+    """The whole MXFP8 all-reduce: fp32 sum in original order."""
+    n_blk = np.asarray(grads[0]).size // MXB
+    out, _ = mx_allreduce_blk(n_ranks, butterfly, grads, np.arange(n_blk, dtype=np.int64))
+    return out.reshape(-1)

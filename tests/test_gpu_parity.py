@@ -226,7 +226,7 @@ def _check_allreduce(name, n, N, butterfly, correlated, B=5.0, seed=0):
                 blk = m[offs[1] + 128 * (s - n2): offs[1] + 128 * (s - n2) + 128]
             else:
                 blk = m[offs[2] + 256 * (s - n2 - n4): offs[2] + 256 * (s - n2 - n4) + 256]
-            assert np.array_equal(blk, f[17:17 + blk.size])
+            assert np.array_equal(blk, f[65:65 + blk.size])
     v_gpu = oracle.vnmse(o0, gr)
     v_orc = oracle.vnmse(exp, gr)
     assert v_gpu == pytest.approx(v_orc, rel=0.01)
