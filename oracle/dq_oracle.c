@@ -925,6 +925,13 @@ void or_mx_encode_block(const float *v, uint8_t *X_out, uint8_t *P)
     for (int i = 0; i < OR_MXB; ++i) P[i] = or_e4m3_encode(ldexp((double)v[i], -x));
 }
 
+/* Decode one block: out_i = P_i * X (exact in fp32; a negative zero stays
+ * negative). */
+void or_mx_decode_block(uint8_t X, const uint8_t *P, float *out)
+{
+    for (int i = 0; i < OR_MXB; ++i) out[i] = (float)ldexp(or_e4m3_value(P[i]), (int)X - 127);
+}
+
 /* Decode one block and add: out_i = fl(P_i * X + add_i) (the product is exact). */
 void or_mx_decode_add_block(uint8_t X, const uint8_t *P, const float *add, float *out)
 {
@@ -950,9 +957,7 @@ void or_mx_quantize(const float *x, int64_t n_blk, uint8_t *msg)
 void or_mx_dequantize(const uint8_t *msg, int64_t n_blk, float *out)
 {
     const uint8_t *P = msg + ((n_blk + 15) / 16) * 16;
-    float zero[OR_MXB];
-    memset(zero, 0, sizeof(zero));
-    for (int64_t k = 0; k < n_blk; ++k) or_mx_decode_add_block(msg[k], P + OR_MXB * k, zero, out + OR_MXB * k);
+    for (int64_t k = 0; k < n_blk; ++k) or_mx_decode_block(msg[k], P + OR_MXB * k, out + OR_MXB * k);
 }
 
 /* The MXFP8 all-reduce followed one block at a time (blocks are            */
@@ -1007,9 +1012,7 @@ int or_mx_allreduce_blk(int32_t n_ranks, int32_t butterfly, const uint16_t *cons
             free(part);
             free(holder);
         }
-        float zero[OR_MXB];
-        memset(zero, 0, sizeof(zero));
-        or_mx_decode_add_block(X, P, zero, &out[k * OR_MXB]);
+        or_mx_decode_block(X, P, &out[k * OR_MXB]);
         if (final_blk) {
             final_blk[k * 33] = X;
             memcpy(&final_blk[k * 33 + 1], P, OR_MXB);

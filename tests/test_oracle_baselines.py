@@ -98,6 +98,10 @@ def test_mx_block_zero_and_saturation():
     v[0], v[1] = 500.0, 300.0                     # amax 500 -> X = 2^0, 500 saturates to 448
     X, P = oracle.mx_encode_block(v)
     assert X == 127 and P[0] == 0x7E and oracle.e4m3_value(P[1]) == 288.0
+    # decoding is element x scale: a negative zero stays negative
+    msg = oracle.mx_quantize(np.concatenate([[-0.0, 0.0, -1e-30], np.ones(29)]).astype(np.float32))
+    d = oracle.mx_dequantize(msg, 1)
+    assert list(np.signbit(d[:3])) == [True, False, True] and np.all(d[:3] == 0)
 
 
 def test_mx_roundtrip_exact_on_representable_blocks():
