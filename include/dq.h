@@ -54,7 +54,11 @@ typedef enum {
     DQ_ERR_CUDA = 4                /* a CUDA call or kernel launch failed        */
 } dq_status;
 
-/* Parameters of one all-reduce round. */
+/* Parameters of one all-reduce round.  The last two fields, with eps and
+ * correlated, switch off one technique each for ablation [S "Key idea and
+ * contribution": variable bitwidth, non-uniform levels, hierarchical scale
+ * quantization, correlated rounding; P Referee Report minor comment 1:
+ * variable vs uniform bitwidth]; zero is the method as published. */
 typedef struct {
     int32_t  n_ranks;      /* N, 1 .. 65535 (butterfly: a power of two)              */
     float    budget_bits;  /* B, average code bits per coordinate, >= 2             */
@@ -63,6 +67,12 @@ typedef struct {
     int32_t  correlated;   /* 1: correlated rounding across ranks, 0: independent  */
     uint64_t seed;         /* key of the counter-based generator                    */
     uint64_t round;        /* training round (part of the generator counter)        */
+    int32_t  fixed_bits;   /* 0: variable allocation; 2, 4 or 8: every super-group
+                              gets that width (dq_plan skips the allocation; the
+                              budget is not used)                                   */
+    int32_t  scale_fp32;   /* 0: UINT8 group scales (E byte + u per group);
+                              1: group scales sent as fp32, sigma = max |x|,
+                              y = x / sigma (no second-level quantization)          */
 } dq_config;
 
 /* Who quantizes, for the stochastic-rounding generator.  Independent
@@ -100,10 +110,12 @@ const char *dq_status_string(dq_status s);
  * c = hi - lo SGs of which n2, n4, n8 have 2, 4, 8 bits:
  *   [E: c exponent bytes, padded to a multiple of 16][u: 16 bytes per SG]
  *   [2-bit codes, 64 B per SG][4-bit codes, 128 B per SG][8-bit, 256 B per SG]
- * Coordinate i of an SG occupies bits [b*i, b*i+b) of the SG's code block,
- * least significant bits first.  [S "Key idea and contribution": groups and
- * super-groups; P Referee Report summary: hierarchical UINT8 group scaling] */
-size_t dq_message_bytes(dq_range r);
+ * With scale_fp32 = 1 the E and u sections are replaced by 16 fp32 scales
+ * (64 B) per SG.  Coordinate i of an SG occupies bits [b*i, b*i+b) of the
+ * SG's code block, least significant bits first.  [S "Key idea and
+ * contribution": groups and super-groups; P Referee Report summary:
+ * hierarchical UINT8 group scaling]  Returns 0 for an invalid range. */
+size_t dq_message_bytes(dq_range r, int32_t scale_fp32);
 
 /* Level table of the library for b in {2, 4, 8} (host, pure): writes 2^b
  * fp32 levels to q_host.  [P ledger: Q = {f(eps, r)}; S "Key idea and
@@ -242,7 +254,8 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads_host, int64_t n
  * count: in, first free slot; out, slots used.  Launches beyond capacity
  * are not recorded (they still run). */
 enum { DQ_LAUNCH_COMPRESS = 0, DQ_LAUNCH_DAR = 1, DQ_LAUNCH_DECODE = 2, DQ_LAUNCH_STATS = 3,
-       DQ_LAUNCH_ALLOCATE_REORDER = 4 /* statistics reduce, allocation and reorder, one bracket */ };
+       DQ_LAUNCH_ALLOCATE_REORDER = 4, /* statistics reduce, allocation and reorder, one bracket */
+       DQ_LAUNCH_MX_HOP = 5, DQ_LAUNCH_MX_DECODE = 6 /* MXFP8 baseline; sgs = coordinates / 256 */ };
 struct dq_launch_log {
     void   **events;
     int32_t *kinds;
@@ -273,6 +286,43 @@ dq_status dq_exchange(const dq_config *cfg, int32_t butterfly, const void *const
                       const dq_plan_info *info, void *ws, size_t ws_bytes,
                       void *const *outs_host, int32_t out_is_bf16,
                       const uint8_t **final_msgs_host, dq_launch_log *log, void *stream);
+
+/* ---- comparison baseline: MXFP8 ------------------------------------------
+ * The pages compare DynamiQ's error with MXFP8's [A Abstract; S
+ * "Evaluation"], citing the OCP Microscaling (MX) v1.0 specification.  This
+ * is that baseline, run over the same N-rank schedules on the GPU: blocks of
+ * 32 coordinates (n_blk blocks = n_blk * 32 coordinates, in original order)
+ * share one E8M0 scale byte X (2^(X-127)); elements are FP8 E4M3.  Encode:
+ * X - 127 = floor(log2 max|v|) - 8, clamped at -127 (X = 0 for an all-zero
+ * block); element = v * 2^(127-X) rounded to nearest-even, saturating at
+ * +-448.  A hop decodes, adds in fp32 (x = fl(dec + addend)) and re-encodes;
+ * there is no mean, allocation or reordering.  Chunk c of N is blocks
+ * [floor(c n_blk / N), floor((c+1) n_blk / N)).
+ * Message of c blocks: [X: c bytes, padded to a multiple of 16]
+ *                      [elements: 32 bytes per block]. */
+
+/* Bytes of the MXFP8 message of n_blk blocks (host, pure; 0 if invalid). */
+size_t dq_mx_message_bytes(int64_t n_blk);
+
+/* Encode n_blk blocks of fp32 x (device, 32 * n_blk floats) into msg
+ * (device, dq_mx_message_bytes(n_blk)). */
+dq_status dq_mx_quantize(const float *x, int64_t n_blk, uint8_t *msg, void *stream);
+
+/* Decode msg into out (device, 32 * n_blk floats). */
+dq_status dq_mx_dequantize(const uint8_t *msg, int64_t n_blk, float *out, void *stream);
+
+/* Device bytes dq_mx_exchange needs (0 for invalid arguments). */
+size_t dq_mx_exchange_workspace_bytes(int32_t n_ranks, int32_t butterfly, int64_t n_blk);
+
+/* The MXFP8 all-reduce of N simulated ranks: grads_host[r] is rank r's bf16
+ * gradient (device, 32 * n_blk values), outs_host[r] its fp32 output (the
+ * sum, identical on every rank).  Ring (butterfly = 0) or butterfly (N a
+ * power of two) with the same hop schedule as dq_exchange.  ws: device
+ * scratch of dq_mx_exchange_workspace_bytes bytes.  final_msgs_host, if not
+ * NULL, receives the N device pointers of the final chunk messages. */
+dq_status dq_mx_exchange(int32_t n_ranks, int32_t butterfly, const void *const *grads_host, int64_t n_blk,
+                         void *ws, size_t ws_bytes, void *const *outs_host, const uint8_t **final_msgs_host,
+                         dq_launch_log *log, void *stream);
 
 #ifdef __cplusplus
 }

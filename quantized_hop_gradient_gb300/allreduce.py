@@ -17,10 +17,15 @@ SG = dq.SG
 class DynamiQAllReduce:
     def __init__(self, n_ranks: int, n_sg: int, *, budget: float = 5.0, eps: float = 1.0,
                  correlated: bool = True, butterfly: bool = False, seed: int = 0,
-                 out_dtype: torch.dtype = torch.float32, device="cuda"):
+                 out_dtype: torch.dtype = torch.float32, device="cuda", fixed_bits: int = 0,
+                 scale_fp32: bool = False):
+        """``fixed_bits`` (2/4/8) and ``scale_fp32`` are ablation switches:
+        uniform bitwidth instead of the allocation, fp32 group scales instead
+        of the UINT8 second level."""
         self.n_ranks, self.n_sg = n_ranks, n_sg
         self.budget, self.eps, self.correlated, self.butterfly = budget, eps, correlated, butterfly
         self.seed = seed
+        self.fixed_bits, self.scale_fp32 = fixed_bits, scale_fp32
         self.out_dtype = out_dtype
         self.device = torch.device(device)
         dq.lib()
@@ -33,7 +38,8 @@ class DynamiQAllReduce:
         self.final = None
 
     def config(self, round: int = 0):
-        return dq.config(self.n_ranks, self.budget, self.eps, self.correlated, self.seed, round)
+        return dq.config(self.n_ranks, self.budget, self.eps, self.correlated, self.seed, round,
+                         self.fixed_bits, self.scale_fp32)
 
     def plan(self, grads, round: int = 0, stream=None, log=None, ready=None, n_sg=None):
         """Statistics, allocation and reordering.  ``ready``: optional
@@ -84,6 +90,46 @@ class DynamiQAllReduce:
         lo = self.chunk_lo()
         i = self.info
         r = dq.rng(lo[c], lo[c + 1], i.n2, i.n2 + i.n4)
-        nb = dq.dq_message_bytes(r)
+        nb = dq.dq_message_bytes(r, self.scale_fp32)
+        off = self.final[c] - self.ws.data_ptr()
+        return self.ws[off:off + nb].cpu()
+
+
+class MXFP8AllReduce:
+    """The MXFP8 comparison baseline over the same N-rank schedules: every
+    hop decodes, adds in fp32 and re-encodes 32-element E4M3 blocks with an
+    E8M0 scale (OCP MX v1.0).  Outputs are fp32 sums."""
+
+    def __init__(self, n_ranks: int, n_coords: int, *, butterfly: bool = False, device="cuda"):
+        if n_coords % dq.MX_BLOCK:
+            raise ValueError("the coordinate count must be a multiple of 32")
+        self.n_ranks, self.n_blk, self.butterfly = n_ranks, n_coords // dq.MX_BLOCK, butterfly
+        self.device = torch.device(device)
+        dq.lib()
+        nb = dq.dq_mx_exchange_workspace_bytes(n_ranks, butterfly, self.n_blk)
+        if nb == 0:
+            raise dq.DQError(dq.DQ_ERR_INVALID_ARG, "dq_mx_exchange_workspace_bytes")
+        self.ws = torch.empty(nb, dtype=torch.uint8, device=self.device)
+        self.final = None
+
+    def chunk_lo(self):
+        return [c * self.n_blk // self.n_ranks for c in range(self.n_ranks + 1)]
+
+    def new_outputs(self):
+        return [torch.empty(self.n_blk * dq.MX_BLOCK, dtype=torch.float32, device=self.device)
+                for _ in range(self.n_ranks)]
+
+    def __call__(self, grads, outs=None, stream=None, log=None):
+        if len(grads) != self.n_ranks:
+            raise ValueError("one gradient per rank")
+        if outs is None:
+            outs = self.new_outputs()
+        self.final = dq.dq_mx_exchange(self.n_ranks, self.butterfly, grads, self.n_blk, self.ws,
+                                       self.ws.numel(), outs, log, stream)
+        return outs
+
+    def final_message(self, c: int) -> torch.Tensor:
+        lo = self.chunk_lo()
+        nb = dq.dq_mx_message_bytes(lo[c + 1] - lo[c])
         off = self.final[c] - self.ws.data_ptr()
         return self.ws[off:off + nb].cpu()

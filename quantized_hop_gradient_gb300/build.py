@@ -15,8 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libdq.so")
-SOURCES = ["dq_api.cu", "dq_codec.cu", "dq_hop.cu", "dq_plan.cu", "dq_static.cu"]
-HEADERS = ["dq_common.cuh", "dq_internal.h"]
+SOURCES = ["dq_api.cu", "dq_codec.cu", "dq_hop.cu", "dq_mx.cu", "dq_plan.cu", "dq_static.cu"]
+HEADERS = ["dq_common.cuh", "dq_internal.h", "dq_sched.h"]
 INCLUDE = os.path.join(os.path.dirname(HERE), "include", "dq.h")
 
 

@@ -12,6 +12,7 @@
 
 #include "dq_common.cuh"
 #include "dq_internal.h"
+#include "dq_sched.h"
 
 namespace dq {
 
@@ -128,20 +129,21 @@ static int64_t overlap(int64_t a, int64_t b, int64_t c, int64_t d)
     return hi > lo ? hi - lo : 0;
 }
 
-size_t msg_bytes(int64_t c, int64_t n2, int64_t n4, int64_t n8)
+size_t msg_bytes(int64_t c, int64_t n2, int64_t n4, int64_t n8, bool scale_fp32)
 {
-    return (size_t)((c + 15) / 16 * 16 + 16 * c + 64 * n2 + 128 * n4 + 256 * n8);
+    const int64_t meta = scale_fp32 ? 64 * c : (c + 15) / 16 * 16 + 16 * c;
+    return (size_t)(meta + 64 * n2 + 128 * n4 + 256 * n8);
 }
 
-MsgView msg_view(uint8_t *base, int64_t lo, int64_t hi, int64_t end2, int64_t end4)
+MsgView msg_view(uint8_t *base, int64_t lo, int64_t hi, int64_t end2, int64_t end4, bool scale_fp32)
 {
     MsgView m;
     m.base = base;
     m.c = hi - lo;
     m.n2 = overlap(lo, hi, 0, end2);
     m.n4 = overlap(lo, hi, end2, end4);
-    m.off_u = (m.c + 15) / 16 * 16;
-    m.off_c2 = m.off_u + 16 * m.c;
+    m.off_u = scale_fp32 ? 0 : (m.c + 15) / 16 * 16;
+    m.off_c2 = m.off_u + (scale_fp32 ? 64 : 16) * m.c;
     m.off_c4 = m.off_c2 + 64 * m.n2;
     m.off_c8 = m.off_c4 + 128 * m.n4;
     return m;
@@ -183,7 +185,9 @@ bool range_ok(const dq_range &r)
 
 bool cfg_ok(const dq_config *c)
 {
-    return c && c->n_ranks >= 1 && c->n_ranks <= 65535 && (c->eps > 0.0);
+    return c && c->n_ranks >= 1 && c->n_ranks <= 65535 && (c->eps > 0.0) &&
+           (c->fixed_bits == 0 || c->fixed_bits == 2 || c->fixed_bits == 4 || c->fixed_bits == 8) &&
+           (c->scale_fp32 == 0 || c->scale_fp32 == 1);
 }
 
 bool stage_ok(const dq_config *cfg, const dq_stage &s)
@@ -222,6 +226,7 @@ void fill_common(HopParams &P, const dq_config *cfg, const float *mu, const int3
     P.key1 = (uint32_t)(cfg->seed >> 32);
     P.round0 = (uint32_t)cfg->round;
     P.round1 = (uint32_t)(cfg->round >> 32);
+    P.scale_fp32 = cfg->scale_fp32;
 }
 
 // A hop task with its input range [in_lo, in_hi).
@@ -230,11 +235,9 @@ struct PendingHop {
     int64_t in_hi;
 };
 
-// Brackets one launch with the caller's events (if a log has room).
-struct LogSlot {
-    dq_launch_log *log;
-    int32_t i;
-};
+}  // namespace
+
+namespace dq {
 
 LogSlot log_begin(dq_launch_log *log, int32_t kind, int64_t sgs, cudaStream_t st)
 {
@@ -250,6 +253,10 @@ void log_end(const LogSlot &s, cudaStream_t st)
 {
     if (s.log) cudaEventRecord(static_cast<cudaEvent_t>(s.log->events[2 * s.i + 1]), st);
 }
+
+}  // namespace dq
+
+namespace {
 
 // Launches hop tasks in batches of at most kMaxTasks (empty tasks dropped).
 cudaError_t run_hops(HopParams &P, const std::vector<PendingHop> &tasks, int64_t end2, int64_t end4, bool has_in,
@@ -298,7 +305,7 @@ cudaError_t run_decodes(DecodeParams &D, const std::vector<PendingDecode> &chunk
             if (c.hi <= c.lo) continue;
             DecodeTask &t = D.task[n++];
             memset(&t, 0, sizeof(t));
-            t.msg = msg_view(const_cast<uint8_t *>(c.msg), c.lo, c.hi, end2, end4);
+            t.msg = msg_view(const_cast<uint8_t *>(c.msg), c.lo, c.hi, end2, end4, D.scale_fp32 != 0);
             t.out = c.out;
             t.lo = c.lo;
             units += set_units(t, c.lo, c.hi, end2, end4, units);
@@ -326,6 +333,7 @@ std::unique_ptr<DecodeParams> decode_params(const dq_config *cfg, const float *m
     D->mu = mu;
     D->perm = perm;
     D->out_is_bf16 = out_is_bf16 ? 1 : 0;
+    D->scale_fp32 = cfg->scale_fp32;
     return D;
 }
 
@@ -350,11 +358,11 @@ const char *dq_status_string(dq_status s)
     return "unknown status";
 }
 
-size_t dq_message_bytes(dq_range r)
+size_t dq_message_bytes(dq_range r, int32_t scale_fp32)
 {
-    if (!range_ok(r)) return 0;
-    const MsgView m = msg_view(nullptr, r.lo, r.hi, r.end2, r.end4);
-    return msg_bytes(m.c, m.n2, m.n4, m.c - m.n2 - m.n4);
+    if (!range_ok(r) || (scale_fp32 != 0 && scale_fp32 != 1)) return 0;
+    const MsgView m = msg_view(nullptr, r.lo, r.hi, r.end2, r.end4, scale_fp32 != 0);
+    return msg_bytes(m.c, m.n2, m.n4, m.c - m.n2 - m.n4, scale_fp32 != 0);
 }
 
 dq_status dq_level_table(int32_t bits, double eps, float *q_host)
@@ -443,7 +451,7 @@ dq_status dq_compress(const dq_config *cfg, dq_range r, dq_stage stage, const vo
     fill_common(*P, cfg, mu, perm);
     PendingHop h;
     h.t = make_task(cfg, stage);
-    h.t.out = msg_view(msg_out, r.lo, r.hi, r.end2, r.end4);
+    h.t.out = msg_view(msg_out, r.lo, r.hi, r.end2, r.end4, cfg->scale_fp32 != 0);
     h.t.addend = g_bf16;
     h.t.in_lo = r.lo;
     h.t.send_lo = r.lo;
@@ -478,8 +486,8 @@ dq_status dq_dar(const dq_config *cfg, dq_range in, dq_stage stage, const uint8_
     fill_common(*P, cfg, mu, perm);
     PendingHop h;
     h.t = make_task(cfg, stage);
-    h.t.in = msg_view(const_cast<uint8_t *>(msg_in), in.lo, in.hi, in.end2, in.end4);
-    h.t.out = msg_view(msg_out, send.lo, send.hi, send.end2, send.end4);
+    h.t.in = msg_view(const_cast<uint8_t *>(msg_in), in.lo, in.hi, in.end2, in.end4, cfg->scale_fp32 != 0);
+    h.t.out = msg_view(msg_out, send.lo, send.hi, send.end2, send.end4, cfg->scale_fp32 != 0);
     h.t.addend = addend;
     h.t.keep_out = keep_out;
     h.t.in_lo = in.lo;
@@ -533,32 +541,12 @@ PlanLayout plan_layout(int32_t n, int64_t J)
     return L;
 }
 
-// Chunk sets of the butterfly: at step s rank r holds chunks
-// [base, base + 2^(L-s)), base = (r >> (L-s)) << (L-s); it keeps the half
-// whose bit (L-1-s) equals its own and sends the other half.
-struct ChunkSpan { int32_t a, b; };
-
-ChunkSpan bfly_half(int32_t L, int32_t s, int32_t r, bool keep)
-{
-    const int32_t width = 1 << (L - s), half = width >> 1, base = (r >> (L - s)) << (L - s);
-    const int32_t my = (r >> (L - 1 - s)) & 1;
-    const int32_t h = keep ? my : 1 - my;
-    return {base + h * half, base + h * half + half};
-}
-
-int32_t log2_exact(int32_t n)
-{
-    int32_t L = 0;
-    while ((1 << L) < n) ++L;
-    return (1 << L) == n ? L : -1;
-}
-
 struct ExchangeLayout {
     std::vector<int64_t> lo;    // chunk cuts
     size_t msg_stride = 0;      // bytes per message buffer
     size_t keep_stride = 0;     // bytes per fp32 keep buffer
     size_t msgs = 0, keeps = 0, finals = 0, total = 0;
-    int32_t L = 0;
+    Schedule S;
 };
 
 bool exchange_layout(const dq_config *cfg, int32_t butterfly, const dq_plan_info *info, ExchangeLayout &X)
@@ -566,23 +554,17 @@ bool exchange_layout(const dq_config *cfg, int32_t butterfly, const dq_plan_info
     const int32_t N = cfg->n_ranks;
     X.lo.assign((size_t)N + 1, 0);
     if (dq_chunk_cuts(info->n2, info->n4, info->n8, N, X.lo.data()) != DQ_OK) return false;
+    if (!build_schedule(N, butterfly != 0, X.S)) return false;
     const int64_t end2 = info->n2, end4 = info->n2 + info->n4;
-    auto bytes = [&](int64_t a, int64_t b) {
-        const MsgView m = msg_view(nullptr, a, b, end2, end4);
-        return msg_bytes(m.c, m.n2, m.n4, m.c - m.n2 - m.n4);
-    };
+    const bool sf = cfg->scale_fp32 != 0;
     size_t mmax = 16, kmax = 16;
-    for (int32_t c = 0; c < N; ++c) mmax = std::max(mmax, bytes(X.lo[c], X.lo[c + 1]));
-    if (butterfly) {
-        X.L = log2_exact(N);
-        if (X.L < 0) return false;
-        for (int32_t s = 0; s < X.L; ++s)
-            for (int32_t r = 0; r < N; ++r) {
-                const ChunkSpan S = bfly_half(X.L, s, r, false), K = bfly_half(X.L, s, r, true);
-                mmax = std::max(mmax, bytes(X.lo[S.a], X.lo[S.b]));
-                kmax = std::max(kmax, (size_t)(X.lo[K.b] - X.lo[K.a]) * kSG * sizeof(float));
-            }
-    }
+    for (const SchedStep &st : X.S.steps)
+        for (const SchedHop &h : st.hops) {
+            const int64_t a = X.lo[h.send.a], b = X.lo[h.send.b];
+            const MsgView m = msg_view(nullptr, a, b, end2, end4, sf);
+            mmax = std::max(mmax, msg_bytes(m.c, m.n2, m.n4, m.c - m.n2 - m.n4, sf));
+            kmax = std::max(kmax, (size_t)(X.lo[h.keep.b] - X.lo[h.keep.a]) * kSG * sizeof(float));
+        }
     X.msg_stride = round256(mmax);
     X.keep_stride = butterfly ? round256(kmax) : 0;
     size_t o = 0;
@@ -612,7 +594,7 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
     const PlanLayout L = plan_layout(N, n_sg);
     if (ws_bytes < L.total) return DQ_ERR_INVALID_ARG;
     if (!aligned16(ws)) return DQ_ERR_ALIGNMENT;
-    if (!(cfg->budget_bits >= 2.0f)) return DQ_ERR_BUDGET_INFEASIBLE;
+    if (!cfg->fixed_bits && !(cfg->budget_bits >= 2.0f)) return DQ_ERR_BUDGET_INFEASIBLE;
     for (int32_t r = 0; r < N; ++r) {
         if (!grads[r]) return DQ_ERR_INVALID_ARG;
         if (!aligned16(grads[r])) return DQ_ERR_ALIGNMENT;
@@ -654,6 +636,20 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
     }
     const LogSlot slot = log_begin(log, DQ_LAUNCH_ALLOCATE_REORDER, n_sg, st);
     if (launch_stats_reduce(mean_all, sq_all, N, n_sg, M, F, mu, st) != cudaSuccess) return DQ_ERR_CUDA;
+    if (cfg->fixed_bits) {
+        // uniform-bitwidth ablation: every super-group gets fixed_bits (the
+        // reorder of a uniform allocation is the identity permutation)
+        if (cudaMemsetAsync(b, cfg->fixed_bits, (size_t)n_sg, st) != cudaSuccess) return DQ_ERR_CUDA;
+        const dq_status s = dq_reorder(b, n_sg, perm, scratch, plan_scratch_bytes(n_sg), stream);
+        if (s != DQ_OK) return s;
+        log_end(slot, st);
+        if (cudaStreamSynchronize(st) != cudaSuccess) return DQ_ERR_CUDA;
+        info->T = NAN;
+        info->n2 = cfg->fixed_bits == 2 ? n_sg : 0;
+        info->n4 = cfg->fixed_bits == 4 ? n_sg : 0;
+        info->n8 = cfg->fixed_bits == 8 ? n_sg : 0;
+        return DQ_OK;
+    }
     dq_status s = dq_allocate(F, n_sg, cfg->budget_bits, b, T, counts, scratch, plan_scratch_bytes(n_sg), stream);
     if (s != DQ_OK) return s;
     s = dq_reorder(b, n_sg, perm, scratch, plan_scratch_bytes(n_sg), stream);
@@ -698,12 +694,14 @@ dq_status dq_exchange(const dq_config *cfg, int32_t butterfly, const void *const
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t end2 = info->n2, end4 = info->n2 + info->n4;
+    const bool sf = cfg->scale_fp32 != 0;
     uint8_t *w = static_cast<uint8_t *>(ws);
-    auto msg = [&](int32_t r, int32_t par) { return w + X.msgs + (size_t)(2 * r + par) * X.msg_stride; };
+    auto msg = [&](int32_t r, int32_t par) {
+        return par < 0 ? w + X.finals + (size_t)r * X.msg_stride : w + X.msgs + (size_t)(2 * r + par) * X.msg_stride;
+    };
     auto keepb = [&](int32_t r, int32_t par) {
         return reinterpret_cast<float *>(w + X.keeps + (size_t)(2 * r + par) * X.keep_stride);
     };
-    auto finb = [&](int32_t r) { return w + X.finals + (size_t)r * X.msg_stride; };
     const std::vector<int64_t> &lo = X.lo;
 
     std::unique_ptr<HopParams> P(new HopParams());
@@ -711,89 +709,34 @@ dq_status dq_exchange(const dq_config *cfg, int32_t butterfly, const void *const
     if (!build_tables(cfg->eps, &P->tab)) return DQ_ERR_INVALID_ARG;
     fill_common(*P, cfg, mu, perm);
 
-    // A task over SG range [a, b): send [sa, sb) to `out`, keep [ka, kb) to `keep`.
-    auto task = [&](dq_stage stage, const uint8_t *in, int64_t a, int64_t b, const void *addend, uint8_t *out,
-                    int64_t sa, int64_t sb, float *keep, int64_t ka, int64_t kb) {
-        PendingHop h;
-        h.t = make_task(cfg, stage);
-        h.t.in = msg_view(const_cast<uint8_t *>(in), a, b, end2, end4);
-        h.t.out = msg_view(out, sa, sb, end2, end4);
-        h.t.addend = addend;
-        h.t.keep_out = keep;
-        h.t.in_lo = a;
-        h.t.send_lo = sb > sa ? sa : b;
-        h.t.send_hi = sb > sa ? sb : b;
-        h.t.keep_lo = kb > ka ? ka : b;
-        h.t.keep_hi = kb > ka ? kb : b;
-        h.in_hi = b;
-        return h;
-    };
-
-    std::vector<const uint8_t *> fin((size_t)N, nullptr);
     std::vector<PendingHop> tasks;
-    cudaError_t e = cudaSuccess;
-    if (!butterfly) {
-        // Ring reduce-scatter: at step t rank r handles chunk (r - 1 - t) mod N;
-        // step 0 compresses it, later steps decode the message of rank r - 1,
-        // add the local gradient and recompress (stage t, quantizing rank r).
-        for (int32_t t = 0; t < N && e == cudaSuccess; ++t) {
-            tasks.clear();
-            for (int32_t r = 0; r < N; ++r) {
-                const int32_t c = (int32_t)((((int64_t)r - 1 - t) % N + N) % N);
-                const int32_t src = (r - 1 + N) % N;
-                tasks.push_back(task(dq_stage{r, t, 0, 1}, t ? msg(src, (t - 1) & 1) : nullptr, lo[c], lo[c + 1],
-                                     grads[r], msg(r, t & 1), lo[c], lo[c + 1], nullptr, 0, 0));
-            }
-            e = run_hops(*P, tasks, end2, end4, t > 0, false, st, log);
+    for (const SchedStep &step : X.S.steps) {
+        tasks.clear();
+        for (const SchedHop &h : step.hops) {
+            const int64_t a = lo[h.in.a], b = lo[h.in.b];
+            const int64_t sa = lo[h.send.a], sb = lo[h.send.b], ka = lo[h.keep.a], kb = lo[h.keep.b];
+            PendingHop ph;
+            ph.t = make_task(cfg, dq_stage{h.rank, h.stage, h.slot, h.n_slots});
+            ph.t.in = msg_view(h.in_rank < 0 ? nullptr : msg(h.in_rank, h.in_par), a, b, end2, end4, sf);
+            ph.t.out = msg_view(msg(h.rank, h.out_par), sa, sb, end2, end4, sf);
+            ph.t.addend = h.add_par < 0 ? grads[h.rank] : (const void *)keepb(h.rank, h.add_par);
+            ph.t.keep_out = kb > ka ? keepb(h.rank, h.keep_par) : nullptr;
+            ph.t.in_lo = a;
+            ph.t.send_lo = sb > sa ? sa : b;
+            ph.t.send_hi = sb > sa ? sb : b;
+            ph.t.keep_lo = kb > ka ? ka : b;
+            ph.t.keep_hi = kb > ka ? kb : b;
+            ph.in_hi = b;
+            tasks.push_back(ph);
         }
-        for (int32_t c = 0; c < N; ++c) fin[c] = msg(c, (N - 1) & 1);  // owner c, step N-1
-    } else {
-        const int32_t L = X.L;
-        if (L == 0) {
-            tasks.push_back(task(dq_stage{0, 0, 0, 1}, nullptr, lo[0], lo[1], grads[0], finb(0), lo[0], lo[1],
-                                 nullptr, 0, 0));
-            e = run_hops(*P, tasks, end2, end4, false, false, st, log);
-        } else {
-            // step 0: compress the half that is sent
-            for (int32_t r = 0; r < N; ++r) {
-                const ChunkSpan S = bfly_half(L, 0, r, false);
-                const int32_t ns = 1 << (L - 1);
-                tasks.push_back(task(dq_stage{r, 0, r & (ns - 1), ns}, nullptr, lo[S.a], lo[S.b], grads[r], msg(r, 0),
-                                     lo[S.a], lo[S.b], nullptr, 0, 0));
-            }
-            e = run_hops(*P, tasks, end2, end4, false, false, st, log);
-            // steps 1 .. L-1: decode the partner's half, add, send one half, keep the other
-            for (int32_t s = 1; s < L && e == cudaSuccess; ++s) {
-                tasks.clear();
-                for (int32_t r = 0; r < N; ++r) {
-                    const ChunkSpan K0 = bfly_half(L, s - 1, r, true), S = bfly_half(L, s, r, false),
-                                    K = bfly_half(L, s, r, true);
-                    const int32_t p = r ^ (N >> s);
-                    const void *add = s == 1 ? grads[r] : (const void *)keepb(r, (s - 1) & 1);
-                    const int32_t ns = 1 << (L - 1 - s);
-                    tasks.push_back(task(dq_stage{r, s, r & (ns - 1), ns}, msg(p, (s - 1) & 1), lo[K0.a], lo[K0.b],
-                                         add, msg(r, s & 1), lo[S.a], lo[S.b], keepb(r, s & 1), lo[K.a], lo[K.b]));
-                }
-                e = run_hops(*P, tasks, end2, end4, true, s >= 2, st, log);
-            }
-            // the owner adds the last half it receives and compresses its chunk once
-            if (e == cudaSuccess) {
-                tasks.clear();
-                for (int32_t r = 0; r < N; ++r) {
-                    const void *add = L == 1 ? grads[r] : (const void *)keepb(r, (L - 1) & 1);
-                    tasks.push_back(task(dq_stage{r, L, 0, 1}, msg(r ^ 1, (L - 1) & 1), lo[r], lo[r + 1], add,
-                                         finb(r), lo[r], lo[r + 1], nullptr, 0, 0));
-                }
-                e = run_hops(*P, tasks, end2, end4, true, L >= 2, st, log);
-            }
-        }
-        for (int32_t r = 0; r < N; ++r) fin[r] = finb(r);
+        if (run_hops(*P, tasks, end2, end4, step.has_in, step.add_f32, st, log) != cudaSuccess) return DQ_ERR_CUDA;
     }
-    if (e != cudaSuccess) return DQ_ERR_CUDA;
 
     // All-gather hands the final chunks to every rank unchanged; each rank
-    // decodes all of them into its own output.
-    // (rank, chunk) pairs in launches of up to kMaxTasks tasks.
+    // decodes all of them into its own output: (rank, chunk) pairs in
+    // launches of up to kMaxTasks tasks.
+    std::vector<const uint8_t *> fin((size_t)N, nullptr);
+    for (int32_t c = 0; c < N; ++c) fin[c] = msg(X.S.fin_rank[c], X.S.fin_par[c]);
     std::vector<PendingDecode> chunks;
     for (int32_t r = 0; r < N; ++r)
         for (int32_t c = 0; c < N; ++c) chunks.push_back(PendingDecode{fin[c], lo[c], lo[c + 1], outs[r]});

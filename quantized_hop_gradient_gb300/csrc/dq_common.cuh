@@ -62,6 +62,8 @@ struct Tables {
 };
 
 // One message (the bytes that carry a range of reordered super-groups).
+// UINT8 scales: E bytes at 0, u bytes at off_u (16 per SG); fp32 scales
+// (ablation): 16 floats per SG at off_u = 0 and no E bytes.
 struct MsgView {
     uint8_t *base;
     int64_t c, n2, n4;                    // SGs in range; of them 2-bit, 4-bit
@@ -96,6 +98,7 @@ struct HopParams {
     const int32_t *perm;
     uint32_t key0, key1;        // seed
     uint32_t round0, round1;    // round
+    int32_t scale_fp32;         // group scales in fp32 (ablation) instead of UINT8
 };
 
 // One chunk decoded by the final decode (same unit structure).
@@ -116,6 +119,7 @@ struct DecodeParams {
     const float *mu;
     const int32_t *perm;
     int32_t out_is_bf16;
+    int32_t scale_fp32;
 };
 
 // Statistics of several ranks in one launch.

@@ -101,12 +101,12 @@ __device__ __forceinline__ void stg_codes(uint8_t *p, const LaneCodes<BITS> &c)
     else *reinterpret_cast<uint4 *>(p) = make_uint4(c.w[0], c.w[1], c.w[2], c.w[3]);
 }
 
-// x = fl(sigma * q_code + x) with one rounding (fused multiply-add),
-// sigma = u * 2^(E-127) (0 when E = 0).
+// x = fl(sigma * q_code + x) with one rounding (fused multiply-add); sigma
+// is u * 2^(E-127) (0 when E = 0) with UINT8 scales, the fp32 scale itself
+// otherwise.
 template <int BITS>
-__device__ __forceinline__ void decode_add(float2 (&x)[8], uint32_t E, uint32_t u, const LaneCodes<BITS> &c)
+__device__ __forceinline__ void decode_add(float2 (&x)[8], float sigma, const LaneCodes<BITS> &c)
 {
-    const float sigma = __fmul_rn((float)u, __uint_as_float(E << 23));
     const float2 s2 = make_float2(sigma, sigma);
     const float *q = Lvl<BITS>::q();
 #pragma unroll
@@ -125,7 +125,9 @@ __device__ __forceinline__ void decode_add(float2 (&x)[8], uint32_t E, uint32_t 
 // packed multiply feeding a packed add into one fused operation even with
 // explicit .rn rounding, so y is formed by scalar __fmul_rn (which is never
 // contracted) and U < p16 is a float compare of U (exact) with p16.
-template <int BITS, bool ONE_LEVEL>
+// SF32 (ablation: scales in fp32): sigma = s, y = fl(x / s) (y = 0 when
+// s = 0); E_out = 0 and u_out holds the bits of s.
+template <int BITS, bool ONE_LEVEL, bool SF32>
 __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], uint32_t ctr0, uint32_t stage_word,
                                                           uint32_t corr2, uint32_t key0, uint32_t key1,
                                                           uint32_t round0, uint32_t round1, uint32_t &E_out,
@@ -134,17 +136,23 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
     float s = 0.0f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) s = fmaxf(s, fmaxf(fabsf(x[k].x), fabsf(x[k].y)));
-    float S = s;
+    float m = 0.0f;
+    if (SF32) {
+        E_out = 0u;
+        u_out = __float_as_uint(s);
+    } else {
+        float S = s;
 #pragma unroll
-    for (int m = 1; m <= 8; m <<= 1) S = fmaxf(S, __shfl_xor_sync(kFull, S, m));
-    const uint32_t E = exponent_byte(S);
-    const float inv2e = __uint_as_float((254u - E) << 23);   // 2^-e (any E: finite)
-    uint32_t u = __float2uint_ru(__fmul_rn(s, inv2e));
-    u = max(u, s > 0.0f ? 1u : 0u);
-    u = min(u, 255u);
-    const float m = __fmul_rn(g_tab.rcp[u], inv2e);
-    E_out = E;
-    u_out = u;
+        for (int sh = 1; sh <= 8; sh <<= 1) S = fmaxf(S, __shfl_xor_sync(kFull, S, sh));
+        const uint32_t E = exponent_byte(S);
+        const float inv2e = __uint_as_float((254u - E) << 23);   // 2^-e (any E: finite)
+        uint32_t u = __float2uint_ru(__fmul_rn(s, inv2e));
+        u = max(u, s > 0.0f ? 1u : 0u);
+        u = min(u, 255u);
+        m = __fmul_rn(g_tab.rcp[u], inv2e);
+        E_out = E;
+        u_out = u;
+    }
 
     // One Philox call per group: coordinate c takes 16-bit field c mod 8,
     // shifted by half a period (xor 0x8000 in each half) for c >= 8.
@@ -165,7 +173,9 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
     for (int w = 0; w < BITS / 2; ++w) out.w[w] = 0u;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const float2 y = make_float2(__fmul_rn(x[k].x, m), __fmul_rn(x[k].y, m));
+        const float2 y = SF32 ? (s > 0.0f ? make_float2(__fdiv_rn(x[k].x, s), __fdiv_rn(x[k].y, s))
+                                          : make_float2(0.0f, 0.0f))
+                              : make_float2(__fmul_rn(x[k].x, m), __fmul_rn(x[k].y, m));
         const float2 tf = f2_fma(y, H2, M2);                  // y*H is exact: one rounding = rint
         const BucketEntry b0 = bk[__float_as_uint(tf.x) & Lvl<BITS>::kMask];
         const BucketEntry b1 = bk[__float_as_uint(tf.y) & Lvl<BITS>::kMask];
@@ -191,13 +201,18 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
     return out;
 }
 
+// Bytes of one staging slot (a pair of super-groups): addends, incoming
+// codes, incoming group scales.
+template <bool ADD_F32, bool SF32>
+__host__ __device__ constexpr int stage_bytes() { return (ADD_F32 ? 2048 : 1024) + 512 + (SF32 ? 128 : 32); }
+
 // One work unit: super-groups j0 .. j0+cnt-1 (one task, one bitwidth).
-template <int BITS, bool HAS_IN, bool ADD_F32, bool ONE_LEVEL>
+template <int BITS, bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32>
 __device__ __forceinline__ void hop_unit(const HopParams &P, const HopTask &t, uint8_t *stg, int64_t j0, int cnt,
                                          int lane)
 {
     constexpr int A_BYTES = ADD_F32 ? 2048 : 1024;
-    constexpr int C_OFF = A_BYTES, U_OFF = A_BYTES + 512, STAGE = A_BYTES + 544;
+    constexpr int C_OFF = A_BYTES, U_OFF = A_BYTES + 512, STAGE = stage_bytes<ADD_F32, SF32>();
     const int half = lane >> 4, hl = lane & 15;
     const uint32_t stg_s = smem_addr(stg);
 
@@ -207,7 +222,7 @@ __device__ __forceinline__ void hop_unit(const HopParams &P, const HopTask &t, u
     if (lane < cnt) {
         old_i = __ldg(P.perm + j0 + lane);
         if (!ADD_F32) mu_i = __ldg(P.mu + old_i);
-        if (HAS_IN) ein_i = __ldg(t.in.base + (j0 + lane - t.in_lo));
+        if (HAS_IN && !SF32) ein_i = __ldg(t.in.base + (j0 + lane - t.in_lo));
     }
     const int npairs = (cnt + 1) >> 1;
 
@@ -228,7 +243,11 @@ __device__ __forceinline__ void hop_unit(const HopParams &P, const HopTask &t, u
             }
             if (HAS_IN) {
                 if (hl < 2 * BITS) cp_async16(st + C_OFF + half * 256 + hl * 16, code_block<BITS>(t.in, sl) + hl * 16);
-                if (hl == 15) cp_async16(st + U_OFF + half * 16, t.in.base + t.in.off_u + sl * 16);
+                if (SF32) {
+                    if (hl < 4) cp_async16(st + U_OFF + half * 64 + hl * 16, t.in.base + t.in.off_u + sl * 64 + hl * 16);
+                } else if (hl == 15) {
+                    cp_async16(st + U_OFF + half * 16, t.in.base + t.in.off_u + sl * 16);
+                }
             }
         }
         cp_async_commit();
@@ -266,9 +285,15 @@ __device__ __forceinline__ void hop_unit(const HopParams &P, const HopTask &t, u
             for (int k = 0; k < 8; ++k) x[k] = f2_sub(make_float2(bf16_lo(w[k]), bf16_hi(w[k])), mu2);
         }
         if (HAS_IN) {
-            const uint32_t u = st[U_OFF + half * 16 + hl];
+            float sigma;
+            if (SF32) {
+                sigma = *reinterpret_cast<const float *>(st + U_OFF + half * 64 + hl * 4);
+            } else {
+                const uint32_t u = st[U_OFF + half * 16 + hl];
+                sigma = __fmul_rn((float)u, __uint_as_float(ein << 23));
+            }
             const LaneCodes<BITS> c = lds_codes<BITS>(st + C_OFF + half * 256 + hl * 2 * BITS);
-            decode_add<BITS>(x, ein, u, c);
+            decode_add<BITS>(x, sigma, c);
         }
         if (!valid) {
 #pragma unroll
@@ -278,12 +303,13 @@ __device__ __forceinline__ void hop_unit(const HopParams &P, const HopTask &t, u
         const bool keep = valid && j >= t.keep_lo && j < t.keep_hi;
         uint32_t E, u;
         const uint32_t ctr0 = (uint32_t)old * 16u + (uint32_t)hl;   // global coordinate index / 16
-        const LaneCodes<BITS> q = quantize_group<BITS, ONE_LEVEL>(x, ctr0, t.stage_word, t.corr2, P.key0, P.key1,
-                                                                  P.round0, P.round1, E, u);
+        const LaneCodes<BITS> q = quantize_group<BITS, ONE_LEVEL, SF32>(x, ctr0, t.stage_word, t.corr2, P.key0,
+                                                                        P.key1, P.round0, P.round1, E, u);
         if (send) {
             const int64_t so = j - t.send_lo;
             stg_codes<BITS>(const_cast<uint8_t *>(code_block<BITS>(t.out, so)) + hl * 2 * BITS, q);
-            t.out.base[t.out.off_u + so * 16 + hl] = (uint8_t)u;
+            if (SF32) *reinterpret_cast<uint32_t *>(t.out.base + t.out.off_u + so * 64 + hl * 4) = u;
+            else t.out.base[t.out.off_u + so * 16 + hl] = (uint8_t)u;
         } else if (keep) {
             float4 *o = reinterpret_cast<float4 *>(t.keep_out + (j - t.keep_lo) * kSG + hl * 16);
 #pragma unroll
@@ -293,19 +319,19 @@ __device__ __forceinline__ void hop_unit(const HopParams &P, const HopTask &t, u
         if ((lane >> 1) == p) e_out = e_pair;
         __syncwarp();
     }
-    if (lane < cnt) {
+    if (!SF32 && lane < cnt) {
         const int64_t j = j0 + lane;
         if (j >= t.send_lo && j < t.send_hi) t.out.base[j - t.send_lo] = (uint8_t)e_out;
     }
 }
 
-template <bool HAS_IN, bool ADD_F32, bool ONE_LEVEL>
+template <bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32>
 __global__ void __launch_bounds__(kWarps * 32) hop_kernel(const __grid_constant__ HopParams P)
 {
     extern __shared__ __align__(16) uint8_t dyn[];
     block_copy(&g_tab, &P.tab);
     __syncthreads();
-    constexpr int STAGE = (ADD_F32 ? 2048 : 1024) + 544;
+    constexpr int STAGE = stage_bytes<ADD_F32, SF32>();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint8_t *stg = dyn + warp * kStages * STAGE;
     const int64_t nw = (int64_t)gridDim.x * kWarps;
@@ -316,9 +342,9 @@ __global__ void __launch_bounds__(kWarps * 32) hop_kernel(const __grid_constant_
         const int64_t j0 = t.seg_lo[seg] + (u - t.unit_begin[seg]) * kUnit;
         const int64_t rem = t.seg_hi[seg] - j0;
         const int cnt = (int)(rem < kUnit ? rem : kUnit);
-        if (seg == 0) hop_unit<2, HAS_IN, ADD_F32, ONE_LEVEL>(P, t, stg, j0, cnt, lane);
-        else if (seg == 1) hop_unit<4, HAS_IN, ADD_F32, ONE_LEVEL>(P, t, stg, j0, cnt, lane);
-        else hop_unit<8, HAS_IN, ADD_F32, ONE_LEVEL>(P, t, stg, j0, cnt, lane);
+        if (seg == 0) hop_unit<2, HAS_IN, ADD_F32, ONE_LEVEL, SF32>(P, t, stg, j0, cnt, lane);
+        else if (seg == 1) hop_unit<4, HAS_IN, ADD_F32, ONE_LEVEL, SF32>(P, t, stg, j0, cnt, lane);
+        else hop_unit<8, HAS_IN, ADD_F32, ONE_LEVEL, SF32>(P, t, stg, j0, cnt, lane);
     }
 }
 
@@ -339,7 +365,7 @@ __device__ __forceinline__ uint32_t ldg_codes4(const uint8_t *blk, int idx)
     return __ldg(blk + idx);
 }
 
-template <int BITS>
+template <int BITS, bool SF32>
 __device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeTask &t, int64_t j0, int cnt, int lane)
 {
     constexpr int kAhead = 8;
@@ -349,7 +375,7 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeT
     if (lane < cnt) {
         old_i = __ldg(P.perm + j0 + lane);
         mu_i = __ldg(P.mu + old_i);
-        ein_i = __ldg(t.msg.base + (j0 + lane - t.lo));
+        if (!SF32) ein_i = __ldg(t.msg.base + (j0 + lane - t.lo));
     }
     const float nr = (float)P.n_ranks;
     const float *q = Lvl<BITS>::q();
@@ -364,9 +390,15 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeT
                 const uint8_t *blk = code_block<BITS>(t.msg, sl);
                 ca[a] = ldg_codes4<BITS>(blk, lane);
                 cb[a] = ldg_codes4<BITS>(blk, 32 + lane);
-                const uint8_t *ub8 = t.msg.base + t.msg.off_u + sl * 16;
-                ua[a] = __ldg(ub8 + g0);
-                ub[a] = __ldg(ub8 + 8 + g0);
+                if (SF32) {   // bits of the fp32 scales of groups g0 and 8 + g0
+                    const uint32_t *sg = reinterpret_cast<const uint32_t *>(t.msg.base + t.msg.off_u + sl * 64);
+                    ua[a] = __ldg(sg + g0);
+                    ub[a] = __ldg(sg + 8 + g0);
+                } else {
+                    const uint8_t *ub8 = t.msg.base + t.msg.off_u + sl * 16;
+                    ua[a] = __ldg(ub8 + g0);
+                    ub[a] = __ldg(ub8 + 8 + g0);
+                }
             }
         }
 #pragma unroll
@@ -378,7 +410,8 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeT
             if (s < cnt) {
                 const float back = __fmul_rn(mu, nr);
                 const float p2e = __uint_as_float(E << 23);
-                const float sa = __fmul_rn((float)ua[a], p2e), sb = __fmul_rn((float)ub[a], p2e);
+                const float sa = SF32 ? __uint_as_float(ua[a]) : __fmul_rn((float)ua[a], p2e);
+                const float sb = SF32 ? __uint_as_float(ub[a]) : __fmul_rn((float)ub[a], p2e);
                 float va[4], vb[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -412,6 +445,7 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeT
 
 constexpr int kDecodeWarps = 16;
 
+template <bool SF32>
 __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kernel(const __grid_constant__ DecodeParams P)
 {
     block_copy(&g_tab, &P.tab);
@@ -425,9 +459,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kernel(const __grid_
         const int64_t j0 = t.seg_lo[seg] + (u - t.unit_begin[seg]) * kUnit;
         const int64_t rem = t.seg_hi[seg] - j0;
         const int cnt = (int)(rem < kUnit ? rem : kUnit);
-        if (seg == 0) decode_unit<2>(P, t, j0, cnt, lane);
-        else if (seg == 1) decode_unit<4>(P, t, j0, cnt, lane);
-        else decode_unit<8>(P, t, j0, cnt, lane);
+        if (seg == 0) decode_unit<2, SF32>(P, t, j0, cnt, lane);
+        else if (seg == 1) decode_unit<4, SF32>(P, t, j0, cnt, lane);
+        else decode_unit<8, SF32>(P, t, j0, cnt, lane);
     }
 }
 
@@ -443,12 +477,32 @@ int grid_for(K kernel, int warps, size_t dyn_smem, int64_t units)
     return (int)(need < cap ? (need < 1 ? 1 : need) : cap);
 }
 
-template <bool HAS_IN, bool ADD_F32, bool ONE_LEVEL>
+template <bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32>
 cudaError_t launch_hop_t(const HopParams &P, cudaStream_t st)
 {
-    const size_t dyn = (size_t)kWarps * kStages * ((ADD_F32 ? 2048 : 1024) + 544);
-    auto k = hop_kernel<HAS_IN, ADD_F32, ONE_LEVEL>;
+    const size_t dyn = (size_t)kWarps * kStages * stage_bytes<ADD_F32, SF32>();
+    auto k = hop_kernel<HAS_IN, ADD_F32, ONE_LEVEL, SF32>;
     k<<<grid_for(k, kWarps, dyn, P.total_units), kWarps * 32, dyn, st>>>(P);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+template <bool SF32>
+cudaError_t launch_hop_s(const HopParams &P, bool has_in, bool add_f32, cudaStream_t st)
+{
+    const bool one = P.tab.one_level != 0;
+    if (!has_in)
+        return one ? launch_hop_t<false, false, true, SF32>(P, st) : launch_hop_t<false, false, false, SF32>(P, st);
+    if (add_f32)
+        return one ? launch_hop_t<true, true, true, SF32>(P, st) : launch_hop_t<true, true, false, SF32>(P, st);
+    return one ? launch_hop_t<true, false, true, SF32>(P, st) : launch_hop_t<true, false, false, SF32>(P, st);
+}
+
+template <bool SF32>
+cudaError_t launch_decode_s(const DecodeParams &P, cudaStream_t st)
+{
+    auto k = decode_kernel<SF32>;
+    k<<<grid_for(k, kDecodeWarps, 0, P.total_units), kDecodeWarps * 32, 0, st>>>(P);
     note_launches(1);
     return cudaGetLastError();
 }
@@ -458,18 +512,13 @@ cudaError_t launch_hop_t(const HopParams &P, cudaStream_t st)
 cudaError_t launch_hop(const HopParams &P, bool has_in, bool add_f32, cudaStream_t st)
 {
     if (P.total_units <= 0) return cudaSuccess;
-    const bool one = P.tab.one_level != 0;
-    if (!has_in) return one ? launch_hop_t<false, false, true>(P, st) : launch_hop_t<false, false, false>(P, st);
-    if (add_f32) return one ? launch_hop_t<true, true, true>(P, st) : launch_hop_t<true, true, false>(P, st);
-    return one ? launch_hop_t<true, false, true>(P, st) : launch_hop_t<true, false, false>(P, st);
+    return P.scale_fp32 ? launch_hop_s<true>(P, has_in, add_f32, st) : launch_hop_s<false>(P, has_in, add_f32, st);
 }
 
 cudaError_t launch_decode(const DecodeParams &P, cudaStream_t st)
 {
     if (P.total_units <= 0) return cudaSuccess;
-    decode_kernel<<<grid_for(decode_kernel, kDecodeWarps, 0, P.total_units), kDecodeWarps * 32, 0, st>>>(P);
-    note_launches(1);
-    return cudaGetLastError();
+    return P.scale_fp32 ? launch_decode_s<true>(P, st) : launch_decode_s<false>(P, st);
 }
 
 }  // namespace dq

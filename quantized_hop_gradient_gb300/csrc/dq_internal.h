@@ -15,8 +15,8 @@ void note_launches(int n);  // adds to the library's launch counter
 bool build_tables(double eps, Tables *out);
 
 // Message view of range [lo, hi) with stream boundaries end2, end4.
-MsgView msg_view(uint8_t *base, int64_t lo, int64_t hi, int64_t end2, int64_t end4);
-size_t msg_bytes(int64_t c, int64_t n2, int64_t n4, int64_t n8);
+MsgView msg_view(uint8_t *base, int64_t lo, int64_t hi, int64_t end2, int64_t end4, bool scale_fp32);
+size_t msg_bytes(int64_t c, int64_t n2, int64_t n4, int64_t n8, bool scale_fp32);
 
 cudaError_t launch_stats(const uint16_t *g, int64_t n_sg, float *mean, float *sq, cudaStream_t st);
 cudaError_t launch_stats_batched(const StatsParams &S, cudaStream_t st);
@@ -30,5 +30,13 @@ size_t plan_scratch_bytes(int64_t n_sg);
 cudaError_t launch_allocate(const float *F, int64_t n_sg, int64_t cap_bits, uint8_t *b, float *T,
                             int64_t *counts, void *ws, cudaStream_t st);
 cudaError_t launch_reorder(const uint8_t *b, int64_t n_sg, int32_t *perm, void *ws, cudaStream_t st);
+
+// Brackets one launch with the caller's events (if a log has room).
+struct LogSlot {
+    dq_launch_log *log;
+    int32_t i;
+};
+LogSlot log_begin(dq_launch_log *log, int32_t kind, int64_t sgs, cudaStream_t st);
+void log_end(const LogSlot &s, cudaStream_t st);
 
 }  // namespace dq

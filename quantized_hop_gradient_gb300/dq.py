@@ -37,7 +37,8 @@ class BudgetInfeasible(DQError):
 
 class dq_config(C.Structure):
     _fields_ = [("n_ranks", C.c_int32), ("budget_bits", C.c_float), ("eps", C.c_double),
-                ("correlated", C.c_int32), ("seed", C.c_uint64), ("round", C.c_uint64)]
+                ("correlated", C.c_int32), ("seed", C.c_uint64), ("round", C.c_uint64),
+                ("fixed_bits", C.c_int32), ("scale_fp32", C.c_int32)]
 
 
 class dq_stage(C.Structure):
@@ -54,6 +55,7 @@ class dq_launch_log(C.Structure):
 
 
 DQ_LAUNCH_COMPRESS, DQ_LAUNCH_DAR, DQ_LAUNCH_DECODE, DQ_LAUNCH_STATS, DQ_LAUNCH_ALLOCATE_REORDER = 0, 1, 2, 3, 4
+DQ_LAUNCH_MX_HOP, DQ_LAUNCH_MX_DECODE = 5, 6
 
 
 class dq_plan_info(C.Structure):
@@ -64,7 +66,7 @@ _SIGS = {
     "dq_version": ([], C.c_char_p),
     "dq_launch_count": ([], C.c_uint64),
     "dq_status_string": ([C.c_int], C.c_char_p),
-    "dq_message_bytes": ([dq_range], C.c_size_t),
+    "dq_message_bytes": ([dq_range, C.c_int32], C.c_size_t),
     "dq_level_table": ([C.c_int32, C.c_double, C.c_void_p], C.c_int),
     "dq_stats": ([C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "dq_stats_reduce": ([C.c_void_p, C.c_void_p, C.c_int32, C.c_int64, C.c_void_p, C.c_void_p,
@@ -90,6 +92,12 @@ _SIGS = {
     "dq_exchange": ([C.POINTER(dq_config), C.c_int32, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
                      C.POINTER(dq_plan_info), C.c_void_p, C.c_size_t, C.c_void_p, C.c_int32,
                      C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+    "dq_mx_message_bytes": ([C.c_int64], C.c_size_t),
+    "dq_mx_quantize": ([C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p], C.c_int),
+    "dq_mx_dequantize": ([C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p], C.c_int),
+    "dq_mx_exchange_workspace_bytes": ([C.c_int32, C.c_int32, C.c_int64], C.c_size_t),
+    "dq_mx_exchange": ([C.c_int32, C.c_int32, C.c_void_p, C.c_int64, C.c_void_p, C.c_size_t, C.c_void_p,
+                        C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
 }
 
 
@@ -146,8 +154,8 @@ def _stream(stream) -> int:
 
 
 def config(n_ranks: int, budget_bits: float = 5.0, eps: float = 1.0, correlated: bool = True,
-           seed: int = 0, round: int = 0) -> dq_config:
-    return dq_config(n_ranks, budget_bits, eps, int(correlated), seed, round)
+           seed: int = 0, round: int = 0, fixed_bits: int = 0, scale_fp32: bool = False) -> dq_config:
+    return dq_config(n_ranks, budget_bits, eps, int(correlated), seed, round, int(fixed_bits), int(scale_fp32))
 
 
 def rng(lo: int, hi: int, end2: int, end4: int) -> dq_range:
@@ -167,8 +175,8 @@ def dq_launch_count() -> int:
     return lib().dq_launch_count()
 
 
-def dq_message_bytes(r: dq_range) -> int:
-    return lib().dq_message_bytes(r)
+def dq_message_bytes(r: dq_range, scale_fp32: bool = False) -> int:
+    return lib().dq_message_bytes(r, int(scale_fp32))
 
 
 def dq_level_table(bits: int, eps: float = 1.0):
@@ -286,3 +294,34 @@ def dq_exchange(cfg, butterfly, grads, n_sg, mu, perm, info, ws, ws_bytes, outs,
                              C.cast(fin, C.c_void_p), C.byref(log.c) if log is not None else None,
                              _stream(stream)), "dq_exchange")
     return [fin[i] for i in range(n)]
+
+
+# ------------------------------------------------------------------ MXFP8 comparison baseline
+MX_BLOCK = 32
+
+
+def dq_mx_message_bytes(n_blk: int) -> int:
+    return lib().dq_mx_message_bytes(n_blk)
+
+
+def dq_mx_quantize(x, n_blk, msg, stream=None):
+    _check(lib().dq_mx_quantize(_ptr(x), n_blk, _ptr(msg), _stream(stream)), "dq_mx_quantize")
+
+
+def dq_mx_dequantize(msg, n_blk, out, stream=None):
+    _check(lib().dq_mx_dequantize(_ptr(msg), n_blk, _ptr(out), _stream(stream)), "dq_mx_dequantize")
+
+
+def dq_mx_exchange_workspace_bytes(n_ranks, butterfly, n_blk) -> int:
+    return lib().dq_mx_exchange_workspace_bytes(n_ranks, int(butterfly), n_blk)
+
+
+def dq_mx_exchange(n_ranks, butterfly, grads, n_blk, ws, ws_bytes, outs, log: LaunchLog = None, stream=None):
+    """Returns the N device addresses of the final chunk messages (inside ws)."""
+    gp = (C.c_void_p * n_ranks)(*[_ptr(g) for g in grads])
+    op = (C.c_void_p * n_ranks)(*[_ptr(o) for o in outs])
+    fin = (C.c_void_p * n_ranks)()
+    _check(lib().dq_mx_exchange(n_ranks, int(butterfly), C.cast(gp, C.c_void_p), n_blk, _ptr(ws), ws_bytes,
+                                C.cast(op, C.c_void_p), C.cast(fin, C.c_void_p),
+                                C.byref(log.c) if log is not None else None, _stream(stream)), "dq_mx_exchange")
+    return [fin[i] for i in range(n_ranks)]

@@ -66,6 +66,18 @@ def test_message_bytes_equal_oracle(L):
         lo = int(rs.integers(0, J + 1))
         hi = int(rs.integers(lo, J + 1))
         assert dq.dq_message_bytes(dq.rng(lo, hi, end2, end4)) == oracle.range_message_bytes(lo, hi, end2, end4 - end2)
+        assert (dq.dq_message_bytes(dq.rng(lo, hi, end2, end4), True)
+                == oracle.range_message_bytes(lo, hi, end2, end4 - end2, True))
+
+
+def test_mx_message_bytes_equal_oracle(L):
+    for n in (0, 1, 15, 16, 17, 1000, 4_194_304):
+        assert dq.dq_mx_message_bytes(n) == oracle.mx_message_bytes(n)
+    assert dq.dq_mx_message_bytes(-1) == 0
+    # the workspace holds two messages per rank (plus fp32 halves and final chunks for the butterfly)
+    assert dq.dq_mx_exchange_workspace_bytes(4, False, 1000) >= 8 * dq.dq_mx_message_bytes(250)
+    assert dq.dq_mx_exchange_workspace_bytes(3, True, 1000) == 0      # butterfly needs 2^k ranks
+    assert dq.dq_mx_exchange_workspace_bytes(4, True, 1000) > dq.dq_mx_exchange_workspace_bytes(4, False, 1000)
 
 
 def test_bad_arguments_rejected_on_the_host(L):
@@ -90,3 +102,11 @@ def test_bad_arguments_rejected_on_the_host(L):
     assert dq.dq_exchange_workspace_bytes(dq.config(3), True, 3, info) == 0   # butterfly needs 2^k ranks
     assert dq.dq_exchange_workspace_bytes(dq.config(3), False, 3, info) > 0
     assert dq.dq_message_bytes(dq.rng(5, 4, 0, 0)) == 0
+    assert dq.dq_message_bytes(dq.rng(0, 4, 0, 0), 2) == 0
+    # ablation switches: only 0/2/4/8 bits and 0/1 scale modes
+    for bad_cfg in (dq.config(4, fixed_bits=3), dq.config(4, fixed_bits=16), dq.config(4, scale_fp32=2)):
+        assert L.dq_compress(bad_cfg, r, dq.stage(0, 0), P, P, P, P, st) == dq.DQ_ERR_INVALID_ARG
+    assert L.dq_mx_quantize(P, -1, P, st) == dq.DQ_ERR_INVALID_ARG
+    assert L.dq_mx_quantize(P + 4, 8, P, st) == dq.DQ_ERR_ALIGNMENT
+    assert L.dq_mx_dequantize(P, 8, None, st) == dq.DQ_ERR_INVALID_ARG
+    assert L.dq_mx_exchange(3, 1, P, 10, P, 1 << 20, P, None, None, st) == dq.DQ_ERR_INVALID_ARG
