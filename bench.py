@@ -414,6 +414,8 @@ def run_gpu(args, rank, world, local):
     barrier(world, dev)
     ms_e2e = max_over_ranks(f0.elapsed_time(f1) / KE, world, dev)
 
+    accuracy, mxfp8 = compare_mxfp8(args, w, grads, outs, ar, dev, N, J, butterfly, peak)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, grads, args.cpu_seconds)
@@ -436,10 +438,56 @@ def run_gpu(args, rank, world, local):
                 "d2h_bytes_per_step": J * SG * 4, "ms_per_step": ms_e2e},
         "gpu_launches": n_launch,
         "clocks": clk,
+        "accuracy": accuracy,
+        "mxfp8": mxfp8,
         "cpu_baseline": cpu,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def compare_mxfp8(args, w, grads, outs, ar, dev, N, J, butterfly, peak):
+    """After the timed region: the vNMSE of the last DynamiQ round and of
+    the MXFP8 baseline on the same gradients, and the MXFP8 all-reduce's
+    time on the same GPU (its hops read 1 + 1/32 B of message, 2 B of bf16
+    gradient and write 1 + 1/32 B per coordinate)."""
+    import torch
+
+    from quantized_hop_gradient_gb300 import dq, study
+    from quantized_hop_gradient_gb300.allreduce import MXFP8AllReduce
+
+    s = study.exact_sum(grads)
+    v_dq = study.vnmse(outs[0], s)
+    mx = MXFP8AllReduce(N, J * SG, butterfly=butterfly, device=dev)
+    for _ in range(2):
+        mx(grads, outs)
+    KM = 5
+    log = dq.LaunchLog(KM * (2 * N + 8))
+    log.c.count = 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(KM):
+        mx(grads, outs, log=log)
+    e1.record()
+    torch.cuda.synchronize()
+    ms_mx = e0.elapsed_time(e1) / KM
+    v_mx = study.vnmse(outs[0], s)
+    hops = [(sgs, t) for k, sgs, t in log.launches() if k == dq.DQ_LAUNCH_MX_HOP]
+    per_round = len(hops) // KM
+    dar = [h for i, h in enumerate(hops) if i % per_round != 0] if not butterfly else []
+    mx_line = {"ms_per_step": ms_mx, "ms_per_gb": ms_mx / (J * SG * 2 / 1e9),
+               "wire_bytes_per_coord": (1 + 1 / 32)}
+    if dar:
+        coords = sum(sgs for sgs, _ in dar) * SG / len(dar)
+        t = sum(tt for _, tt in dar) / len(dar) * 1e-3
+        gbs = coords * (2 + 2 * (1 + 1 / 32)) / t / 1e9
+        mx_line.update({"dar_avg_launch_ms": t * 1e3, "dar_gcoords_per_s": coords / t / 1e9, "dar_gbs": gbs,
+                        "dar_hbm_frac": gbs / peak})
+    del mx
+    torch.cuda.empty_cache()
+    msg = stream_message_bytes(dq, ar.info, N) / (J * SG)
+    return ({"vnmse": v_dq, "vnmse_mxfp8": v_mx, "mxfp8_over_dynamiq": v_mx / v_dq if v_dq > 0 else None,
+             "wire_bytes_per_coord": msg, "rounds_measured": 1}, mx_line)
 
 
 # --------------------------------------------------------------------------- streamed workloads
