@@ -255,7 +255,8 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads_host, int64_t n
  * are not recorded (they still run). */
 enum { DQ_LAUNCH_COMPRESS = 0, DQ_LAUNCH_DAR = 1, DQ_LAUNCH_DECODE = 2, DQ_LAUNCH_STATS = 3,
        DQ_LAUNCH_ALLOCATE_REORDER = 4, /* statistics reduce, allocation and reorder, one bracket */
-       DQ_LAUNCH_MX_HOP = 5, DQ_LAUNCH_MX_DECODE = 6 /* MXFP8 baseline; sgs = coordinates / 256 */ };
+       DQ_LAUNCH_MX_HOP = 5, DQ_LAUNCH_MX_DECODE = 6, /* MXFP8 baseline; sgs = coordinates / 256 */
+       DQ_LAUNCH_FUSED_RING = 7 /* dq_exchange_fused: all hops and the decode; sgs = J * (N + 1) */ };
 struct dq_launch_log {
     void   **events;
     int32_t *kinds;
@@ -286,6 +287,46 @@ dq_status dq_exchange(const dq_config *cfg, int32_t butterfly, const void *const
                       const dq_plan_info *info, void *ws, size_t ws_bytes,
                       void *const *outs_host, int32_t out_is_bf16,
                       const uint8_t **final_msgs_host, dq_launch_log *log, void *stream);
+
+/* ---- the ring exchange in one launch -------------------------------------
+ * Device status words (int32) written by the fused exchange: */
+#define DQ_DEVICE_OK 0
+#define DQ_DEVICE_BARRIER_TIMEOUT 1   /* a grid-barrier wait ran out; outputs are invalid */
+
+/* Device bytes dq_exchange_fused needs (ring; 1 <= N <= 16), 0 otherwise. */
+size_t dq_exchange_fused_workspace_bytes(const dq_config *cfg, int64_t n_sg, const dq_plan_info *info);
+
+/* The ring exchange of dq_exchange (same results, bit for bit) as ONE
+ * cooperative launch: the N hop steps and the final decode run in a
+ * persistent kernel, separated by device-wide barriers instead of kernel
+ * boundaries [S "Key idea and contribution": hop-by-hop fused decompress-
+ * accumulate-recompress; the barrier replaces the network hand-off].  It
+ * removes the per-step launches, which dominate small buckets.
+ *   Ring only, 1 <= N <= 16; arguments as for dq_exchange; ws of
+ *   dq_exchange_fused_workspace_bytes bytes.
+ *   status_dev: device int32 (4-byte aligned), set to DQ_DEVICE_OK before
+ *   the launch; every barrier wait is bounded (about a second of SM
+ *   clock) and, when it runs out, the kernel sets DQ_DEVICE_BARRIER_TIMEOUT
+ *   and returns instead of waiting on.  Read it after the stream is
+ *   synchronised; the outputs are valid only when it is DQ_DEVICE_OK.
+ *   Every CTA is resident at once (cudaLaunchCooperativeKernel); other work
+ *   running on the GPU at the same time delays the launch, it cannot
+ *   deadlock it. */
+dq_status dq_exchange_fused(const dq_config *cfg, const void *const *grads_host, int64_t n_sg,
+                            const float *mu, const int32_t *perm, const dq_plan_info *info, void *ws,
+                            size_t ws_bytes, void *const *outs_host, int32_t out_is_bf16,
+                            int32_t *status_dev, const uint8_t **final_msgs_host, dq_launch_log *log,
+                            void *stream);
+
+/* Test of the failure path of the fused exchange's barrier, with no
+ * counterpart in the paper: n_blocks CTAs (1 .. number of SMs) run one
+ * barrier that waits for n_blocks + missing arrivals, each wait bounded by
+ * timeout_cycles (<= 8e9).  missing = 0: every CTA passes, *status_dev stays
+ * DQ_DEVICE_OK.  missing > 0: the wait runs out, *status_dev becomes
+ * DQ_DEVICE_BARRIER_TIMEOUT and the kernel returns; the context stays
+ * usable.  scratch: device, 4 bytes (the arrival counter). */
+dq_status dq_barrier_selftest(int32_t n_blocks, int32_t missing, int64_t timeout_cycles, void *scratch,
+                              int32_t *status_dev, void *stream);
 
 /* ---- comparison baseline: MXFP8 ------------------------------------------
  * The pages compare DynamiQ's error with MXFP8's [A Abstract; S

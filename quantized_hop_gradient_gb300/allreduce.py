@@ -36,6 +36,7 @@ class DynamiQAllReduce:
         self.ws = torch.empty(0, dtype=torch.uint8, device=self.device)
         self.info = None
         self.final = None
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
 
     def config(self, round: int = 0):
         return dq.config(self.n_ranks, self.budget, self.eps, self.correlated, self.seed, round,
@@ -57,29 +58,48 @@ class DynamiQAllReduce:
         if self.ws.numel() < nbytes:
             self.ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
 
-    def exchange(self, grads, outs, round: int = 0, stream=None, log=None):
+    def exchange(self, grads, outs, round: int = 0, stream=None, log=None, fused: bool = False):
+        """``fused``: the ring exchange as one cooperative launch (ring, at
+        most 16 ranks); its device status is in ``self.status`` (check with
+        ``check_status`` after synchronising)."""
         cfg = self.config(round)
         n_sg = getattr(self, "cur_sg", self.n_sg)
+        bf16 = self.out_dtype == torch.bfloat16
+        if fused:
+            if self.butterfly:
+                raise ValueError("the fused exchange is the ring's")
+            need = dq.dq_exchange_fused_workspace_bytes(cfg, n_sg, self.info)
+            if need == 0:
+                raise dq.DQError(dq.DQ_ERR_INVALID_ARG, "dq_exchange_fused_workspace_bytes")
+            self.reserve(need)
+            self.final = dq.dq_exchange_fused(cfg, grads, n_sg, self.mu, self.perm, self.info, self.ws,
+                                              self.ws.numel(), outs, self.status, bf16, log, stream)
+            return outs
         need = dq.dq_exchange_workspace_bytes(cfg, self.butterfly, n_sg, self.info)
         if need == 0:
             raise dq.DQError(dq.DQ_ERR_INVALID_ARG, "dq_exchange_workspace_bytes")
         self.reserve(need)
         self.final = dq.dq_exchange(cfg, self.butterfly, grads, n_sg, self.mu, self.perm, self.info,
-                                    self.ws, self.ws.numel(), outs, self.out_dtype == torch.bfloat16, log,
-                                    stream)
+                                    self.ws, self.ws.numel(), outs, bf16, log, stream)
         return outs
+
+    def check_status(self):
+        """Raises if the last fused exchange reported a device error."""
+        s = int(self.status.item())
+        if s != dq.DQ_DEVICE_OK:
+            raise RuntimeError(f"fused exchange: device status {s} (barrier timeout)")
 
     def new_outputs(self):
         return [torch.empty(self.n_sg * SG, dtype=self.out_dtype, device=self.device)
                 for _ in range(self.n_ranks)]
 
-    def __call__(self, grads, round: int = 0, outs=None, stream=None):
+    def __call__(self, grads, round: int = 0, outs=None, stream=None, fused: bool = False):
         if len(grads) != self.n_ranks:
             raise ValueError("one gradient per rank")
         if outs is None:
             outs = self.new_outputs()
         self.plan(grads, round, stream)
-        return self.exchange(grads, outs, round, stream)
+        return self.exchange(grads, outs, round, stream, fused=fused)
 
     def chunk_lo(self):
         i = self.info

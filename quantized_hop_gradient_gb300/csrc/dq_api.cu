@@ -748,3 +748,115 @@ dq_status dq_exchange(const dq_config *cfg, int32_t butterfly, const void *const
 }
 
 }  // extern "C"
+
+// --------------------------------------------------------------------------- fused ring exchange
+namespace {
+
+constexpr long long kBarrierTimeoutCycles = 2000000000LL;   // about one second at the SM clock
+
+bool fused_ok(const dq_config *cfg) { return cfg_ok(cfg) && cfg->n_ranks <= kMaxFusedRanks; }
+
+}  // namespace
+
+extern "C" {
+
+size_t dq_exchange_fused_workspace_bytes(const dq_config *cfg, int64_t n_sg, const dq_plan_info *info)
+{
+    if (!fused_ok(cfg) || !info || n_sg < 1) return 0;
+    ExchangeLayout X;
+    if (!exchange_layout(cfg, 0, info, X)) return 0;
+    return X.total + 256;   // + the barrier's arrival counter
+}
+
+dq_status dq_exchange_fused(const dq_config *cfg, const void *const *grads, int64_t n_sg, const float *mu,
+                            const int32_t *perm, const dq_plan_info *info, void *ws, size_t ws_bytes,
+                            void *const *outs, int32_t out_is_bf16, int32_t *status_dev,
+                            const uint8_t **final_msgs, dq_launch_log *log, void *stream)
+{
+    if (!fused_ok(cfg) || !grads || !mu || !perm || !info || !ws || !outs || !status_dev || n_sg < 1 ||
+        n_sg >= kMaxSG)
+        return DQ_ERR_INVALID_ARG;
+    if (info->n2 < 0 || info->n4 < 0 || info->n8 < 0 || info->n2 + info->n4 + info->n8 != n_sg)
+        return DQ_ERR_INVALID_ARG;
+    const int32_t N = cfg->n_ranks;
+    ExchangeLayout X;
+    if (!exchange_layout(cfg, 0, info, X)) return DQ_ERR_INVALID_ARG;
+    if (ws_bytes < X.total + 256) return DQ_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return DQ_ERR_ALIGNMENT;
+    if ((uintptr_t)status_dev & 3u) return DQ_ERR_ALIGNMENT;
+    for (int32_t r = 0; r < N; ++r) {
+        if (!grads[r] || !outs[r]) return DQ_ERR_INVALID_ARG;
+        if (!aligned16(grads[r]) || !aligned16(outs[r])) return DQ_ERR_ALIGNMENT;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t end2 = info->n2, end4 = info->n2 + info->n4;
+    const bool sf = cfg->scale_fp32 != 0;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+
+    std::unique_ptr<FusedRingParams> P(new FusedRingParams());
+    memset(P.get(), 0, sizeof(FusedRingParams));
+    if (!build_tables(cfg->eps, &P->tab)) return DQ_ERR_INVALID_ARG;
+    int64_t units = 0;
+    for (int32_t c = 0; c < N; ++c) {
+        const int64_t a = X.lo[c], b = X.lo[c + 1];
+        P->chunk[c] = msg_view(nullptr, a, b, end2, end4, sf);
+        P->lo[c] = a;
+        HopTask t;   // segment and unit bookkeeping of chunk c
+        memset(&t, 0, sizeof(t));
+        units += set_units(t, a, b, end2, end4, units);
+        for (int s = 0; s < 3; ++s) {
+            P->seg_lo[c][s] = t.seg_lo[s];
+            P->seg_hi[c][s] = t.seg_hi[s];
+            P->unit_begin[c][s] = t.unit_begin[s];
+        }
+        P->unit_begin[c][3] = t.unit_begin[3];
+        P->grads[c] = grads[c];
+        P->outs[c] = outs[c];
+    }
+    P->lo[N] = X.lo[N];
+    P->msgs = w + X.msgs;
+    P->msg_stride = (int64_t)X.msg_stride;
+    P->units = units;
+    P->n_ranks = N;
+    P->correlated = cfg->correlated ? 1 : 0;
+    P->mu = mu;
+    P->perm = perm;
+    P->key0 = (uint32_t)cfg->seed;
+    P->key1 = (uint32_t)(cfg->seed >> 32);
+    P->round0 = (uint32_t)cfg->round;
+    P->round1 = (uint32_t)(cfg->round >> 32);
+    P->out_is_bf16 = out_is_bf16 ? 1 : 0;
+    P->scale_fp32 = cfg->scale_fp32;
+    P->barrier = reinterpret_cast<unsigned int *>(w + X.total);
+    P->status = status_dev;
+    P->timeout_cycles = kBarrierTimeoutCycles;
+    if (cudaMemsetAsync(P->barrier, 0, sizeof(unsigned int), st) != cudaSuccess) return DQ_ERR_CUDA;
+    if (cudaMemsetAsync(status_dev, 0, sizeof(int32_t), st) != cudaSuccess) return DQ_ERR_CUDA;
+    const LogSlot slot = log_begin(log, DQ_LAUNCH_FUSED_RING, n_sg * (N + 1), st);
+    const cudaError_t e = launch_fused_ring(*P, st);
+    log_end(slot, st);
+    if (e != cudaSuccess) return DQ_ERR_CUDA;
+    if (final_msgs)
+        for (int32_t c = 0; c < N; ++c) final_msgs[c] = w + X.msgs + (size_t)(2 * c + ((N - 1) & 1)) * X.msg_stride;
+    return DQ_OK;
+}
+
+dq_status dq_barrier_selftest(int32_t n_blocks, int32_t missing, int64_t timeout_cycles, void *scratch,
+                              int32_t *status_dev, void *stream)
+{
+    if (n_blocks < 1 || n_blocks > 1024 || missing < 0 || missing > 1024 || timeout_cycles < 1 ||
+        timeout_cycles > 4 * kBarrierTimeoutCycles || !scratch || !status_dev)
+        return DQ_ERR_INVALID_ARG;
+    if (((uintptr_t)scratch & 3u) || ((uintptr_t)status_dev & 3u)) return DQ_ERR_ALIGNMENT;
+    int dev = 0, coop = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DQ_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) return DQ_ERR_CUDA;
+    if (n_blocks > sm_count()) return DQ_ERR_INVALID_ARG;   // one small CTA per SM at most: all resident
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned int *counter = static_cast<unsigned int *>(scratch);
+    if (cudaMemsetAsync(counter, 0, sizeof(unsigned int), st) != cudaSuccess) return DQ_ERR_CUDA;
+    if (cudaMemsetAsync(status_dev, 0, sizeof(int32_t), st) != cudaSuccess) return DQ_ERR_CUDA;
+    return cuda_status(launch_barrier_selftest(n_blocks, missing, (long long)timeout_cycles, counter, status_dev, st));
+}
+
+}  // extern "C"

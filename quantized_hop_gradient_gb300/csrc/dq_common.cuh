@@ -132,6 +132,36 @@ struct StatsParams {
     float *sq_all;
 };
 
+// The whole ring exchange of one round in one cooperative launch: N hop
+// steps and the final decode, separated by grid barriers.  Chunk c's
+// message layout, units and range are the same at every step; only the
+// message buffers and the quantizing rank rotate.
+constexpr int kMaxFusedRanks = 16;
+constexpr int32_t kDeviceBarrierTimeout = 1;   // status word: a barrier wait ran out
+
+struct FusedRingParams {
+    Tables tab;
+    MsgView chunk[kMaxFusedRanks];             // message layout of chunk c (base unset)
+    int64_t lo[kMaxFusedRanks + 1];            // chunk cuts (reordered super-groups)
+    int64_t seg_lo[kMaxFusedRanks][3], seg_hi[kMaxFusedRanks][3];
+    int64_t unit_begin[kMaxFusedRanks][4];     // first unit of each segment of chunk c; [3] = end
+    const void *grads[kMaxFusedRanks];
+    void *outs[kMaxFusedRanks];
+    uint8_t *msgs;                             // two message buffers per rank, msg_stride apart
+    int64_t msg_stride;
+    int64_t units;                             // work units per phase
+    int32_t n_ranks;
+    int32_t correlated;
+    const float *mu;
+    const int32_t *perm;
+    uint32_t key0, key1, round0, round1;
+    int32_t out_is_bf16;
+    int32_t scale_fp32;
+    unsigned int *barrier;                     // arrival counter, zero at launch
+    int32_t *status;                           // zero at launch; kDeviceBarrierTimeout on a timeout
+    long long timeout_cycles;                  // bound of every barrier wait (SM clock cycles)
+};
+
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon et al., SC 2011): ten rounds; each multiplies words
 // 0 and 2 by the Philox constants (full 64-bit products), xors the high

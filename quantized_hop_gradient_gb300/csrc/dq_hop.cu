@@ -11,6 +11,8 @@
 // and broadcast by shuffles.  The gradient (or fp32 partial), the incoming
 // codes and the incoming UINT8 scales of a pair of super-groups are staged
 // in shared memory by cp.async, one pair ahead of the computation.
+#include <algorithm>
+
 #include "dq_common.cuh"
 #include "dq_internal.h"
 
@@ -206,9 +208,13 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
 template <bool ADD_F32, bool SF32>
 __host__ __device__ constexpr int stage_bytes() { return (ADD_F32 ? 2048 : 1024) + 512 + (SF32 ? 128 : 32); }
 
-// One work unit: super-groups j0 .. j0+cnt-1 (one task, one bitwidth).
-template <int BITS, bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32>
-__device__ __forceinline__ void hop_unit(const HopParams &P, const HopTask &t, uint8_t *stg, int64_t j0, int cnt,
+// One work unit: super-groups j0 .. j0+cnt-1 (one task, one bitwidth).  PP
+// supplies perm, mu and the generator key and round.  Message bytes are
+// read through L2 (cp.async.cg, ld.cg), never the non-coherent path, so a
+// message written earlier in the same launch by other CTAs is read
+// correctly after a grid barrier.
+template <int BITS, bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32, typename PP>
+__device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t *stg, int64_t j0, int cnt,
                                          int lane)
 {
     constexpr int A_BYTES = ADD_F32 ? 2048 : 1024;
@@ -222,7 +228,7 @@ __device__ __forceinline__ void hop_unit(const HopParams &P, const HopTask &t, u
     if (lane < cnt) {
         old_i = __ldg(P.perm + j0 + lane);
         if (!ADD_F32) mu_i = __ldg(P.mu + old_i);
-        if (HAS_IN && !SF32) ein_i = __ldg(t.in.base + (j0 + lane - t.in_lo));
+        if (HAS_IN && !SF32) ein_i = __ldcg(t.in.base + (j0 + lane - t.in_lo));
     }
     const int npairs = (cnt + 1) >> 1;
 
@@ -323,6 +329,11 @@ __device__ __forceinline__ void hop_unit(const HopParams &P, const HopTask &t, u
         const int64_t j = j0 + lane;
         if (j >= t.send_lo && j < t.send_hi) t.out.base[j - t.send_lo] = (uint8_t)e_out;
     }
+    // the unit holding the send range's last super-group zeroes the E padding
+    if (!SF32 && t.send_hi > t.send_lo && t.send_hi - 1 >= j0 && t.send_hi - 1 < j0 + cnt) {
+        const int64_t c = t.send_hi - t.send_lo, pad = (c + 15) / 16 * 16;
+        if (lane < pad - c) t.out.base[c + lane] = 0;
+    }
 }
 
 template <bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32>
@@ -360,14 +371,22 @@ template <int BITS>
 __device__ __forceinline__ uint32_t ldg_codes4(const uint8_t *blk, int idx)
 {
     // codes of 4 consecutive coordinates starting at coordinate 4*idx
-    if (BITS == 8) return __ldg(reinterpret_cast<const uint32_t *>(blk) + idx);
-    if (BITS == 4) return __ldg(reinterpret_cast<const unsigned short *>(blk) + idx);
-    return __ldg(blk + idx);
+    if (BITS == 8) return __ldcg(reinterpret_cast<const uint32_t *>(blk) + idx);
+    if (BITS == 4) return __ldcg(reinterpret_cast<const unsigned short *>(blk) + idx);
+    return __ldcg(blk + idx);
 }
 
-template <int BITS, bool SF32>
-__device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeTask &t, int64_t j0, int cnt, int lane)
+// Decode super-groups j0 .. j0+cnt-1 of message `msg` (range starting at
+// lo) into every one of the n_outs outputs.  PP supplies perm, mu, n_ranks
+// and out_is_bf16.
+template <int BITS, bool SF32, typename PP>
+__device__ __forceinline__ void decode_unit(const PP &P, const MsgView &msg, int64_t lo, void *const *outs,
+                                            int n_outs, int64_t j0, int cnt, int lane)
 {
+    struct {
+        const MsgView &msg;
+        int64_t lo;
+    } t{msg, lo};
     constexpr int kAhead = 8;
     int32_t old_i = 0;
     float mu_i = 0.0f;
@@ -375,7 +394,7 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeT
     if (lane < cnt) {
         old_i = __ldg(P.perm + j0 + lane);
         mu_i = __ldg(P.mu + old_i);
-        if (!SF32) ein_i = __ldg(t.msg.base + (j0 + lane - t.lo));
+        if (!SF32) ein_i = __ldcg(t.msg.base + (j0 + lane - t.lo));
     }
     const float nr = (float)P.n_ranks;
     const float *q = Lvl<BITS>::q();
@@ -392,12 +411,12 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeT
                 cb[a] = ldg_codes4<BITS>(blk, 32 + lane);
                 if (SF32) {   // bits of the fp32 scales of groups g0 and 8 + g0
                     const uint32_t *sg = reinterpret_cast<const uint32_t *>(t.msg.base + t.msg.off_u + sl * 64);
-                    ua[a] = __ldg(sg + g0);
-                    ub[a] = __ldg(sg + 8 + g0);
+                    ua[a] = __ldcg(sg + g0);
+                    ub[a] = __ldcg(sg + 8 + g0);
                 } else {
                     const uint8_t *ub8 = t.msg.base + t.msg.off_u + sl * 16;
-                    ua[a] = __ldg(ub8 + g0);
-                    ub[a] = __ldg(ub8 + 8 + g0);
+                    ua[a] = __ldcg(ub8 + g0);
+                    ub[a] = __ldcg(ub8 + 8 + g0);
                 }
             }
         }
@@ -420,7 +439,6 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeT
                     vb[i] = __fmaf_rn(sb, q[(cb[a] >> (BITS * i)) & mask], back);
                 }
                 if (P.out_is_bf16) {
-                    uint16_t *o = static_cast<uint16_t *>(t.out) + (int64_t)old * kSG;
                     const uint2 wa = make_uint2(
                         (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(va[0])) |
                             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(va[1])) << 16),
@@ -431,12 +449,19 @@ __device__ __forceinline__ void decode_unit(const DecodeParams &P, const DecodeT
                             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(vb[1])) << 16),
                         (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(vb[2])) |
                             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(vb[3])) << 16));
-                    __stcs(reinterpret_cast<uint2 *>(o + 4 * lane), wa);
-                    __stcs(reinterpret_cast<uint2 *>(o + 128 + 4 * lane), wb);
+                    for (int oi = 0; oi < n_outs; ++oi) {
+                        uint16_t *o = static_cast<uint16_t *>(outs[oi]) + (int64_t)old * kSG;
+                        __stcs(reinterpret_cast<uint2 *>(o + 4 * lane), wa);
+                        __stcs(reinterpret_cast<uint2 *>(o + 128 + 4 * lane), wb);
+                    }
                 } else {
-                    float *o = static_cast<float *>(t.out) + (int64_t)old * kSG;
-                    __stcs(reinterpret_cast<float4 *>(o + 4 * lane), make_float4(va[0], va[1], va[2], va[3]));
-                    __stcs(reinterpret_cast<float4 *>(o + 128 + 4 * lane), make_float4(vb[0], vb[1], vb[2], vb[3]));
+                    const float4 fa = make_float4(va[0], va[1], va[2], va[3]);
+                    const float4 fb = make_float4(vb[0], vb[1], vb[2], vb[3]);
+                    for (int oi = 0; oi < n_outs; ++oi) {
+                        float *o = static_cast<float *>(outs[oi]) + (int64_t)old * kSG;
+                        __stcs(reinterpret_cast<float4 *>(o + 4 * lane), fa);
+                        __stcs(reinterpret_cast<float4 *>(o + 128 + 4 * lane), fb);
+                    }
                 }
             }
         }
@@ -459,9 +484,117 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kernel(const __grid_
         const int64_t j0 = t.seg_lo[seg] + (u - t.unit_begin[seg]) * kUnit;
         const int64_t rem = t.seg_hi[seg] - j0;
         const int cnt = (int)(rem < kUnit ? rem : kUnit);
-        if (seg == 0) decode_unit<2, SF32>(P, t, j0, cnt, lane);
-        else if (seg == 1) decode_unit<4, SF32>(P, t, j0, cnt, lane);
-        else decode_unit<8, SF32>(P, t, j0, cnt, lane);
+        if (seg == 0) decode_unit<2, SF32>(P, t.msg, t.lo, &t.out, 1, j0, cnt, lane);
+        else if (seg == 1) decode_unit<4, SF32>(P, t.msg, t.lo, &t.out, 1, j0, cnt, lane);
+        else decode_unit<8, SF32>(P, t.msg, t.lo, &t.out, 1, j0, cnt, lane);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Grid barrier of a cooperative launch.  Thread 0 of each CTA makes the
+// CTA's writes visible (fence), arrives on the counter and waits, with a
+// bound, for gridDim.x * (phase + 1) arrivals.  The wait gives up when the
+// status word is already set (another CTA timed out) or after
+// timeout_cycles of the SM clock, setting the status; every thread of the
+// CTA then learns the outcome, and a CTA that gave up returns from the
+// kernel, so no CTA waits forever.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ bool grid_barrier(unsigned *counter, int32_t *status, unsigned target,
+                                             long long timeout_cycles)
+{
+    __shared__ int ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(counter, 1u);
+        const long long t0 = clock64();
+        int good = 1;
+        while (ld_acquire_u32(counter) < target) {
+            if (*(volatile int32_t *)status != 0) { good = 0; break; }
+            if (clock64() - t0 > timeout_cycles) {
+                atomicCAS(status, 0, kDeviceBarrierTimeout);
+                good = 0;
+                break;
+            }
+            __nanosleep(64);
+        }
+        __threadfence();
+        ok = good;
+    }
+    __syncthreads();
+    return ok != 0;
+}
+
+__global__ void barrier_selftest_kernel(unsigned *counter, int32_t *status, unsigned target, long long timeout)
+{
+    grid_barrier(counter, status, target, timeout);
+}
+
+// The ring exchange of one round, fused: at step t every chunk c is handled
+// by rank r = (c + 1 + t) mod N, reading rank r-1's message of step t-1 and
+// writing its own (buffer parity t & 1); step 0 quantizes the local
+// gradient.  After the last step the owners' messages are decoded into every
+// output (one read, N writes).  Grid barriers separate the phases.
+template <bool ONE_LEVEL, bool SF32>
+__global__ void __launch_bounds__(kWarps * 32) fused_ring_kernel(const __grid_constant__ FusedRingParams P)
+{
+    extern __shared__ __align__(16) uint8_t dyn[];
+    block_copy(&g_tab, &P.tab);
+    __syncthreads();
+    constexpr int STAGE = stage_bytes<false, SF32>();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t *stg = dyn + warp * kStages * STAGE;
+    const int N = P.n_ranks;
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    for (int t = 0; t <= N; ++t) {
+        for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < P.units; u += nw) {
+            int c = 0;
+            while (c + 1 < N && u >= P.unit_begin[c + 1][0]) ++c;
+            int seg = 0;
+            while (seg < 2 && u >= P.unit_begin[c][seg + 1]) ++seg;
+            const int64_t j0 = P.seg_lo[c][seg] + (u - P.unit_begin[c][seg]) * kUnit;
+            const int64_t rem = P.seg_hi[c][seg] - j0;
+            const int cnt = (int)(rem < kUnit ? rem : kUnit);
+            if (t == N) {   // final decode of chunk c (owner c, step N-1)
+                MsgView m = P.chunk[c];
+                m.base = P.msgs + (2 * (int64_t)c + ((N - 1) & 1)) * P.msg_stride;
+                if (seg == 0) decode_unit<2, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
+                else if (seg == 1) decode_unit<4, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
+                else decode_unit<8, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
+                continue;
+            }
+            const int r = (c + 1 + t) % N, src = (r - 1 + N) % N;
+            HopTask T;
+            T.in = P.chunk[c];
+            T.in.base = P.msgs + (2 * (int64_t)src + ((t - 1) & 1)) * P.msg_stride;
+            T.out = P.chunk[c];
+            T.out.base = P.msgs + (2 * (int64_t)r + (t & 1)) * P.msg_stride;
+            T.addend = P.grads[r];
+            T.keep_out = nullptr;
+            T.in_lo = P.lo[c];
+            T.send_lo = P.lo[c];
+            T.send_hi = P.lo[c + 1];
+            T.keep_lo = T.keep_hi = P.lo[c + 1];
+            T.stage_word = (uint32_t)t | (P.correlated ? 0xFFFF0000u : ((uint32_t)r << 16));
+            T.corr2 = 0u;   // one quantizer per ring stage: stratum offset 0
+            if (t == 0) {
+                if (seg == 0) hop_unit<2, false, false, ONE_LEVEL, SF32>(P, T, stg, j0, cnt, lane);
+                else if (seg == 1) hop_unit<4, false, false, ONE_LEVEL, SF32>(P, T, stg, j0, cnt, lane);
+                else hop_unit<8, false, false, ONE_LEVEL, SF32>(P, T, stg, j0, cnt, lane);
+            } else {
+                if (seg == 0) hop_unit<2, true, false, ONE_LEVEL, SF32>(P, T, stg, j0, cnt, lane);
+                else if (seg == 1) hop_unit<4, true, false, ONE_LEVEL, SF32>(P, T, stg, j0, cnt, lane);
+                else hop_unit<8, true, false, ONE_LEVEL, SF32>(P, T, stg, j0, cnt, lane);
+            }
+        }
+        if (t < N && !grid_barrier(P.barrier, P.status, gridDim.x * (unsigned)(t + 1), P.timeout_cycles)) return;
     }
 }
 
@@ -519,6 +652,48 @@ cudaError_t launch_decode(const DecodeParams &P, cudaStream_t st)
 {
     if (P.total_units <= 0) return cudaSuccess;
     return P.scale_fp32 ? launch_decode_s<true>(P, st) : launch_decode_s<false>(P, st);
+}
+
+namespace {
+
+template <bool ONE_LEVEL, bool SF32>
+cudaError_t launch_fused_t(const FusedRingParams &P, cudaStream_t st)
+{
+    const size_t dyn = (size_t)kWarps * kStages * stage_bytes<false, SF32>();
+    auto k = fused_ring_kernel<ONE_LEVEL, SF32>;
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kWarps * 32, dyn);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorLaunchOutOfResources;
+    // every CTA must be resident at once (cooperative launch): at most the
+    // CTAs that fit, and no more than the work needs
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    const int64_t need = std::max<int64_t>(1, (P.units + kWarps - 1) / kWarps);
+    const int grid = (int)std::min(cap, need);
+    void *args[] = {const_cast<FusedRingParams *>(&P)};
+    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(k), dim3(grid), dim3(kWarps * 32), args, dyn, st);
+    note_launches(1);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fused_ring(const FusedRingParams &P, cudaStream_t st)
+{
+    const bool one = P.tab.one_level != 0;
+    if (P.scale_fp32) return one ? launch_fused_t<true, true>(P, st) : launch_fused_t<false, true>(P, st);
+    return one ? launch_fused_t<true, false>(P, st) : launch_fused_t<false, false>(P, st);
+}
+
+cudaError_t launch_barrier_selftest(int32_t n_blocks, int32_t missing, long long timeout_cycles, unsigned *counter,
+                                    int32_t *status, cudaStream_t st)
+{
+    unsigned target = (unsigned)n_blocks + (unsigned)missing;
+    void *args[] = {&counter, &status, &target, &timeout_cycles};
+    const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(barrier_selftest_kernel),
+                                                      dim3(n_blocks), dim3(32), args, 0, st);
+    note_launches(1);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace dq

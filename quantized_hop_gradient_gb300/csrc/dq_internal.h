@@ -24,6 +24,12 @@ cudaError_t launch_stats_reduce(const float *mean_all, const float *sq_all, int3
                                 float *M, float *F, float *mu, cudaStream_t st);
 cudaError_t launch_hop(const HopParams &P, bool has_in, bool add_f32, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams &P, cudaStream_t st);
+// Cooperative launches (every CTA resident): the fused ring exchange, and a
+// lone grid barrier whose target is `missing` arrivals more than the grid
+// provides (missing > 0 makes the bounded wait run out).
+cudaError_t launch_fused_ring(const FusedRingParams &P, cudaStream_t st);
+cudaError_t launch_barrier_selftest(int32_t n_blocks, int32_t missing, long long timeout_cycles,
+                                    unsigned int *counter, int32_t *status, cudaStream_t st);
 
 // Allocation (radix select of T) and reordering; ws is device scratch.
 size_t plan_scratch_bytes(int64_t n_sg);

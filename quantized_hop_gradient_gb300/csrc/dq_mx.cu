@@ -163,6 +163,10 @@ __global__ void __launch_bounds__(kMxWarps * 32) mx_hop_kernel(const __grid_cons
                 const int64_t so = b - t.send_lo;
                 reinterpret_cast<uint32_t *>(t.out + t.out_pad + so * kMxBlk)[sub] = w;
                 if (sub == 0) t.out[so] = (uint8_t)X;
+                if (b == t.send_hi - 1 && sub > 0) {   // zero the scale section's padding
+                    const int64_t c = t.send_hi - t.send_lo;
+                    for (int64_t q = c + sub - 1; q < t.out_pad; q += 7) t.out[q] = 0;
+                }
             } else if (b >= t.keep_lo && b < t.keep_hi) {
                 reinterpret_cast<float4 *>(t.keep + (b - t.keep_lo) * kMxBlk)[sub] = x;
             }

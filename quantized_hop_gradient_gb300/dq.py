@@ -55,7 +55,9 @@ class dq_launch_log(C.Structure):
 
 
 DQ_LAUNCH_COMPRESS, DQ_LAUNCH_DAR, DQ_LAUNCH_DECODE, DQ_LAUNCH_STATS, DQ_LAUNCH_ALLOCATE_REORDER = 0, 1, 2, 3, 4
-DQ_LAUNCH_MX_HOP, DQ_LAUNCH_MX_DECODE = 5, 6
+DQ_LAUNCH_MX_HOP, DQ_LAUNCH_MX_DECODE, DQ_LAUNCH_FUSED_RING = 5, 6, 7
+DQ_DEVICE_OK, DQ_DEVICE_BARRIER_TIMEOUT = 0, 1
+MAX_FUSED_RANKS = 16
 
 
 class dq_plan_info(C.Structure):
@@ -92,6 +94,12 @@ _SIGS = {
     "dq_exchange": ([C.POINTER(dq_config), C.c_int32, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
                      C.POINTER(dq_plan_info), C.c_void_p, C.c_size_t, C.c_void_p, C.c_int32,
                      C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+    "dq_exchange_fused_workspace_bytes": ([C.POINTER(dq_config), C.c_int64, C.POINTER(dq_plan_info)],
+                                           C.c_size_t),
+    "dq_exchange_fused": ([C.POINTER(dq_config), C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
+                           C.POINTER(dq_plan_info), C.c_void_p, C.c_size_t, C.c_void_p, C.c_int32, C.c_void_p,
+                           C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+    "dq_barrier_selftest": ([C.c_int32, C.c_int32, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "dq_mx_message_bytes": ([C.c_int64], C.c_size_t),
     "dq_mx_quantize": ([C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p], C.c_int),
     "dq_mx_dequantize": ([C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p], C.c_int),
@@ -325,3 +333,30 @@ def dq_mx_exchange(n_ranks, butterfly, grads, n_blk, ws, ws_bytes, outs, log: La
                                 C.cast(op, C.c_void_p), C.cast(fin, C.c_void_p),
                                 C.byref(log.c) if log is not None else None, _stream(stream)), "dq_mx_exchange")
     return [fin[i] for i in range(n_ranks)]
+
+
+# ------------------------------------------------------------------ fused ring exchange
+def dq_exchange_fused_workspace_bytes(cfg, n_sg, info) -> int:
+    return lib().dq_exchange_fused_workspace_bytes(C.byref(cfg), n_sg, C.byref(info))
+
+
+def dq_exchange_fused(cfg, grads, n_sg, mu, perm, info, ws, ws_bytes, outs, status, out_is_bf16=False,
+                      log: LaunchLog = None, stream=None):
+    """The ring exchange in one cooperative launch.  ``status``: a device
+    int32 tensor that ends as DQ_DEVICE_OK (or DQ_DEVICE_BARRIER_TIMEOUT).
+    Returns the N device addresses of the final chunk messages."""
+    n = len(grads)
+    gp = (C.c_void_p * n)(*[_ptr(g) for g in grads])
+    op = (C.c_void_p * n)(*[_ptr(o) for o in outs])
+    fin = (C.c_void_p * n)()
+    _check(lib().dq_exchange_fused(C.byref(cfg), C.cast(gp, C.c_void_p), n_sg, _ptr(mu), _ptr(perm),
+                                   C.byref(info), _ptr(ws), ws_bytes, C.cast(op, C.c_void_p), int(out_is_bf16),
+                                   _ptr(status), C.cast(fin, C.c_void_p),
+                                   C.byref(log.c) if log is not None else None, _stream(stream)),
+           "dq_exchange_fused")
+    return [fin[i] for i in range(n)]
+
+
+def dq_barrier_selftest(n_blocks, missing, timeout_cycles, scratch, status, stream=None):
+    _check(lib().dq_barrier_selftest(n_blocks, missing, timeout_cycles, _ptr(scratch), _ptr(status),
+                                     _stream(stream)), "dq_barrier_selftest")

@@ -15,8 +15,10 @@ from .allreduce import DynamiQAllReduce
 
 
 class BucketedAllReduce:
-    def __init__(self, n_ranks: int, bucket_sg: int, *, overlap: bool = True, **kw):
-        self.n_ranks, self.bucket_sg, self.overlap = n_ranks, bucket_sg, overlap
+    def __init__(self, n_ranks: int, bucket_sg: int, *, overlap: bool = True, fused: bool = False, **kw):
+        """``fused``: each bucket's ring exchange as one cooperative launch
+        (dq_exchange_fused)."""
+        self.n_ranks, self.bucket_sg, self.overlap, self.fused = n_ranks, bucket_sg, overlap, fused
         self.sets = [DynamiQAllReduce(n_ranks, bucket_sg, **kw) for _ in range(2)]
         self.plan_stream = torch.cuda.Stream() if overlap else None
         self.ev_plan = [torch.cuda.Event(), torch.cuda.Event()]
@@ -43,7 +45,7 @@ class BucketedAllReduce:
         for k in range(len(buckets)):
             s = k & 1
             main.wait_event(self.ev_plan[s])
-            self.sets[s].exchange(buckets[k], outs[k], round=round0 + k)
+            self.sets[s].exchange(buckets[k], outs[k], round=round0 + k, fused=self.fused)
             self.ev_done[s].record(main)
             if k + 1 < len(buckets):
                 plan(k + 1)

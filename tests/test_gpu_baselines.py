@@ -96,6 +96,8 @@ def _check(gr, N, butterfly, B=5.0, eps=1.0, correlated=True, fixed_bits=0, scal
             continue
         m = ar.final_message(c).numpy()
         n2, n4, _ = oracle.range_counts(a, b, ar.info.n2, ar.info.n4)
+        if not scale_fp32:
+            assert np.all(m[b - a: -(-(b - a) // 16) * 16] == 0)   # zero E padding, as the oracle writes it
         for s in range(b - a):
             meta, blk = _final_meta_and_codes(m, b - a, n2, n4, s, scale_fp32)
             f = fin[a + s]
@@ -220,6 +222,7 @@ def test_mx_allreduce_bit_exact(N, butterfly):
         m = mx.final_message(c).numpy()
         pad = -(-(b - a) // 16) * 16
         assert np.array_equal(m[: b - a], fin[a:b, 0])
+        assert np.all(m[b - a: pad] == 0)                  # zero padding, as the oracle writes it
         assert np.array_equal(m[pad: pad + 32 * (b - a)].reshape(-1, 32), fin[a:b, 1:])
 
 
