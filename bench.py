@@ -46,6 +46,9 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=0, help="steps of the end-to-end timing (0: auto)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    p.add_argument("--exchange", choices=["auto", "fused", "multi"], default="auto",
+                   help="ring exchange as one cooperative launch (fused) or one launch per step (multi); "
+                        "auto: fused for rings of up to 16 ranks")
     p.add_argument("--bucket-pool", type=int, default=16,
                    help="streamed workloads: distinct buckets kept resident and cycled through a full pass")
     return p.parse_args(argv)
@@ -202,7 +205,8 @@ def launch_bytes(kind: int, sgs: int, msg_per_sg: float, fp32_addend: bool = Fal
     stats: bf16 gradient 512 B/SG + mean and squared norm 8 B/SG;
     allocate + reorder span: N x 8 B/SG of statistics read, M, F, mu written
     (12 B/SG), then about five passes over F (20 B/SG) and the bitwidths and
-    permutation (about 7 B/SG)."""
+    permutation (about 7 B/SG); fused ring exchange: the compress, N-1 DARs
+    and a decode that reads each message once and writes N outputs."""
     if kind == 0:
         return sgs * (512 + msg_per_sg + 8)
     if kind == 1:
@@ -211,6 +215,10 @@ def launch_bytes(kind: int, sgs: int, msg_per_sg: float, fp32_addend: bool = Fal
         return sgs * (msg_per_sg + 1024 + 8)
     if kind == 3:
         return sgs * (512 + 8)
+    if kind == 7:   # fused ring: sgs = J (N + 1); compress, N - 1 DARs, one decode read, N outputs
+        J = sgs / (n_ranks + 1)
+        return J * ((512 + msg_per_sg + 8) + (n_ranks - 1) * (2 * msg_per_sg + 512 + 8) +
+                    (msg_per_sg + 8 + 1024 * n_ranks))
     return sgs * (8 * n_ranks + 12 + 20 + 7)
 
 
@@ -278,64 +286,87 @@ def run_gpu(args, rank, world, local):
     ar = DynamiQAllReduce(N, J, budget=w.budget, correlated=w.correlated, butterfly=butterfly, seed=0)
     outs = ar.new_outputs()
     K, W = args.steps, max(args.warmup, 0)
+    fusable = not butterfly and N <= dq.MAX_FUSED_RANKS
+    fused = fusable if args.exchange == "auto" else (args.exchange == "fused")
+    if fused and not fusable:
+        raise SystemExit("the fused exchange covers rings of up to 16 ranks")
 
-    def step(i, log=None):
+    def step(i, log=None, fused=fused):
         ar.plan(grads, round=i, log=log)
-        ar.exchange(grads, outs, round=i, log=log)
+        ar.exchange(grads, outs, round=i, log=log, fused=fused)
 
-    clocks = ClockSampler(local).start()
+    def measure(fused_, steps, first, sample_clocks=False):
+        """Times `steps` rounds (CUDA events on the launching stream, a
+        barrier and a synchronize on both sides) and records every launch."""
+        log = dq.LaunchLog(steps * (6 * N + 12))
+        log.c.count = 0
+        torch.cuda.synchronize()
+        barrier(world, dev)
+        torch.cuda.synchronize()
+        n0 = dq.dq_launch_count()
+        clocks = ClockSampler(local).start() if sample_clocks else None
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        e0.record()
+        for i in range(steps):
+            step(first + i, log, fused_)
+        e1.record()
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier(world, dev)
+        if fused_:
+            ar.check_status()
+        clk = clocks.stop(t0, t1) if clocks else None
+        return e0.elapsed_time(e1) / steps, log, dq.dq_launch_count() - n0, clk
+
     for i in range(W):
         step(i)
     torch.cuda.synchronize()
-    log = dq.LaunchLog(K * (6 * N + 12))
-    log.c.count = 0
-    torch.cuda.synchronize()
-    barrier(world, dev)
-    torch.cuda.synchronize()
-    n_launch0 = dq.dq_launch_count()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0 = time.time()
-    e0.record()
-    for i in range(K):
-        step(W + i, log)
-    e1.record()
-    torch.cuda.synchronize()
-    t1 = time.time()
-    barrier(world, dev)
-    n_launch = dq.dq_launch_count() - n_launch0
-    clk = clocks.stop(t0, t1)
-    ms = e0.elapsed_time(e1) / K
+    ms, log, n_launch, clk = measure(fused, K, W, sample_clocks=True)
     ms_max = max_over_ranks(ms, world, dev)
 
     # per-launch times of the recorded kernels
     msg_total = stream_message_bytes(dq, ar.info, N)
     msg_per_sg = msg_total / J
-    per_kind = {}
-    for kind, sgs, t in log.launches():
-        d = per_kind.setdefault(kind, {"launches": 0, "ms": 0.0, "sgs": 0, "bytes": 0.0})
-        d["launches"] += 1
-        d["ms"] += t
-        d["sgs"] += sgs
-        d["bytes"] += launch_bytes(kind, sgs, msg_per_sg, fp32_addend=False, n_ranks=N)
-    names = {0: "compress", 1: "dar", 2: "decode", 3: "stats", 4: "allocate_reorder"}
-    peak, peak_kind = measured_peaks()
-    kernels = {}
-    for kind, d in per_kind.items():
-        avg_ms = d["ms"] / d["launches"]
-        gbs = d["bytes"] / d["launches"] / (avg_ms * 1e-3) / 1e9
-        kernels[names[kind]] = {"launches_per_step": d["launches"] / K, "avg_launch_ms": avg_ms,
-                                "share_of_step": d["ms"] / K / ms, "alg_bytes_per_launch": d["bytes"] / d["launches"],
-                                "achieved_gbs": gbs,
+    names = {0: "compress", 1: "dar", 2: "decode", 3: "stats", 4: "allocate_reorder", 7: "fused_ring"}
+
+    def per_kernel(log_, steps, ms_step):
+        per_kind = {}
+        for kind, sgs, t in log_.launches():
+            d = per_kind.setdefault(kind, {"launches": 0, "ms": 0.0, "sgs": 0, "bytes": 0.0})
+            d["launches"] += 1
+            d["ms"] += t
+            d["sgs"] += sgs
+            d["bytes"] += launch_bytes(kind, sgs, msg_per_sg, fp32_addend=False, n_ranks=N)
+        out = {}
+        for kind, d in per_kind.items():
+            avg_ms = d["ms"] / d["launches"]
+            gbs = d["bytes"] / d["launches"] / (avg_ms * 1e-3) / 1e9
+            out[names[kind]] = {"launches_per_step": d["launches"] / steps, "avg_launch_ms": avg_ms,
+                                "share_of_step": d["ms"] / steps / ms_step,
+                                "alg_bytes_per_launch": d["bytes"] / d["launches"], "achieved_gbs": gbs,
                                 "gcoords_per_s": d["sgs"] / d["launches"] * SG / (avg_ms * 1e-3) / 1e9}
+        return out
+
+    peak, peak_kind = measured_peaks()
+    kernels = per_kernel(log, K, ms)
+    kernels_multi = None
+    ms_multi = None
+    if fused:
+        # the per-step kernels of the multi-launch exchange, for the hop breakdown
+        step(W + K, None, False)
+        KM = max(3, min(K, 10))
+        ms_multi, log_m, _, _ = measure(False, KM, W + K + 1)
+        kernels_multi = per_kernel(log_m, KM, ms_multi)
     dominant = max((k for k in kernels if k != "allocate_reorder"), key=lambda k: kernels[k]["share_of_step"])
     dk = kernels[dominant]
     kname = {"compress": "hop_kernel<false,false>", "dar": "hop_kernel<true,false>", "decode": "decode_kernel",
-             "stats": "stats_kernel"}
+             "stats": "stats_kernel", "fused_ring": "fused_ring_kernel"}
     traffic, _ = ncu_counters(kname[dominant], w.name)
     roofline = {"bound": "hbm", "kernel": kname[dominant], "achieved": dk["achieved_gbs"], "peak": peak,
                 "unit": "GB/s", "frac": dk["achieved_gbs"] / peak, "peak_source": peak_kind,
                 "traffic": traffic, "alg_bytes_per_launch": dk["alg_bytes_per_launch"]}
-    dar = kernels.get("dar", {})
+    dar = (kernels_multi or kernels).get("dar", {})
     # The DAR hop is bound by instruction issue, not HBM: its issue roofline
     # (warp-instructions per super-group from the committed ncu capture,
     # times super-groups per launch, over the measured launch time) against
@@ -386,7 +417,7 @@ def run_gpu(args, rank, world, local):
         b = i & 1
         ar.plan(gbuf[b], round=i, ready=ev_in[b])
         main.wait_event(ev_out)
-        ar.exchange(gbuf[b], outs, round=i)
+        ar.exchange(gbuf[b], outs, round=i, fused=fused)
         ev_free[b].record(main)
         ev_dec.record(main)
         cout.wait_event(ev_dec)
@@ -432,7 +463,10 @@ def run_gpu(args, rank, world, local):
         "dar": {"gcoords_per_s_per_hop": dar.get("gcoords_per_s"), "achieved_gbs": dar.get("achieved_gbs"),
                 "hbm_frac": (dar["achieved_gbs"] / peak) if dar else None, "avg_launch_ms": dar.get("avg_launch_ms"),
                 "issue_roofline": dar_issue},
+        "exchange": "fused (one cooperative launch per round)" if fused else "one launch per step",
         "kernels": kernels,
+        "kernels_multi_launch": kernels_multi,
+        "ms_per_step_multi_launch": ms_multi,
         "roofline": roofline,
         "e2e": {"value": ms_e2e / (world * gb), "unit": UNIT, "h2d_bytes_per_step": N * J * SG * 2,
                 "d2h_bytes_per_step": J * SG * 4, "ms_per_step": ms_e2e},
