@@ -22,6 +22,7 @@ namespace {
 
 constexpr int kWarps = 4;       // warps per block
 constexpr int kStages = 2;      // pairs of super-groups in flight per warp
+constexpr int kHopBlocksPerSM = 5;  // register budget: up to 102 per thread (measured best)
 
 __shared__ __align__(16) Tables g_tab;
 
@@ -337,7 +338,7 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
 }
 
 template <bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32>
-__global__ void __launch_bounds__(kWarps * 32) hop_kernel(const __grid_constant__ HopParams P)
+__global__ void __launch_bounds__(kWarps * 32, kHopBlocksPerSM) hop_kernel(const __grid_constant__ HopParams P)
 {
     extern __shared__ __align__(16) uint8_t dyn[];
     block_copy(&g_tab, &P.tab);
