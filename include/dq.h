@@ -33,8 +33,10 @@
  *     (cudaGetLastError); nothing is launched when validation fails.
  *   - Calls on one stream are ordered; calls that share output buffers must
  *     not overlap on different streams.
- *   - Non-finite gradient values are outside the method's domain: results
- *     are unspecified (no fault, no hang).
+ *   - Non-finite gradient values are outside the method's domain.  dq_plan
+ *     detects them (they make a super-group's squared-norm sum F_j NaN or
+ *     infinite) and returns DQ_ERR_NONFINITE; the other entry points do not
+ *     check, and their results are then unspecified (no fault, no hang).
  */
 #ifndef DQ_H
 #define DQ_H
@@ -51,7 +53,10 @@ typedef enum {
     DQ_ERR_INVALID_ARG = 1,        /* null pointer, bad size, bad range, bad N   */
     DQ_ERR_ALIGNMENT = 2,          /* a pointer is not 16-byte aligned           */
     DQ_ERR_BUDGET_INFEASIBLE = 3,  /* budget below 2 bits per coordinate         */
-    DQ_ERR_CUDA = 4                /* a CUDA call or kernel launch failed        */
+    DQ_ERR_CUDA = 4,               /* a CUDA call or kernel launch failed        */
+    DQ_ERR_NONFINITE = 5           /* dq_plan: a super-group's statistics are not
+                                      finite (NaN or infinite gradient values, or
+                                      squares beyond the fp32 range)             */
 } dq_status;
 
 /* Parameters of one all-reduce round.  The last two fields, with eps and
@@ -240,7 +245,9 @@ size_t dq_plan_workspace_bytes(int32_t n_ranks, int64_t n_sg);
  *   be NULL): the statistics of rank r wait on event r, so a rank's
  *   statistics start as soon as its gradient is ready (e.g. its upload or
  *   its backward pass finished) while other ranks' are still in flight.
- *   log: NULL or a dq_launch_log to fill (see below). */
+ *   log: NULL or a dq_launch_log to fill (see below).
+ *   Returns DQ_ERR_NONFINITE (after the sync) when some M_j or F_j is not
+ *   finite; mu, perm and info are then not meaningful. */
 typedef struct dq_launch_log dq_launch_log;
 dq_status dq_plan(const dq_config *cfg, const void *const *grads_host, int64_t n_sg,
                   float *mu, int32_t *perm, void *plan_ws, size_t plan_ws_bytes,

@@ -354,6 +354,7 @@ const char *dq_status_string(dq_status s)
     case DQ_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
     case DQ_ERR_BUDGET_INFEASIBLE: return "budget below 2 bits per coordinate";
     case DQ_ERR_CUDA: return "CUDA error";
+    case DQ_ERR_NONFINITE: return "non-finite gradient statistics (NaN or infinite input)";
     }
     return "unknown status";
 }
@@ -608,7 +609,9 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
     uint8_t *b = w + L.b;
     float *T = reinterpret_cast<float *>(w + L.T);
     int64_t *counts = reinterpret_cast<int64_t *>(w + L.counts);
+    int32_t *nonfinite = reinterpret_cast<int32_t *>(w + L.counts + 32);   // inside the counts slot
     void *scratch = w + L.scratch;
+    if (cudaMemsetAsync(nonfinite, 0, sizeof(int32_t), st) != cudaSuccess) return DQ_ERR_CUDA;
     if (rank_ready) {  // one launch per rank, each after its rank's event
         for (int32_t r = 0; r < N; ++r) {
             if (rank_ready[r] && cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(rank_ready[r]), 0) != cudaSuccess)
@@ -635,7 +638,8 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
         }
     }
     const LogSlot slot = log_begin(log, DQ_LAUNCH_ALLOCATE_REORDER, n_sg, st);
-    if (launch_stats_reduce(mean_all, sq_all, N, n_sg, M, F, mu, st) != cudaSuccess) return DQ_ERR_CUDA;
+    if (launch_stats_reduce(mean_all, sq_all, N, n_sg, M, F, mu, st, nonfinite) != cudaSuccess) return DQ_ERR_CUDA;
+    int32_t h_nonfinite = 0;
     if (cfg->fixed_bits) {
         // uniform-bitwidth ablation: every super-group gets fixed_bits (the
         // reorder of a uniform allocation is the identity permutation)
@@ -643,7 +647,10 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
         const dq_status s = dq_reorder(b, n_sg, perm, scratch, plan_scratch_bytes(n_sg), stream);
         if (s != DQ_OK) return s;
         log_end(slot, st);
+        if (cudaMemcpyAsync(&h_nonfinite, nonfinite, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+            return DQ_ERR_CUDA;
         if (cudaStreamSynchronize(st) != cudaSuccess) return DQ_ERR_CUDA;
+        if (h_nonfinite) return DQ_ERR_NONFINITE;
         info->T = NAN;
         info->n2 = cfg->fixed_bits == 2 ? n_sg : 0;
         info->n4 = cfg->fixed_bits == 4 ? n_sg : 0;
@@ -655,11 +662,13 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
     s = dq_reorder(b, n_sg, perm, scratch, plan_scratch_bytes(n_sg), stream);
     if (s != DQ_OK) return s;
     log_end(slot, st);
-    int64_t hc[3];
+    int64_t hc[5];   // counts[3], padding, the non-finite flag
     float hT = 0.0f;
     if (cudaMemcpyAsync(hc, counts, sizeof(hc), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DQ_ERR_CUDA;
     if (cudaMemcpyAsync(&hT, T, sizeof(hT), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DQ_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return DQ_ERR_CUDA;
+    memcpy(&h_nonfinite, reinterpret_cast<const uint8_t *>(hc) + 32, sizeof(int32_t));
+    if (h_nonfinite) return DQ_ERR_NONFINITE;
     info->T = hT;
     info->n2 = hc[0];
     info->n4 = hc[1];

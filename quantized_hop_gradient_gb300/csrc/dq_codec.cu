@@ -100,11 +100,15 @@ __global__ void __launch_bounds__(256) stats_batched_kernel(const __grid_constan
 }
 
 // Metadata all-reduce: M_j and F_j summed over ranks 0..N-1 in order, and
-// the mean every worker subtracts, mu_j = fl(M_j / N).
+// the mean every worker subtracts, mu_j = fl(M_j / N).  `nonfinite`
+// (optional) is set to 1 when some M_j or F_j is not finite: a NaN or
+// infinite gradient value, or squares or sums beyond the fp32 range, which
+// the allocation cannot take.
 __global__ void __launch_bounds__(256) stats_reduce_kernel(const float *__restrict__ mean_all,
                                                            const float *__restrict__ sq_all, int32_t n,
                                                            int64_t n_sg, float *__restrict__ M,
-                                                           float *__restrict__ F, float *__restrict__ mu)
+                                                           float *__restrict__ F, float *__restrict__ mu,
+                                                           int32_t *__restrict__ nonfinite)
 {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const float nf = (float)n;
@@ -117,6 +121,7 @@ __global__ void __launch_bounds__(256) stats_reduce_kernel(const float *__restri
         if (M) M[j] = m;
         F[j] = f;
         mu[j] = __fdiv_rn(m, nf);
+        if (nonfinite && !(isfinite(m) && isfinite(f))) atomicOr(nonfinite, 1);
     }
 }
 
@@ -146,12 +151,12 @@ cudaError_t launch_stats_batched(const StatsParams &S, cudaStream_t st)
 }
 
 cudaError_t launch_stats_reduce(const float *mean_all, const float *sq_all, int32_t n, int64_t n_sg,
-                                float *M, float *F, float *mu, cudaStream_t st)
+                                float *M, float *F, float *mu, cudaStream_t st, int32_t *nonfinite)
 {
     int64_t blocks = (n_sg + 255) / 256;
     const int64_t cap = (int64_t)sm_count() * 8;
     blocks = blocks < 1 ? 1 : (blocks < cap ? blocks : cap);
-    stats_reduce_kernel<<<(int)blocks, 256, 0, st>>>(mean_all, sq_all, n, n_sg, M, F, mu);
+    stats_reduce_kernel<<<(int)blocks, 256, 0, st>>>(mean_all, sq_all, n, n_sg, M, F, mu, nonfinite);
     note_launches(1);
     return cudaGetLastError();
 }

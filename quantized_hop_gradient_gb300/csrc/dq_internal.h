@@ -21,7 +21,7 @@ size_t msg_bytes(int64_t c, int64_t n2, int64_t n4, int64_t n8, bool scale_fp32)
 cudaError_t launch_stats(const uint16_t *g, int64_t n_sg, float *mean, float *sq, cudaStream_t st);
 cudaError_t launch_stats_batched(const StatsParams &S, cudaStream_t st);
 cudaError_t launch_stats_reduce(const float *mean_all, const float *sq_all, int32_t n, int64_t n_sg,
-                                float *M, float *F, float *mu, cudaStream_t st);
+                                float *M, float *F, float *mu, cudaStream_t st, int32_t *nonfinite = nullptr);
 cudaError_t launch_hop(const HopParams &P, bool has_in, bool add_f32, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams &P, cudaStream_t st);
 // Cooperative launches (every CTA resident): the fused ring exchange, and a

@@ -19,7 +19,7 @@ import torch
 from . import build as _build
 
 SG = 256
-DQ_OK, DQ_ERR_INVALID_ARG, DQ_ERR_ALIGNMENT, DQ_ERR_BUDGET_INFEASIBLE, DQ_ERR_CUDA = range(5)
+DQ_OK, DQ_ERR_INVALID_ARG, DQ_ERR_ALIGNMENT, DQ_ERR_BUDGET_INFEASIBLE, DQ_ERR_CUDA, DQ_ERR_NONFINITE = range(6)
 
 _lock = threading.Lock()
 _lib = None
@@ -33,6 +33,10 @@ class DQError(RuntimeError):
 
 class BudgetInfeasible(DQError):
     pass
+
+
+class NonFinite(DQError):
+    """dq_plan found a NaN or infinite super-group statistic."""
 
 
 class dq_config(C.Structure):
@@ -141,6 +145,8 @@ def status_string(s: int) -> str:
 def _check(status: int, what: str):
     if status == DQ_ERR_BUDGET_INFEASIBLE:
         raise BudgetInfeasible(status, what)
+    if status == DQ_ERR_NONFINITE:
+        raise NonFinite(status, what)
     if status != DQ_OK:
         raise DQError(status, what)
 

@@ -37,6 +37,7 @@ def test_exports_every_declared_entry_point(L):
 def test_version_and_status_strings(L):
     assert "sm_103a" in dq.dq_version()
     assert dq.status_string(dq.DQ_ERR_BUDGET_INFEASIBLE).startswith("budget")
+    assert "non-finite" in dq.status_string(dq.DQ_ERR_NONFINITE)
 
 
 @pytest.mark.parametrize("eps", [1.0, 0.25, 0.5, 3.7, 4.0, math.inf])

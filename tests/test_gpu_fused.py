@@ -123,3 +123,18 @@ def test_barrier_timeout_reports_status_and_context_survives():
     assert int(scratch[0].item()) == n
     # the context is still usable: a fused exchange right after is correct
     test_fused_is_one_launch()
+
+
+def test_plan_reports_nonfinite_gradients():
+    """A NaN, an infinity, or values whose squares overflow fp32 make the
+    plan fail with DQ_ERR_NONFINITE; a clean plan afterwards succeeds."""
+    N, J = 4, 300
+    gr = grads_for("ring4_1m", 256 * J, N, seed=3)
+    ar = DynamiQAllReduce(N, J)
+    for bad in (float("nan"), float("inf"), -float("inf"), 3.0e38):
+        gd = [dev_u16(g) for g in gr]
+        gd[2][256 * 123 + 7] = bad
+        with pytest.raises(dq.NonFinite):
+            ar.plan(gd)
+    ar.plan([dev_u16(g) for g in gr])
+    assert ar.info.n2 + ar.info.n4 + ar.info.n8 == J
