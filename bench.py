@@ -163,10 +163,24 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+# The device code of each profiled kernel: its own file plus the shared
+# definitions (the launch parameters and tables come from the host files, so
+# those count too where they shape the kernel's work).
+KERNEL_SOURCES = {
+    "hop_kernel": ["dq_common.cuh", "dq_hop.cu"],
+    "decode_kernel": ["dq_common.cuh", "dq_hop.cu"],
+    "fused_ring_kernel": ["dq_common.cuh", "dq_hop.cu"],
+    "stats_kernel": ["dq_common.cuh", "dq_codec.cu"],
+    "mx_hop_kernel": ["dq_common.cuh", "dq_mx.cu"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """sha256 prefix of the files that define `kernel` (its name before any
+    template arguments)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_hop_gradient_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel.split("<")[0]]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:12]
@@ -179,7 +193,7 @@ def ncu_counters(kernel: str, workload: str):
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None, None
-    want = kernel_source_hash()
+    want = kernel_source_hash(kernel)
     with open(p) as f:
         for line in f:
             parts = line.split()
