@@ -48,7 +48,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     p.add_argument("--exchange", choices=["auto", "fused", "multi"], default="auto",
                    help="ring exchange as one cooperative launch (fused) or one launch per step (multi); "
-                        "auto: fused for rings of up to 16 ranks")
+                        "auto: fused where it is the faster path (rings of up to 16 ranks, up to 2^19 "
+                        "super-groups per worker)")
     p.add_argument("--bucket-pool", type=int, default=16,
                    help="streamed workloads: distinct buckets kept resident and cycled through a full pass")
     return p.parse_args(argv)
@@ -215,7 +216,8 @@ def launch_bytes(kind: int, sgs: int, msg_per_sg: float, fp32_addend: bool = Fal
     input byte read once and every output byte written once, nothing else.
     compress: bf16 gradient 512 B/SG + message out + mean and perm 8 B/SG;
     DAR: message in + addend (512 B/SG bf16, 1 KiB fp32) + message out + 8 B/SG;
-    decode: message in + fp32 output 1 KiB/SG + 8 B/SG;
+    decode: fp32 output 1 KiB per super-group written, message in + 8 B per
+    super-group read (once for up to 16 outputs);
     stats: bf16 gradient 512 B/SG + mean and squared norm 8 B/SG;
     allocate + reorder span: N x 8 B/SG of statistics read, M, F, mu written
     (12 B/SG), then about five passes over F (20 B/SG) and the bitwidths and
@@ -225,8 +227,8 @@ def launch_bytes(kind: int, sgs: int, msg_per_sg: float, fp32_addend: bool = Fal
         return sgs * (512 + msg_per_sg + 8)
     if kind == 1:
         return sgs * (2 * msg_per_sg + (1024 if fp32_addend else 512) + 8)
-    if kind == 2:
-        return sgs * (msg_per_sg + 1024 + 8)
+    if kind == 2:   # sgs = super-groups written; each launch reads a message once for up to 16 outputs
+        return sgs * 1024 + sgs / min(n_ranks, 16) * (msg_per_sg + 8)
     if kind == 3:
         return sgs * (512 + 8)
     if kind == 7:   # fused ring: sgs = J (N + 1); compress, N - 1 DARs, one decode read, N outputs
@@ -281,7 +283,7 @@ def run_gpu(args, rank, world, local):
     import torch
 
     from quantized_hop_gradient_gb300 import dq, synth
-    from quantized_hop_gradient_gb300.allreduce import DynamiQAllReduce
+    from quantized_hop_gradient_gb300.allreduce import DynamiQAllReduce, use_fused
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the CUDA path has no CPU fallback)")
@@ -301,7 +303,7 @@ def run_gpu(args, rank, world, local):
     outs = ar.new_outputs()
     K, W = args.steps, max(args.warmup, 0)
     fusable = not butterfly and N <= dq.MAX_FUSED_RANKS
-    fused = fusable if args.exchange == "auto" else (args.exchange == "fused")
+    fused = use_fused(N, butterfly, J) if args.exchange == "auto" else (args.exchange == "fused")
     if fused and not fusable:
         raise SystemExit("the fused exchange covers rings of up to 16 ranks")
 
@@ -562,7 +564,8 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
     bucket_sg = w.bucket // SG
     kw = dict(budget=w.budget, correlated=w.correlated, butterfly=w.topology == "butterfly", seed=0)
     # rings of up to 16 ranks run each bucket's exchange as one cooperative launch
-    fusable = w.topology == "ring" and N <= dq.MAX_FUSED_RANKS
+    from quantized_hop_gradient_gb300.allreduce import use_fused
+    fusable = use_fused(N, w.topology == "butterfly", bucket_sg)
     ov = BucketedAllReduce(N, bucket_sg, overlap=True, fused=fusable, **kw)
     ml = BucketedAllReduce(N, bucket_sg, overlap=True, fused=False, **kw)
     sq = BucketedAllReduce(N, bucket_sg, overlap=False, fused=False, **kw)

@@ -257,7 +257,9 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads_host, int64_t n
 /* Optional record of the kernel launches of dq_plan and dq_exchange, for timing them on
  * the launching stream.  events: host array of 2*capacity cudaEvent_t created
  * by the caller (timing enabled); launch i is bracketed by events[2i] and
- * events[2i+1].  kinds[i]: DQ_LAUNCH_*; sgs[i]: super-groups it processed.
+ * events[2i+1].  kinds[i]: DQ_LAUNCH_*; sgs[i]: super-groups it processed
+ * (a decode launch counts each super-group once per output it writes: the
+ * exchange decodes each chunk once into up to 16 ranks' outputs).
  * count: in, first free slot; out, slots used.  Launches beyond capacity
  * are not recorded (they still run). */
 enum { DQ_LAUNCH_COMPRESS = 0, DQ_LAUNCH_DAR = 1, DQ_LAUNCH_DECODE = 2, DQ_LAUNCH_STATS = 3,

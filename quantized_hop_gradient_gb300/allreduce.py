@@ -13,6 +13,18 @@ from . import dq
 
 SG = dq.SG
 
+# Largest per-worker size (super-groups) at which the fused ring exchange is
+# the faster one on a GB300: measured equal-or-better up to 2^26 coordinates
+# per worker (0.37 vs 0.50 ms at 2^22, 1.81 vs 1.91 ms at 2^26), 6-7% slower
+# at 3.4e8 and 1e9 coordinates, where launches are few and the separate
+# decode kernel, with more warps per SM, streams its outputs faster.
+FUSED_MAX_SG = 1 << 19
+
+
+def use_fused(n_ranks: int, butterfly: bool, n_sg: int) -> bool:
+    """Whether the ring exchange should run as one cooperative launch."""
+    return (not butterfly) and n_ranks <= dq.MAX_FUSED_RANKS and n_sg <= FUSED_MAX_SG
+
 
 class DynamiQAllReduce:
     def __init__(self, n_ranks: int, n_sg: int, *, budget: float = 5.0, eps: float = 1.0,
@@ -58,12 +70,15 @@ class DynamiQAllReduce:
         if self.ws.numel() < nbytes:
             self.ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
 
-    def exchange(self, grads, outs, round: int = 0, stream=None, log=None, fused: bool = False):
-        """``fused``: the ring exchange as one cooperative launch (ring, at
-        most 16 ranks); its device status is in ``self.status`` (check with
-        ``check_status`` after synchronising)."""
+    def exchange(self, grads, outs, round: int = 0, stream=None, log=None, fused=False):
+        """``fused``: True runs the ring exchange as one cooperative launch
+        (ring, at most 16 ranks), "auto" does so where that is the faster
+        path (``use_fused``); its device status is in ``self.status`` (check
+        with ``check_status`` after synchronising)."""
         cfg = self.config(round)
         n_sg = getattr(self, "cur_sg", self.n_sg)
+        if fused == "auto":
+            fused = use_fused(self.n_ranks, self.butterfly, n_sg)
         bf16 = self.out_dtype == torch.bfloat16
         if fused:
             if self.butterfly:

@@ -309,7 +309,7 @@ cudaError_t run_decodes(DecodeParams &D, const std::vector<PendingDecode> &chunk
             t.out = c.out;
             t.lo = c.lo;
             units += set_units(t, c.lo, c.hi, end2, end4, units);
-            sgs += c.hi - c.lo;
+            sgs += (c.hi - c.lo) * std::max(1, D.n_outs);   // super-groups written
         }
         D.n_tasks = n;
         D.total_units = units;
@@ -741,16 +741,19 @@ dq_status dq_exchange(const dq_config *cfg, int32_t butterfly, const void *const
         if (run_hops(*P, tasks, end2, end4, step.has_in, step.add_f32, st, log) != cudaSuccess) return DQ_ERR_CUDA;
     }
 
-    // All-gather hands the final chunks to every rank unchanged; each rank
-    // decodes all of them into its own output: (rank, chunk) pairs in
-    // launches of up to kMaxTasks tasks.
+    // All-gather hands the final chunks to every rank unchanged; every rank
+    // decodes all of them into its own output.  Each launch reads the chunk
+    // messages once and writes up to kMaxDecodeOuts ranks' outputs.
     std::vector<const uint8_t *> fin((size_t)N, nullptr);
     for (int32_t c = 0; c < N; ++c) fin[c] = msg(X.S.fin_rank[c], X.S.fin_par[c]);
     std::vector<PendingDecode> chunks;
-    for (int32_t r = 0; r < N; ++r)
-        for (int32_t c = 0; c < N; ++c) chunks.push_back(PendingDecode{fin[c], lo[c], lo[c + 1], outs[r]});
+    for (int32_t c = 0; c < N; ++c) chunks.push_back(PendingDecode{fin[c], lo[c], lo[c + 1], nullptr});
     std::unique_ptr<DecodeParams> D = decode_params(cfg, mu, perm, out_is_bf16, P->tab);
-    if (run_decodes(*D, chunks, end2, end4, st, log) != cudaSuccess) return DQ_ERR_CUDA;
+    for (int32_t r0 = 0; r0 < N; r0 += kMaxDecodeOuts) {
+        D->n_outs = std::min(N - r0, kMaxDecodeOuts);
+        for (int32_t i = 0; i < D->n_outs; ++i) D->outs[i] = outs[r0 + i];
+        if (run_decodes(*D, chunks, end2, end4, st, log) != cudaSuccess) return DQ_ERR_CUDA;
+    }
     if (final_msgs)
         for (int32_t c = 0; c < N; ++c) final_msgs[c] = fin[c];
     return DQ_OK;

@@ -110,6 +110,8 @@ struct DecodeTask {
     int64_t unit_begin[4];
 };
 
+constexpr int kMaxDecodeOuts = 16;
+
 struct DecodeParams {
     Tables tab;
     DecodeTask task[kMaxTasks];
@@ -120,6 +122,10 @@ struct DecodeParams {
     const int32_t *perm;
     int32_t out_is_bf16;
     int32_t scale_fp32;
+    // n_outs > 0: every task is decoded into all of outs[0..n_outs) (one
+    // read of the message, n_outs writes) and the tasks' `out` is unused
+    int32_t n_outs;
+    void *outs[kMaxDecodeOuts];
 };
 
 // Statistics of several ranks in one launch.

@@ -485,9 +485,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kernel(const __grid_
         const int64_t j0 = t.seg_lo[seg] + (u - t.unit_begin[seg]) * kUnit;
         const int64_t rem = t.seg_hi[seg] - j0;
         const int cnt = (int)(rem < kUnit ? rem : kUnit);
-        if (seg == 0) decode_unit<2, SF32>(P, t.msg, t.lo, &t.out, 1, j0, cnt, lane);
-        else if (seg == 1) decode_unit<4, SF32>(P, t.msg, t.lo, &t.out, 1, j0, cnt, lane);
-        else decode_unit<8, SF32>(P, t.msg, t.lo, &t.out, 1, j0, cnt, lane);
+        void *const *outs = P.n_outs > 0 ? P.outs : &t.out;
+        const int n_outs = P.n_outs > 0 ? P.n_outs : 1;
+        if (seg == 0) decode_unit<2, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane);
+        else if (seg == 1) decode_unit<4, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane);
+        else decode_unit<8, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane);
     }
 }
 

@@ -138,3 +138,23 @@ def test_plan_reports_nonfinite_gradients():
             ar.plan(gd)
     ar.plan([dev_u16(g) for g in gr])
     assert ar.info.n2 + ar.info.n4 + ar.info.n8 == J
+
+
+def test_multi_launch_exchange_structure():
+    """Ring of 8 through dq_exchange: one compress launch, seven DAR launches
+    and one decode launch that reads each chunk once and writes all eight
+    outputs (its log entry counts J super-groups per output)."""
+    N = 8
+    gr = grads_for("ring4_1m", 256 * 400, N, seed=2)
+    J = gr[0].size // 256
+    ar = DynamiQAllReduce(N, J)
+    gd = [dev_u16(g) for g in gr]
+    outs = ar.new_outputs()
+    ar.plan(gd)
+    torch.cuda.synchronize()
+    log = dq.LaunchLog(32)
+    ar.exchange(gd, outs, log=log)
+    torch.cuda.synchronize()
+    got = log.launches()
+    assert [k for k, _, _ in got] == [dq.DQ_LAUNCH_COMPRESS] + [dq.DQ_LAUNCH_DAR] * 7 + [dq.DQ_LAUNCH_DECODE]
+    assert got[-1][1] == J * N
