@@ -872,3 +872,8 @@ dq_status dq_barrier_selftest(int32_t n_blocks, int32_t missing, int64_t timeout
 }
 
 }  // extern "C"
+
+// Kernel parameters are limited to 32,764 bytes.
+static_assert(sizeof(dq::HopParams) <= 32764, "HopParams exceeds the kernel parameter limit");
+static_assert(sizeof(dq::DecodeParams) <= 32764, "DecodeParams exceeds the kernel parameter limit");
+static_assert(sizeof(dq::FusedRingParams) <= 32764, "FusedRingParams exceeds the kernel parameter limit");

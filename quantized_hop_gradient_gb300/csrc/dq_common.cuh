@@ -264,8 +264,3 @@ __device__ __forceinline__ void locate_unit(const Task *tasks, int n_tasks, int6
 }
 
 }  // namespace dq
-
-// Kernel parameters are limited to 32,764 bytes.
-static_assert(sizeof(dq::HopParams) <= 32764, "HopParams exceeds the kernel parameter limit");
-static_assert(sizeof(dq::DecodeParams) <= 32764, "DecodeParams exceeds the kernel parameter limit");
-static_assert(sizeof(dq::FusedRingParams) <= 32764, "FusedRingParams exceeds the kernel parameter limit");
