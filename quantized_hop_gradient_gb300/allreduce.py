@@ -70,7 +70,7 @@ class DynamiQAllReduce:
         if self.ws.numel() < nbytes:
             self.ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
 
-    def exchange(self, grads, outs, round: int = 0, stream=None, log=None, fused=False):
+    def exchange(self, grads, outs, round: int = 0, stream=None, log=None, fused="auto"):
         """``fused``: True runs the ring exchange as one cooperative launch
         (ring, at most 16 ranks), "auto" does so where that is the faster
         path (``use_fused``); its device status is in ``self.status`` (check
@@ -108,7 +108,7 @@ class DynamiQAllReduce:
         return [torch.empty(self.n_sg * SG, dtype=self.out_dtype, device=self.device)
                 for _ in range(self.n_ranks)]
 
-    def __call__(self, grads, round: int = 0, outs=None, stream=None, fused: bool = False):
+    def __call__(self, grads, round: int = 0, outs=None, stream=None, fused="auto"):
         if len(grads) != self.n_ranks:
             raise ValueError("one gradient per rank")
         if outs is None:

@@ -384,10 +384,6 @@ template <int BITS, bool SF32, typename PP>
 __device__ __forceinline__ void decode_unit(const PP &P, const MsgView &msg, int64_t lo, void *const *outs,
                                             int n_outs, int64_t j0, int cnt, int lane)
 {
-    struct {
-        const MsgView &msg;
-        int64_t lo;
-    } t{msg, lo};
     constexpr int kAhead = 8;
     int32_t old_i = 0;
     float mu_i = 0.0f;
@@ -395,7 +391,7 @@ __device__ __forceinline__ void decode_unit(const PP &P, const MsgView &msg, int
     if (lane < cnt) {
         old_i = __ldg(P.perm + j0 + lane);
         mu_i = __ldg(P.mu + old_i);
-        if (!SF32) ein_i = __ldcg(t.msg.base + (j0 + lane - t.lo));
+        if (!SF32) ein_i = __ldcg(msg.base + (j0 + lane - lo));
     }
     const float nr = (float)P.n_ranks;
     const float *q = Lvl<BITS>::q();
@@ -406,16 +402,16 @@ __device__ __forceinline__ void decode_unit(const PP &P, const MsgView &msg, int
         for (int a = 0; a < kAhead; ++a) {
             ca[a] = cb[a] = ua[a] = ub[a] = 0u;
             if (s0 + a < cnt) {
-                const int64_t sl = j0 + s0 + a - t.lo;
-                const uint8_t *blk = code_block<BITS>(t.msg, sl);
+                const int64_t sl = j0 + s0 + a - lo;
+                const uint8_t *blk = code_block<BITS>(msg, sl);
                 ca[a] = ldg_codes4<BITS>(blk, lane);
                 cb[a] = ldg_codes4<BITS>(blk, 32 + lane);
                 if (SF32) {   // bits of the fp32 scales of groups g0 and 8 + g0
-                    const uint32_t *sg = reinterpret_cast<const uint32_t *>(t.msg.base + t.msg.off_u + sl * 64);
+                    const uint32_t *sg = reinterpret_cast<const uint32_t *>(msg.base + msg.off_u + sl * 64);
                     ua[a] = __ldcg(sg + g0);
                     ub[a] = __ldcg(sg + 8 + g0);
                 } else {
-                    const uint8_t *ub8 = t.msg.base + t.msg.off_u + sl * 16;
+                    const uint8_t *ub8 = msg.base + msg.off_u + sl * 16;
                     ua[a] = __ldcg(ub8 + g0);
                     ub[a] = __ldcg(ub8 + 8 + g0);
                 }

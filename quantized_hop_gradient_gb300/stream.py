@@ -15,9 +15,9 @@ from .allreduce import DynamiQAllReduce
 
 
 class BucketedAllReduce:
-    def __init__(self, n_ranks: int, bucket_sg: int, *, overlap: bool = True, fused: bool = False, **kw):
+    def __init__(self, n_ranks: int, bucket_sg: int, *, overlap: bool = True, fused="auto", **kw):
         """``fused``: each bucket's ring exchange as one cooperative launch
-        (dq_exchange_fused)."""
+        (dq_exchange_fused): True, False, or "auto" (where it is faster)."""
         self.n_ranks, self.bucket_sg, self.overlap, self.fused = n_ranks, bucket_sg, overlap, fused
         self.sets = [DynamiQAllReduce(n_ranks, bucket_sg, **kw) for _ in range(2)]
         self.plan_stream = torch.cuda.Stream() if overlap else None

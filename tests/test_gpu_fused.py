@@ -153,7 +153,7 @@ def test_multi_launch_exchange_structure():
     ar.plan(gd)
     torch.cuda.synchronize()
     log = dq.LaunchLog(32)
-    ar.exchange(gd, outs, log=log)
+    ar.exchange(gd, outs, log=log, fused=False)
     torch.cuda.synchronize()
     got = log.launches()
     assert [k for k, _, _ in got] == [dq.DQ_LAUNCH_COMPRESS] + [dq.DQ_LAUNCH_DAR] * 7 + [dq.DQ_LAUNCH_DECODE]
