@@ -48,7 +48,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     p.add_argument("--exchange", choices=["auto", "fused", "multi"], default="auto",
                    help="ring exchange as one cooperative launch (fused) or one launch per step (multi); "
-                        "auto: fused where it is the faster path (rings of up to 16 ranks, up to 2^19 "
+                        "auto: fused where it is the faster path (rings of up to 64 ranks, up to 2^19 "
                         "super-groups per worker)")
     p.add_argument("--bucket-pool", type=int, default=16,
                    help="streamed workloads: distinct buckets kept resident and cycled through a full pass")
@@ -305,7 +305,7 @@ def run_gpu(args, rank, world, local):
     fusable = not butterfly and N <= dq.MAX_FUSED_RANKS
     fused = use_fused(N, butterfly, J) if args.exchange == "auto" else (args.exchange == "fused")
     if fused and not fusable:
-        raise SystemExit("the fused exchange covers rings of up to 16 ranks")
+        raise SystemExit("the fused exchange covers rings of up to 64 ranks")
 
     def step(i, log=None, fused=fused):
         ar.plan(grads, round=i, log=log)
@@ -563,7 +563,7 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
     seq_out = [outs_pool[i % len(full)] for i in range(nb - 1)] + [outs_pool[-1]]
     bucket_sg = w.bucket // SG
     kw = dict(budget=w.budget, correlated=w.correlated, butterfly=w.topology == "butterfly", seed=0)
-    # rings of up to 16 ranks run each bucket's exchange as one cooperative launch
+    # rings of up to 64 ranks run each bucket's exchange as one cooperative launch
     from quantized_hop_gradient_gb300.allreduce import use_fused
     fusable = use_fused(N, w.topology == "butterfly", bucket_sg)
     ov = BucketedAllReduce(N, bucket_sg, overlap=True, fused=fusable, **kw)

@@ -302,7 +302,7 @@ dq_status dq_exchange(const dq_config *cfg, int32_t butterfly, const void *const
 #define DQ_DEVICE_OK 0
 #define DQ_DEVICE_BARRIER_TIMEOUT 1   /* a grid-barrier wait ran out; outputs are invalid */
 
-/* Device bytes dq_exchange_fused needs (ring; 1 <= N <= 16), 0 otherwise. */
+/* Device bytes dq_exchange_fused needs (ring; 1 <= N <= 64), 0 otherwise. */
 size_t dq_exchange_fused_workspace_bytes(const dq_config *cfg, int64_t n_sg, const dq_plan_info *info);
 
 /* The ring exchange of dq_exchange (same results, bit for bit) as ONE
@@ -311,7 +311,7 @@ size_t dq_exchange_fused_workspace_bytes(const dq_config *cfg, int64_t n_sg, con
  * boundaries [S "Key idea and contribution": hop-by-hop fused decompress-
  * accumulate-recompress; the barrier replaces the network hand-off].  It
  * removes the per-step launches, which dominate small buckets.
- *   Ring only, 1 <= N <= 16; arguments as for dq_exchange; ws of
+ *   Ring only, 1 <= N <= 64; arguments as for dq_exchange; ws of
  *   dq_exchange_fused_workspace_bytes bytes.
  *   status_dev: device int32 (4-byte aligned), set to DQ_DEVICE_OK before
  *   the launch; every barrier wait is bounded (about a second of SM

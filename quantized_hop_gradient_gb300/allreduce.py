@@ -72,7 +72,7 @@ class DynamiQAllReduce:
 
     def exchange(self, grads, outs, round: int = 0, stream=None, log=None, fused="auto"):
         """``fused``: True runs the ring exchange as one cooperative launch
-        (ring, at most 16 ranks), "auto" does so where that is the faster
+        (ring, at most 64 ranks), "auto" does so where that is the faster
         path (``use_fused``); its device status is in ``self.status`` (check
         with ``check_status`` after synchronising)."""
         cfg = self.config(round)

@@ -142,7 +142,7 @@ struct StatsParams {
 // steps and the final decode, separated by grid barriers.  Chunk c's
 // message layout, units and range are the same at every step; only the
 // message buffers and the quantizing rank rotate.
-constexpr int kMaxFusedRanks = 16;
+constexpr int kMaxFusedRanks = 64;
 constexpr int32_t kDeviceBarrierTimeout = 1;   // status word: a barrier wait ran out
 
 struct FusedRingParams {

@@ -61,7 +61,7 @@ class dq_launch_log(C.Structure):
 DQ_LAUNCH_COMPRESS, DQ_LAUNCH_DAR, DQ_LAUNCH_DECODE, DQ_LAUNCH_STATS, DQ_LAUNCH_ALLOCATE_REORDER = 0, 1, 2, 3, 4
 DQ_LAUNCH_MX_HOP, DQ_LAUNCH_MX_DECODE, DQ_LAUNCH_FUSED_RING = 5, 6, 7
 DQ_DEVICE_OK, DQ_DEVICE_BARRIER_TIMEOUT = 0, 1
-MAX_FUSED_RANKS = 16
+MAX_FUSED_RANKS = 64
 
 
 class dq_plan_info(C.Structure):

@@ -111,8 +111,8 @@ def test_bad_arguments_rejected_on_the_host(L):
     assert L.dq_mx_quantize(P + 4, 8, P, st) == dq.DQ_ERR_ALIGNMENT
     assert L.dq_mx_dequantize(P, 8, None, st) == dq.DQ_ERR_INVALID_ARG
     assert L.dq_mx_exchange(3, 1, P, 10, P, 1 << 20, P, None, None, st) == dq.DQ_ERR_INVALID_ARG
-    # fused exchange: ring of at most 16 ranks, a status word is required
-    assert dq.dq_exchange_fused_workspace_bytes(dq.config(17), 3, info) == 0
+    # fused exchange: ring of at most 64 ranks, a status word is required
+    assert dq.dq_exchange_fused_workspace_bytes(dq.config(65), 3, info) == 0
     assert dq.dq_exchange_fused_workspace_bytes(dq.config(3), 3, info) > dq.dq_exchange_workspace_bytes(
         dq.config(3), False, 3, info)
     assert L.dq_exchange_fused(dq.config(3), P, 3, P, P, info, P, 1 << 30, P, 0, None, None, None,

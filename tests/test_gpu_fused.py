@@ -52,7 +52,7 @@ def _run(gr, N, fused, **kw):
     return ar, [o.cpu() for o in outs], msgs, lo
 
 
-@pytest.mark.parametrize("N", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("N", [1, 2, 3, 8, 16, 33, 64])
 def test_fused_equals_oracle_and_multi_launch(N):
     gr = grads_for("bert_large_ring8", 256 * 700 + 13, N, seed=N)
     ar, outs, msgs, lo = _run(gr, N, True, budget=5.0, correlated=True)
@@ -100,11 +100,11 @@ def test_fused_is_one_launch():
 
 
 def test_fused_rejects_what_it_does_not_cover():
-    ar = DynamiQAllReduce(17, 64)
+    ar = DynamiQAllReduce(65, 64)
     ar.info = dq.dq_plan_info(0.0, 0, 64, 0)
-    assert dq.dq_exchange_fused_workspace_bytes(ar.config(), 64, ar.info) == 0   # more than 16 ranks
+    assert dq.dq_exchange_fused_workspace_bytes(ar.config(), 64, ar.info) == 0   # more than 64 ranks
     with pytest.raises(dq.DQError):
-        ar.exchange([torch.zeros(64 * 256, dtype=torch.bfloat16, device=DEV)] * 17, ar.new_outputs(), fused=True)
+        ar.exchange([torch.zeros(64 * 256, dtype=torch.bfloat16, device=DEV)] * 65, ar.new_outputs(), fused=True)
 
 
 def test_barrier_timeout_reports_status_and_context_survives():
