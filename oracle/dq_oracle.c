@@ -411,15 +411,17 @@ static int get_code(const uint8_t *blk, int bits, int i)
 /* Reading of normalisation and rounding:                                   */
 /*   y = clamp(fl(x * m_g), -1, 1), m_g = fl(fl(1/u_g) * 2^-e) (y = 0 when  */
 /*   u_g = 0); k = the largest level index with q_k <= y; if k is the top   */
-/*   level the code is k, otherwise p = fl(fl(y - q_k) * G_k) and the code  */
-/*   is k+1 when U * 2^-16 < p (U the 16-bit uniform of this coordinate),   */
-/*   else k.                                                                */
+/*   level the code is k, otherwise with d = fl(y - q_k) the code is k+1    */
+/*   when U * 2^-16 < d * G_k, the product taken exactly (U the 16-bit      */
+/*   uniform of this coordinate), else k.                                   */
 /* ------------------------------------------------------------------------ */
 /* Stochastic rounding of one normalised value y in [-1, 1] (both scale
  * modes): k = the largest level index with q_k <= y; the top level is kept;
- * otherwise p = fl(fl(y - q_k) * G_k) and the code is k+1 when the 16-bit
- * uniform U of coordinate idx has U * 2^-16 < p, else k.  (y = q_k gives
- * p = 0: always k.) */
+ * otherwise d = fl(y - q_k) and the code is k+1 when the 16-bit uniform U of
+ * coordinate idx has U * 2^-16 < d * G_k, else k.  The rounding probability
+ * d * G_k is compared EXACTLY, without rounding the product: both factors
+ * are binary32, so binary64 holds their product and U * 2^-16 exactly.
+ * (y = q_k gives d = 0: always k.) */
 static int round_to_level(float y, int L, const float *q, const float *G, const or_rng *r, int64_t idx)
 {
     int lo = 0, hi = L - 1;              /* largest k with q[k] <= y */
@@ -429,9 +431,9 @@ static int round_to_level(float y, int L, const float *q, const float *G, const 
         else hi = mid - 1;
     }
     if (lo == L - 1) return lo;
-    float p = (y - q[lo]) * G[lo];
+    float d = y - q[lo];
     uint32_t U = or_uniform16(r, idx);
-    return ((float)U * (1.0f / 65536.0f) < p) ? lo + 1 : lo;
+    return ((double)U * (1.0 / 65536.0) < (double)d * (double)G[lo]) ? lo + 1 : lo;
 }
 
 void or_quantize_sg(const float *x, int bits, const float *q, const float *G,

@@ -49,13 +49,14 @@ static void levels(int bits, double eps, float *q)
     }
 }
 
-// Decode levels, {q_k, G16_k} (G16 = fl(1/fl(q_{k+1}-q_k)) * 2^16, 0 for the
-// top level, then a sentinel {+inf, 0}) and the level-search buckets of one
-// bitwidth.  H is the smallest power of two with 1/H <= the smallest gap
-// (capped at the table's capacity); bucket r (r = rint(y*H)) covers
-// [(r-1/2)/H, (r+1/2)/H] and is stored at index r & mask.  Returns whether
-// every bucket holds at most one level above its lower edge.
-static bool fill_bitwidth(int bits, double eps, float *qdec, float2 *qg, BucketEntry *bk, int mask, float *H_out)
+// Levels, G16_k = fl(1/fl(q_{k+1}-q_k)) * 2^16 (0 for the top level) and the
+// level-search buckets of one bitwidth.  H is the smallest power of two with
+// 1/H <= the smallest gap (capped at the table's capacity); with r8 =
+// rint(8H y), bucket b = floor(r8/8) covers [(b - 1/16)/H, (b + 15/16)/H)
+// (a tie at the lower edge rounds to the even r8 = 8b) and is stored at
+// index b & mask.  Returns whether every bucket holds at most one level
+// above its lower edge.
+static bool fill_bitwidth(int bits, double eps, float *qdec, float *g16, BucketEntry *bk, int mask, float *mul_out)
 {
     const int L = 1 << bits;
     float q[256];
@@ -69,29 +70,28 @@ static bool fill_bitwidth(int bits, double eps, float *qdec, float2 *qg, BucketE
             if (gap < min_gap) min_gap = gap;
         }
         qdec[k] = q[k];
-        qg[k] = make_float2(q[k], G);
+        g16[k] = G;
     }
-    qg[L] = make_float2(INFINITY, 0.0f);
     const int hmax = mask / 2;   // 2H + 1 buckets must fit in the mask + 1 slots
     int H = 2;
     while (2 * H <= hmax && 1.0 / (double)H > (double)min_gap) H *= 2;
-    *H_out = (float)H;
+    *mul_out = (float)(8 * H);
     for (int i = 0; i <= mask; ++i) {   // unused slots: harmless entries
         bk[i].boundary = INFINITY;
-        bk[i].kb8 = 0;
+        bk[i].kb4 = 0;
     }
     bool one = true;
-    for (int r = -H; r <= H; ++r) {
-        const double lo = ((double)r - 0.5) / (double)H, hi = ((double)r + 0.5) / (double)H;
+    for (int b = -H; b <= H; ++b) {
+        const double lo = ((double)b - 0.0625) / (double)H, hi = ((double)b + 0.9375) / (double)H;
         int kb = 0;
         for (int k = 0; k < L; ++k)
             if ((double)q[k] <= lo) kb = k;
         int above = 0;
         for (int k = 0; k < L; ++k)
-            if ((double)q[k] > lo && (double)q[k] <= hi) ++above;
+            if ((double)q[k] > lo && (double)q[k] < hi) ++above;
         if (above > 1) one = false;
-        BucketEntry &e = bk[r & mask];
-        e.kb8 = 8 * kb;
+        BucketEntry &e = bk[b & mask];
+        e.kb4 = 4 * kb;
         e.boundary = kb + 1 < L ? q[kb + 1] : INFINITY;
     }
     return one;
@@ -109,9 +109,9 @@ bool build_tables(double eps, Tables *out)
     if (it == cache.end()) {
         std::unique_ptr<Tables> t(new Tables());
         memset(t.get(), 0, sizeof(Tables));
-        bool one = fill_bitwidth(2, eps, t->q2, t->qg2, t->bk2, kMask2, &t->H2);
-        one = fill_bitwidth(4, eps, t->q4, t->qg4, t->bk4, kMask4, &t->H4) && one;
-        one = fill_bitwidth(8, eps, t->q8, t->qg8, t->bk8, kMask8, &t->H8) && one;
+        bool one = fill_bitwidth(2, eps, t->q2, t->g2, t->bk2, kMask2, &t->mul2);
+        one = fill_bitwidth(4, eps, t->q4, t->g4, t->bk4, kMask4, &t->mul4) && one;
+        one = fill_bitwidth(8, eps, t->q8, t->g8, t->bk8, kMask8, &t->mul8) && one;
         t->one_level = one ? 1 : 0;
         t->rcp[0] = 0.0f;
         for (int u = 1; u < 256; ++u) t->rcp[u] = 1.0f / (float)u;

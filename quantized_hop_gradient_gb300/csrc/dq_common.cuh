@@ -27,37 +27,38 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 // ---------------------------------------------------------------------------
 // Level tables for one eps, built on the host and copied to shared memory.
 //
-// q*[k]   : the levels (decode).
-// qg*[k]  : {q_k, G16_k}, G16_k = fl(1/fl(q_{k+1} - q_k)) * 2^16 (exact
-//           scaling), G16 of the top level 0, then a sentinel {+inf, 0}.
+// q*[k]   : the levels (decode and search).
+// g*[k]   : G16_k = fl(1/fl(q_{k+1} - q_k)) * 2^16 (exact scaling), 0 for the
+//           top level.
 // bk*[i]  : level-search buckets.  For y in [-1, 1] and H a power of two,
-//           r = rint(y*H) (ties to even) is read from the bit pattern of
-//           fl(y*H + 1.5*2^23); bucket r covers [(r-1/2)/H, (r+1/2)/H].  The
-//           entry sits at index r & MASK (negative r wrap to the top of the
-//           table), so any bit pattern indexes inside the table.  It holds
-//           the next level above the bucket's lower edge (boundary) and 8x
-//           the index kb of the largest level at or below that edge.
+//           r8 = rint(8H*y) (ties to even) sits in the low bits of the bit
+//           pattern of fl(8H*y + 1.5*2^23); bucket b = floor(r8 / 8) covers
+//           [(b - 1/16)/H, (b + 15/16)/H).  The entry of bucket b sits at
+//           byte offset (8*b) & (8*MASK) -- the bit pattern ANDed with a
+//           constant -- so any bit pattern (NaN included) indexes inside the
+//           table.  It holds the next level above the bucket's lower edge
+//           (boundary) and 4x the index kb of the largest level at or below
+//           that edge (a byte offset into q* and g*).
 // rcp[u]  : fl(1/u) for the UINT8 scales, rcp[0] = 0.
+// mul*    : 8H of each bitwidth.
 // ---------------------------------------------------------------------------
 constexpr int kMask2 = 63, kMask4 = 255, kMask8 = 1023;   // tables of MASK+1 entries
 // H is a power of two with 2H + 1 <= MASK + 1: at most 16, 64 and 256.
-constexpr uint32_t kMagicBits = 0x4B400000u;              // bits of 1.5 * 2^23
-constexpr float kMagic = 12582912.0f;
+constexpr float kMagic = 12582912.0f;                     // 1.5 * 2^23
 
 struct BucketEntry {
     float boundary;
-    int32_t kb8;
+    int32_t kb4;
 };
 
 struct Tables {
-    float q2[4], q4[16], q8[256];
-    float2 qg2[5], qg4[17], qg8[257];
-    float2 pad0_;
-    BucketEntry bk2[kMask2 + 1];
-    BucketEntry bk4[kMask4 + 1];
     BucketEntry bk8[kMask8 + 1];
+    BucketEntry bk4[kMask4 + 1];
+    BucketEntry bk2[kMask2 + 1];
+    float q2[4], q4[16], q8[256];
+    float g2[4], g4[16], g8[256];
     float rcp[256];
-    float H2, H4, H8;
+    float mul2, mul4, mul8;
     int32_t one_level;   // every bucket holds at most one level above its lower edge
 };
 
@@ -192,6 +193,21 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32
 // bf16 pair (low half = first element) -> two fp32, exact.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// fl(float(b) - c) for the bf16 b in the low / high half of w: the
+// mixed-precision subtract widens b exactly and rounds once.
+__device__ __forceinline__ float bf16_lo_minus(uint32_t w, float c)
+{
+    float r;
+    asm("{ .reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tsub.rn.f32.bf16 %0, l, %2; }" : "=f"(r) : "r"(w), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float bf16_hi_minus(uint32_t w, float c)
+{
+    float r;
+    asm("{ .reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tsub.rn.f32.bf16 %0, h, %2; }" : "=f"(r) : "r"(w), "f"(c));
+    return r;
+}
 
 // ---------------------------------------------------------------------------
 // Packed fp32 pairs (Blackwell .f32x2): two IEEE binary32 operations with the

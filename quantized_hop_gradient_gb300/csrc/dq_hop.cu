@@ -8,9 +8,20 @@
 // shuffle, a super-group maximum four, and each lane draws one Philox call
 // (eight 16-bit fields) for its sixteen coordinates.  The unit's
 // permutation entries, means and exponent bytes are loaded once, coalesced,
-// and broadcast by shuffles.  The gradient (or fp32 partial), the incoming
-// codes and the incoming UINT8 scales of a pair of super-groups are staged
-// in shared memory by cp.async, one pair ahead of the computation.
+// and broadcast by shuffles; its message addresses and its send and keep
+// masks are computed once per unit.  The gradient (or fp32 partial), the
+// incoming codes and the incoming UINT8 scales of a pair of super-groups are
+// staged in shared memory by cp.async, one pair ahead of the computation.
+//
+// Per coordinate the quantizer costs a packed fused multiply-add for y, one
+// for the bucket index, an AND, three shared-memory loads (bucket, level,
+// reciprocal gap), two compares, a packed subtract and a packed fused
+// multiply-add rounded upward for the rounding decision, and the code
+// packing.  Levels and reciprocal gaps sit in separate tables, so the two
+// operands of each packed operation load straight into adjacent registers.
+// y feeds several instructions; a compiler that fused its multiply into
+// the subtract that follows would change the rounding, which the GPU parity
+// tests (bit-exact against the oracle) detect.
 #include <algorithm>
 
 #include "dq_common.cuh"
@@ -22,10 +33,9 @@ namespace {
 
 constexpr int kWarps = 4;       // warps per block
 constexpr int kStages = 2;      // pairs of super-groups in flight per warp
-constexpr int kHopBlocksPerSM = 5;  // register budget: up to 102 per thread (measured best)
+constexpr int kHopBlocksPerSM = 5;  // register budget: up to 102 per thread
 
 __shared__ __align__(16) Tables g_tab;
-
 // e for S > 0: with S = (1 + f) 2^(eb-127), 255 * 2^e >= S holds first at
 // e = eb - 134 when (1 + f) <= 510/256 (mantissa field <= 0x7F0000), else at
 // eb - 133; subnormal S (eb = 0) and tiny S clamp to -126.  Byte E = e + 127,
@@ -44,24 +54,41 @@ template <int BITS> struct Lvl;
 template <> struct Lvl<2> {
     static constexpr int kMask = kMask2;
     __device__ static const float *q() { return g_tab.q2; }
-    __device__ static const float2 *qg() { return g_tab.qg2; }
+    __device__ static const float *g() { return g_tab.g2; }
     __device__ static const BucketEntry *bk() { return g_tab.bk2; }
-    __device__ static float H() { return g_tab.H2; }
+    __device__ static float mul() { return g_tab.mul2; }
 };
 template <> struct Lvl<4> {
     static constexpr int kMask = kMask4;
     __device__ static const float *q() { return g_tab.q4; }
-    __device__ static const float2 *qg() { return g_tab.qg4; }
+    __device__ static const float *g() { return g_tab.g4; }
     __device__ static const BucketEntry *bk() { return g_tab.bk4; }
-    __device__ static float H() { return g_tab.H4; }
+    __device__ static float mul() { return g_tab.mul4; }
 };
 template <> struct Lvl<8> {
     static constexpr int kMask = kMask8;
     __device__ static const float *q() { return g_tab.q8; }
-    __device__ static const float2 *qg() { return g_tab.qg8; }
+    __device__ static const float *g() { return g_tab.g8; }
     __device__ static const BucketEntry *bk() { return g_tab.bk8; }
-    __device__ static float H() { return g_tab.H8; }
+    __device__ static float mul() { return g_tab.mul8; }
 };
+
+// shared-memory load at a byte offset from a table
+template <typename T>
+__device__ __forceinline__ T lds_at(const void *base, uint32_t byte_off)
+{
+    return *reinterpret_cast<const T *>(reinterpret_cast<const char *>(base) + byte_off);
+}
+
+// a * b + c with ONE rounding toward +infinity.
+__device__ __forceinline__ float2 f2_fma_rp(float2 a, float2 b, float2 c)
+{
+    float2 r;
+    asm("{ .reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mov.b64 c, {%6, %7};\n\tfma.rp.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d; }"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
 
 // Codes of one lane: 16 coordinates of BITS bits, coordinate i at bit BITS*i.
 template <int BITS> struct LaneCodes { uint32_t w[BITS / 2]; };
@@ -72,12 +99,19 @@ __device__ __forceinline__ uint32_t code_of(const LaneCodes<BITS> &c, int i)
     return (c.w[(BITS * i) >> 5] >> ((BITS * i) & 31)) & ((1u << BITS) - 1u);
 }
 
+// Byte offset of the code block of super-group s of a message (bitwidth BITS).
+template <int BITS>
+__device__ __forceinline__ int64_t code_block_off(const MsgView &m, int64_t s)
+{
+    if (BITS == 2) return m.off_c2 + 64 * s;
+    if (BITS == 4) return m.off_c4 + 128 * (s - m.n2);
+    return m.off_c8 + 256 * (s - m.n2 - m.n4);
+}
+
 template <int BITS>
 __device__ __forceinline__ const uint8_t *code_block(const MsgView &m, int64_t s)
 {
-    if (BITS == 2) return m.base + m.off_c2 + 64 * s;
-    if (BITS == 4) return m.base + m.off_c4 + 128 * (s - m.n2);
-    return m.base + m.off_c8 + 256 * (s - m.n2 - m.n4);
+    return m.base + code_block_off<BITS>(m, s);
 }
 
 template <int BITS>
@@ -104,9 +138,20 @@ __device__ __forceinline__ void stg_codes(uint8_t *p, const LaneCodes<BITS> &c)
     else *reinterpret_cast<uint4 *>(p) = make_uint4(c.w[0], c.w[1], c.w[2], c.w[3]);
 }
 
+// 4x the code of coordinate i of a lane (a byte offset into a level table)
+template <int BITS>
+__device__ __forceinline__ uint32_t code_off(const LaneCodes<BITS> &c, int i)
+{
+    const int bit = (BITS * i) & 31;
+    const uint32_t w = c.w[(BITS * i) >> 5];
+    const uint32_t v = bit >= 2 ? (w >> (bit >= 2 ? bit - 2 : 0)) : (w << 2);
+    return v & (((1u << BITS) - 1u) << 2);
+}
+
 // x = fl(sigma * q_code + x) with one rounding (fused multiply-add); sigma
 // is u * 2^(E-127) (0 when E = 0) with UINT8 scales, the fp32 scale itself
-// otherwise.
+// otherwise.  One level-table load per code: the 2- and 4-bit tables span
+// 4 and 16 banks, so their loads never conflict.
 template <int BITS>
 __device__ __forceinline__ void decode_add(float2 (&x)[8], float sigma, const LaneCodes<BITS> &c)
 {
@@ -114,25 +159,27 @@ __device__ __forceinline__ void decode_add(float2 (&x)[8], float sigma, const La
     const float *q = Lvl<BITS>::q();
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const float2 lv = make_float2(q[code_of<BITS>(c, 2 * k)], q[code_of<BITS>(c, 2 * k + 1)]);
+        const float2 lv = make_float2(lds_at<float>(q, code_off<BITS>(c, 2 * k)), lds_at<float>(q, code_off<BITS>(c, 2 * k + 1)));
         x[k] = f2_fma(s2, lv, x[k]);
     }
 }
 
 // Quantization of one lane's group (16 values).  Scale hierarchy: s = group
 // max |x|; S = super-group max (half-warp); E from S; u = smallest integer
-// with u * 2^e >= s; m = fl(fl(1/u) * 2^-e).  Per coordinate: y = fl(x * m);
-// k = largest level <= y (bucket table, then exact compares); p16 =
-// fl(fl(y - q_k) * G16_k) = p * 2^16; code = k + (U < p16).
-// Packed multiplies are only followed by compares here: ptxas contracts a
-// packed multiply feeding a packed add into one fused operation even with
-// explicit .rn rounding, so y is formed by scalar __fmul_rn (which is never
-// contracted) and U < p16 is a float compare of U (exact) with p16.
+// with u * 2^e >= s; m = fl(fl(1/u) * 2^-e).  Per coordinate: y = fl(x * m)
+// (a fused multiply-add with -0, which adds nothing and rounds once); k =
+// the largest level <= y (bucket table, then exact compares); d = fl(y -
+// q_k); the code is k + 1 when U < d * G16_k exactly, else k.  The exact
+// comparison is t = fl_up(d * G16_k + 2^23) = 2^23 + ceil(d * G16_k) (one
+// upward rounding: d * G16_k < 2^16) against the fp32 2^23 + U built from
+// U's bits.  y needs no clamp: |y| <= 1 + 2^-23, the top level has G16 = 0,
+// and below the bottom level d < 0.
 // SF32 (ablation: scales in fp32): sigma = s, y = fl(x / s) (y = 0 when
 // s = 0); E_out = 0 and u_out holds the bits of s.
+// off: the correlated-rounding offset of this quantizer, in [0, 2^16).
 template <int BITS, bool ONE_LEVEL, bool SF32>
 __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], uint32_t ctr0, uint32_t stage_word,
-                                                          uint32_t corr2, uint32_t key0, uint32_t key1,
+                                                          uint32_t off, uint32_t key0, uint32_t key1,
                                                           uint32_t round0, uint32_t round1, uint32_t &E_out,
                                                           uint32_t &u_out)
 {
@@ -158,48 +205,58 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
     }
 
     // One Philox call per group: coordinate c takes 16-bit field c mod 8,
-    // shifted by half a period (xor 0x8000 in each half) for c >= 8.
+    // plus 2^15 (mod 2^16) for c >= 8, plus the correlated offset.  Word A
+    // carries coordinate 2i's field in its low half, word B coordinate
+    // 2i+1's in its high half (carries out of a half are never read).
     uint32_t r0[4] = {ctr0, stage_word, round0, round1};
     philox4x32_10(r0, key0, key1);
-    const uint32_t rw[8] = {__vadd2(r0[0], corr2), __vadd2(r0[1], corr2), __vadd2(r0[2], corr2),
-                            __vadd2(r0[3], corr2), __vadd2(r0[0] ^ 0x80008000u, corr2),
-                            __vadd2(r0[1] ^ 0x80008000u, corr2), __vadd2(r0[2] ^ 0x80008000u, corr2),
-                            __vadd2(r0[3] ^ 0x80008000u, corr2)};
+    const uint32_t offh = off << 16;
+    uint32_t A[8], B[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        A[i] = r0[i] + off;
+        B[i] = r0[i] + offh;
+        A[i + 4] = A[i] ^ 0x8000u;
+        B[i + 4] = B[i] ^ 0x80000000u;
+    }
 
-    const float2 *qg = Lvl<BITS>::qg();
+    const float *q = Lvl<BITS>::q();
+    const float *g = Lvl<BITS>::g();
     const BucketEntry *bk = Lvl<BITS>::bk();
-    const float H = Lvl<BITS>::H();
-    const float2 H2 = make_float2(H, H), M2 = make_float2(kMagic, kMagic);
+    constexpr uint32_t kB = (uint32_t)Lvl<BITS>::kMask << 3;
+    const float mul = Lvl<BITS>::mul();
+    const float2 mul2 = make_float2(mul, mul), M2 = make_float2(kMagic, kMagic);
+    const float2 m2 = make_float2(m, m), nz2 = make_float2(-0.0f, -0.0f);
     const float2 C2 = make_float2(8388608.0f, 8388608.0f);   // 2^23
     LaneCodes<BITS> out;
 #pragma unroll
     for (int w = 0; w < BITS / 2; ++w) out.w[w] = 0u;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const float2 y = SF32 ? (s > 0.0f ? make_float2(__fdiv_rn(x[k].x, s), __fdiv_rn(x[k].y, s))
-                                          : make_float2(0.0f, 0.0f))
-                              : make_float2(__fmul_rn(x[k].x, m), __fmul_rn(x[k].y, m));
-        const float2 tf = f2_fma(y, H2, M2);                  // y*H is exact: one rounding = rint
-        const BucketEntry b0 = bk[__float_as_uint(tf.x) & Lvl<BITS>::kMask];
-        const BucketEntry b1 = bk[__float_as_uint(tf.y) & Lvl<BITS>::kMask];
-        int k80 = b0.kb8 + (y.x >= b0.boundary ? 8 : 0);
-        int k81 = b1.kb8 + (y.y >= b1.boundary ? 8 : 0);
+        float2 y;
+        if (SF32) y = s > 0.0f ? make_float2(__fdiv_rn(x[k].x, s), __fdiv_rn(x[k].y, s)) : make_float2(0.0f, 0.0f);
+        else y = f2_fma(x[k], m2, nz2);
+        const float2 tf = f2_fma(y, mul2, M2);                 // 8H*y is exact: one rounding = rint
+        const BucketEntry b0 = lds_at<BucketEntry>(bk, __float_as_uint(tf.x) & kB);
+        const BucketEntry b1 = lds_at<BucketEntry>(bk, __float_as_uint(tf.y) & kB);
+        uint32_t k40 = (uint32_t)b0.kb4 + (y.x >= b0.boundary ? 4u : 0u);
+        uint32_t k41 = (uint32_t)b1.kb4 + (y.y >= b1.boundary ? 4u : 0u);
         if (!ONE_LEVEL) {  // buckets wider than a gap: walk up (bounded by the top level)
-            constexpr int kTop8 = 8 * ((1 << BITS) - 1);
-            while (k80 < kTop8 && y.x >= qg[(k80 >> 3) + 1].x) k80 += 8;
-            while (k81 < kTop8 && y.y >= qg[(k81 >> 3) + 1].x) k81 += 8;
+            constexpr uint32_t kTop4 = 4u * ((1u << BITS) - 1u);
+            while (k40 < kTop4 && y.x >= lds_at<float>(q, k40 + 4)) k40 += 4;
+            while (k41 < kTop4 && y.y >= lds_at<float>(q, k41 + 4)) k41 += 4;
         }
-        const float2 l0 = *reinterpret_cast<const float2 *>(reinterpret_cast<const char *>(qg) + k80);
-        const float2 l1 = *reinterpret_cast<const float2 *>(reinterpret_cast<const char *>(qg) + k81);
-        const float2 p16 = f2_mul(f2_sub(y, make_float2(l0.x, l1.x)), make_float2(l0.y, l1.y));
-        const float2 Ub = make_float2(__uint_as_float(__byte_perm(rw[k], 0x4B00u, 0x5410u)),   // 2^23 + U
-                                      __uint_as_float(__byte_perm(rw[k], 0x4B00u, 0x5432u)));
-        const float2 Uf = f2_sub(Ub, C2);                      // U, exactly
-        const uint32_t c0 = (uint32_t)(k80 >> 3) + (Uf.x < p16.x ? 1u : 0u);
-        const uint32_t c1 = (uint32_t)(k81 >> 3) + (Uf.y < p16.y ? 1u : 0u);
+        const float2 qv = make_float2(lds_at<float>(q, k40), lds_at<float>(q, k41));
+        const float2 gv = make_float2(lds_at<float>(g, k40), lds_at<float>(g, k41));
+        const float2 t = f2_fma_rp(f2_sub(y, qv), gv, C2);     // 2^23 + ceil(d * G16)
+        const float U0 = __uint_as_float(__byte_perm(A[k], 0x4B00u, 0x5410u));   // 2^23 + U
+        const float U1 = __uint_as_float(__byte_perm(B[k], 0x4B00u, 0x5432u));
+        k40 += U0 < t.x ? 4u : 0u;
+        k41 += U1 < t.y ? 4u : 0u;
         const int i0 = 2 * k, i1 = 2 * k + 1;
-        out.w[(BITS * i0) >> 5] |= c0 << ((BITS * i0) & 31);
-        out.w[(BITS * i1) >> 5] |= c1 << ((BITS * i1) & 31);
+        const int s0 = (BITS * i0) & 31, s1 = (BITS * i1) & 31;
+        out.w[(BITS * i0) >> 5] |= s0 >= 2 ? (k40 << (s0 >= 2 ? s0 - 2 : 0)) : (k40 >> 2);
+        out.w[(BITS * i1) >> 5] |= s1 >= 2 ? (k41 << (s1 >= 2 ? s1 - 2 : 0)) : (k41 >> 2);
     }
     return out;
 }
@@ -213,47 +270,67 @@ __host__ __device__ constexpr int stage_bytes() { return (ADD_F32 ? 2048 : 1024)
 // supplies perm, mu and the generator key and round.  Message bytes are
 // read through L2 (cp.async.cg, ld.cg), never the non-coherent path, so a
 // message written earlier in the same launch by other CTAs is read
-// correctly after a grid barrier.
+// correctly after a grid barrier.  A half-warp whose super-group lies past
+// the unit's end computes on stale staging data and stores nothing.
 template <int BITS, bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32, typename PP>
 __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t *stg, int64_t j0, int cnt,
                                          int lane)
 {
     constexpr int A_BYTES = ADD_F32 ? 2048 : 1024;
     constexpr int C_OFF = A_BYTES, U_OFF = A_BYTES + 512, STAGE = stage_bytes<ADD_F32, SF32>();
+    constexpr int CB = 32 * BITS;                 // code bytes per super-group
+    constexpr int UB = SF32 ? 64 : 16;            // scale bytes per super-group
     const int half = lane >> 4, hl = lane & 15;
     const uint32_t stg_s = smem_addr(stg);
 
     int32_t old_i = 0;
     float mu_i = 0.0f;
     uint32_t ein_i = 0;
+    const int64_t jl = j0 + lane;
     if (lane < cnt) {
-        old_i = __ldg(P.perm + j0 + lane);
+        old_i = __ldg(P.perm + jl);
         if (!ADD_F32) mu_i = __ldg(P.mu + old_i);
-        if (HAS_IN && !SF32) ein_i = __ldcg(t.in.base + (j0 + lane - t.in_lo));
+        if (HAS_IN && !SF32) ein_i = __ldcg(t.in.base + (jl - t.in_lo));
     }
+    // super-groups of the unit (bit s) that are sent or kept
+    const int64_t send_lo = t.send_lo, send_hi = t.send_hi;
+    const unsigned send_m = __ballot_sync(kFull, lane < cnt && jl >= send_lo && jl < send_hi);
+    const unsigned keep_m = __ballot_sync(kFull, lane < cnt && jl >= t.keep_lo && jl < t.keep_hi);
     const int npairs = (cnt + 1) >> 1;
+
+    // this lane's addresses for super-group 0 of the unit; super-group s
+    // adds s times the per-super-group stride
+    const int64_t sl0 = j0 - t.in_lo;
+    const uint8_t *in_c = HAS_IN ? t.in.base + code_block_off<BITS>(t.in, sl0) + hl * 16 : nullptr;
+    const uint8_t *in_u = HAS_IN ? t.in.base + t.in.off_u + sl0 * UB + hl * 16 : nullptr;
+    const char *add_f = ADD_F32 ? static_cast<const char *>(t.addend) + sl0 * 1024 + hl * 64 : nullptr;
+    const char *add_b = static_cast<const char *>(t.addend) + hl * 32;
+    const int64_t so0 = j0 - send_lo;
+    uint8_t *out_c = t.out.base + code_block_off<BITS>(t.out, so0) + hl * (2 * BITS);
+    uint8_t *out_u = t.out.base + t.out.off_u + so0 * UB + hl * (SF32 ? 4 : 1);
+    float *keep_p = t.keep_out + (j0 - t.keep_lo) * kSG + hl * 16;
+    const uint32_t stage_word = t.stage_word, corr = t.corr2 & 0xFFFFu;
 
     auto issue = [&](int pp) {
         const int s = 2 * pp + half;
         const int32_t old = __shfl_sync(kFull, old_i, s & 31);
         if (pp < npairs && s < cnt) {
             const uint32_t st = stg_s + (uint32_t)((pp % kStages) * STAGE);
-            const int64_t sl = j0 + s - t.in_lo;
             if (ADD_F32) {
-                const float *src = static_cast<const float *>(t.addend) + sl * kSG + hl * 16;
+                const char *src = add_f + (int64_t)s * 1024;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) cp_async16(st + half * 1024 + k * 256 + hl * 16, src + 4 * k);
+                for (int k = 0; k < 4; ++k) cp_async16(st + half * 1024 + k * 256 + hl * 16, src + 16 * k);
             } else {
-                const uint16_t *src = static_cast<const uint16_t *>(t.addend) + (int64_t)old * kSG + hl * 16;
+                const char *src = add_b + (int64_t)old * 512;
                 cp_async16(st + half * 512 + hl * 16, src);
-                cp_async16(st + half * 512 + 256 + hl * 16, src + 8);
+                cp_async16(st + half * 512 + 256 + hl * 16, src + 16);
             }
             if (HAS_IN) {
-                if (hl < 2 * BITS) cp_async16(st + C_OFF + half * 256 + hl * 16, code_block<BITS>(t.in, sl) + hl * 16);
+                if (hl < 2 * BITS) cp_async16(st + C_OFF + half * 256 + hl * 16, in_c + (int64_t)s * CB);
                 if (SF32) {
-                    if (hl < 4) cp_async16(st + U_OFF + half * 64 + hl * 16, t.in.base + t.in.off_u + sl * 64 + hl * 16);
-                } else if (hl == 15) {
-                    cp_async16(st + U_OFF + half * 16, t.in.base + t.in.off_u + sl * 16);
+                    if (hl < 4) cp_async16(st + U_OFF + half * 64 + hl * 16, in_u + (int64_t)s * UB);
+                } else if (hl == 0) {
+                    cp_async16(st + U_OFF + half * 16, in_u + (int64_t)s * UB);
                 }
             }
         }
@@ -269,8 +346,6 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
         __syncwarp();
         const uint8_t *st = stg + (p % kStages) * STAGE;
         const int s = 2 * p + half;
-        const bool valid = s < cnt;
-        const int64_t j = j0 + s;
         const int32_t old = __shfl_sync(kFull, old_i, s & 31);
         const float mu = __shfl_sync(kFull, mu_i, s & 31);
         const uint32_t ein = __shfl_sync(kFull, ein_i, s & 31);
@@ -287,9 +362,8 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
             const uint4 a = *reinterpret_cast<const uint4 *>(st + half * 512 + hl * 16);
             const uint4 b = *reinterpret_cast<const uint4 *>(st + half * 512 + 256 + hl * 16);
             const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            const float2 mu2 = make_float2(mu, mu);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) x[k] = f2_sub(make_float2(bf16_lo(w[k]), bf16_hi(w[k])), mu2);
+            for (int k = 0; k < 8; ++k) x[k] = make_float2(bf16_lo_minus(w[k], mu), bf16_hi_minus(w[k], mu));
         }
         if (HAS_IN) {
             float sigma;
@@ -302,23 +376,21 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
             const LaneCodes<BITS> c = lds_codes<BITS>(st + C_OFF + half * 256 + hl * 2 * BITS);
             decode_add<BITS>(x, sigma, c);
         }
-        if (!valid) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) x[k] = make_float2(0.0f, 0.0f);
+        const bool send = (send_m >> s) & 1u;
+        const bool keep = (keep_m >> s) & 1u;
+        uint32_t E = 0u, u = 0u;
+        if (__any_sync(kFull, send)) {
+            const uint32_t ctr0 = (uint32_t)old * 16u + (uint32_t)hl;   // global coordinate index / 16
+            const LaneCodes<BITS> q = quantize_group<BITS, ONE_LEVEL, SF32>(x, ctr0, stage_word, corr, P.key0,
+                                                                            P.key1, P.round0, P.round1, E, u);
+            if (send) {
+                stg_codes<BITS>(out_c + (int64_t)s * CB, q);
+                if (SF32) *reinterpret_cast<uint32_t *>(out_u + (int64_t)s * UB) = u;
+                else out_u[(int64_t)s * UB] = (uint8_t)u;
+            }
         }
-        const bool send = valid && j >= t.send_lo && j < t.send_hi;
-        const bool keep = valid && j >= t.keep_lo && j < t.keep_hi;
-        uint32_t E, u;
-        const uint32_t ctr0 = (uint32_t)old * 16u + (uint32_t)hl;   // global coordinate index / 16
-        const LaneCodes<BITS> q = quantize_group<BITS, ONE_LEVEL, SF32>(x, ctr0, t.stage_word, t.corr2, P.key0,
-                                                                        P.key1, P.round0, P.round1, E, u);
-        if (send) {
-            const int64_t so = j - t.send_lo;
-            stg_codes<BITS>(const_cast<uint8_t *>(code_block<BITS>(t.out, so)) + hl * 2 * BITS, q);
-            if (SF32) *reinterpret_cast<uint32_t *>(t.out.base + t.out.off_u + so * 64 + hl * 4) = u;
-            else t.out.base[t.out.off_u + so * 16 + hl] = (uint8_t)u;
-        } else if (keep) {
-            float4 *o = reinterpret_cast<float4 *>(t.keep_out + (j - t.keep_lo) * kSG + hl * 16);
+        if (keep) {
+            float4 *o = reinterpret_cast<float4 *>(keep_p + (int64_t)s * kSG);
 #pragma unroll
             for (int k = 0; k < 4; ++k) o[k] = make_float4(x[2 * k].x, x[2 * k].y, x[2 * k + 1].x, x[2 * k + 1].y);
         }
@@ -326,13 +398,10 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
         if ((lane >> 1) == p) e_out = e_pair;
         __syncwarp();
     }
-    if (!SF32 && lane < cnt) {
-        const int64_t j = j0 + lane;
-        if (j >= t.send_lo && j < t.send_hi) t.out.base[j - t.send_lo] = (uint8_t)e_out;
-    }
+    if (!SF32 && ((send_m >> lane) & 1u)) t.out.base[jl - send_lo] = (uint8_t)e_out;
     // the unit holding the send range's last super-group zeroes the E padding
-    if (!SF32 && t.send_hi > t.send_lo && t.send_hi - 1 >= j0 && t.send_hi - 1 < j0 + cnt) {
-        const int64_t c = t.send_hi - t.send_lo, pad = (c + 15) / 16 * 16;
+    if (!SF32 && send_hi > send_lo && send_hi - 1 >= j0 && send_hi - 1 < j0 + cnt) {
+        const int64_t c = send_hi - send_lo, pad = (c + 15) / 16 * 16;
         if (lane < pad - c) t.out.base[c + lane] = 0;
     }
 }
