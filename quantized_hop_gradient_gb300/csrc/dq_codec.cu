@@ -18,6 +18,8 @@ namespace dq {
 // fp32 addition is commutative, so the lanes on both sides of a shuffle
 // compute the same value.  mean = sum * 2^-8.
 // ---------------------------------------------------------------------------
+constexpr int kStatsAhead = 8;   // pairs of super-groups a warp loads before it reduces any
+
 __device__ __forceinline__ float group_tree16(float (&a)[16])
 {
 #pragma unroll
@@ -38,7 +40,7 @@ __device__ __forceinline__ float half_tree16(float v)
 __device__ __forceinline__ void stats_pairs(const uint16_t *__restrict__ g, int64_t n_sg, float *__restrict__ mean,
                                             float *__restrict__ sq, int64_t pb, int64_t stride, int lane)
 {
-    constexpr int kAhead = 2;   // pairs of super-groups loaded before any is reduced
+    constexpr int kAhead = kStatsAhead;
     const int half = lane >> 4, hl = lane & 15;
     uint4 v[kAhead][2];
 #pragma unroll
@@ -74,29 +76,29 @@ __device__ __forceinline__ void stats_pairs(const uint16_t *__restrict__ g, int6
     }
 }
 
+// Both kernels run flat: each warp reduces one block of kStatsAhead pairs
+// and exits (short-lived blocks stream from HBM faster than a persistent
+// grid-stride loop).
 __global__ void __launch_bounds__(256) stats_kernel(const uint16_t *__restrict__ g, int64_t n_sg,
                                                     float *__restrict__ mean, float *__restrict__ sq)
 {
     const int lane = threadIdx.x & 31;
-    const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_pairs = (n_sg + 1) >> 1;
-    for (int64_t pb = w0; pb < n_pairs; pb += nw * 2) stats_pairs(g, n_sg, mean, sq, pb, nw, lane);
+    if (b * kStatsAhead < n_pairs) stats_pairs(g, n_sg, mean, sq, b * kStatsAhead, 1, lane);
 }
 
 // Several ranks: warp-blocks of pairs are numbered rank by rank.
 __global__ void __launch_bounds__(256) stats_batched_kernel(const __grid_constant__ StatsParams S)
 {
     const int lane = threadIdx.x & 31;
-    const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_pairs = (S.n_sg + 1) >> 1;
-    const int64_t per_rank = (n_pairs + 1) >> 1;   // blocks of two pairs (kAhead) per rank
-    for (int64_t b = w0; b < per_rank * S.n_ranks; b += nw) {
-        const int r = (int)(b / per_rank);
-        const int64_t pb = (b - (int64_t)r * per_rank) * 2;
-        stats_pairs(S.g[r], S.n_sg, S.mean_all + (int64_t)r * S.n_sg, S.sq_all + (int64_t)r * S.n_sg, pb, 1, lane);
-    }
+    const int64_t per_rank = (n_pairs + kStatsAhead - 1) / kStatsAhead;   // blocks of kStatsAhead pairs per rank
+    if (b >= per_rank * S.n_ranks) return;
+    const int r = (int)(b / per_rank);
+    const int64_t pb = (b - (int64_t)r * per_rank) * kStatsAhead;
+    stats_pairs(S.g[r], S.n_sg, S.mean_all + (int64_t)r * S.n_sg, S.sq_all + (int64_t)r * S.n_sg, pb, 1, lane);
 }
 
 // Metadata all-reduce: M_j and F_j summed over ranks 0..N-1 in order, and
@@ -128,16 +130,16 @@ __global__ void __launch_bounds__(256) stats_reduce_kernel(const float *__restri
 // ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
-static int grid_for(int64_t work_warps)
+static unsigned flat_grid(int64_t work_warps)
 {
     const int64_t blocks = (work_warps + 7) / 8;
-    const int64_t cap = (int64_t)sm_count() * 8;
-    return (int)(blocks < 1 ? 1 : (blocks < cap ? blocks : cap));
+    return (unsigned)(blocks < 1 ? 1 : blocks);
 }
 
 cudaError_t launch_stats(const uint16_t *g, int64_t n_sg, float *mean, float *sq, cudaStream_t st)
 {
-    stats_kernel<<<grid_for((n_sg + 1) / 2), 256, 0, st>>>(g, n_sg, mean, sq);
+    const int64_t n_pairs = (n_sg + 1) >> 1;
+    stats_kernel<<<flat_grid((n_pairs + kStatsAhead - 1) / kStatsAhead), 256, 0, st>>>(g, n_sg, mean, sq);
     note_launches(1);
     return cudaGetLastError();
 }
@@ -145,7 +147,7 @@ cudaError_t launch_stats(const uint16_t *g, int64_t n_sg, float *mean, float *sq
 cudaError_t launch_stats_batched(const StatsParams &S, cudaStream_t st)
 {
     const int64_t n_pairs = (S.n_sg + 1) >> 1;
-    stats_batched_kernel<<<grid_for(((n_pairs + 1) >> 1) * S.n_ranks), 256, 0, st>>>(S);
+    stats_batched_kernel<<<flat_grid((n_pairs + kStatsAhead - 1) / kStatsAhead * S.n_ranks), 256, 0, st>>>(S);
     note_launches(1);
     return cudaGetLastError();
 }

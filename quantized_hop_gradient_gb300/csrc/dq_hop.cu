@@ -191,9 +191,12 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
         E_out = 0u;
         u_out = __float_as_uint(s);
     } else {
-        float S = s;
-#pragma unroll
-        for (int sh = 1; sh <= 8; sh <<= 1) S = fmaxf(S, __shfl_xor_sync(kFull, S, sh));
+        // super-group maximum: s >= 0, so the bit patterns order like the values
+        const bool hi_half = (threadIdx.x & 16u) != 0u;
+        const uint32_t sb = __float_as_uint(s);
+        const uint32_t m0 = __reduce_max_sync(kFull, hi_half ? 0u : sb);
+        const uint32_t m1 = __reduce_max_sync(kFull, hi_half ? sb : 0u);
+        const float S = __uint_as_float(hi_half ? m1 : m0);
         const uint32_t E = exponent_byte(S);
         const float inv2e = __uint_as_float((254u - E) << 23);   // 2^-e (any E: finite)
         uint32_t u = __float2uint_ru(__fmul_rn(s, inv2e));
@@ -534,24 +537,132 @@ __device__ __forceinline__ void decode_unit(const PP &P, const MsgView &msg, int
     }
 }
 
+// 32-byte streaming store of eight fp32 (the address must be 32-byte aligned).
+__device__ __forceinline__ void stcs_f32x8(float *p, const float (&v)[8])
+{
+    asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v[0]), "f"(v[1]),
+                 "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                 : "memory");
+}
+
+// The same decode with lane l owning coordinates 8l .. 8l+7 (half of group
+// l/2), so one warp store writes a whole super-group: 1 KiB of fp32 with
+// 32-byte stores (outputs 32-byte aligned) or 512 bytes of bf16 with
+// 16-byte stores.  Half as many store instructions as the 16-byte mapping,
+// which keeps the global store queue from throttling the warps.
+template <int BITS, bool SF32, typename PP>
+__device__ __forceinline__ void decode_unit_wide(const PP &P, const MsgView &msg, int64_t lo, void *const *outs,
+                                                 int n_outs, int64_t j0, int cnt, int lane)
+{
+    constexpr int kAhead = 8;
+    int32_t old_i = 0;
+    float mu_i = 0.0f;
+    uint32_t ein_i = 0;
+    if (lane < cnt) {
+        old_i = __ldg(P.perm + j0 + lane);
+        mu_i = __ldg(P.mu + old_i);
+        if (!SF32) ein_i = __ldcg(msg.base + (j0 + lane - lo));
+    }
+    const float nr = (float)P.n_ranks;
+    const float *q = Lvl<BITS>::q();
+    const int g = lane >> 1;
+    for (int s0 = 0; s0 < cnt; s0 += kAhead) {
+        uint32_t c0[kAhead], c1[kAhead], ua[kAhead];
+#pragma unroll
+        for (int a = 0; a < kAhead; ++a) {
+            c0[a] = c1[a] = ua[a] = 0u;
+            if (s0 + a < cnt) {
+                const int64_t sl = j0 + s0 + a - lo;
+                const uint8_t *blk = code_block<BITS>(msg, sl);
+                if (BITS == 2) {
+                    c0[a] = __ldcg(reinterpret_cast<const unsigned short *>(blk) + lane);
+                } else if (BITS == 4) {
+                    c0[a] = __ldcg(reinterpret_cast<const unsigned int *>(blk) + lane);
+                } else {
+                    const uint2 v = __ldcg(reinterpret_cast<const uint2 *>(blk) + lane);
+                    c0[a] = v.x;
+                    c1[a] = v.y;
+                }
+                if (SF32) ua[a] = __ldcg(reinterpret_cast<const unsigned int *>(msg.base + msg.off_u + sl * 64) + g);
+                else ua[a] = __ldcg(msg.base + msg.off_u + sl * 16 + g);
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < kAhead; ++a) {
+            const int s = s0 + a;
+            const int32_t old = __shfl_sync(kFull, old_i, s & 31);
+            const float mu = __shfl_sync(kFull, mu_i, s & 31);
+            const uint32_t E = __shfl_sync(kFull, ein_i, s & 31);
+            if (s < cnt) {
+                const float back = __fmul_rn(mu, nr);
+                const float sigma = SF32 ? __uint_as_float(ua[a]) : __fmul_rn((float)ua[a], __uint_as_float(E << 23));
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t w = (BITS == 8 && i >= 4) ? c1[a] : c0[a];
+                    const int bit = (BITS * i) & 31;
+                    const uint32_t off = (bit >= 2 ? (w >> (bit >= 2 ? bit - 2 : 0)) : (w << 2)) & (((1u << BITS) - 1u) << 2);
+                    v[i] = __fmaf_rn(sigma, lds_at<float>(q, off), back);
+                }
+                if (P.out_is_bf16) {
+                    uint32_t h[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        h[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i])) |
+                               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i + 1])) << 16);
+                    const uint4 hv = make_uint4(h[0], h[1], h[2], h[3]);
+                    for (int oi = 0; oi < n_outs; ++oi)
+                        __stcs(reinterpret_cast<uint4 *>(static_cast<uint16_t *>(outs[oi]) + (int64_t)old * kSG + 8 * lane), hv);
+                } else {
+                    for (int oi = 0; oi < n_outs; ++oi)
+                        stcs_f32x8(static_cast<float *>(outs[oi]) + (int64_t)old * kSG + 8 * lane, v);
+                }
+            }
+        }
+    }
+}
+
 constexpr int kDecodeWarps = 16;
+// The final decode runs flat: each warp decodes one slice of 32 / kDecodeSplit
+// super-groups and exits; short-lived blocks stream their writes to HBM
+// faster than a persistent grid-stride loop (7.7 vs 6.6 TB/s measured for
+// plain 1 KiB row writes on a GB300).
+constexpr int kDecodeSplit = 8;
+
+// Copy only the decode levels (q2, q4, q8: contiguous in Tables) to shared memory.
+__device__ __forceinline__ void copy_levels(Tables *dst, const Tables *src)
+{
+    static_assert(offsetof(Tables, q4) == offsetof(Tables, q2) + 16 && offsetof(Tables, q8) == offsetof(Tables, q4) + 64,
+                  "levels contiguous");
+    static_assert(offsetof(Tables, q2) % 16 == 0, "16-byte aligned");
+    const int4 *s = reinterpret_cast<const int4 *>(src->q2);
+    int4 *d = reinterpret_cast<int4 *>(dst->q2);
+    for (int i = threadIdx.x; i < (4 + 16 + 256) / 4; i += blockDim.x) d[i] = s[i];
+}
 
 template <bool SF32>
 __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kernel(const __grid_constant__ DecodeParams P)
 {
-    block_copy(&g_tab, &P.tab);
+    copy_levels(&g_tab, &P.tab);
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t nw = (int64_t)gridDim.x * kDecodeWarps;
-    for (int64_t u = (int64_t)blockIdx.x * kDecodeWarps + warp; u < P.total_units; u += nw) {
-        int ti, seg;
-        locate_unit(P.task, P.n_tasks, u, ti, seg);
-        const DecodeTask &t = P.task[ti];
-        const int64_t j0 = t.seg_lo[seg] + (u - t.unit_begin[seg]) * kUnit;
-        const int64_t rem = t.seg_hi[seg] - j0;
-        const int cnt = (int)(rem < kUnit ? rem : kUnit);
-        void *const *outs = P.n_outs > 0 ? P.outs : &t.out;
-        const int n_outs = P.n_outs > 0 ? P.n_outs : 1;
+    const int64_t w = (int64_t)blockIdx.x * kDecodeWarps + warp;
+    const int64_t u = w / kDecodeSplit;
+    if (u >= P.total_units) return;
+    int ti, seg;
+    locate_unit(P.task, P.n_tasks, u, ti, seg);
+    const DecodeTask &t = P.task[ti];
+    const int64_t j0 = t.seg_lo[seg] + (u - t.unit_begin[seg]) * kUnit + (w % kDecodeSplit) * (kUnit / kDecodeSplit);
+    const int64_t rem = t.seg_hi[seg] - j0;
+    if (rem <= 0) return;
+    const int cnt = (int)(rem < kUnit / kDecodeSplit ? rem : kUnit / kDecodeSplit);
+    void *const *outs = P.n_outs > 0 ? P.outs : &t.out;
+    const int n_outs = P.n_outs > 0 ? P.n_outs : 1;
+    if (P.out_is_bf16 || P.out_align32) {
+        if (seg == 0) decode_unit_wide<2, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane);
+        else if (seg == 1) decode_unit_wide<4, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane);
+        else decode_unit_wide<8, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane);
+    } else {
         if (seg == 0) decode_unit<2, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane);
         else if (seg == 1) decode_unit<4, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane);
         else decode_unit<8, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane);
@@ -633,9 +744,15 @@ __global__ void __launch_bounds__(kWarps * 32) fused_ring_kernel(const __grid_co
             if (t == N) {   // final decode of chunk c (owner c, step N-1)
                 MsgView m = P.chunk[c];
                 m.base = P.msgs + (2 * (int64_t)c + ((N - 1) & 1)) * P.msg_stride;
-                if (seg == 0) decode_unit<2, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
-                else if (seg == 1) decode_unit<4, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
-                else decode_unit<8, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
+                if (P.out_is_bf16 || P.out_align32) {
+                    if (seg == 0) decode_unit_wide<2, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
+                    else if (seg == 1) decode_unit_wide<4, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
+                    else decode_unit_wide<8, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
+                } else {
+                    if (seg == 0) decode_unit<2, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
+                    else if (seg == 1) decode_unit<4, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
+                    else decode_unit<8, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
+                }
                 continue;
             }
             const int r = (c + 1 + t) % N, src = (r - 1 + N) % N;
@@ -703,7 +820,8 @@ template <bool SF32>
 cudaError_t launch_decode_s(const DecodeParams &P, cudaStream_t st)
 {
     auto k = decode_kernel<SF32>;
-    k<<<grid_for(k, kDecodeWarps, 0, P.total_units), kDecodeWarps * 32, 0, st>>>(P);
+    const int64_t warps = P.total_units * kDecodeSplit;
+    k<<<(unsigned)((warps + kDecodeWarps - 1) / kDecodeWarps), kDecodeWarps * 32, 0, st>>>(P);
     note_launches(1);
     return cudaGetLastError();
 }
