@@ -227,10 +227,12 @@ cudaError_t launch_mx_hop(const MxParams &P, bool has_in, bool add_f32, cudaStre
     return cudaGetLastError();
 }
 
+// The decode is launched flat (one unit per warp, grid sized to the work):
+// short-lived blocks stream its writes faster than a persistent loop.
 cudaError_t launch_mx_decode(const MxDecodeParams &P, cudaStream_t st)
 {
     if (P.total_units <= 0) return cudaSuccess;
-    mx_decode_kernel<<<mx_grid(mx_decode_kernel, P.total_units), kMxWarps * 32, 0, st>>>(P);
+    mx_decode_kernel<<<(unsigned)((P.total_units + kMxWarps - 1) / kMxWarps), kMxWarps * 32, 0, st>>>(P);
     note_launches(1);
     return cudaGetLastError();
 }
