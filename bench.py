@@ -48,7 +48,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     p.add_argument("--exchange", choices=["auto", "fused", "multi"], default="auto",
                    help="ring exchange as one cooperative launch (fused) or one launch per step (multi); "
-                        "auto: fused where it is the faster path (rings of up to 64 ranks, up to 2^19 "
+                        "auto: fused where it is the faster path (allreduce.use_fused: rings of up to 64 ranks, up to 2^16 "
                         "super-groups per worker)")
     p.add_argument("--bucket-pool", type=int, default=16,
                    help="streamed workloads: distinct buckets kept resident and cycled through a full pass")

@@ -14,11 +14,12 @@ from . import dq
 SG = dq.SG
 
 # Largest per-worker size (super-groups) at which the fused ring exchange is
-# the faster one on a GB300: measured equal-or-better up to 2^26 coordinates
-# per worker (0.37 vs 0.50 ms at 2^22, 1.81 vs 1.91 ms at 2^26), 6-7% slower
-# at 3.4e8 and 1e9 coordinates, where launches are few and the separate
-# decode kernel, with more warps per SM, streams its outputs faster.
-FUSED_MAX_SG = 1 << 19
+# the faster one on a GB300 (BERT-large distribution, 8 ranks): 0.367 vs
+# 0.432 ms at 2^22 coordinates per worker, 0.631 vs 0.694 ms at 2^24; above
+# that the per-step launches win (1.053 vs 1.175 ms at 2^25, 1.684 vs 1.740
+# ms at 2^26), their flat-launched final decode streaming the outputs faster
+# than the cooperative kernel's last phase.
+FUSED_MAX_SG = 1 << 16
 
 
 def use_fused(n_ranks: int, butterfly: bool, n_sg: int) -> bool:

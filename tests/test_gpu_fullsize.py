@@ -93,6 +93,7 @@ def test_llama3_8b_buckets_full_size():
     buckets of 13,107,200 coordinates, two streams, the fused exchange.  The
     first bucket, one from the middle and the short last bucket (of 613)
     are reduced as one stream and compared with the oracle in full."""
+    from quantized_hop_gradient_gb300.allreduce import use_fused
     from quantized_hop_gradient_gb300.stream import BucketedAllReduce
     build.build()
     w = synth.WORKLOADS["llama3_8b_ring8_buckets"]
@@ -103,7 +104,7 @@ def test_llama3_8b_buckets_full_size():
     assert buckets[-1][0].numel() < w.bucket and buckets[0][0].numel() == w.bucket
     outs = [[torch.empty(g.numel(), dtype=torch.float32, device="cuda") for g in b] for b in buckets]
     ar = BucketedAllReduce(N, w.bucket // 256, overlap=True, budget=w.budget, correlated=w.correlated, seed=0)
-    assert all(s.n_sg <= 1 << 19 for s in ar.sets)        # the fused exchange applies
+    assert all(use_fused(N, False, s.n_sg) for s in ar.sets)   # the fused exchange applies
     ar.run(buckets, outs, round0=100)
     torch.cuda.synchronize()
     for s in ar.sets:
