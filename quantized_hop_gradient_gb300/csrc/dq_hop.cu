@@ -33,7 +33,7 @@ namespace {
 
 constexpr int kWarps = 4;       // warps per block
 constexpr int kStages = 2;      // pairs of super-groups in flight per warp
-constexpr int kHopBlocksPerSM = 5;  // register budget: up to 102 per thread
+constexpr int kHopBlocksPerSM = 4;  // register budget: up to 128 per thread (measured best of 4, 5, 6)
 
 __shared__ __align__(16) Tables g_tab;
 // e for S > 0: with S = (1 + f) 2^(eb-127), 255 * 2^e >= S holds first at

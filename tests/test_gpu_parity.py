@@ -179,6 +179,12 @@ def test_compress_dar_decode_bit_exact(eps, correlated):
         o16 = torch.zeros(p.b.size * 256, dtype=torch.bfloat16, device=DEV)
         dq.dq_decode(cfg, r, out, M, perm, o16, out_is_bf16=True)
         assert torch.equal(o16.cpu(), torch.from_numpy(e32).to(torch.bfloat16))
+        # an fp32 output 16- but not 32-byte aligned takes the 16-byte-store decode
+        ob = torch.zeros(p.b.size * 256 + 4, device=DEV)
+        o32u = ob[4:]
+        assert o32u.data_ptr() % 32 == 16
+        dq.dq_decode(cfg, r, out, M, perm, o32u)
+        assert np.array_equal(bits32(host(o32u)), bits32(e32)), ("decode, 16-byte aligned output", a, b)
 
 
 # --------------------------------------------------------------------------- whole all-reduce
@@ -259,3 +265,26 @@ def test_fewer_supergroups_than_ranks():
     _check_allreduce("ring4_1m", 3 * 256, 8, False, False)
     _check_allreduce("ring4_1m", 3 * 256, 8, True, True)
     _check_allreduce("ring4_1m", 200, 4, False, True)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_exchange_outputs_16_byte_aligned(fused):
+    """Outputs 16- but not 32-byte aligned take the decode's 16-byte stores
+    (in the per-step exchange and in the fused one); the results are the
+    same bits as with aligned outputs."""
+    N = 4
+    _, gr = grads_for("ring4_1m", 256 * 1500, N=N, seed=9)
+    J = gr[0].size // 256
+    ar = DynamiQAllReduce(N, J, budget=5.0, correlated=True, seed=0)
+    ga = [dev_u16(g) for g in gr]
+    ref = [o.clone() for o in ar(ga, round=2, fused=fused)]
+    bufs = [torch.zeros(J * 256 + 4, device=DEV) for _ in range(N)]
+    outs = [b[4:] for b in bufs]
+    assert all(o.data_ptr() % 32 == 16 for o in outs)
+    ar(ga, round=2, outs=outs, fused=fused)
+    torch.cuda.synchronize()
+    if fused:
+        ar.check_status()
+    for r in range(N):
+        assert torch.equal(outs[r].view(torch.int32), ref[r].view(torch.int32)), r
+
