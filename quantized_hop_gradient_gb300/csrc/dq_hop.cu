@@ -183,9 +183,20 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
                                                           uint32_t round0, uint32_t round1, uint32_t &E_out,
                                                           uint32_t &u_out)
 {
-    float s = 0.0f;
+    // group maximum as a three-level tree of three-way maxima (max is exact,
+    // so the order does not change the result; 0 joins in as before)
+    float a[17];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) s = fmaxf(s, fmaxf(fabsf(x[k].x), fabsf(x[k].y)));
+    for (int k = 0; k < 8; ++k) {
+        a[2 * k] = fabsf(x[k].x);
+        a[2 * k + 1] = fabsf(x[k].y);
+    }
+    a[16] = 0.0f;
+    float l1[6];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) l1[i] = fmaxf(fmaxf(a[3 * i], a[3 * i + 1]), a[3 * i + 2]);
+    l1[5] = fmaxf(a[15], a[16]);
+    const float s = fmaxf(fmaxf(fmaxf(l1[0], l1[1]), l1[2]), fmaxf(fmaxf(l1[3], l1[4]), l1[5]));
     float m = 0.0f;
     if (SF32) {
         E_out = 0u;
@@ -199,8 +210,10 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
         const float S = __uint_as_float(hi_half ? m1 : m0);
         const uint32_t E = exponent_byte(S);
         const float inv2e = __uint_as_float((254u - E) << 23);   // 2^-e (any E: finite)
-        uint32_t u = __float2uint_ru(__fmul_rn(s, inv2e));
-        u = max(u, s > 0.0f ? 1u : 0u);
+        // u = ceil(s * 2^-e): s * 2^-e is exact and at most 255, so one fused
+        // multiply-add rounded upward onto 2^23 leaves 2^23 + u (the clamp
+        // only guards non-finite inputs)
+        uint32_t u = __float_as_uint(__fmaf_ru(s, inv2e, 8388608.0f)) - 0x4B000000u;
         u = min(u, 255u);
         m = __fmul_rn(g_tab.rcp[u], inv2e);
         E_out = E;
