@@ -563,11 +563,14 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
     seq_out = [outs_pool[i % len(full)] for i in range(nb - 1)] + [outs_pool[-1]]
     bucket_sg = w.bucket // SG
     kw = dict(budget=w.budget, correlated=w.correlated, butterfly=w.topology == "butterfly", seed=0)
-    # rings of up to 64 ranks run each bucket's exchange as one cooperative launch
+    # the overlapped stream picks its exchange itself ("auto": per-step launches
+    # beside the next bucket's planning); the cooperative one-launch exchange
+    # (rings of up to 64 ranks) is timed beside it for comparison
     from quantized_hop_gradient_gb300.allreduce import use_fused
     fusable = use_fused(N, w.topology == "butterfly", bucket_sg)
-    ov = BucketedAllReduce(N, bucket_sg, overlap=True, fused=fusable, **kw)
-    ml = BucketedAllReduce(N, bucket_sg, overlap=True, fused=False, **kw)
+    ov = BucketedAllReduce(N, bucket_sg, overlap=True, fused="auto", **kw)
+    alt = BucketedAllReduce(N, bucket_sg, overlap=True, fused=not ov.fused, **kw) \
+        if (fusable or ov.fused) else None
     sq = BucketedAllReduce(N, bucket_sg, overlap=False, fused=False, **kw)
     K, W = args.steps, max(args.warmup, 0)
 
@@ -592,15 +595,20 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
     t1 = time.time()
     n_launch = dq.dq_launch_count() - n0
     clk = clocks.stop(t0, t1)
-    if fusable:
+    if ov.fused:
         for s_ in ov.sets:
             s_.check_status()
     sq.run(seq, seq_out, round0=(W + K) * nb)          # warm-up pass (workspace allocation)
     ms_seq = timed(sq, 1, W + K + 1)
-    ms_ml = ms
-    if fusable:
-        ml.run(seq, seq_out, round0=(W + K + 2) * nb)
-        ms_ml = timed(ml, 2, W + K + 3)
+    ms_alt = None
+    if alt is not None:
+        alt.run(seq, seq_out, round0=(W + K + 2) * nb)
+        ms_alt = timed(alt, 2, W + K + 3)
+        if alt.fused:
+            for s_ in alt.sets:
+                s_.check_status()
+    ms_fused = ms if ov.fused else ms_alt
+    ms_ml = ms_alt if ov.fused else ms
     ms_max = max_over_ranks(ms, world, dev)
     gb = w.n * 2 / 1e9
     line = {
@@ -615,8 +623,7 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
         "per_bucket_ms": ms_max / nb,
         "two_streams": {"ms_per_pass_overlapped": ms, "ms_per_pass_one_stream": ms_seq,
                         "saved_frac": 1.0 - ms / ms_seq},
-        "fused_exchange": {"used": fusable, "ms_per_pass_fused": ms if fusable else None,
-                           "ms_per_pass_multi_launch": ms_ml},
+        "fused_exchange": {"used": ov.fused, "ms_per_pass_fused": ms_fused, "ms_per_pass_multi_launch": ms_ml},
         "gpu_launches": n_launch, "clocks": clk, "cpu_baseline": None, "e2e": None,
     }
     if rank == 0:

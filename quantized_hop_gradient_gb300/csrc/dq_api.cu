@@ -646,6 +646,25 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
     const LogSlot slot = log_begin(log, DQ_LAUNCH_ALLOCATE_REORDER, n_sg, st);
     if (launch_stats_reduce(mean_all, sq_all, N, n_sg, M, F, mu, st, nonfinite) != cudaSuccess) return DQ_ERR_CUDA;
     int32_t h_nonfinite = 0;
+    if (n_sg <= small_plan_max_sg()) {
+        // small problems: allocation and reorder in one launch
+        const int64_t cap = (int64_t)floor((double)cfg->budget_bits * (double)n_sg);
+        if (launch_plan_small(F, n_sg, cap, cfg->fixed_bits, b, T, counts, perm, st) != cudaSuccess)
+            return DQ_ERR_CUDA;
+        log_end(slot, st);
+        int64_t hc[5];   // counts[3], padding, the non-finite flag
+        float hT = 0.0f;
+        if (cudaMemcpyAsync(hc, counts, sizeof(hc), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DQ_ERR_CUDA;
+        if (cudaMemcpyAsync(&hT, T, sizeof(hT), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DQ_ERR_CUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return DQ_ERR_CUDA;
+        memcpy(&h_nonfinite, reinterpret_cast<const uint8_t *>(hc) + 32, sizeof(int32_t));
+        if (h_nonfinite) return DQ_ERR_NONFINITE;
+        info->T = cfg->fixed_bits ? NAN : hT;
+        info->n2 = hc[0];
+        info->n4 = hc[1];
+        info->n8 = hc[2];
+        return DQ_OK;
+    }
     if (cfg->fixed_bits) {
         // uniform-bitwidth ablation: every super-group gets fixed_bits (the
         // reorder of a uniform allocation is the identity permutation)

@@ -36,6 +36,10 @@ size_t plan_scratch_bytes(int64_t n_sg);
 cudaError_t launch_allocate(const float *F, int64_t n_sg, int64_t cap_bits, uint8_t *b, float *T,
                             int64_t *counts, void *ws, cudaStream_t st);
 cudaError_t launch_reorder(const uint8_t *b, int64_t n_sg, int32_t *perm, void *ws, cudaStream_t st);
+// allocation and reorder of up to small_plan_max_sg() super-groups in one launch
+int64_t small_plan_max_sg();
+cudaError_t launch_plan_small(const float *F, int64_t n_sg, int64_t cap_bits, int32_t fixed_bits, uint8_t *b,
+                              float *T, int64_t *counts, int32_t *perm, cudaStream_t st);
 
 // Brackets one launch with the caller's events (if a log has room).
 struct LogSlot {

@@ -24,6 +24,7 @@ namespace {
 constexpr int kAllocThreads = 256;
 constexpr int kTile = 2048;            // super-groups per reorder tile
 constexpr int kTileThreads = 256;      // 8 super-groups per thread
+constexpr int64_t kSmallPlanMaxSG = 16384;   // single-block plan: F in 64 KB of shared memory; above this the multi-kernel path is faster
 
 struct AllocState {
     unsigned long long hist[256];
@@ -243,6 +244,133 @@ __global__ void __launch_bounds__(kTileThreads) reorder_scatter_kernel(const uin
     }
 }
 
+// --------------------------------------------------------------------------- small problems
+// Allocation and reorder in one block, for up to kSmallPlanMaxSG super-groups
+// (F held in shared memory): the same weighted radix select and stable
+// partition as the kernels above, without their 12 launches.  Histogram
+// updates are combined per warp (__match_any_sync) before the shared
+// atomic, since the top digit of F is mostly its exponent and few bins
+// take most keys.  fixed_bits != 0 gives every super-group that width.
+constexpr int kSmallPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kSmallPlanThreads) plan_small_kernel(const float *__restrict__ F, int32_t n,
+                                                                       long long R, int32_t all8, int32_t fixed_bits,
+                                                                       uint8_t *__restrict__ b, float *T,
+                                                                       int64_t *counts, int32_t *__restrict__ perm)
+{
+    extern __shared__ float sF[];
+    __shared__ unsigned int hist[256];
+    __shared__ int s_d;
+    __shared__ unsigned long long s_higher;
+    __shared__ unsigned long long warp_tot[kSmallPlanThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nth = blockDim.x;
+    for (int j = tid; j < n; j += nth) sF[j] = F[j];
+    __syncthreads();
+
+    uint32_t t = 0u;
+    if (!fixed_bits && !all8) {
+        uint32_t prefix = 0u;
+        long long above = 0;
+        for (int pass = 0; pass < 4; ++pass) {
+            for (int i = tid; i < 256; i += nth) hist[i] = 0u;
+            __syncthreads();
+            const int shift = 24 - 8 * pass;
+            for (int base = wid * 32; base < n; base += nth) {
+                const int j = base + lane;
+                uint32_t bin4 = 256u, bin8 = 256u;   // 256: no bin
+                if (j < n) {
+                    const float f = sF[j];
+                    const uint32_t k4 = key4_of(f), k8 = key8_of(f);
+                    if (pass == 0 || (k4 >> (shift + 8)) == (prefix >> (shift + 8))) bin4 = (k4 >> shift) & 255u;
+                    if (pass == 0 || (k8 >> (shift + 8)) == (prefix >> (shift + 8))) bin8 = (k8 >> shift) & 255u;
+                }
+                const unsigned p4 = __match_any_sync(kFull, bin4);
+                if (bin4 < 256u && lane == __ffs(p4) - 1) atomicAdd(&hist[bin4], 2u * (unsigned)__popc(p4));
+                const unsigned p8 = __match_any_sync(kFull, bin8);
+                if (bin8 < 256u && lane == __ffs(p8) - 1) atomicAdd(&hist[bin8], 4u * (unsigned)__popc(p8));
+            }
+            __syncthreads();
+            if (wid == 0) {   // the largest digit d with above + sum_{d' >= d} hist[d'] > R
+                unsigned long long h[8], loc = 0ull;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    h[i] = hist[8 * lane + i];
+                    loc += h[i];
+                }
+                unsigned long long incl = loc;   // weight of lanes >= this lane
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const unsigned long long o = __shfl_down_sync(kFull, incl, off);
+                    if (lane + off < 32) incl += o;
+                }
+                unsigned long long gt = incl - loc;   // weight of the bins above 8*lane + i
+                int best = -1;
+                unsigned long long best_gt = 0ull;
+#pragma unroll
+                for (int i = 7; i >= 0; --i) {
+                    if (best < 0 && above + (long long)(gt + h[i]) > R) {
+                        best = 8 * lane + i;
+                        best_gt = gt;
+                    }
+                    gt += h[i];
+                }
+                const unsigned q = __ballot_sync(kFull, best >= 0);
+                const int src = q ? 31 - __clz((int)q) : 0;
+                const int d = __shfl_sync(kFull, best, src);
+                const unsigned long long dgt = __shfl_sync(kFull, best_gt, src);
+                const unsigned long long total = __shfl_sync(kFull, incl, 0);
+                const unsigned long long h0 = __shfl_sync(kFull, h[0], 0);
+                if (lane == 0) {
+                    s_d = q ? d : 0;
+                    s_higher = q ? dgt : total - h0;
+                }
+            }
+            __syncthreads();
+            prefix |= (uint32_t)s_d << shift;
+            above += (long long)s_higher;
+            __syncthreads();
+        }
+        t = prefix + 1u;
+    }
+
+    // assign and count: thread tid takes a contiguous run of super-groups
+    const int per = (n + nth - 1) / nth;
+    const int lo = min(n, tid * per), hi = min(n, lo + per);
+    unsigned long long mine = 0ull;   // packed counts: class k in bits [21k, 21k+21)
+    for (int j = lo; j < hi; ++j) {
+        const float f = sF[j];
+        uint8_t bits;
+        if (fixed_bits) bits = (uint8_t)fixed_bits;
+        else bits = key8_of(f) >= t ? 8 : (key4_of(f) >= t ? 4 : 2);
+        b[j] = bits;
+        mine += 1ull << (21 * class_of(bits));
+    }
+    unsigned long long inc = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned long long o = __shfl_up_sync(kFull, inc, off);
+        if (lane >= off) inc += o;
+    }
+    if (lane == 31) warp_tot[wid] = inc;
+    __syncthreads();
+    unsigned long long pre = inc - mine, all = 0ull;
+    for (int w = 0; w < nth / 32; ++w) {
+        if (w < wid) pre += warp_tot[w];
+        all += warp_tot[w];
+    }
+    const long long tot0 = (long long)(all & 0x1FFFFFull), tot1 = (long long)((all >> 21) & 0x1FFFFFull),
+                    tot2 = (long long)((all >> 42) & 0x1FFFFFull);
+    long long pos[3] = {(long long)(pre & 0x1FFFFFull), tot0 + (long long)((pre >> 21) & 0x1FFFFFull),
+                        tot0 + tot1 + (long long)((pre >> 42) & 0x1FFFFFull)};
+    for (int j = lo; j < hi; ++j) perm[pos[class_of(b[j])]++] = j;
+    if (tid == 0) {
+        counts[0] = tot0;
+        counts[1] = tot1;
+        counts[2] = tot2;
+        *T = __uint_as_float(t);
+    }
+}
+
 }  // namespace
 
 size_t plan_scratch_bytes(int64_t n_sg)
@@ -283,6 +411,29 @@ cudaError_t launch_reorder(const uint8_t *b, int64_t n_sg, int32_t *perm, void *
     reorder_scan_kernel<<<1, 1024, 0, st>>>(tiles, n_tiles);
     reorder_scatter_kernel<<<(int)n_tiles, kTileThreads, 0, st>>>(b, n_sg, tiles, perm);
     note_launches(3);
+    return cudaGetLastError();
+}
+
+int64_t small_plan_max_sg() { return kSmallPlanMaxSG; }
+
+cudaError_t launch_plan_small(const float *F, int64_t n_sg, int64_t cap_bits, int32_t fixed_bits, uint8_t *b,
+                              float *T, int64_t *counts, int32_t *perm, cudaStream_t st)
+{
+    if (n_sg < 1 || n_sg > kSmallPlanMaxSG) return cudaErrorInvalidValue;
+    const size_t smem = (size_t)n_sg * sizeof(float);
+    static bool attr_set[128] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (dev >= 0 && dev < 128 && !attr_set[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(plan_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)(kSmallPlanMaxSG * sizeof(float)));
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const long long R = (long long)(cap_bits - 2 * n_sg);
+    const int all8 = R >= 6 * (long long)n_sg ? 1 : 0;
+    plan_small_kernel<<<1, kSmallPlanThreads, smem, st>>>(F, (int32_t)n_sg, R, all8, fixed_bits, b, T, counts, perm);
+    note_launches(1);
     return cudaGetLastError();
 }
 

@@ -11,14 +11,22 @@ from __future__ import annotations
 
 import torch
 
-from .allreduce import DynamiQAllReduce
+from .allreduce import DynamiQAllReduce, use_fused
 
 
 class BucketedAllReduce:
     def __init__(self, n_ranks: int, bucket_sg: int, *, overlap: bool = True, fused="auto", **kw):
         """``fused``: each bucket's ring exchange as one cooperative launch
-        (dq_exchange_fused): True, False, or "auto" (where it is faster)."""
-        self.n_ranks, self.bucket_sg, self.overlap, self.fused = n_ranks, bucket_sg, overlap, fused
+        (dq_exchange_fused): True, False, or "auto".  "auto" takes the
+        per-step launches when planning overlaps the exchange: the next
+        bucket's planning runs beside them, while a cooperative exchange
+        holds every SM, and the single-block planning of small buckets (up
+        to 16,384 super-groups) then cannot start until it ends.  Without
+        overlap "auto" follows ``use_fused``."""
+        self.n_ranks, self.bucket_sg, self.overlap = n_ranks, bucket_sg, overlap
+        if fused == "auto":
+            fused = (not overlap) and use_fused(n_ranks, kw.get("butterfly", False), bucket_sg)
+        self.fused = bool(fused)
         self.sets = [DynamiQAllReduce(n_ranks, bucket_sg, **kw) for _ in range(2)]
         self.plan_stream = torch.cuda.Stream() if overlap else None
         self.ev_plan = [torch.cuda.Event(), torch.cuda.Event()]

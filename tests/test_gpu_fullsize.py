@@ -90,9 +90,11 @@ def test_gemma1b_ring16_full_size_sampled():
 
 def test_llama3_8b_buckets_full_size():
     """The streamed Llama-3-8B workload in its bench configuration: 25 MB
-    buckets of 13,107,200 coordinates, two streams, the fused exchange.  The
-    first bucket, one from the middle and the short last bucket (of 613)
-    are reduced as one stream and compared with the oracle in full."""
+    buckets of 13,107,200 coordinates, two streams, with the exchange the
+    stream picks (per-step launches beside the next bucket's planning) and
+    with the cooperative one-launch exchange.  The first bucket, one from
+    the middle and the short last bucket (of 613) are reduced as one stream
+    and compared with the oracle in full."""
     from quantized_hop_gradient_gb300.allreduce import use_fused
     from quantized_hop_gradient_gb300.stream import BucketedAllReduce
     build.build()
@@ -102,17 +104,23 @@ def test_llama3_8b_buckets_full_size():
     picks = [0, nb // 2, nb - 1]
     buckets = [synth.generate_bucket(w, k, "cuda", seed=0) for k in picks]
     assert buckets[-1][0].numel() < w.bucket and buckets[0][0].numel() == w.bucket
-    outs = [[torch.empty(g.numel(), dtype=torch.float32, device="cuda") for g in b] for b in buckets]
-    ar = BucketedAllReduce(N, w.bucket // 256, overlap=True, budget=w.budget, correlated=w.correlated, seed=0)
-    assert all(use_fused(N, False, s.n_sg) for s in ar.sets)   # the fused exchange applies
-    ar.run(buckets, outs, round0=100)
-    torch.cuda.synchronize()
-    for s in ar.sets:
-        s.check_status()
+    exps = []
     for i, b in enumerate(buckets):
         gu = [synth.as_u16(g) for g in b]
         cfg = oracle.Config(N, w.budget, correlated=w.correlated, seed=0, round=100 + i)
-        _, exp = oracle.allreduce(cfg, gu)
-        for r in (0, N - 1):
-            got = outs[i][r].cpu().numpy()
-            assert np.array_equal(got.view(np.int32), exp.view(np.int32)), (picks[i], r)
+        exps.append(oracle.allreduce(cfg, gu)[1])
+    for fused in ("auto", True):
+        outs = [[torch.empty(g.numel(), dtype=torch.float32, device="cuda") for g in b] for b in buckets]
+        ar = BucketedAllReduce(N, w.bucket // 256, overlap=True, fused=fused, budget=w.budget,
+                               correlated=w.correlated, seed=0)
+        assert ar.fused == (fused is True)
+        assert all(use_fused(N, False, s.n_sg) for s in ar.sets)   # the size allows the one-launch exchange
+        ar.run(buckets, outs, round0=100)
+        torch.cuda.synchronize()
+        if ar.fused:
+            for s in ar.sets:
+                s.check_status()
+        for i in range(len(buckets)):
+            for r in (0, N - 1):
+                got = outs[i][r].cpu().numpy()
+                assert np.array_equal(got.view(np.int32), exps[i].view(np.int32)), (fused, picks[i], r)

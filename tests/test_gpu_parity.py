@@ -288,3 +288,22 @@ def test_exchange_outputs_16_byte_aligned(fused):
     for r in range(N):
         assert torch.equal(outs[r].view(torch.int32), ref[r].view(torch.int32)), r
 
+
+
+# --------------------------------------------------------------------------- planning: one launch or twelve
+@pytest.mark.parametrize("J,B", [(1, 5.0), (4097, 2.0), (4097, 8.0), (3000, 3.3), (16384, 5.0), (16385, 5.0)])
+def test_plan_single_block_and_multi_kernel_paths(J, B):
+    """dq_plan allocates and reorders up to 16,384 super-groups in one
+    single-block launch and above that with the multi-kernel radix select;
+    both give the oracle's threshold, bitwidth counts and permutation (the
+    two sizes around the switch, and the all-2-bit and all-8-bit budgets)."""
+    N = 2
+    _, gr = grads_for("bert_large_ring8", J * 256, N=N, seed=J)
+    ar = DynamiQAllReduce(N, J, budget=B, correlated=True, seed=0)
+    info = ar.plan([dev_u16(g) for g in gr], round=1)
+    torch.cuda.synchronize()
+    p = oracle.plan(oracle.Config(N, B, correlated=True, seed=0, round=1), gr)
+    assert (info.n2, info.n4, info.n8) == tuple(int(c) for c in p.counts)
+    assert bits32(np.array([info.T], np.float32))[0] == bits32(np.array([p.T], np.float32))[0]
+    assert np.array_equal(host(ar.perm), p.perm)
+    assert np.array_equal(bits32(host(ar.mu)), bits32(p.M / np.float32(N)))
