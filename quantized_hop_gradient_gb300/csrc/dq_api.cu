@@ -51,12 +51,13 @@ static void levels(int bits, double eps, float *q)
 
 // Levels, G16_k = fl(1/fl(q_{k+1}-q_k)) * 2^16 (0 for the top level) and the
 // level-search buckets of one bitwidth.  H is the smallest power of two with
-// 1/H <= the smallest gap (capped at the table's capacity); with r8 =
-// rint(8H y), bucket b = floor(r8/8) covers [(b - 1/16)/H, (b + 15/16)/H)
-// (a tie at the lower edge rounds to the even r8 = 8b) and is stored at
-// index b & mask.  Returns whether every bucket holds at most one level
-// above its lower edge.
-static bool fill_bitwidth(int bits, double eps, float *qdec, float *g16, BucketEntry *bk, int mask, float *mul_out)
+// 1/H <= the smallest gap (capped at the table's capacity); with r =
+// rint(sub H y), bucket b = floor(r/sub) covers [(b - 1/(2 sub))/H,
+// (b + 1 - 1/(2 sub))/H) (a tie at the lower edge rounds to the even r =
+// sub b) and is stored at index b & mask.  Returns whether every bucket
+// holds at most one level above its lower edge.
+static bool fill_bitwidth(int bits, double eps, float *qdec, float *g16, BucketEntry *bk, int mask, int sub,
+                          float *mul_out)
 {
     const int L = 1 << bits;
     float q[256];
@@ -75,14 +76,15 @@ static bool fill_bitwidth(int bits, double eps, float *qdec, float *g16, BucketE
     const int hmax = mask / 2;   // 2H + 1 buckets must fit in the mask + 1 slots
     int H = 2;
     while (2 * H <= hmax && 1.0 / (double)H > (double)min_gap) H *= 2;
-    *mul_out = (float)(8 * H);
+    *mul_out = (float)(sub * H);
     for (int i = 0; i <= mask; ++i) {   // unused slots: harmless entries
         bk[i].boundary = INFINITY;
         bk[i].kb4 = 0;
     }
     bool one = true;
     for (int b = -H; b <= H; ++b) {
-        const double lo = ((double)b - 0.0625) / (double)H, hi = ((double)b + 0.9375) / (double)H;
+        const double half = 0.5 / (double)sub;
+        const double lo = ((double)b - half) / (double)H, hi = ((double)b + 1.0 - half) / (double)H;
         int kb = 0;
         for (int k = 0; k < L; ++k)
             if ((double)q[k] <= lo) kb = k;
@@ -109,9 +111,9 @@ bool build_tables(double eps, Tables *out)
     if (it == cache.end()) {
         std::unique_ptr<Tables> t(new Tables());
         memset(t.get(), 0, sizeof(Tables));
-        bool one = fill_bitwidth(2, eps, t->q2, t->g2, t->bk2, kMask2, &t->mul2);
-        one = fill_bitwidth(4, eps, t->q4, t->g4, t->bk4, kMask4, &t->mul4) && one;
-        one = fill_bitwidth(8, eps, t->q8, t->g8, t->bk8, kMask8, &t->mul8) && one;
+        bool one = fill_bitwidth(2, eps, t->q2, t->g2, t->bk2, kMask2, kSub2, &t->mul2);
+        one = fill_bitwidth(4, eps, t->q4, t->g4, t->bk4, kMask4, kSub4, &t->mul4) && one;
+        one = fill_bitwidth(8, eps, t->q8, t->g8, t->bk8, kMask8, kSub8, &t->mul8) && one;
         t->one_level = one ? 1 : 0;
         t->rcp[0] = 0.0f;
         for (int u = 1; u < 256; ++u) t->rcp[u] = 1.0f / (float)u;

@@ -31,19 +31,24 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 // g*[k]   : G16_k = fl(1/fl(q_{k+1} - q_k)) * 2^16 (exact scaling), 0 for the
 //           top level.
 // bk*[i]  : level-search buckets.  For y in [-1, 1] and H a power of two,
-//           r8 = rint(8H*y) (ties to even) sits in the low bits of the bit
-//           pattern of fl(8H*y + 1.5*2^23); bucket b = floor(r8 / 8) covers
-//           [(b - 1/16)/H, (b + 15/16)/H).  The entry of bucket b sits at
-//           byte offset (8*b) & (8*MASK) -- the bit pattern ANDed with a
-//           constant -- so any bit pattern (NaN included) indexes inside the
-//           table.  It holds the next level above the bucket's lower edge
+//           r = rint(S*H*y) (ties to even; S = 8 for 2 and 8 bits, 128 for 4
+//           bits) sits in the low bits of the bit pattern of
+//           fl(S*H*y + 1.5*2^23); bucket b = floor(r / S) covers
+//           [(b - 1/(2S))/H, (b + 1 - 1/(2S))/H).  The entry of bucket b sits
+//           at index b & MASK, found as the bit pattern ANDed with a constant
+//           -- so any bit pattern (NaN included) indexes inside the table.
+//           It holds the next level above the bucket's lower edge
 //           (boundary) and 4x the index kb of the largest level at or below
-//           that edge (a byte offset into q* and g*).
+//           that edge (a byte offset into q* and g*).  The 4-bit table is
+//           expanded in shared memory to 16 copies, one per lane of a
+//           half-warp, so its lookups never meet in a bank.
 // rcp[u]  : fl(1/u) for the UINT8 scales, rcp[0] = 0.
-// mul*    : 8H of each bitwidth.
+// mul*    : S*H of each bitwidth.
 // ---------------------------------------------------------------------------
-constexpr int kMask2 = 63, kMask4 = 255, kMask8 = 1023;   // tables of MASK+1 entries
-// H is a power of two with 2H + 1 <= MASK + 1: at most 16, 64 and 256.
+constexpr int kMask2 = 63, kMask4 = 127, kMask8 = 1023;   // tables of MASK+1 entries
+constexpr int kSub2 = 8, kSub4 = 128, kSub8 = 8;          // S of each bitwidth
+constexpr int kCopies4 = 16;                              // lane copies of the 4-bit table
+// H is a power of two with 2H + 1 <= MASK + 1: at most 16, 32 and 256.
 constexpr float kMagic = 12582912.0f;                     // 1.5 * 2^23
 
 struct BucketEntry {

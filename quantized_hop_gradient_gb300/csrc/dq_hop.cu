@@ -36,6 +36,15 @@ constexpr int kStages = 2;      // pairs of super-groups in flight per warp
 constexpr int kHopBlocksPerSM = 4;  // register budget: up to 128 per thread (measured best of 4, 5, 6)
 
 __shared__ __align__(16) Tables g_tab;
+// The 4-bit buckets, one copy per half-warp lane: row b (128 bytes) holds
+// 16 copies of entry b, and lane l reads copy l mod 16, so the 16 lanes of a
+// half-warp always read 16 different bank pairs.
+__shared__ __align__(16) BucketEntry g_bk4c[(kMask4 + 1) * kCopies4];
+
+__device__ __forceinline__ void expand_bk4()
+{
+    for (int i = threadIdx.x; i < (kMask4 + 1) * kCopies4; i += blockDim.x) g_bk4c[i] = g_tab.bk4[i / kCopies4];
+}
 // e for S > 0: with S = (1 + f) 2^(eb-127), 255 * 2^e >= S holds first at
 // e = eb - 134 when (1 + f) <= 510/256 (mantissa field <= 0x7F0000), else at
 // eb - 133; subnormal S (eb = 0) and tiny S clamp to -126.  Byte E = e + 127,
@@ -62,7 +71,7 @@ template <> struct Lvl<4> {
     static constexpr int kMask = kMask4;
     __device__ static const float *q() { return g_tab.q4; }
     __device__ static const float *g() { return g_tab.g4; }
-    __device__ static const BucketEntry *bk() { return g_tab.bk4; }
+    __device__ static const BucketEntry *bk() { return g_bk4c; }
     __device__ static float mul() { return g_tab.mul4; }
 };
 template <> struct Lvl<8> {
@@ -239,7 +248,10 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
     const float *q = Lvl<BITS>::q();
     const float *g = Lvl<BITS>::g();
     const BucketEntry *bk = Lvl<BITS>::bk();
-    constexpr uint32_t kB = (uint32_t)Lvl<BITS>::kMask << 3;
+    // byte offset of bucket b: 8b (2, 8 bits: r = rint(8Hy), 8b = r & ~7) or,
+    // for the lane-copied 4-bit table, 128b + 8 (lane mod 16) (r = rint(128Hy))
+    constexpr uint32_t kB = BITS == 4 ? (uint32_t)Lvl<BITS>::kMask << 7 : (uint32_t)Lvl<BITS>::kMask << 3;
+    const uint32_t lane_copy = BITS == 4 ? (threadIdx.x & 15u) << 3 : 0u;
     const float mul = Lvl<BITS>::mul();
     const float2 mul2 = make_float2(mul, mul), M2 = make_float2(kMagic, kMagic);
     const float2 m2 = make_float2(m, m), nz2 = make_float2(-0.0f, -0.0f);
@@ -252,9 +264,9 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
         float2 y;
         if (SF32) y = s > 0.0f ? make_float2(__fdiv_rn(x[k].x, s), __fdiv_rn(x[k].y, s)) : make_float2(0.0f, 0.0f);
         else y = f2_fma(x[k], m2, nz2);
-        const float2 tf = f2_fma(y, mul2, M2);                 // 8H*y is exact: one rounding = rint
-        const BucketEntry b0 = lds_at<BucketEntry>(bk, __float_as_uint(tf.x) & kB);
-        const BucketEntry b1 = lds_at<BucketEntry>(bk, __float_as_uint(tf.y) & kB);
+        const float2 tf = f2_fma(y, mul2, M2);                 // S*H*y is exact: one rounding = rint
+        const BucketEntry b0 = lds_at<BucketEntry>(bk, (__float_as_uint(tf.x) & kB) | lane_copy);
+        const BucketEntry b1 = lds_at<BucketEntry>(bk, (__float_as_uint(tf.y) & kB) | lane_copy);
         uint32_t k40 = (uint32_t)b0.kb4 + (y.x >= b0.boundary ? 4u : 0u);
         uint32_t k41 = (uint32_t)b1.kb4 + (y.y >= b1.boundary ? 4u : 0u);
         if (!ONE_LEVEL) {  // buckets wider than a gap: walk up (bounded by the top level)
@@ -427,6 +439,8 @@ __global__ void __launch_bounds__(kWarps * 32, kHopBlocksPerSM) hop_kernel(const
 {
     extern __shared__ __align__(16) uint8_t dyn[];
     block_copy(&g_tab, &P.tab);
+    __syncthreads();
+    expand_bk4();
     __syncthreads();
     constexpr int STAGE = stage_bytes<ADD_F32, SF32>();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -740,6 +754,8 @@ __global__ void __launch_bounds__(kWarps * 32) fused_ring_kernel(const __grid_co
     extern __shared__ __align__(16) uint8_t dyn[];
     block_copy(&g_tab, &P.tab);
     __syncthreads();
+    expand_bk4();
+    __syncthreads();
     constexpr int STAGE = stage_bytes<false, SF32>();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint8_t *stg = dyn + warp * kStages * STAGE;
@@ -796,6 +812,21 @@ __global__ void __launch_bounds__(kWarps * 32) fused_ring_kernel(const __grid_co
     }
 }
 
+// Opts a kernel in to `dyn` bytes of dynamic shared memory (needed once its
+// static plus dynamic shared memory passes 48 KB), once per device; `done`
+// is the caller's per-kernel record.
+template <typename K>
+cudaError_t allow_dyn_smem(K kernel, size_t dyn, bool (&done)[128])
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    if (done[dev]) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(reinterpret_cast<const void *>(kernel), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    if (e == cudaSuccess) done[dev] = true;
+    return e;
+}
+
 template <typename K>
 int grid_for(K kernel, int warps, size_t dyn_smem, int64_t units)
 {
@@ -813,6 +844,9 @@ cudaError_t launch_hop_t(const HopParams &P, cudaStream_t st)
 {
     const size_t dyn = (size_t)kWarps * kStages * stage_bytes<ADD_F32, SF32>();
     auto k = hop_kernel<HAS_IN, ADD_F32, ONE_LEVEL, SF32>;
+    static bool opted[128] = {false};   // one record per instantiation of this launcher
+    const cudaError_t ea = allow_dyn_smem(k, dyn, opted);
+    if (ea != cudaSuccess) return ea;
     k<<<grid_for(k, kWarps, dyn, P.total_units), kWarps * 32, dyn, st>>>(P);
     note_launches(1);
     return cudaGetLastError();
@@ -860,8 +894,11 @@ cudaError_t launch_fused_t(const FusedRingParams &P, cudaStream_t st)
 {
     const size_t dyn = (size_t)kWarps * kStages * stage_bytes<false, SF32>();
     auto k = fused_ring_kernel<ONE_LEVEL, SF32>;
+    static bool opted[128] = {false};   // one record per instantiation of this launcher
+    cudaError_t e = allow_dyn_smem(k, dyn, opted);
+    if (e != cudaSuccess) return e;
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kWarps * 32, dyn);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kWarps * 32, dyn);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorLaunchOutOfResources;
     // every CTA must be resident at once (cooperative launch): at most the
