@@ -667,9 +667,108 @@ __device__ __forceinline__ void copy_levels(Tables *dst, const Tables *src)
     for (int i = threadIdx.x; i < (4 + 16 + 256) / 4; i += blockDim.x) d[i] = s[i];
 }
 
+// Bulk (TMA) copy of `bytes` from this CTA's shared memory to global
+// memory; completion is tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void *gdst, uint32_t ssrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+                 : "memory");
+}
+
+// The decode of up to kDecodeSlice super-groups with the stores handed to
+// the bulk-copy engine: the warp writes its decoded rows to shared memory
+// (lane l owns coordinates 8l .. 8l+7), makes them visible to the async
+// proxy, and each lane issues the copy of one (row, output) pair, then
+// waits until its copies have completed (the shared memory must outlive
+// them).  The global store queue then carries none of the output.
+constexpr int kDecodeSlice = kUnit / kDecodeSplit;
+
+template <int BITS, bool SF32, typename PP>
+__device__ __forceinline__ void decode_unit_bulk(const PP &P, const MsgView &msg, int64_t lo, void *const *outs,
+                                                 int n_outs, int64_t j0, int cnt, int lane, uint8_t *rows)
+{
+    int32_t old_i = 0;
+    float mu_i = 0.0f;
+    uint32_t ein_i = 0;
+    if (lane < cnt) {
+        old_i = __ldg(P.perm + j0 + lane);
+        mu_i = __ldg(P.mu + old_i);
+        if (!SF32) ein_i = __ldcg(msg.base + (j0 + lane - lo));
+    }
+    const float nr = (float)P.n_ranks;
+    const float *q = Lvl<BITS>::q();
+    const int g = lane >> 1;
+    const int row_bytes = P.out_is_bf16 ? 512 : 1024;
+    uint32_t c0[kDecodeSlice], c1[kDecodeSlice], ua[kDecodeSlice];
+#pragma unroll
+    for (int a = 0; a < kDecodeSlice; ++a) {
+        c0[a] = c1[a] = ua[a] = 0u;
+        if (a < cnt) {
+            const int64_t sl = j0 + a - lo;
+            const uint8_t *blk = code_block<BITS>(msg, sl);
+            if (BITS == 2) {
+                c0[a] = __ldcg(reinterpret_cast<const unsigned short *>(blk) + lane);
+            } else if (BITS == 4) {
+                c0[a] = __ldcg(reinterpret_cast<const unsigned int *>(blk) + lane);
+            } else {
+                const uint2 v = __ldcg(reinterpret_cast<const uint2 *>(blk) + lane);
+                c0[a] = v.x;
+                c1[a] = v.y;
+            }
+            if (SF32) ua[a] = __ldcg(reinterpret_cast<const unsigned int *>(msg.base + msg.off_u + sl * 64) + g);
+            else ua[a] = __ldcg(msg.base + msg.off_u + sl * 16 + g);
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < kDecodeSlice; ++a) {
+        const float mu = __shfl_sync(kFull, mu_i, a);
+        const uint32_t E = __shfl_sync(kFull, ein_i, a);
+        if (a < cnt) {
+            const float back = __fmul_rn(mu, nr);
+            const float sigma = SF32 ? __uint_as_float(ua[a]) : __fmul_rn((float)ua[a], __uint_as_float(E << 23));
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t w = (BITS == 8 && i >= 4) ? c1[a] : c0[a];
+                const int bit = (BITS * i) & 31;
+                const uint32_t off = (bit >= 2 ? (w >> (bit >= 2 ? bit - 2 : 0)) : (w << 2)) & (((1u << BITS) - 1u) << 2);
+                v[i] = __fmaf_rn(sigma, lds_at<float>(q, off), back);
+            }
+            if (P.out_is_bf16) {
+                uint32_t h[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    h[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i])) |
+                           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i + 1])) << 16);
+                *reinterpret_cast<uint4 *>(rows + a * 512 + 16 * lane) = make_uint4(h[0], h[1], h[2], h[3]);
+            } else {
+                float4 *r = reinterpret_cast<float4 *>(rows + a * 1024 + 32 * lane);
+                r[0] = make_float4(v[0], v[1], v[2], v[3]);
+                r[1] = make_float4(v[4], v[5], v[6], v[7]);
+            }
+        }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    const uint32_t rows_s = smem_addr(rows);
+    const int pairs = cnt * n_outs;
+    for (int pbase = 0; pbase < pairs; pbase += 32) {
+        const int pi = pbase + lane;
+        const int a = pi < pairs ? pi / n_outs : 0;
+        const int32_t old = __shfl_sync(kFull, old_i, a);
+        if (pi < pairs) {
+            char *dst = static_cast<char *>(outs[pi - a * n_outs]) + (int64_t)old * row_bytes;
+            bulk_store(dst, rows_s + (uint32_t)(a * row_bytes), (uint32_t)row_bytes);
+        }
+    }
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 template <bool SF32>
 __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kernel(const __grid_constant__ DecodeParams P)
 {
+    extern __shared__ __align__(128) uint8_t drows[];
     copy_levels(&g_tab, &P.tab);
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -685,15 +784,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kernel(const __grid_
     const int cnt = (int)(rem < kUnit / kDecodeSplit ? rem : kUnit / kDecodeSplit);
     void *const *outs = P.n_outs > 0 ? P.outs : &t.out;
     const int n_outs = P.n_outs > 0 ? P.n_outs : 1;
-    if (P.out_is_bf16 || P.out_align32) {
-        if (seg == 0) decode_unit_wide<2, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane);
-        else if (seg == 1) decode_unit_wide<4, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane);
-        else decode_unit_wide<8, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane);
-    } else {
-        if (seg == 0) decode_unit<2, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane);
-        else if (seg == 1) decode_unit<4, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane);
-        else decode_unit<8, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane);
-    }
+    uint8_t *rows = drows + warp * kDecodeSlice * 1024;
+    if (seg == 0) decode_unit_bulk<2, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane, rows);
+    else if (seg == 1) decode_unit_bulk<4, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane, rows);
+    else decode_unit_bulk<8, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane, rows);
 }
 
 // ---------------------------------------------------------------------------
@@ -867,8 +961,12 @@ template <bool SF32>
 cudaError_t launch_decode_s(const DecodeParams &P, cudaStream_t st)
 {
     auto k = decode_kernel<SF32>;
+    const size_t dyn = (size_t)kDecodeWarps * kDecodeSlice * 1024;
+    static bool opted[128] = {false};   // one record per instantiation of this launcher
+    const cudaError_t ea = allow_dyn_smem(k, dyn, opted);
+    if (ea != cudaSuccess) return ea;
     const int64_t warps = P.total_units * kDecodeSplit;
-    k<<<(unsigned)((warps + kDecodeWarps - 1) / kDecodeWarps), kDecodeWarps * 32, 0, st>>>(P);
+    k<<<(unsigned)((warps + kDecodeWarps - 1) / kDecodeWarps), kDecodeWarps * 32, dyn, st>>>(P);
     note_launches(1);
     return cudaGetLastError();
 }
