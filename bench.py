@@ -19,6 +19,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -176,14 +177,22 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and blank lines (string literals in
+    these files hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(kernel: str) -> str:
-    """sha256 prefix of the files that define `kernel` (its name before any
-    template arguments)."""
+    """sha256 prefix of the code (comments and blank lines dropped) of the
+    files that define `kernel` (its name before any template arguments)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_hop_gradient_gb300", "csrc")
     for name in KERNEL_SOURCES[kernel.split("<")[0]]:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:12]
 
 

@@ -461,11 +461,14 @@ __global__ void __launch_bounds__(kWarps * 32, kHopBlocksPerSM) hop_kernel(const
 
 // ---------------------------------------------------------------------------
 // Final decode: out[perm[j]*256 + i] = fl(sigma * q_code + fl(mu_j * N)) (one
-// rounding), fp32 or bf16.  Output-bound (4 bytes out per 0.69 in), so the
-// mapping makes every store instruction cover contiguous memory: lane l of
-// the warp decodes coordinates 4l..4l+3 (group l/4) and 128+4l..131+4l
-// (group 8 + l/4) of a super-group, so each warp store writes 512
-// contiguous bytes.  Eight super-groups are loaded before any is computed.
+// rounding), fp32 or bf16.  Output-bound (4 bytes out per 0.69 in).  Three
+// variants: decode_unit_bulk (the decode kernel) writes through the
+// bulk-copy engine; the fused exchange's last phase stores directly, with
+// decode_unit_wide when every output is 32-byte aligned and decode_unit
+// otherwise.  decode_unit: lane l of the warp decodes coordinates 4l..4l+3
+// (group l/4) and 128+4l..131+4l (group 8 + l/4) of a super-group, so each
+// warp store writes 512 contiguous bytes.  Eight super-groups are loaded
+// before any is computed.
 // ---------------------------------------------------------------------------
 template <int BITS>
 __device__ __forceinline__ uint32_t ldg_codes4(const uint8_t *blk, int idx)
@@ -575,8 +578,7 @@ __device__ __forceinline__ void stcs_f32x8(float *p, const float (&v)[8])
 // The same decode with lane l owning coordinates 8l .. 8l+7 (half of group
 // l/2), so one warp store writes a whole super-group: 1 KiB of fp32 with
 // 32-byte stores (outputs 32-byte aligned) or 512 bytes of bf16 with
-// 16-byte stores.  Half as many store instructions as the 16-byte mapping,
-// which keeps the global store queue from throttling the warps.
+// 16-byte stores, half as many store instructions as decode_unit.
 template <int BITS, bool SF32, typename PP>
 __device__ __forceinline__ void decode_unit_wide(const PP &P, const MsgView &msg, int64_t lo, void *const *outs,
                                                  int n_outs, int64_t j0, int cnt, int lane)
