@@ -57,7 +57,7 @@ static void levels(int bits, double eps, float *q)
 // sub b) and is stored at index b & mask.  Returns whether every bucket
 // holds at most one level above its lower edge.
 static bool fill_bitwidth(int bits, double eps, float *qdec, float *g16, BucketEntry *bk, int mask, int sub,
-                          float *mul_out)
+                          int off, float *mul_out)
 {
     const int L = 1 << bits;
     float q[256];
@@ -92,7 +92,7 @@ static bool fill_bitwidth(int bits, double eps, float *qdec, float *g16, BucketE
         for (int k = 0; k < L; ++k)
             if ((double)q[k] > lo && (double)q[k] < hi) ++above;
         if (above > 1) one = false;
-        BucketEntry &e = bk[b & mask];
+        BucketEntry &e = bk[(b + off) & mask];
         e.kb4 = 4 * kb;
         e.boundary = kb + 1 < L ? q[kb + 1] : INFINITY;
     }
@@ -111,9 +111,9 @@ bool build_tables(double eps, Tables *out)
     if (it == cache.end()) {
         std::unique_ptr<Tables> t(new Tables());
         memset(t.get(), 0, sizeof(Tables));
-        bool one = fill_bitwidth(2, eps, t->q2, t->g2, t->bk2, kMask2, kSub2, &t->mul2);
-        one = fill_bitwidth(4, eps, t->q4, t->g4, t->bk4, kMask4, kSub4, &t->mul4) && one;
-        one = fill_bitwidth(8, eps, t->q8, t->g8, t->bk8, kMask8, kSub8, &t->mul8) && one;
+        bool one = fill_bitwidth(2, eps, t->q2, t->g2, t->bk2, kMask2, kSub2, 0, &t->mul2);
+        one = fill_bitwidth(4, eps, t->q4, t->g4, t->bk4, kMask4, kSub4, 0, &t->mul4) && one;
+        one = fill_bitwidth(8, eps, t->q8, t->g8, t->bk8, kMask8, kSub8, kOff8, &t->mul8) && one;
         t->one_level = one ? 1 : 0;
         t->rcp[0] = 0.0f;
         for (int u = 1; u < 256; ++u) t->rcp[u] = 1.0f / (float)u;

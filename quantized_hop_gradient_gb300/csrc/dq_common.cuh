@@ -46,7 +46,8 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 // mul*    : S*H of each bitwidth.
 // ---------------------------------------------------------------------------
 constexpr int kMask2 = 63, kMask4 = 127, kMask8 = 1023;   // tables of MASK+1 entries
-constexpr int kSub2 = 8, kSub4 = 128, kSub8 = 8;          // S of each bitwidth
+constexpr int kSub2 = 8, kSub4 = 128, kSub8 = 128;        // S of each bitwidth
+constexpr int kOff8 = 256;   // 8-bit buckets are stored at b + 256 (0 .. 512 for y in [-1, 1])
 constexpr int kCopies4 = 16;                              // lane copies of the 4-bit table
 // H is a power of two with 2H + 1 <= MASK + 1: at most 16, 32 and 256.
 constexpr float kMagic = 12582912.0f;                     // 1.5 * 2^23

@@ -31,9 +31,9 @@ namespace dq {
 
 namespace {
 
-constexpr int kWarps = 4;       // warps per block
+constexpr int kWarps = 16;      // warps per block
 constexpr int kStages = 2;      // pairs of super-groups in flight per warp
-constexpr int kHopBlocksPerSM = 4;  // register budget: up to 128 per thread (measured best of 4, 5, 6)
+constexpr int kHopBlocksPerSM = 1;  // one block per SM (its tables fill most of shared memory); 128 registers
 
 __shared__ __align__(16) Tables g_tab;
 // The 4-bit buckets, one copy per half-warp lane: row b (128 bytes) holds
@@ -44,6 +44,38 @@ __shared__ __align__(16) BucketEntry g_bk4c[(kMask4 + 1) * kCopies4];
 __device__ __forceinline__ void expand_bk4()
 {
     for (int i = threadIdx.x; i < (kMask4 + 1) * kCopies4; i += blockDim.x) g_bk4c[i] = g_tab.bk4[i / kCopies4];
+}
+
+// The 8-bit tables of the hop kernels, at the start of dynamic shared
+// memory, one copy per half-warp lane c: buckets (row b + 256, 128 bytes per
+// row) whose entry for copy c holds 64 kb + 4c, and the levels and
+// reciprocal gaps (64 bytes per level), so the level and gap of copy c sit
+// at byte 64 k + 4c.  The 16 lanes of a half-warp never meet in a bank (pair).
+extern __shared__ __align__(16) uint8_t g_dyn[];
+constexpr int kCopies8 = 16;
+constexpr int kRows8 = 2 * kOff8 + 1;
+constexpr int kBk8cBytes = kRows8 * kCopies8 * 8;
+constexpr int kL8cBytes = 256 * kCopies8 * 4;
+constexpr int kTab8Bytes = kBk8cBytes + 2 * kL8cBytes;
+static_assert(kTab8Bytes % 16 == 0, "16-byte aligned staging");
+// rows up to 1023 (a non-finite y) stay inside the smallest dynamic allocation
+static_assert(1024 * kCopies8 * 8 <= kTab8Bytes + kWarps * kStages * (1024 + 512 + 32), "garbage rows in bounds");
+__device__ __forceinline__ const BucketEntry *bk8c() { return reinterpret_cast<const BucketEntry *>(g_dyn); }
+__device__ __forceinline__ const float *q8c() { return reinterpret_cast<const float *>(g_dyn + kBk8cBytes); }
+__device__ __forceinline__ const float *g8c() { return reinterpret_cast<const float *>(g_dyn + kBk8cBytes + kL8cBytes); }
+
+__device__ __forceinline__ void expand_tab8()
+{
+    BucketEntry *bk = reinterpret_cast<BucketEntry *>(g_dyn);
+    for (int i = threadIdx.x; i < kRows8 * kCopies8; i += blockDim.x) {
+        const BucketEntry e = g_tab.bk8[i / kCopies8];
+        bk[i] = BucketEntry{e.boundary, e.kb4 * 16 + (i % kCopies8) * 4};
+    }
+    float *q = reinterpret_cast<float *>(g_dyn + kBk8cBytes), *g = reinterpret_cast<float *>(g_dyn + kBk8cBytes + kL8cBytes);
+    for (int i = threadIdx.x; i < 256 * kCopies8; i += blockDim.x) {
+        q[i] = g_tab.q8[i / kCopies8];
+        g[i] = g_tab.g8[i / kCopies8];
+    }
 }
 // e for S > 0: with S = (1 + f) 2^(eb-127), 255 * 2^e >= S holds first at
 // e = eb - 134 when (1 + f) <= 510/256 (mantissa field <= 0x7F0000), else at
@@ -165,6 +197,20 @@ template <int BITS>
 __device__ __forceinline__ void decode_add(float2 (&x)[8], float sigma, const LaneCodes<BITS> &c)
 {
     const float2 s2 = make_float2(sigma, sigma);
+    if (BITS == 8) {   // lane copies: byte 64 code + 4 (lane mod 16)
+        const float *q = q8c();
+        const uint32_t c4 = (threadIdx.x & 15u) << 2;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i0 = 2 * k, i1 = 2 * k + 1;
+            const uint32_t w0 = c.w[i0 >> 2], w1 = c.w[i1 >> 2];
+            const int b0 = 8 * (i0 & 3), b1 = 8 * (i1 & 3);
+            const uint32_t o0 = ((b0 >= 6 ? (w0 >> (b0 >= 6 ? b0 - 6 : 0)) : (w0 << 6)) & 0x3FC0u) | c4;
+            const uint32_t o1 = ((b1 >= 6 ? (w1 >> (b1 >= 6 ? b1 - 6 : 0)) : (w1 << 6)) & 0x3FC0u) | c4;
+            x[k] = f2_fma(s2, make_float2(lds_at<float>(q, o0), lds_at<float>(q, o1)), x[k]);
+        }
+        return;
+    }
     const float *q = Lvl<BITS>::q();
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -245,15 +291,19 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
         B[i + 4] = B[i] ^ 0x80000000u;
     }
 
-    const float *q = Lvl<BITS>::q();
-    const float *g = Lvl<BITS>::g();
-    const BucketEntry *bk = Lvl<BITS>::bk();
-    // byte offset of bucket b: 8b (2, 8 bits: r = rint(8Hy), 8b = r & ~7) or,
-    // for the lane-copied 4-bit table, 128b + 8 (lane mod 16) (r = rint(128Hy))
-    constexpr uint32_t kB = BITS == 4 ? (uint32_t)Lvl<BITS>::kMask << 7 : (uint32_t)Lvl<BITS>::kMask << 3;
-    const uint32_t lane_copy = BITS == 4 ? (threadIdx.x & 15u) << 3 : 0u;
+    // 8 bits: lane copies, level byte offsets 64 k + 4 (lane mod 16), steps of 64
+    const float *q = BITS == 8 ? q8c() : Lvl<BITS>::q();
+    const float *g = BITS == 8 ? g8c() : Lvl<BITS>::g();
+    const BucketEntry *bk = BITS == 8 ? bk8c() : Lvl<BITS>::bk();
+    constexpr uint32_t kStep = BITS == 8 ? 64u : 4u;
+    // byte offset of bucket b: 8b (2 bits: r = rint(8Hy), 8b = r & ~7) or,
+    // for the lane-copied 4- and 8-bit tables, 128b + 8 (lane mod 16)
+    // (r = rint(128Hy); 8 bits: b + 256)
+    constexpr uint32_t kB = BITS == 2 ? (uint32_t)Lvl<BITS>::kMask << 3 : (uint32_t)Lvl<BITS>::kMask << 7;
+    const uint32_t lane_copy = BITS == 2 ? 0u : (threadIdx.x & 15u) << 3;
     const float mul = Lvl<BITS>::mul();
-    const float2 mul2 = make_float2(mul, mul), M2 = make_float2(kMagic, kMagic);
+    const float magic = BITS == 8 ? kMagic + (float)(kOff8 * kSub8) : kMagic;
+    const float2 mul2 = make_float2(mul, mul), M2 = make_float2(magic, magic);
     const float2 m2 = make_float2(m, m), nz2 = make_float2(-0.0f, -0.0f);
     const float2 C2 = make_float2(8388608.0f, 8388608.0f);   // 2^23
     LaneCodes<BITS> out;
@@ -267,24 +317,33 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
         const float2 tf = f2_fma(y, mul2, M2);                 // S*H*y is exact: one rounding = rint
         const BucketEntry b0 = lds_at<BucketEntry>(bk, (__float_as_uint(tf.x) & kB) | lane_copy);
         const BucketEntry b1 = lds_at<BucketEntry>(bk, (__float_as_uint(tf.y) & kB) | lane_copy);
-        uint32_t k40 = (uint32_t)b0.kb4 + (y.x >= b0.boundary ? 4u : 0u);
-        uint32_t k41 = (uint32_t)b1.kb4 + (y.y >= b1.boundary ? 4u : 0u);
+        uint32_t k40 = (uint32_t)b0.kb4 + (y.x >= b0.boundary ? kStep : 0u);
+        uint32_t k41 = (uint32_t)b1.kb4 + (y.y >= b1.boundary ? kStep : 0u);
+        if (BITS == 8) {   // a non-finite y reaches rows past 512: keep its offsets inside the tables
+            k40 &= 0x3FFCu;
+            k41 &= 0x3FFCu;
+        }
         if (!ONE_LEVEL) {  // buckets wider than a gap: walk up (bounded by the top level)
-            constexpr uint32_t kTop4 = 4u * ((1u << BITS) - 1u);
-            while (k40 < kTop4 && y.x >= lds_at<float>(q, k40 + 4)) k40 += 4;
-            while (k41 < kTop4 && y.y >= lds_at<float>(q, k41 + 4)) k41 += 4;
+            constexpr uint32_t kTop = kStep * ((1u << BITS) - 1u);
+            while (k40 < kTop && y.x >= lds_at<float>(q, k40 + kStep)) k40 += kStep;
+            while (k41 < kTop && y.y >= lds_at<float>(q, k41 + kStep)) k41 += kStep;
         }
         const float2 qv = make_float2(lds_at<float>(q, k40), lds_at<float>(q, k41));
         const float2 gv = make_float2(lds_at<float>(g, k40), lds_at<float>(g, k41));
         const float2 t = f2_fma_rp(f2_sub(y, qv), gv, C2);     // 2^23 + ceil(d * G16)
         const float U0 = __uint_as_float(__byte_perm(A[k], 0x4B00u, 0x5410u));   // 2^23 + U
         const float U1 = __uint_as_float(__byte_perm(B[k], 0x4B00u, 0x5432u));
-        k40 += U0 < t.x ? 4u : 0u;
-        k41 += U1 < t.y ? 4u : 0u;
+        k40 += U0 < t.x ? kStep : 0u;
+        k41 += U1 < t.y ? kStep : 0u;
         const int i0 = 2 * k, i1 = 2 * k + 1;
         const int s0 = (BITS * i0) & 31, s1 = (BITS * i1) & 31;
-        out.w[(BITS * i0) >> 5] |= s0 >= 2 ? (k40 << (s0 >= 2 ? s0 - 2 : 0)) : (k40 >> 2);
-        out.w[(BITS * i1) >> 5] |= s1 >= 2 ? (k41 << (s1 >= 2 ? s1 - 2 : 0)) : (k41 >> 2);
+        if (BITS == 8) {   // code = offset / 64 (the lane part is below bit 6)
+            out.w[(BITS * i0) >> 5] |= (k40 >> 6) << s0;
+            out.w[(BITS * i1) >> 5] |= (k41 >> 6) << s1;
+        } else {
+            out.w[(BITS * i0) >> 5] |= s0 >= 2 ? (k40 << (s0 >= 2 ? s0 - 2 : 0)) : (k40 >> 2);
+            out.w[(BITS * i1) >> 5] |= s1 >= 2 ? (k41 << (s1 >= 2 ? s1 - 2 : 0)) : (k41 >> 2);
+        }
     }
     return out;
 }
@@ -437,16 +496,18 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
 template <bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32>
 __global__ void __launch_bounds__(kWarps * 32, kHopBlocksPerSM) hop_kernel(const __grid_constant__ HopParams P)
 {
-    extern __shared__ __align__(16) uint8_t dyn[];
     block_copy(&g_tab, &P.tab);
     __syncthreads();
     expand_bk4();
+    expand_tab8();
     __syncthreads();
+    uint8_t *dyn = g_dyn + kTab8Bytes;
     constexpr int STAGE = stage_bytes<ADD_F32, SF32>();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint8_t *stg = dyn + warp * kStages * STAGE;
-    const int64_t nw = (int64_t)gridDim.x * kWarps;
-    for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < P.total_units; u += nw) {
+    const int wpb = (int)(blockDim.x >> 5);   // warps per block: sized to the launch, at most kWarps
+    const int64_t nw = (int64_t)gridDim.x * wpb;
+    for (int64_t u = (int64_t)blockIdx.x * wpb + warp; u < P.total_units; u += nw) {
         int ti, seg;
         locate_unit(P.task, P.n_tasks, u, ti, seg);
         const HopTask &t = P.task[ti];
@@ -845,20 +906,22 @@ __global__ void barrier_selftest_kernel(unsigned *counter, int32_t *status, unsi
 // gradient.  After the last step the owners' messages are decoded into every
 // output (one read, N writes).  Grid barriers separate the phases.
 template <bool ONE_LEVEL, bool SF32>
-__global__ void __launch_bounds__(kWarps * 32) fused_ring_kernel(const __grid_constant__ FusedRingParams P)
+__global__ void __launch_bounds__(kWarps * 32, 1) fused_ring_kernel(const __grid_constant__ FusedRingParams P)
 {
-    extern __shared__ __align__(16) uint8_t dyn[];
     block_copy(&g_tab, &P.tab);
     __syncthreads();
     expand_bk4();
+    expand_tab8();
     __syncthreads();
+    uint8_t *dyn = g_dyn + kTab8Bytes;
     constexpr int STAGE = stage_bytes<false, SF32>();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint8_t *stg = dyn + warp * kStages * STAGE;
     const int N = P.n_ranks;
-    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    const int wpb = (int)(blockDim.x >> 5);   // warps per block: sized to the launch, at most kWarps
+    const int64_t nw = (int64_t)gridDim.x * wpb;
     for (int t = 0; t <= N; ++t) {
-        for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < P.units; u += nw) {
+        for (int64_t u = (int64_t)blockIdx.x * wpb + warp; u < P.units; u += nw) {
             int c = 0;
             while (c + 1 < N && u >= P.unit_begin[c + 1][0]) ++c;
             int seg = 0;
@@ -923,6 +986,17 @@ cudaError_t allow_dyn_smem(K kernel, size_t dyn, bool (&done)[128])
     return e;
 }
 
+// Warps per block of a hop launch: one block per SM (its tables fill most of
+// shared memory), as many warps as spread the launch's units over all SMs,
+// at most kWarps.  The dynamic allocation always covers kWarps warps of
+// staging, so a bucket row read for a non-finite value stays inside it.
+inline int hop_block_warps(int64_t units)
+{
+    const int64_t sms = sm_count();
+    const int64_t w = (units + sms - 1) / sms;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(kWarps, w));
+}
+
 template <typename K>
 int grid_for(K kernel, int warps, size_t dyn_smem, int64_t units)
 {
@@ -938,12 +1012,13 @@ int grid_for(K kernel, int warps, size_t dyn_smem, int64_t units)
 template <bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32>
 cudaError_t launch_hop_t(const HopParams &P, cudaStream_t st)
 {
-    const size_t dyn = (size_t)kWarps * kStages * stage_bytes<ADD_F32, SF32>();
+    const size_t dyn = (size_t)kTab8Bytes + (size_t)kWarps * kStages * stage_bytes<ADD_F32, SF32>();
     auto k = hop_kernel<HAS_IN, ADD_F32, ONE_LEVEL, SF32>;
     static bool opted[128] = {false};   // one record per instantiation of this launcher
     const cudaError_t ea = allow_dyn_smem(k, dyn, opted);
     if (ea != cudaSuccess) return ea;
-    k<<<grid_for(k, kWarps, dyn, P.total_units), kWarps * 32, dyn, st>>>(P);
+    const int wpb = hop_block_warps(P.total_units);
+    k<<<grid_for(k, wpb, dyn, P.total_units), wpb * 32, dyn, st>>>(P);
     note_launches(1);
     return cudaGetLastError();
 }
@@ -992,22 +1067,23 @@ namespace {
 template <bool ONE_LEVEL, bool SF32>
 cudaError_t launch_fused_t(const FusedRingParams &P, cudaStream_t st)
 {
-    const size_t dyn = (size_t)kWarps * kStages * stage_bytes<false, SF32>();
+    const size_t dyn = (size_t)kTab8Bytes + (size_t)kWarps * kStages * stage_bytes<false, SF32>();
     auto k = fused_ring_kernel<ONE_LEVEL, SF32>;
     static bool opted[128] = {false};   // one record per instantiation of this launcher
     cudaError_t e = allow_dyn_smem(k, dyn, opted);
     if (e != cudaSuccess) return e;
+    const int wpb = hop_block_warps(P.units);
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kWarps * 32, dyn);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, wpb * 32, dyn);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorLaunchOutOfResources;
     // every CTA must be resident at once (cooperative launch): at most the
     // CTAs that fit, and no more than the work needs
     const int64_t cap = (int64_t)sm_count() * per_sm;
-    const int64_t need = std::max<int64_t>(1, (P.units + kWarps - 1) / kWarps);
+    const int64_t need = std::max<int64_t>(1, (P.units + wpb - 1) / wpb);
     const int grid = (int)std::min(cap, need);
     void *args[] = {const_cast<FusedRingParams *>(&P)};
-    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(k), dim3(grid), dim3(kWarps * 32), args, dyn, st);
+    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(k), dim3(grid), dim3(wpb * 32), args, dyn, st);
     note_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
