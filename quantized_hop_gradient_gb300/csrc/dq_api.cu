@@ -219,15 +219,29 @@ HopTask make_task(const dq_config *cfg, const dq_stage &s)
     return t;
 }
 
+// The Philox key schedule of a launch (seed as key, round as counter words 2
+// and 3): round keys and round 0's lane-independent part.
+PhiloxKeys philox_keys(uint64_t seed, uint64_t round)
+{
+    const uint32_t M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    PhiloxKeys K;
+    for (int r = 0; r < 10; ++r) {
+        K.k0[r] = (uint32_t)seed + (uint32_t)r * W0;
+        K.k1[r] = (uint32_t)(seed >> 32) + (uint32_t)r * W1;
+    }
+    const uint64_t p = (uint64_t)M1 * (uint32_t)round;
+    K.a0 = (uint32_t)(p >> 32) ^ K.k0[0];
+    K.l1 = (uint32_t)p;
+    K.r1k = (uint32_t)(round >> 32) ^ K.k1[0];
+    return K;
+}
+
 void fill_common(HopParams &P, const dq_config *cfg, const float *mu, const int32_t *perm)
 {
     P.n_ranks = cfg->n_ranks;
     P.mu = mu;
     P.perm = perm;
-    P.key0 = (uint32_t)cfg->seed;
-    P.key1 = (uint32_t)(cfg->seed >> 32);
-    P.round0 = (uint32_t)cfg->round;
-    P.round1 = (uint32_t)(cfg->round >> 32);
+    P.ph = philox_keys(cfg->seed, cfg->round);
     P.scale_fp32 = cfg->scale_fp32;
 }
 
@@ -860,10 +874,7 @@ dq_status dq_exchange_fused(const dq_config *cfg, const void *const *grads, int6
     P->correlated = cfg->correlated ? 1 : 0;
     P->mu = mu;
     P->perm = perm;
-    P->key0 = (uint32_t)cfg->seed;
-    P->key1 = (uint32_t)(cfg->seed >> 32);
-    P->round0 = (uint32_t)cfg->round;
-    P->round1 = (uint32_t)(cfg->round >> 32);
+    P->ph = philox_keys(cfg->seed, cfg->round);
     P->out_is_bf16 = out_is_bf16 ? 1 : 0;
     P->scale_fp32 = cfg->scale_fp32;
     P->out_align32 = 1;

@@ -95,6 +95,19 @@ struct HopTask {
 
 constexpr int kMaxTasks = 32;
 
+// Philox4x32-10 with key (seed low, seed high) and counter words 2, 3 =
+// (round low, round high), prepared once per launch on the host: the round
+// keys of rounds 1..9 (the key plus r times the Weyl constants) and round 0's
+// part that involves no lane value (the product of word 2, its high half
+// xored with the key).  The kernels then read every key straight from the
+// launch parameters.
+struct PhiloxKeys {
+    uint32_t k0[10], k1[10];    // round keys (k0[0], k1[0] = the seed)
+    uint32_t a0;                // mulhi(M1, round low) ^ k0[0]
+    uint32_t l1;                // M1 * round low
+    uint32_t r1k;               // round high ^ k1[0]
+};
+
 struct HopParams {
     Tables tab;
     HopTask task[kMaxTasks];
@@ -103,8 +116,7 @@ struct HopParams {
     int64_t total_units;
     const float *mu;
     const int32_t *perm;
-    uint32_t key0, key1;        // seed
-    uint32_t round0, round1;    // round
+    PhiloxKeys ph;              // generator key schedule (seed, round)
     int32_t scale_fp32;         // group scales in fp32 (ablation) instead of UINT8
 };
 
@@ -170,7 +182,7 @@ struct FusedRingParams {
     int32_t correlated;
     const float *mu;
     const int32_t *perm;
-    uint32_t key0, key1, round0, round1;
+    PhiloxKeys ph;                             // generator key schedule (seed, round)
     int32_t out_is_bf16;
     int32_t scale_fp32;
     int32_t out_align32;                       // every output is 32-byte aligned
@@ -183,19 +195,22 @@ struct FusedRingParams {
 // Philox4x32-10 (Salmon et al., SC 2011): ten rounds; each multiplies words
 // 0 and 2 by the Philox constants (full 64-bit products), xors the high
 // halves into words 1 and 3 with the round key, and bumps the key by the
-// Weyl constants between rounds.
+// Weyl constants between rounds.  Here on the counter (c0, c1, round low,
+// round high) with the key schedule K prepared on the host (PhiloxKeys).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32_t k1)
+__device__ __forceinline__ void philox4x32_10_keyed(uint32_t c[4], uint32_t c0, uint32_t c1, const PhiloxKeys &K)
 {
     const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
-    const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    c[0] = K.a0 ^ c1;              // round 0
+    c[1] = K.l1;
+    c[2] = __umulhi(M0, c0) ^ K.r1k;
+    c[3] = M0 * c0;
 #pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        if (r) { k0 += W0; k1 += W1; }
+    for (int r = 1; r < 10; ++r) {
         const uint32_t hi0 = __umulhi(M0, c[0]), lo0 = M0 * c[0];
         const uint32_t hi1 = __umulhi(M1, c[2]), lo1 = M1 * c[2];
-        const uint32_t n0 = hi1 ^ c[1] ^ k0;
-        const uint32_t n2 = hi0 ^ c[3] ^ k1;
+        const uint32_t n0 = hi1 ^ c[1] ^ K.k0[r];
+        const uint32_t n2 = hi0 ^ c[3] ^ K.k1[r];
         c[0] = n0; c[1] = lo1; c[2] = n2; c[3] = lo0;
     }
 }

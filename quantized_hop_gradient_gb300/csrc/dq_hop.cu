@@ -51,20 +51,31 @@ __device__ __forceinline__ void expand_bk4()
 // row) whose entry for copy c holds 64 kb + 4c, and the levels and
 // reciprocal gaps (64 bytes per level), so the level and gap of copy c sit
 // at byte 64 k + 4c.  The 16 lanes of a half-warp never meet in a bank (pair).
+// After them, in the kernels whose addends are bf16 (fp32 addends leave no
+// room), the decoder's 4-bit pair table: entry p (a code byte: low nibble =
+// first coordinate's code) holds the two levels, one copy per half-warp
+// lane, copy c of entry p at byte 128 p + 8c.
 extern __shared__ __align__(16) uint8_t g_dyn[];
 constexpr int kCopies8 = 16;
 constexpr int kRows8 = 2 * kOff8 + 1;
 constexpr int kBk8cBytes = kRows8 * kCopies8 * 8;
 constexpr int kL8cBytes = 256 * kCopies8 * 4;
+constexpr int kQ4pBytes = 256 * kCopies4 * 8;
 constexpr int kTab8Bytes = kBk8cBytes + 2 * kL8cBytes;
-static_assert(kTab8Bytes % 16 == 0, "16-byte aligned staging");
+__host__ __device__ constexpr int tab_bytes(bool add_f32) { return kTab8Bytes + (add_f32 ? 0 : kQ4pBytes); }
+static_assert(kTab8Bytes % 16 == 0 && kQ4pBytes % 16 == 0, "16-byte aligned staging");
 // rows up to 1023 (a non-finite y) stay inside the smallest dynamic allocation
 static_assert(1024 * kCopies8 * 8 <= kTab8Bytes + kWarps * kStages * (1024 + 512 + 32), "garbage rows in bounds");
 __device__ __forceinline__ const BucketEntry *bk8c() { return reinterpret_cast<const BucketEntry *>(g_dyn); }
 __device__ __forceinline__ const float *q8c() { return reinterpret_cast<const float *>(g_dyn + kBk8cBytes); }
 __device__ __forceinline__ const float *g8c() { return reinterpret_cast<const float *>(g_dyn + kBk8cBytes + kL8cBytes); }
+__device__ __forceinline__ const float2 *q4p() { return reinterpret_cast<const float2 *>(g_dyn + kBk8cBytes + 2 * kL8cBytes); }
+// The decoder's 2-bit pair table: entry p (four bits: low two = first
+// coordinate's code) holds the two levels; 16 entries of 8 bytes cover the
+// 32 banks once, so any lookup pattern is conflict-free.
+__shared__ __align__(16) float2 g_q2p[16];
 
-__device__ __forceinline__ void expand_tab8()
+__device__ __forceinline__ void expand_tables(bool pair4)
 {
     BucketEntry *bk = reinterpret_cast<BucketEntry *>(g_dyn);
     for (int i = threadIdx.x; i < kRows8 * kCopies8; i += blockDim.x) {
@@ -76,6 +87,12 @@ __device__ __forceinline__ void expand_tab8()
         q[i] = g_tab.q8[i / kCopies8];
         g[i] = g_tab.g8[i / kCopies8];
     }
+    float2 *p4 = reinterpret_cast<float2 *>(g_dyn + kBk8cBytes + 2 * kL8cBytes);
+    for (int i = threadIdx.x; pair4 && i < 256 * kCopies4; i += blockDim.x) {
+        const int p = i / kCopies4;
+        p4[i] = make_float2(g_tab.q4[p & 15], g_tab.q4[p >> 4]);
+    }
+    for (int i = threadIdx.x; i < 16; i += blockDim.x) g_q2p[i] = make_float2(g_tab.q2[i & 3], g_tab.q2[i >> 2]);
 }
 // e for S > 0: with S = (1 + f) 2^(eb-127), 255 * 2^e >= S holds first at
 // e = eb - 134 when (1 + f) <= 510/256 (mantissa field <= 0x7F0000), else at
@@ -179,25 +196,15 @@ __device__ __forceinline__ void stg_codes(uint8_t *p, const LaneCodes<BITS> &c)
     else *reinterpret_cast<uint4 *>(p) = make_uint4(c.w[0], c.w[1], c.w[2], c.w[3]);
 }
 
-// 4x the code of coordinate i of a lane (a byte offset into a level table)
-template <int BITS>
-__device__ __forceinline__ uint32_t code_off(const LaneCodes<BITS> &c, int i)
-{
-    const int bit = (BITS * i) & 31;
-    const uint32_t w = c.w[(BITS * i) >> 5];
-    const uint32_t v = bit >= 2 ? (w >> (bit >= 2 ? bit - 2 : 0)) : (w << 2);
-    return v & (((1u << BITS) - 1u) << 2);
-}
-
 // x = fl(sigma * q_code + x) with one rounding (fused multiply-add); sigma
 // is u * 2^(E-127) (0 when E = 0) with UINT8 scales, the fp32 scale itself
-// otherwise.  One level-table load per code: the 2- and 4-bit tables span
-// 4 and 16 banks, so their loads never conflict.
-template <int BITS>
+// otherwise.  2 and 4 bits: one 8-byte pair-table load per two codes (both
+// tables conflict-free); 8 bits: one lane-copy level load per code.
+template <int BITS, bool PAIR4>
 __device__ __forceinline__ void decode_add(float2 (&x)[8], float sigma, const LaneCodes<BITS> &c)
 {
     const float2 s2 = make_float2(sigma, sigma);
-    if (BITS == 8) {   // lane copies: byte 64 code + 4 (lane mod 16)
+    if constexpr (BITS == 8) {   // lane copies: byte 64 code + 4 (lane mod 16)
         const float *q = q8c();
         const uint32_t c4 = (threadIdx.x & 15u) << 2;
 #pragma unroll
@@ -209,13 +216,33 @@ __device__ __forceinline__ void decode_add(float2 (&x)[8], float sigma, const La
             const uint32_t o1 = ((b1 >= 6 ? (w1 >> (b1 >= 6 ? b1 - 6 : 0)) : (w1 << 6)) & 0x3FC0u) | c4;
             x[k] = f2_fma(s2, make_float2(lds_at<float>(q, o0), lds_at<float>(q, o1)), x[k]);
         }
-        return;
-    }
-    const float *q = Lvl<BITS>::q();
+    } else if constexpr (BITS == 4 && !PAIR4) {   // one level load per code (16 entries: 16 banks)
+        const float *q = Lvl<4>::q();
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const float2 lv = make_float2(lds_at<float>(q, code_off<BITS>(c, 2 * k)), lds_at<float>(q, code_off<BITS>(c, 2 * k + 1)));
-        x[k] = f2_fma(s2, lv, x[k]);
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t w = c.w[k >> 2];
+            const int b = 8 * (k & 3);
+            const uint32_t o0 = (b >= 2 ? (w >> (b >= 2 ? b - 2 : 0)) : (w << 2)) & 0x3Cu;
+            const uint32_t o1 = (w >> (b + 2)) & 0x3Cu;
+            x[k] = f2_fma(s2, make_float2(lds_at<float>(q, o0), lds_at<float>(q, o1)), x[k]);
+        }
+    } else if constexpr (BITS == 4) {   // pair k = code byte k: byte offset 128 byte + 8 (lane mod 16)
+        const float2 *q = q4p();
+        const uint32_t c8 = (threadIdx.x & 15u) << 3;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t w = c.w[k >> 2];
+            const int b = 8 * (k & 3);
+            const uint32_t o = ((b >= 7 ? (w >> (b >= 7 ? b - 7 : 0)) : (w << 7)) & 0x7F80u) | c8;
+            x[k] = f2_fma(s2, lds_at<float2>(q, o), x[k]);
+        }
+    } else {   // 2 bits: pair k = bits 4k .. 4k+3, byte offset 8 * nibble
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t w = c.w[0];
+            const uint32_t o = (k == 0 ? (w << 3) : (w >> (k == 0 ? 0 : 4 * k - 3))) & 0x78u;
+            x[k] = f2_fma(s2, lds_at<float2>(g_q2p, o), x[k]);
+        }
     }
 }
 
@@ -234,8 +261,7 @@ __device__ __forceinline__ void decode_add(float2 (&x)[8], float sigma, const La
 // off: the correlated-rounding offset of this quantizer, in [0, 2^16).
 template <int BITS, bool ONE_LEVEL, bool SF32>
 __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], uint32_t ctr0, uint32_t stage_word,
-                                                          uint32_t off, uint32_t key0, uint32_t key1,
-                                                          uint32_t round0, uint32_t round1, uint32_t &E_out,
+                                                          uint32_t off, const PhiloxKeys &K, uint32_t &E_out,
                                                           uint32_t &u_out)
 {
     // group maximum as a three-level tree of three-way maxima (max is exact,
@@ -279,8 +305,8 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
     // plus 2^15 (mod 2^16) for c >= 8, plus the correlated offset.  Word A
     // carries coordinate 2i's field in its low half, word B coordinate
     // 2i+1's in its high half (carries out of a half are never read).
-    uint32_t r0[4] = {ctr0, stage_word, round0, round1};
-    philox4x32_10(r0, key0, key1);
+    uint32_t r0[4];
+    philox4x32_10_keyed(r0, ctr0, stage_word, K);
     const uint32_t offh = off << 16;
     uint32_t A[8], B[8];
 #pragma unroll
@@ -461,15 +487,14 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
                 sigma = __fmul_rn((float)u, __uint_as_float(ein << 23));
             }
             const LaneCodes<BITS> c = lds_codes<BITS>(st + C_OFF + half * 256 + hl * 2 * BITS);
-            decode_add<BITS>(x, sigma, c);
+            decode_add<BITS, !ADD_F32>(x, sigma, c);
         }
         const bool send = (send_m >> s) & 1u;
         const bool keep = (keep_m >> s) & 1u;
         uint32_t E = 0u, u = 0u;
         if (__any_sync(kFull, send)) {
             const uint32_t ctr0 = (uint32_t)old * 16u + (uint32_t)hl;   // global coordinate index / 16
-            const LaneCodes<BITS> q = quantize_group<BITS, ONE_LEVEL, SF32>(x, ctr0, stage_word, corr, P.key0,
-                                                                            P.key1, P.round0, P.round1, E, u);
+            const LaneCodes<BITS> q = quantize_group<BITS, ONE_LEVEL, SF32>(x, ctr0, stage_word, corr, P.ph, E, u);
             if (send) {
                 stg_codes<BITS>(out_c + (int64_t)s * CB, q);
                 if (SF32) *reinterpret_cast<uint32_t *>(out_u + (int64_t)s * UB) = u;
@@ -499,9 +524,9 @@ __global__ void __launch_bounds__(kWarps * 32, kHopBlocksPerSM) hop_kernel(const
     block_copy(&g_tab, &P.tab);
     __syncthreads();
     expand_bk4();
-    expand_tab8();
+    expand_tables(!ADD_F32 && HAS_IN);
     __syncthreads();
-    uint8_t *dyn = g_dyn + kTab8Bytes;
+    uint8_t *dyn = g_dyn + tab_bytes(ADD_F32);
     constexpr int STAGE = stage_bytes<ADD_F32, SF32>();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint8_t *stg = dyn + warp * kStages * STAGE;
@@ -911,9 +936,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) fused_ring_kernel(const __grid
     block_copy(&g_tab, &P.tab);
     __syncthreads();
     expand_bk4();
-    expand_tab8();
+    expand_tables(true);
     __syncthreads();
-    uint8_t *dyn = g_dyn + kTab8Bytes;
+    uint8_t *dyn = g_dyn + tab_bytes(false);
     constexpr int STAGE = stage_bytes<false, SF32>();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint8_t *stg = dyn + warp * kStages * STAGE;
@@ -1012,7 +1037,7 @@ int grid_for(K kernel, int warps, size_t dyn_smem, int64_t units)
 template <bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32>
 cudaError_t launch_hop_t(const HopParams &P, cudaStream_t st)
 {
-    const size_t dyn = (size_t)kTab8Bytes + (size_t)kWarps * kStages * stage_bytes<ADD_F32, SF32>();
+    const size_t dyn = (size_t)tab_bytes(ADD_F32) + (size_t)kWarps * kStages * stage_bytes<ADD_F32, SF32>();
     auto k = hop_kernel<HAS_IN, ADD_F32, ONE_LEVEL, SF32>;
     static bool opted[128] = {false};   // one record per instantiation of this launcher
     const cudaError_t ea = allow_dyn_smem(k, dyn, opted);
@@ -1067,7 +1092,7 @@ namespace {
 template <bool ONE_LEVEL, bool SF32>
 cudaError_t launch_fused_t(const FusedRingParams &P, cudaStream_t st)
 {
-    const size_t dyn = (size_t)kTab8Bytes + (size_t)kWarps * kStages * stage_bytes<false, SF32>();
+    const size_t dyn = (size_t)tab_bytes(false) + (size_t)kWarps * kStages * stage_bytes<false, SF32>();
     auto k = fused_ring_kernel<ONE_LEVEL, SF32>;
     static bool opted[128] = {false};   // one record per instantiation of this launcher
     cudaError_t e = allow_dyn_smem(k, dyn, opted);
