@@ -366,9 +366,9 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
         if (BITS == 8) {   // code = offset / 64 (the lane part is below bit 6)
             out.w[(BITS * i0) >> 5] |= (k40 >> 6) << s0;
             out.w[(BITS * i1) >> 5] |= (k41 >> 6) << s1;
-        } else {
-            out.w[(BITS * i0) >> 5] |= s0 >= 2 ? (k40 << (s0 >= 2 ? s0 - 2 : 0)) : (k40 >> 2);
-            out.w[(BITS * i1) >> 5] |= s1 >= 2 ? (k41 << (s1 >= 2 ? s1 - 2 : 0)) : (k41 >> 2);
+        } else {   // codes never overlap, so adding them packs (a shift-and-add each)
+            out.w[(BITS * i0) >> 5] += s0 >= 2 ? (k40 << (s0 >= 2 ? s0 - 2 : 0)) : (k40 >> 2);
+            out.w[(BITS * i1) >> 5] += s1 >= 2 ? (k41 << (s1 >= 2 ? s1 - 2 : 0)) : (k41 >> 2);
         }
     }
     return out;
