@@ -572,9 +572,9 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
     seq_out = [outs_pool[i % len(full)] for i in range(nb - 1)] + [outs_pool[-1]]
     bucket_sg = w.bucket // SG
     kw = dict(budget=w.budget, correlated=w.correlated, butterfly=w.topology == "butterfly", seed=0)
-    # the overlapped stream picks its exchange itself ("auto": per-step launches
-    # beside the next bucket's planning); the cooperative one-launch exchange
-    # (rings of up to 64 ranks) is timed beside it for comparison
+    # the overlapped stream picks its exchange itself ("auto": the cooperative
+    # one-launch exchange for rings of up to 64 ranks and 2^16 super-groups);
+    # the other exchange is timed beside it for comparison
     from quantized_hop_gradient_gb300.allreduce import use_fused
     fusable = use_fused(N, w.topology == "butterfly", bucket_sg)
     ov = BucketedAllReduce(N, bucket_sg, overlap=True, fused="auto", **kw)

@@ -17,15 +17,14 @@ from .allreduce import DynamiQAllReduce, use_fused
 class BucketedAllReduce:
     def __init__(self, n_ranks: int, bucket_sg: int, *, overlap: bool = True, fused="auto", **kw):
         """``fused``: each bucket's ring exchange as one cooperative launch
-        (dq_exchange_fused): True, False, or "auto".  "auto" takes the
-        per-step launches when planning overlaps the exchange: the next
-        bucket's planning runs beside them, while a cooperative exchange
-        holds every SM, and the single-block planning of small buckets (up
-        to 16,384 super-groups) then cannot start until it ends.  Without
-        overlap "auto" follows ``use_fused``."""
+        (dq_exchange_fused): True, False, or "auto", which follows
+        ``use_fused``.  The one-launch exchange wins with or without the
+        overlap: 25 MB buckets of an 8-rank ring took 0.322 ms each against
+        0.373 with per-step launches, the next bucket's planning on the
+        second stream in both."""
         self.n_ranks, self.bucket_sg, self.overlap = n_ranks, bucket_sg, overlap
         if fused == "auto":
-            fused = (not overlap) and use_fused(n_ranks, kw.get("butterfly", False), bucket_sg)
+            fused = use_fused(n_ranks, kw.get("butterfly", False), bucket_sg)
         self.fused = bool(fused)
         self.sets = [DynamiQAllReduce(n_ranks, bucket_sg, **kw) for _ in range(2)]
         self.plan_stream = torch.cuda.Stream() if overlap else None

@@ -91,8 +91,8 @@ def test_gemma1b_ring16_full_size_sampled():
 def test_llama3_8b_buckets_full_size():
     """The streamed Llama-3-8B workload in its bench configuration: 25 MB
     buckets of 13,107,200 coordinates, two streams, with the exchange the
-    stream picks (per-step launches beside the next bucket's planning) and
-    with the cooperative one-launch exchange.  The first bucket, one from
+    stream picks (the cooperative one-launch exchange) and with per-step
+    launches.  The first bucket, one from
     the middle and the short last bucket (of 613) are reduced as one stream
     and compared with the oracle in full."""
     from quantized_hop_gradient_gb300.allreduce import use_fused
@@ -109,11 +109,11 @@ def test_llama3_8b_buckets_full_size():
         gu = [synth.as_u16(g) for g in b]
         cfg = oracle.Config(N, w.budget, correlated=w.correlated, seed=0, round=100 + i)
         exps.append(oracle.allreduce(cfg, gu)[1])
-    for fused in ("auto", True):
+    for fused in (False, "auto"):
         outs = [[torch.empty(g.numel(), dtype=torch.float32, device="cuda") for g in b] for b in buckets]
         ar = BucketedAllReduce(N, w.bucket // 256, overlap=True, fused=fused, budget=w.budget,
                                correlated=w.correlated, seed=0)
-        assert ar.fused == (fused is True)
+        assert ar.fused == (fused == "auto")   # "auto" takes the one-launch exchange at this size
         assert all(use_fused(N, False, s.n_sg) for s in ar.sets)   # the size allows the one-launch exchange
         ar.run(buckets, outs, round0=100)
         torch.cuda.synchronize()
