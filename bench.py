@@ -49,7 +49,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     p.add_argument("--exchange", choices=["auto", "fused", "multi"], default="auto",
                    help="ring exchange as one cooperative launch (fused) or one launch per step (multi); "
-                        "auto: fused where it is the faster path (allreduce.use_fused: rings of up to 64 ranks, up to 2^16 "
+                        "auto: fused where it is the faster path (allreduce.use_fused: rings of up to 64 ranks, up to 2^17 "
                         "super-groups per worker)")
     p.add_argument("--bucket-pool", type=int, default=16,
                    help="streamed workloads: distinct buckets kept resident and cycled through a full pass")
@@ -573,7 +573,7 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
     bucket_sg = w.bucket // SG
     kw = dict(budget=w.budget, correlated=w.correlated, butterfly=w.topology == "butterfly", seed=0)
     # the overlapped stream picks its exchange itself ("auto": the cooperative
-    # one-launch exchange for rings of up to 64 ranks and 2^16 super-groups);
+    # one-launch exchange for rings of up to 64 ranks and 2^17 super-groups);
     # the other exchange is timed beside it for comparison
     from quantized_hop_gradient_gb300.allreduce import use_fused
     fusable = use_fused(N, w.topology == "butterfly", bucket_sg)

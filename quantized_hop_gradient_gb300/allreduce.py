@@ -14,12 +14,12 @@ from . import dq
 SG = dq.SG
 
 # Largest per-worker size (super-groups) at which the fused ring exchange is
-# the faster one on a GB300 (BERT-large distribution, 8 ranks): 0.367 vs
-# 0.432 ms at 2^22 coordinates per worker, 0.631 vs 0.694 ms at 2^24; above
-# that the per-step launches win (1.053 vs 1.175 ms at 2^25, 1.684 vs 1.740
-# ms at 2^26), their flat-launched final decode streaming the outputs faster
-# than the cooperative kernel's last phase.
-FUSED_MAX_SG = 1 << 16
+# the faster one on a GB300 (BERT-large distribution, 8 ranks, exchange
+# alone): 0.332 vs 0.377 ms at 2^24 coordinates per worker, 0.620 vs 0.637 ms
+# at 2^25; behind above that (1.173 vs 1.137 ms at 2^26, 4.91 vs 4.64 ms at
+# 335 M coordinates), where the per-step path's flat launches stream HBM
+# faster than the persistent cooperative kernel.
+FUSED_MAX_SG = 1 << 17
 
 
 def use_fused(n_ranks: int, butterfly: bool, n_sg: int) -> bool:

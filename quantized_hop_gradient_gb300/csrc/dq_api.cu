@@ -329,12 +329,6 @@ cudaError_t run_decodes(DecodeParams &D, const std::vector<PendingDecode> &chunk
         }
         D.n_tasks = n;
         D.total_units = units;
-        bool a32 = true;
-        if (D.n_outs > 0)
-            for (int32_t k = 0; k < D.n_outs; ++k) a32 = a32 && ((uintptr_t)D.outs[k] & 31u) == 0;
-        else
-            for (int k = 0; k < n; ++k) a32 = a32 && ((uintptr_t)D.task[k].out & 31u) == 0;
-        D.out_align32 = a32 ? 1 : 0;
         if (n > 0) {
             const LogSlot slot = log_begin(log, DQ_LAUNCH_DECODE, sgs, st);
             const cudaError_t e = launch_decode(D, st);
@@ -877,8 +871,6 @@ dq_status dq_exchange_fused(const dq_config *cfg, const void *const *grads, int6
     P->ph = philox_keys(cfg->seed, cfg->round);
     P->out_is_bf16 = out_is_bf16 ? 1 : 0;
     P->scale_fp32 = cfg->scale_fp32;
-    P->out_align32 = 1;
-    for (int32_t r = 0; r < N; ++r) P->out_align32 &= ((uintptr_t)P->outs[r] & 31u) == 0 ? 1 : 0;
     P->barrier = reinterpret_cast<unsigned int *>(w + X.total);
     P->status = status_dev;
     P->timeout_cycles = kBarrierTimeoutCycles;

@@ -145,9 +145,6 @@ struct DecodeParams {
     // read of the message, n_outs writes) and the tasks' `out` is unused
     int32_t n_outs;
     void *outs[kMaxDecodeOuts];
-    // every output address this launch writes is 32-byte aligned (fp32
-    // outputs then go out as 32-byte stores)
-    int32_t out_align32;
 };
 
 // Statistics of several ranks in one launch.
@@ -185,7 +182,6 @@ struct FusedRingParams {
     PhiloxKeys ph;                             // generator key schedule (seed, round)
     int32_t out_is_bf16;
     int32_t scale_fp32;
-    int32_t out_align32;                       // every output is 32-byte aligned
     unsigned int *barrier;                     // arrival counter, zero at launch
     int32_t *status;                           // zero at launch; kDeviceBarrierTimeout on a timeout
     long long timeout_cycles;                  // bound of every barrier wait (SM clock cycles)

@@ -547,196 +547,10 @@ __global__ void __launch_bounds__(kWarps * 32, kHopBlocksPerSM) hop_kernel(const
 
 // ---------------------------------------------------------------------------
 // Final decode: out[perm[j]*256 + i] = fl(sigma * q_code + fl(mu_j * N)) (one
-// rounding), fp32 or bf16.  Output-bound (4 bytes out per 0.69 in).  Three
-// variants: decode_unit_bulk (the decode kernel) writes through the
-// bulk-copy engine; the fused exchange's last phase stores directly, with
-// decode_unit_wide when every output is 32-byte aligned and decode_unit
-// otherwise.  decode_unit: lane l of the warp decodes coordinates 4l..4l+3
-// (group l/4) and 128+4l..131+4l (group 8 + l/4) of a super-group, so each
-// warp store writes 512 contiguous bytes.  Eight super-groups are loaded
-// before any is computed.
+// rounding), fp32 or bf16.  Output-bound (4 bytes out per 0.69 in): both the
+// decode kernel and the fused exchange's last phase hand the stores to the
+// bulk-copy engine (decode_unit_bulk).
 // ---------------------------------------------------------------------------
-template <int BITS>
-__device__ __forceinline__ uint32_t ldg_codes4(const uint8_t *blk, int idx)
-{
-    // codes of 4 consecutive coordinates starting at coordinate 4*idx
-    if (BITS == 8) return __ldcg(reinterpret_cast<const uint32_t *>(blk) + idx);
-    if (BITS == 4) return __ldcg(reinterpret_cast<const unsigned short *>(blk) + idx);
-    return __ldcg(blk + idx);
-}
-
-// Decode super-groups j0 .. j0+cnt-1 of message `msg` (range starting at
-// lo) into every one of the n_outs outputs.  PP supplies perm, mu, n_ranks
-// and out_is_bf16.
-template <int BITS, bool SF32, typename PP>
-__device__ __forceinline__ void decode_unit(const PP &P, const MsgView &msg, int64_t lo, void *const *outs,
-                                            int n_outs, int64_t j0, int cnt, int lane)
-{
-    constexpr int kAhead = 8;
-    int32_t old_i = 0;
-    float mu_i = 0.0f;
-    uint32_t ein_i = 0;
-    if (lane < cnt) {
-        old_i = __ldg(P.perm + j0 + lane);
-        mu_i = __ldg(P.mu + old_i);
-        if (!SF32) ein_i = __ldcg(msg.base + (j0 + lane - lo));
-    }
-    const float nr = (float)P.n_ranks;
-    const float *q = Lvl<BITS>::q();
-    const int g0 = lane >> 2;
-    for (int s0 = 0; s0 < cnt; s0 += kAhead) {
-        uint32_t ca[kAhead], cb[kAhead], ua[kAhead], ub[kAhead];
-#pragma unroll
-        for (int a = 0; a < kAhead; ++a) {
-            ca[a] = cb[a] = ua[a] = ub[a] = 0u;
-            if (s0 + a < cnt) {
-                const int64_t sl = j0 + s0 + a - lo;
-                const uint8_t *blk = code_block<BITS>(msg, sl);
-                ca[a] = ldg_codes4<BITS>(blk, lane);
-                cb[a] = ldg_codes4<BITS>(blk, 32 + lane);
-                if (SF32) {   // bits of the fp32 scales of groups g0 and 8 + g0
-                    const uint32_t *sg = reinterpret_cast<const uint32_t *>(msg.base + msg.off_u + sl * 64);
-                    ua[a] = __ldcg(sg + g0);
-                    ub[a] = __ldcg(sg + 8 + g0);
-                } else {
-                    const uint8_t *ub8 = msg.base + msg.off_u + sl * 16;
-                    ua[a] = __ldcg(ub8 + g0);
-                    ub[a] = __ldcg(ub8 + 8 + g0);
-                }
-            }
-        }
-#pragma unroll
-        for (int a = 0; a < kAhead; ++a) {
-            const int s = s0 + a;
-            const int32_t old = __shfl_sync(kFull, old_i, s & 31);
-            const float mu = __shfl_sync(kFull, mu_i, s & 31);
-            const uint32_t E = __shfl_sync(kFull, ein_i, s & 31);
-            if (s < cnt) {
-                const float back = __fmul_rn(mu, nr);
-                const float p2e = __uint_as_float(E << 23);
-                const float sa = SF32 ? __uint_as_float(ua[a]) : __fmul_rn((float)ua[a], p2e);
-                const float sb = SF32 ? __uint_as_float(ub[a]) : __fmul_rn((float)ub[a], p2e);
-                float va[4], vb[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t mask = (1u << BITS) - 1u;
-                    va[i] = __fmaf_rn(sa, q[(ca[a] >> (BITS * i)) & mask], back);
-                    vb[i] = __fmaf_rn(sb, q[(cb[a] >> (BITS * i)) & mask], back);
-                }
-                if (P.out_is_bf16) {
-                    const uint2 wa = make_uint2(
-                        (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(va[0])) |
-                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(va[1])) << 16),
-                        (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(va[2])) |
-                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(va[3])) << 16));
-                    const uint2 wb = make_uint2(
-                        (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(vb[0])) |
-                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(vb[1])) << 16),
-                        (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(vb[2])) |
-                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(vb[3])) << 16));
-                    for (int oi = 0; oi < n_outs; ++oi) {
-                        uint16_t *o = static_cast<uint16_t *>(outs[oi]) + (int64_t)old * kSG;
-                        __stcs(reinterpret_cast<uint2 *>(o + 4 * lane), wa);
-                        __stcs(reinterpret_cast<uint2 *>(o + 128 + 4 * lane), wb);
-                    }
-                } else {
-                    const float4 fa = make_float4(va[0], va[1], va[2], va[3]);
-                    const float4 fb = make_float4(vb[0], vb[1], vb[2], vb[3]);
-                    for (int oi = 0; oi < n_outs; ++oi) {
-                        float *o = static_cast<float *>(outs[oi]) + (int64_t)old * kSG;
-                        __stcs(reinterpret_cast<float4 *>(o + 4 * lane), fa);
-                        __stcs(reinterpret_cast<float4 *>(o + 128 + 4 * lane), fb);
-                    }
-                }
-            }
-        }
-    }
-}
-
-// 32-byte streaming store of eight fp32 (the address must be 32-byte aligned).
-__device__ __forceinline__ void stcs_f32x8(float *p, const float (&v)[8])
-{
-    asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v[0]), "f"(v[1]),
-                 "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
-                 : "memory");
-}
-
-// The same decode with lane l owning coordinates 8l .. 8l+7 (half of group
-// l/2), so one warp store writes a whole super-group: 1 KiB of fp32 with
-// 32-byte stores (outputs 32-byte aligned) or 512 bytes of bf16 with
-// 16-byte stores, half as many store instructions as decode_unit.
-template <int BITS, bool SF32, typename PP>
-__device__ __forceinline__ void decode_unit_wide(const PP &P, const MsgView &msg, int64_t lo, void *const *outs,
-                                                 int n_outs, int64_t j0, int cnt, int lane)
-{
-    constexpr int kAhead = 8;
-    int32_t old_i = 0;
-    float mu_i = 0.0f;
-    uint32_t ein_i = 0;
-    if (lane < cnt) {
-        old_i = __ldg(P.perm + j0 + lane);
-        mu_i = __ldg(P.mu + old_i);
-        if (!SF32) ein_i = __ldcg(msg.base + (j0 + lane - lo));
-    }
-    const float nr = (float)P.n_ranks;
-    const float *q = Lvl<BITS>::q();
-    const int g = lane >> 1;
-    for (int s0 = 0; s0 < cnt; s0 += kAhead) {
-        uint32_t c0[kAhead], c1[kAhead], ua[kAhead];
-#pragma unroll
-        for (int a = 0; a < kAhead; ++a) {
-            c0[a] = c1[a] = ua[a] = 0u;
-            if (s0 + a < cnt) {
-                const int64_t sl = j0 + s0 + a - lo;
-                const uint8_t *blk = code_block<BITS>(msg, sl);
-                if (BITS == 2) {
-                    c0[a] = __ldcg(reinterpret_cast<const unsigned short *>(blk) + lane);
-                } else if (BITS == 4) {
-                    c0[a] = __ldcg(reinterpret_cast<const unsigned int *>(blk) + lane);
-                } else {
-                    const uint2 v = __ldcg(reinterpret_cast<const uint2 *>(blk) + lane);
-                    c0[a] = v.x;
-                    c1[a] = v.y;
-                }
-                if (SF32) ua[a] = __ldcg(reinterpret_cast<const unsigned int *>(msg.base + msg.off_u + sl * 64) + g);
-                else ua[a] = __ldcg(msg.base + msg.off_u + sl * 16 + g);
-            }
-        }
-#pragma unroll
-        for (int a = 0; a < kAhead; ++a) {
-            const int s = s0 + a;
-            const int32_t old = __shfl_sync(kFull, old_i, s & 31);
-            const float mu = __shfl_sync(kFull, mu_i, s & 31);
-            const uint32_t E = __shfl_sync(kFull, ein_i, s & 31);
-            if (s < cnt) {
-                const float back = __fmul_rn(mu, nr);
-                const float sigma = SF32 ? __uint_as_float(ua[a]) : __fmul_rn((float)ua[a], __uint_as_float(E << 23));
-                float v[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t w = (BITS == 8 && i >= 4) ? c1[a] : c0[a];
-                    const int bit = (BITS * i) & 31;
-                    const uint32_t off = (bit >= 2 ? (w >> (bit >= 2 ? bit - 2 : 0)) : (w << 2)) & (((1u << BITS) - 1u) << 2);
-                    v[i] = __fmaf_rn(sigma, lds_at<float>(q, off), back);
-                }
-                if (P.out_is_bf16) {
-                    uint32_t h[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        h[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i])) |
-                               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i + 1])) << 16);
-                    const uint4 hv = make_uint4(h[0], h[1], h[2], h[3]);
-                    for (int oi = 0; oi < n_outs; ++oi)
-                        __stcs(reinterpret_cast<uint4 *>(static_cast<uint16_t *>(outs[oi]) + (int64_t)old * kSG + 8 * lane), hv);
-                } else {
-                    for (int oi = 0; oi < n_outs; ++oi)
-                        stcs_f32x8(static_cast<float *>(outs[oi]) + (int64_t)old * kSG + 8 * lane, v);
-                }
-            }
-        }
-    }
-}
-
 constexpr int kDecodeWarps = 16;
 // The final decode runs flat: each warp decodes one slice of 32 / kDecodeSplit
 // super-groups and exits; short-lived blocks stream their writes to HBM
@@ -766,15 +580,22 @@ __device__ __forceinline__ void bulk_store(void *gdst, uint32_t ssrc, uint32_t b
 // The decode of up to kDecodeSlice super-groups with the stores handed to
 // the bulk-copy engine: the warp writes its decoded rows to shared memory
 // (lane l owns coordinates 8l .. 8l+7), makes them visible to the async
-// proxy, and each lane issues the copy of one (row, output) pair, then
-// waits until its copies have completed (the shared memory must outlive
-// them).  The global store queue then carries none of the output.
+// proxy, and each lane issues the copy of one (row, output) pair.  WAIT_ALL:
+// then waits until its copies have completed (the shared memory must
+// outlive them).  Otherwise the caller alternates two row buffers: before
+// writing, every lane waits until at most its latest copy group is still
+// reading (the one from the other buffer), and the caller waits for all
+// copies at the end.  The global store queue carries none of the output.
 constexpr int kDecodeSlice = kUnit / kDecodeSplit;
 
-template <int BITS, bool SF32, typename PP>
+template <int BITS, bool SF32, bool WAIT_ALL, typename PP>
 __device__ __forceinline__ void decode_unit_bulk(const PP &P, const MsgView &msg, int64_t lo, void *const *outs,
                                                  int n_outs, int64_t j0, int cnt, int lane, uint8_t *rows)
 {
+    if (!WAIT_ALL) {
+        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncwarp();
+    }
     int32_t old_i = 0;
     float mu_i = 0.0f;
     uint32_t ein_i = 0;
@@ -850,7 +671,7 @@ __device__ __forceinline__ void decode_unit_bulk(const PP &P, const MsgView &msg
         }
     }
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    if (WAIT_ALL) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 template <bool SF32>
@@ -873,9 +694,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) decode_kernel(const __grid_
     void *const *outs = P.n_outs > 0 ? P.outs : &t.out;
     const int n_outs = P.n_outs > 0 ? P.n_outs : 1;
     uint8_t *rows = drows + warp * kDecodeSlice * 1024;
-    if (seg == 0) decode_unit_bulk<2, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane, rows);
-    else if (seg == 1) decode_unit_bulk<4, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane, rows);
-    else decode_unit_bulk<8, SF32>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane, rows);
+    if (seg == 0) decode_unit_bulk<2, SF32, true>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane, rows);
+    else if (seg == 1) decode_unit_bulk<4, SF32, true>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane, rows);
+    else decode_unit_bulk<8, SF32, true>(P, t.msg, t.lo, outs, n_outs, j0, cnt, lane, rows);
 }
 
 // ---------------------------------------------------------------------------
@@ -946,6 +767,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) fused_ring_kernel(const __grid
     const int wpb = (int)(blockDim.x >> 5);   // warps per block: sized to the launch, at most kWarps
     const int64_t nw = (int64_t)gridDim.x * wpb;
     for (int t = 0; t <= N; ++t) {
+        int slice = 0;   // the final decode alternates two row buffers per warp
         for (int64_t u = (int64_t)blockIdx.x * wpb + warp; u < P.units; u += nw) {
             int c = 0;
             while (c + 1 < N && u >= P.unit_begin[c + 1][0]) ++c;
@@ -957,14 +779,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1) fused_ring_kernel(const __grid
             if (t == N) {   // final decode of chunk c (owner c, step N-1)
                 MsgView m = P.chunk[c];
                 m.base = P.msgs + (2 * (int64_t)c + ((N - 1) & 1)) * P.msg_stride;
-                if (P.out_is_bf16 || P.out_align32) {
-                    if (seg == 0) decode_unit_wide<2, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
-                    else if (seg == 1) decode_unit_wide<4, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
-                    else decode_unit_wide<8, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
-                } else {
-                    if (seg == 0) decode_unit<2, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
-                    else if (seg == 1) decode_unit<4, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
-                    else decode_unit<8, SF32>(P, m, P.lo[c], P.outs, N, j0, cnt, lane);
+                for (int s0 = 0; s0 < cnt; s0 += kDecodeSlice, ++slice) {
+                    const int n = cnt - s0 < kDecodeSlice ? cnt - s0 : kDecodeSlice;
+                    // (in the tables' shared memory, dead by then)
+                    uint8_t *rb = g_dyn + (2 * warp + (slice & 1)) * kDecodeSlice * 1024;
+                    if (seg == 0) decode_unit_bulk<2, SF32, false>(P, m, P.lo[c], P.outs, N, j0 + s0, n, lane, rb);
+                    else if (seg == 1) decode_unit_bulk<4, SF32, false>(P, m, P.lo[c], P.outs, N, j0 + s0, n, lane, rb);
+                    else decode_unit_bulk<8, SF32, false>(P, m, P.lo[c], P.outs, N, j0 + s0, n, lane, rb);
                 }
                 continue;
             }
@@ -994,6 +815,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) fused_ring_kernel(const __grid
         }
         if (t < N && !grid_barrier(P.barrier, P.status, gridDim.x * (unsigned)(t + 1), P.timeout_cycles)) return;
     }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // the decode's copies
 }
 
 // Opts a kernel in to `dyn` bytes of dynamic shared memory (needed once its

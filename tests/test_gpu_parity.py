@@ -179,7 +179,7 @@ def test_compress_dar_decode_bit_exact(eps, correlated):
         o16 = torch.zeros(p.b.size * 256, dtype=torch.bfloat16, device=DEV)
         dq.dq_decode(cfg, r, out, M, perm, o16, out_is_bf16=True)
         assert torch.equal(o16.cpu(), torch.from_numpy(e32).to(torch.bfloat16))
-        # an fp32 output 16- but not 32-byte aligned takes the 16-byte-store decode
+        # an fp32 output 16- but not 32-byte aligned (the decode's bulk copies need 16)
         ob = torch.zeros(p.b.size * 256 + 4, device=DEV)
         o32u = ob[4:]
         assert o32u.data_ptr() % 32 == 16
@@ -269,9 +269,9 @@ def test_fewer_supergroups_than_ranks():
 
 @pytest.mark.parametrize("fused", [False, True])
 def test_exchange_outputs_16_byte_aligned(fused):
-    """Outputs 16- but not 32-byte aligned take the decode's 16-byte stores
-    (in the per-step exchange and in the fused one); the results are the
-    same bits as with aligned outputs."""
+    """Outputs 16- but not 32-byte aligned (the decode's bulk copies need
+    16-byte alignment only, in the per-step exchange and in the fused one)
+    give the same bits as aligned outputs."""
     N = 4
     _, gr = grads_for("ring4_1m", 256 * 1500, N=N, seed=9)
     J = gr[0].size // 256
