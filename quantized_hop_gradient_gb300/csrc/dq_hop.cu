@@ -259,7 +259,7 @@ __device__ __forceinline__ void decode_add(float2 (&x)[8], float sigma, const La
 // SF32 (ablation: scales in fp32): sigma = s, y = fl(x / s) (y = 0 when
 // s = 0); E_out = 0 and u_out holds the bits of s.
 // off: the correlated-rounding offset of this quantizer, in [0, 2^16).
-template <int BITS, bool ONE_LEVEL, bool SF32>
+template <int BITS, bool ONE_LEVEL, bool SF32, bool OFF>
 __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], uint32_t ctr0, uint32_t stage_word,
                                                           uint32_t off, const PhiloxKeys &K, uint32_t &E_out,
                                                           uint32_t &u_out)
@@ -311,8 +311,8 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
     uint32_t A[8], B[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        A[i] = r0[i] + off;
-        B[i] = r0[i] + offh;
+        A[i] = OFF ? r0[i] + off : r0[i];   // !OFF: every offset of the launch is 0
+        B[i] = OFF ? r0[i] + offh : r0[i];
         A[i + 4] = A[i] ^ 0x8000u;
         B[i + 4] = B[i] ^ 0x80000000u;
     }
@@ -385,7 +385,7 @@ __host__ __device__ constexpr int stage_bytes() { return (ADD_F32 ? 2048 : 1024)
 // message written earlier in the same launch by other CTAs is read
 // correctly after a grid barrier.  A half-warp whose super-group lies past
 // the unit's end computes on stale staging data and stores nothing.
-template <int BITS, bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32, typename PP>
+template <int BITS, bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32, bool OFF, typename PP>
 __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t *stg, int64_t j0, int cnt,
                                          int lane)
 {
@@ -494,7 +494,7 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
         uint32_t E = 0u, u = 0u;
         if (__any_sync(kFull, send)) {
             const uint32_t ctr0 = (uint32_t)old * 16u + (uint32_t)hl;   // global coordinate index / 16
-            const LaneCodes<BITS> q = quantize_group<BITS, ONE_LEVEL, SF32>(x, ctr0, stage_word, corr, P.ph, E, u);
+            const LaneCodes<BITS> q = quantize_group<BITS, ONE_LEVEL, SF32, OFF>(x, ctr0, stage_word, corr, P.ph, E, u);
             if (send) {
                 stg_codes<BITS>(out_c + (int64_t)s * CB, q);
                 if (SF32) *reinterpret_cast<uint32_t *>(out_u + (int64_t)s * UB) = u;
@@ -518,7 +518,7 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
     }
 }
 
-template <bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32>
+template <bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32, bool OFF>
 __global__ void __launch_bounds__(kWarps * 32, kHopBlocksPerSM) hop_kernel(const __grid_constant__ HopParams P)
 {
     block_copy(&g_tab, &P.tab);
@@ -539,9 +539,9 @@ __global__ void __launch_bounds__(kWarps * 32, kHopBlocksPerSM) hop_kernel(const
         const int64_t j0 = t.seg_lo[seg] + (u - t.unit_begin[seg]) * kUnit;
         const int64_t rem = t.seg_hi[seg] - j0;
         const int cnt = (int)(rem < kUnit ? rem : kUnit);
-        if (seg == 0) hop_unit<2, HAS_IN, ADD_F32, ONE_LEVEL, SF32>(P, t, stg, j0, cnt, lane);
-        else if (seg == 1) hop_unit<4, HAS_IN, ADD_F32, ONE_LEVEL, SF32>(P, t, stg, j0, cnt, lane);
-        else hop_unit<8, HAS_IN, ADD_F32, ONE_LEVEL, SF32>(P, t, stg, j0, cnt, lane);
+        if (seg == 0) hop_unit<2, HAS_IN, ADD_F32, ONE_LEVEL, SF32, OFF>(P, t, stg, j0, cnt, lane);
+        else if (seg == 1) hop_unit<4, HAS_IN, ADD_F32, ONE_LEVEL, SF32, OFF>(P, t, stg, j0, cnt, lane);
+        else hop_unit<8, HAS_IN, ADD_F32, ONE_LEVEL, SF32, OFF>(P, t, stg, j0, cnt, lane);
     }
 }
 
@@ -804,13 +804,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1) fused_ring_kernel(const __grid
             T.stage_word = (uint32_t)t | (P.correlated ? 0xFFFF0000u : ((uint32_t)r << 16));
             T.corr2 = 0u;   // one quantizer per ring stage: stratum offset 0
             if (t == 0) {
-                if (seg == 0) hop_unit<2, false, false, ONE_LEVEL, SF32>(P, T, stg, j0, cnt, lane);
-                else if (seg == 1) hop_unit<4, false, false, ONE_LEVEL, SF32>(P, T, stg, j0, cnt, lane);
-                else hop_unit<8, false, false, ONE_LEVEL, SF32>(P, T, stg, j0, cnt, lane);
+                if (seg == 0) hop_unit<2, false, false, ONE_LEVEL, SF32, false>(P, T, stg, j0, cnt, lane);
+                else if (seg == 1) hop_unit<4, false, false, ONE_LEVEL, SF32, false>(P, T, stg, j0, cnt, lane);
+                else hop_unit<8, false, false, ONE_LEVEL, SF32, false>(P, T, stg, j0, cnt, lane);
             } else {
-                if (seg == 0) hop_unit<2, true, false, ONE_LEVEL, SF32>(P, T, stg, j0, cnt, lane);
-                else if (seg == 1) hop_unit<4, true, false, ONE_LEVEL, SF32>(P, T, stg, j0, cnt, lane);
-                else hop_unit<8, true, false, ONE_LEVEL, SF32>(P, T, stg, j0, cnt, lane);
+                if (seg == 0) hop_unit<2, true, false, ONE_LEVEL, SF32, false>(P, T, stg, j0, cnt, lane);
+                else if (seg == 1) hop_unit<4, true, false, ONE_LEVEL, SF32, false>(P, T, stg, j0, cnt, lane);
+                else hop_unit<8, true, false, ONE_LEVEL, SF32, false>(P, T, stg, j0, cnt, lane);
             }
         }
         if (t < N && !grid_barrier(P.barrier, P.status, gridDim.x * (unsigned)(t + 1), P.timeout_cycles)) return;
@@ -856,11 +856,11 @@ int grid_for(K kernel, int warps, size_t dyn_smem, int64_t units)
     return (int)(need < cap ? (need < 1 ? 1 : need) : cap);
 }
 
-template <bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32>
+template <bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32, bool OFF = true>
 cudaError_t launch_hop_t(const HopParams &P, cudaStream_t st)
 {
     const size_t dyn = (size_t)tab_bytes(ADD_F32) + (size_t)kWarps * kStages * stage_bytes<ADD_F32, SF32>();
-    auto k = hop_kernel<HAS_IN, ADD_F32, ONE_LEVEL, SF32>;
+    auto k = hop_kernel<HAS_IN, ADD_F32, ONE_LEVEL, SF32, OFF>;
     static bool opted[128] = {false};   // one record per instantiation of this launcher
     const cudaError_t ea = allow_dyn_smem(k, dyn, opted);
     if (ea != cudaSuccess) return ea;
@@ -874,6 +874,10 @@ template <bool SF32>
 cudaError_t launch_hop_s(const HopParams &P, bool has_in, bool add_f32, cudaStream_t st)
 {
     const bool one = P.tab.one_level != 0;
+    bool off = false;   // some task shifts its uniforms (correlated rounding with several slots)
+    for (int i = 0; i < P.n_tasks; ++i) off = off || P.task[i].corr2 != 0u;
+    if (!SF32 && one && !add_f32 && !off)   // the ring's kernels: no offsets to add
+        return has_in ? launch_hop_t<true, false, true, SF32, false>(P, st) : launch_hop_t<false, false, true, SF32, false>(P, st);
     if (!has_in)
         return one ? launch_hop_t<false, false, true, SF32>(P, st) : launch_hop_t<false, false, false, SF32>(P, st);
     if (add_f32)
