@@ -258,7 +258,8 @@ __device__ __forceinline__ void decode_add(float2 (&x)[8], float sigma, const La
 // and below the bottom level d < 0.
 // SF32 (ablation: scales in fp32): sigma = s, y = fl(x / s) (y = 0 when
 // s = 0); E_out = 0 and u_out holds the bits of s.
-// off: the correlated-rounding offset of this quantizer, in [0, 2^16).
+// off: the correlated-rounding offset of this quantizer, in [0, 2^16); OFF =
+// false compiles it out (every quantizer of the launch has offset 0).
 template <int BITS, bool ONE_LEVEL, bool SF32, bool OFF>
 __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], uint32_t ctr0, uint32_t stage_word,
                                                           uint32_t off, const PhiloxKeys &K, uint32_t &E_out,
