@@ -69,6 +69,7 @@ def lib():
             L.or_quantize_sg.argtypes = [P, C.c_int, P, P, P, i64, P, P, P]
             L.or_quantize_sg_f32.argtypes = [P, C.c_int, P, P, P, i64, P, P]
             L.or_dequantize_sg.argtypes = [C.c_uint8, P, P, C.c_int, P, P]
+            L.or_decode_add_sg.argtypes = [C.c_uint8, P, P, C.c_int, P, P, P]
             L.or_decode_add_sg_f32.argtypes = [P, P, C.c_int, P, P, P]
             L.or_e4m3_value.argtypes = [C.c_uint8]
             L.or_e4m3_value.restype = C.c_double
@@ -255,6 +256,17 @@ def quantize_sg_f32(x, bits: int, *, eps=1.0, seed=0, round=0, n_ranks=1, correl
     codes = np.zeros(SG * bits // 8, np.uint8)
     lib().or_quantize_sg_f32(_addr(x), bits, _addr(q), _addr(G), C.addressof(r), idx0, _addr(sig), _addr(codes))
     return sig, codes
+
+
+def decode_add_sg(E: int, u, codes, bits: int, add, *, eps=1.0) -> np.ndarray:
+    """Decode one super-group with UINT8 scales and add ``add`` (fp32[256])."""
+    u = _c(u, np.uint8)
+    codes = _c(codes, np.uint8)
+    add = _c(add, np.float32)
+    q = level_table(bits, eps)
+    out = np.zeros(SG, np.float32)
+    lib().or_decode_add_sg(E, _addr(u), _addr(codes), bits, _addr(q), _addr(add), _addr(out))
+    return out
 
 
 def decode_add_sg_f32(sig, codes, bits: int, add, *, eps=1.0) -> np.ndarray:
