@@ -178,9 +178,11 @@ dq_status dq_reorder(const uint8_t *b, int64_t n_sg, int32_t *perm, void *ws, si
  *   DQ_ERR_INVALID_ARG without touching the GPU (use dq_reorder then).
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.  All calls share the one array: calls that
- *   overlap on the GPU (different streams, or different host threads without
- *   ordering) race and must not be made. */
+ *   before any stream capture.  The address is kept for the life of the
+ *   process: after cudaDeviceReset (or any teardown of the device's primary
+ *   context) later calls on that device are invalid.  All calls share the one
+ *   array: calls that overlap on the GPU (different streams, or different host
+ *   threads without ordering) race and must not be made. */
 #define DQ_REORDER_STATIC_MAX_SG 8388608
 dq_status dq_reorder_static(const uint8_t *b, int64_t n_sg, int32_t *perm, void *stream);
 
@@ -326,6 +328,20 @@ dq_status dq_exchange_fused(const dq_config *cfg, const void *const *grads_host,
                             size_t ws_bytes, void *const *outs_host, int32_t out_is_bf16,
                             int32_t *status_dev, const uint8_t **final_msgs_host, dq_launch_log *log,
                             void *stream);
+
+/* Reads a device status word into host memory [boundary of the hot path:
+ * device-side errors of an asynchronous call are reported through a status
+ * word that the caller reads after the work; the paper itself defines no
+ * interface].  status_dev: device int32, 4-byte aligned -- the word passed
+ * to dq_exchange_fused or dq_barrier_selftest (caller-owned).  status_host:
+ * host int32 that receives it: DQ_DEVICE_OK or DQ_DEVICE_BARRIER_TIMEOUT.
+ * Enqueues a 4-byte device-to-host copy on `stream` and synchronises that
+ * stream, so the value read includes every kernel enqueued on the stream
+ * before the call.  This entry point and dq_plan are the only ones that
+ * synchronise.  Errors: DQ_ERR_INVALID_ARG (null pointer), DQ_ERR_ALIGNMENT,
+ * DQ_ERR_CUDA (the copy or the synchronisation failed, e.g. an earlier
+ * kernel on the stream faulted; *status_host is then left unchanged). */
+dq_status dq_get_device_status(const int32_t *status_dev, int32_t *status_host, void *stream);
 
 /* Test of the failure path of the fused exchange's barrier, with no
  * counterpart in the paper: n_blocks CTAs (1 .. number of SMs) run one

@@ -101,7 +101,7 @@ class DynamiQAllReduce:
 
     def check_status(self):
         """Raises if the last fused exchange reported a device error."""
-        s = int(self.status.item())
+        s = dq.dq_get_device_status(self.status)
         if s != dq.DQ_DEVICE_OK:
             raise RuntimeError(f"fused exchange: device status {s} (barrier timeout)")
 

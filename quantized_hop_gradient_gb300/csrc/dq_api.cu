@@ -23,15 +23,15 @@ void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_
 
 int sm_count()
 {
-    static int cache[128] = {0};
+    static std::atomic<int> cache[128];   // zero-initialised (static storage); 0 = not yet read
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 152;
-    if (cache[dev] == 0) {
-        int n = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
 // --------------------------------------------------------------------------- level tables
@@ -882,6 +882,18 @@ dq_status dq_exchange_fused(const dq_config *cfg, const void *const *grads, int6
     if (e != cudaSuccess) return DQ_ERR_CUDA;
     if (final_msgs)
         for (int32_t c = 0; c < N; ++c) final_msgs[c] = w + X.msgs + (size_t)(2 * c + ((N - 1) & 1)) * X.msg_stride;
+    return DQ_OK;
+}
+
+dq_status dq_get_device_status(const int32_t *status_dev, int32_t *status_host, void *stream)
+{
+    if (!status_dev || !status_host) return DQ_ERR_INVALID_ARG;
+    if ((uintptr_t)status_dev & 3u) return DQ_ERR_ALIGNMENT;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, status_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DQ_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return DQ_ERR_CUDA;
+    *status_host = v;
     return DQ_OK;
 }
 

@@ -23,6 +23,7 @@
 // the subtract that follows would change the rounding, which the GPU parity
 // tests (bit-exact against the oracle) detect.
 #include <algorithm>
+#include <mutex>
 
 #include "dq_common.cuh"
 #include "dq_internal.h"
@@ -825,8 +826,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) fused_ring_kernel(const __grid
 template <typename K>
 cudaError_t allow_dyn_smem(K kernel, size_t dyn, bool (&done)[128])
 {
+    static std::mutex mu;   // first calls from several host threads may meet here
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
     if (done[dev]) return cudaSuccess;
     const cudaError_t e =
         cudaFuncSetAttribute(reinterpret_cast<const void *>(kernel), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);

@@ -32,7 +32,9 @@ cudaError_t launch_barrier_selftest(int32_t n_blocks, int32_t missing, long long
                                     unsigned int *counter, int32_t *status, cudaStream_t st);
 
 // Allocation (radix select of T) and reordering; ws is device scratch.
+constexpr int kReorderTile = 2048;   // super-groups per reorder tile (4 int64 of scratch each)
 size_t plan_scratch_bytes(int64_t n_sg);
+size_t reorder_scratch_bytes(int64_t n_sg);   // bytes of ws that launch_reorder uses
 cudaError_t launch_allocate(const float *F, int64_t n_sg, int64_t cap_bits, uint8_t *b, float *T,
                             int64_t *counts, void *ws, cudaStream_t st);
 cudaError_t launch_reorder(const uint8_t *b, int64_t n_sg, int32_t *perm, void *ws, cudaStream_t st);

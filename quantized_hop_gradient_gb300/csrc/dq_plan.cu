@@ -14,6 +14,8 @@
 //
 // Reordering.  A stable counting sort of the super-groups by bitwidth
 // (2, 4, 8): per-tile counts, one scan over tiles, then a stable scatter.
+#include <mutex>
+
 #include "dq_common.cuh"
 #include "dq_internal.h"
 
@@ -22,7 +24,7 @@ namespace dq {
 namespace {
 
 constexpr int kAllocThreads = 256;
-constexpr int kTile = 2048;            // super-groups per reorder tile
+constexpr int kTile = kReorderTile;    // super-groups per reorder tile
 constexpr int kTileThreads = 256;      // 8 super-groups per thread
 constexpr int64_t kSmallPlanMaxSG = 16384;   // single-block plan: F in 64 KB of shared memory; above this the multi-kernel path is faster
 
@@ -373,10 +375,15 @@ __global__ void __launch_bounds__(kSmallPlanThreads) plan_small_kernel(const flo
 
 }  // namespace
 
-size_t plan_scratch_bytes(int64_t n_sg)
+size_t reorder_scratch_bytes(int64_t n_sg)
 {
     const int64_t n_tiles = (n_sg + kTile - 1) / kTile;
-    const size_t reorder = (size_t)(n_tiles > 0 ? n_tiles : 1) * 4 * sizeof(long long);
+    return (size_t)(n_tiles > 0 ? n_tiles : 1) * 4 * sizeof(long long);
+}
+
+size_t plan_scratch_bytes(int64_t n_sg)
+{
+    const size_t reorder = reorder_scratch_bytes(n_sg);
     const size_t alloc = sizeof(AllocState);
     const size_t m = reorder > alloc ? reorder : alloc;
     return (m + 255) / 256 * 256;
@@ -421,14 +428,20 @@ cudaError_t launch_plan_small(const float *F, int64_t n_sg, int64_t cap_bits, in
 {
     if (n_sg < 1 || n_sg > kSmallPlanMaxSG) return cudaErrorInvalidValue;
     const size_t smem = (size_t)n_sg * sizeof(float);
+    // the attribute is set once per device; the lock makes first calls from
+    // several host threads safe
+    static std::mutex mu;
     static bool attr_set[128] = {false};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-    if (dev >= 0 && dev < 128 && !attr_set[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(plan_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)(kSmallPlanMaxSG * sizeof(float)));
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_set[dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(plan_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       (int)(kSmallPlanMaxSG * sizeof(float)));
+            if (e != cudaSuccess) return e;
+            attr_set[dev] = true;
+        }
     }
     const long long R = (long long)(cap_bits - 2 * n_sg);
     const int all8 = R >= 6 * (long long)n_sg ? 1 : 0;

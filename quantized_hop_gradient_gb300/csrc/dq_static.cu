@@ -13,8 +13,8 @@
 
 namespace {
 
-constexpr int64_t kTileSG = 2048;                               // super-groups per reorder tile
-constexpr int64_t kMaxTiles = DQ_REORDER_STATIC_MAX_SG / kTileSG;
+// one scratch slot of 4 int64 per reorder tile (the tile size is dq_reorder's)
+constexpr int64_t kMaxTiles = (DQ_REORDER_STATIC_MAX_SG + dq::kReorderTile - 1) / dq::kReorderTile;
 
 // Per-tile counts and offsets of the reorder: 4 int64 per tile.  Every entry
 // a call reads is written earlier in the same call, so nothing needs to be
@@ -46,6 +46,9 @@ extern "C" dq_status dq_reorder_static(const uint8_t *b, int64_t n_sg, int32_t *
 {
     if (n_sg < 1 || n_sg > DQ_REORDER_STATIC_MAX_SG) return DQ_ERR_INVALID_ARG;
     if (!b || !perm) return DQ_ERR_INVALID_ARG;
+    // the reorder must fit the array (holds by construction; checked so that
+    // a change of the tile layout fails here instead of writing past it)
+    if (dq::reorder_scratch_bytes(n_sg) > sizeof(g_reorder_scratch)) return DQ_ERR_INVALID_ARG;
     void *ws = nullptr;
     const dq_status s = scratch_address(&ws);
     if (s != DQ_OK) return s;

@@ -82,6 +82,7 @@ _SIGS = {
                      C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
     "dq_reorder": ([C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
     "dq_reorder_static": ([C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p], C.c_int),
+    "dq_get_device_status": ([C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "dq_chunk_cuts": ([C.c_int64, C.c_int64, C.c_int64, C.c_int32, C.c_void_p], C.c_int),
     "dq_compress": ([C.POINTER(dq_config), dq_range, dq_stage, C.c_void_p, C.c_void_p,
                      C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
@@ -361,6 +362,14 @@ def dq_exchange_fused(cfg, grads, n_sg, mu, perm, info, ws, ws_bytes, outs, stat
                                    C.byref(log.c) if log is not None else None, _stream(stream)),
            "dq_exchange_fused")
     return [fin[i] for i in range(n)]
+
+
+def dq_get_device_status(status_dev, stream=None) -> int:
+    """The device status word ``status_dev`` (an int32 device tensor) read
+    into host memory; synchronises ``stream``."""
+    out = C.c_int32(-1)
+    _check(lib().dq_get_device_status(_ptr(status_dev), C.addressof(out), _stream(stream)), "dq_get_device_status")
+    return out.value
 
 
 def dq_barrier_selftest(n_blocks, missing, timeout_cycles, scratch, status, stream=None):

@@ -1,6 +1,7 @@
 """The C ABI without a GPU: the library builds and loads, exports every
 entry point that include/dq.h declares, its host-side pure functions agree
 with the oracle, and bad arguments are rejected before any CUDA call."""
+import ctypes
 import math
 import os
 import re
@@ -120,3 +121,7 @@ def test_bad_arguments_rejected_on_the_host(L):
     assert L.dq_barrier_selftest(0, 0, 1000, P, P, st) == dq.DQ_ERR_INVALID_ARG
     assert L.dq_barrier_selftest(4, 0, 0, P, P, st) == dq.DQ_ERR_INVALID_ARG
     assert L.dq_barrier_selftest(4, 0, 1000, P + 2, P, st) == dq.DQ_ERR_ALIGNMENT
+    host = (ctypes.c_int32 * 1)()
+    assert L.dq_get_device_status(None, ctypes.addressof(host), st) == dq.DQ_ERR_INVALID_ARG
+    assert L.dq_get_device_status(P, None, st) == dq.DQ_ERR_INVALID_ARG
+    assert L.dq_get_device_status(P + 2, ctypes.addressof(host), st) == dq.DQ_ERR_ALIGNMENT

@@ -121,6 +121,12 @@ def test_barrier_timeout_reports_status_and_context_survives():
     torch.cuda.synchronize()
     assert int(status.item()) == dq.DQ_DEVICE_BARRIER_TIMEOUT
     assert int(scratch[0].item()) == n
+    # the same two states read through the C ABI's status call (it
+    # synchronises the stream itself)
+    dq.dq_barrier_selftest(n, 0, 2_000_000, scratch, status)
+    assert dq.dq_get_device_status(status) == dq.DQ_DEVICE_OK
+    dq.dq_barrier_selftest(n, 1, 2_000_000, scratch, status)
+    assert dq.dq_get_device_status(status) == dq.DQ_DEVICE_BARRIER_TIMEOUT
     # the context is still usable: a fused exchange right after is correct
     test_fused_is_one_launch()
 

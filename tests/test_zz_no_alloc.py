@@ -36,6 +36,25 @@ def test_reorder_static_matches_reorder_on_two_calls():
         assert torch.equal(got, ref), f"call {trial}: {(got != ref).sum().item()} entries differ"
 
 
+def test_reorder_static_at_its_maximum_size():
+    """n_sg = DQ_REORDER_STATIC_MAX_SG uses the last tile slot of the fixed
+    array; the result must still match dq_reorder."""
+    L = dq.lib()
+    J = dq.REORDER_STATIC_MAX_SG
+    rs = np.random.default_rng(7)
+    b = torch.from_numpy(rs.choice([2, 4, 8], J, p=[0.3, 0.4, 0.3]).astype(np.uint8)).cuda()
+    ref = torch.empty(J, dtype=torch.int32, device="cuda")
+    ws = torch.empty(dq.dq_workspace_bytes(J), dtype=torch.uint8, device="cuda")
+    dq.dq_reorder(b, J, ref, ws, ws.numel())
+    got = torch.full((J,), -1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    status = L.dq_reorder_static(ctypes.c_void_p(b.data_ptr()), J, ctypes.c_void_p(got.data_ptr()),
+                                 ctypes.c_void_p(stream))
+    assert status == dq.DQ_OK, dq.status_string(status)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref)
+
+
 def test_reorder_static_rejects_sizes_above_its_maximum():
     L = dq.lib()
     too_big = dq.REORDER_STATIC_MAX_SG + 1
