@@ -51,6 +51,9 @@ def parse_args(argv=None):
                    help="ring exchange as one cooperative launch (fused) or one launch per step (multi); "
                         "auto: fused where it is the faster path (allreduce.use_fused: rings of up to 64 ranks, up to 2^17 "
                         "super-groups per worker)")
+    p.add_argument("--lean", action="store_true",
+                   help="the timed rounds only: no end-to-end, MXFP8, budget-sweep or accuracy legs and no extra "
+                        "workloads (for profiler captures, whose launch lists stay short)")
     p.add_argument("--extras", default="",
                    help="comma-separated workloads measured after the headline one ('none': skip; default: "
                         + ",".join(EXTRA_WORKLOADS) + ")")
@@ -463,6 +466,8 @@ def measure_round(args, w, dev, world, K, W, full: bool, local: int = 0):
            "kernels_multi_launch": kernels_multi, "ms_per_step_multi_launch": ms_multi, "roofline": roofline,
            "gpu_launches": n_launch, "clocks": clk, "steps": K, "warmup": W}
 
+    if args.lean:
+        return res, grads
     # accuracy of the last timed round's configuration (round K + W + ...: a fresh round, same inputs)
     s_exact = study.exact_sum(grads)
     step(10_000)
@@ -629,13 +634,13 @@ def run_gpu(args, rank, world, local):
     gb = main["grad_gb_per_worker"]
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.lean:
         cpu = cpu_baseline(w, grads, args.cpu_seconds)
     del grads
     torch.cuda.empty_cache()
 
     extras = {}
-    names = [] if (world > 1 or args.extras == "none" or args.coords) else \
+    names = [] if (world > 1 or args.extras == "none" or args.coords or args.lean) else \
         [x for x in (args.extras.split(",") if args.extras else EXTRA_WORKLOADS) if x and x != w.name]
     for name in names:
         xw = synth.WORKLOADS[name]
@@ -667,12 +672,12 @@ def run_gpu(args, rank, world, local):
         "kernels_multi_launch": main["kernels_multi_launch"],
         "ms_per_step_multi_launch": main["ms_per_step_multi_launch"],
         "roofline": main["roofline"],
-        "e2e": main["e2e"],
+        "e2e": main.get("e2e"),
         "gpu_launches": main["gpu_launches"],
         "clocks": main["clocks"],
-        "accuracy": main["accuracy"],
-        "mxfp8": main["mxfp8"],
-        "budget_sweep": main["budget_sweep"],
+        "accuracy": main.get("accuracy"),
+        "mxfp8": main.get("mxfp8"),
+        "budget_sweep": main.get("budget_sweep"),
         "extra_workloads": extras or None,
         "cpu_baseline": cpu,
     }

@@ -9,16 +9,19 @@
 // (eight 16-bit fields) for its sixteen coordinates.  The unit's
 // permutation entries, means and exponent bytes are loaded once, coalesced,
 // and broadcast by shuffles; its message addresses and its send and keep
-// masks are computed once per unit.  The gradient (or fp32 partial), the
-// incoming codes and the incoming UINT8 scales of a pair of super-groups are
-// staged in shared memory by cp.async, one pair ahead of the computation.
+// masks are computed once per unit.  The incoming codes and UINT8 scales
+// (and an fp32 partial sum) of a pair of super-groups are staged in shared
+// memory by cp.async, one pair ahead of the computation; a bf16 gradient
+// goes straight to registers, also one pair ahead.
 //
 // Per coordinate the quantizer costs a packed fused multiply-add for y, one
-// for the bucket index, an AND, three shared-memory loads (bucket, level,
-// reciprocal gap), two compares, a packed subtract and a packed fused
-// multiply-add rounded upward for the rounding decision, and the code
-// packing.  Levels and reciprocal gaps sit in separate tables, so the two
-// operands of each packed operation load straight into adjacent registers.
+// for the bucket index, an AND, two or three shared-memory loads (the
+// bucket, then the level and its reciprocal gap), two compares, a subtract
+// and a fused multiply-add rounded upward for the rounding decision, and
+// the code packing.  For 2 and 4 bits the levels and reciprocal gaps sit in
+// separate small tables, so the two operands of each packed operation load
+// straight into adjacent registers; for 8 bits one 8-byte load from a
+// lane-copied table of {level, gap} pairs gives both without bank conflicts.
 // y feeds several instructions; a compiler that fused its multiply into
 // the subtract that follows would change the rounding, which the GPU parity
 // tests (bit-exact against the oracle) detect.
@@ -49,9 +52,11 @@ __device__ __forceinline__ void expand_bk4()
 
 // The 8-bit tables of the hop kernels, at the start of dynamic shared
 // memory, one copy per half-warp lane c: buckets (row b + 256, 128 bytes per
-// row) whose entry for copy c holds 64 kb + 4c, and the levels and
-// reciprocal gaps (64 bytes per level), so the level and gap of copy c sit
-// at byte 64 k + 4c.  The 16 lanes of a half-warp never meet in a bank (pair).
+// row) whose entry for copy c holds 128 kb + 8c, and the levels interleaved
+// with their reciprocal gaps (128 bytes per level), so the pair {q_k, G16_k}
+// of copy c sits at byte 128 k + 8c.  An 8-byte load is served per
+// half-warp, whose 16 lanes then always read 16 different bank pairs: one
+// conflict-free load per coordinate gives both the level and its gap.
 // After them, in the kernels whose addends are bf16 (fp32 addends leave no
 // room), the decoder's 4-bit pair table: entry p (a code byte: low nibble =
 // first coordinate's code) holds the two levels, one copy per half-warp
@@ -60,17 +65,14 @@ extern __shared__ __align__(16) uint8_t g_dyn[];
 constexpr int kCopies8 = 16;
 constexpr int kRows8 = 2 * kOff8 + 1;
 constexpr int kBk8cBytes = kRows8 * kCopies8 * 8;
-constexpr int kL8cBytes = 256 * kCopies8 * 4;
+constexpr int kQG8cBytes = 256 * kCopies8 * 8;
 constexpr int kQ4pBytes = 256 * kCopies4 * 8;
-constexpr int kTab8Bytes = kBk8cBytes + 2 * kL8cBytes;
+constexpr int kTab8Bytes = kBk8cBytes + kQG8cBytes;
 __host__ __device__ constexpr int tab_bytes(bool add_f32) { return kTab8Bytes + (add_f32 ? 0 : kQ4pBytes); }
 static_assert(kTab8Bytes % 16 == 0 && kQ4pBytes % 16 == 0, "16-byte aligned staging");
-// rows up to 1023 (a non-finite y) stay inside the smallest dynamic allocation
-static_assert(1024 * kCopies8 * 8 <= kTab8Bytes + kWarps * kStages * (1024 + 512 + 32), "garbage rows in bounds");
 __device__ __forceinline__ const BucketEntry *bk8c() { return reinterpret_cast<const BucketEntry *>(g_dyn); }
-__device__ __forceinline__ const float *q8c() { return reinterpret_cast<const float *>(g_dyn + kBk8cBytes); }
-__device__ __forceinline__ const float *g8c() { return reinterpret_cast<const float *>(g_dyn + kBk8cBytes + kL8cBytes); }
-__device__ __forceinline__ const float2 *q4p() { return reinterpret_cast<const float2 *>(g_dyn + kBk8cBytes + 2 * kL8cBytes); }
+__device__ __forceinline__ const float2 *qg8c() { return reinterpret_cast<const float2 *>(g_dyn + kBk8cBytes); }
+__device__ __forceinline__ const float2 *q4p() { return reinterpret_cast<const float2 *>(g_dyn + kBk8cBytes + kQG8cBytes); }
 // The decoder's 2-bit pair table: entry p (four bits: low two = first
 // coordinate's code) holds the two levels; 16 entries of 8 bytes cover the
 // 32 banks once, so any lookup pattern is conflict-free.
@@ -81,14 +83,12 @@ __device__ __forceinline__ void expand_tables(bool pair4)
     BucketEntry *bk = reinterpret_cast<BucketEntry *>(g_dyn);
     for (int i = threadIdx.x; i < kRows8 * kCopies8; i += blockDim.x) {
         const BucketEntry e = g_tab.bk8[i / kCopies8];
-        bk[i] = BucketEntry{e.boundary, e.kb4 * 16 + (i % kCopies8) * 4};
+        bk[i] = BucketEntry{e.boundary, e.kb4 * 32 + (i % kCopies8) * 8};
     }
-    float *q = reinterpret_cast<float *>(g_dyn + kBk8cBytes), *g = reinterpret_cast<float *>(g_dyn + kBk8cBytes + kL8cBytes);
-    for (int i = threadIdx.x; i < 256 * kCopies8; i += blockDim.x) {
-        q[i] = g_tab.q8[i / kCopies8];
-        g[i] = g_tab.g8[i / kCopies8];
-    }
-    float2 *p4 = reinterpret_cast<float2 *>(g_dyn + kBk8cBytes + 2 * kL8cBytes);
+    float2 *qg = reinterpret_cast<float2 *>(g_dyn + kBk8cBytes);
+    for (int i = threadIdx.x; i < 256 * kCopies8; i += blockDim.x)
+        qg[i] = make_float2(g_tab.q8[i / kCopies8], g_tab.g8[i / kCopies8]);
+    float2 *p4 = reinterpret_cast<float2 *>(g_dyn + kBk8cBytes + kQG8cBytes);
     for (int i = threadIdx.x; pair4 && i < 256 * kCopies4; i += blockDim.x) {
         const int p = i / kCopies4;
         p4[i] = make_float2(g_tab.q4[p & 15], g_tab.q4[p >> 4]);
@@ -149,6 +149,23 @@ __device__ __forceinline__ float2 f2_fma_rp(float2 a, float2 b, float2 c)
     return r;
 }
 
+// k + STEP when a >= b, else k: one compare and one predicated add (the
+// select-then-add a compiler makes of the conditional costs one more).  A NaN
+// operand compares false either way.
+template <uint32_t STEP>
+__device__ __forceinline__ uint32_t add_if_ge(uint32_t k, float a, float b)
+{
+    asm("{ .reg .pred p;\n\tsetp.ge.f32 p, %1, %2;\n\t@p add.u32 %0, %0, %3; }" : "+r"(k) : "f"(a), "f"(b), "n"(STEP));
+    return k;
+}
+// k + STEP when a < b, else k.
+template <uint32_t STEP>
+__device__ __forceinline__ uint32_t add_if_lt(uint32_t k, float a, float b)
+{
+    asm("{ .reg .pred p;\n\tsetp.lt.f32 p, %1, %2;\n\t@p add.u32 %0, %0, %3; }" : "+r"(k) : "f"(a), "f"(b), "n"(STEP));
+    return k;
+}
+
 // Codes of one lane: 16 coordinates of BITS bits, coordinate i at bit BITS*i.
 template <int BITS> struct LaneCodes { uint32_t w[BITS / 2]; };
 
@@ -205,16 +222,16 @@ template <int BITS, bool PAIR4>
 __device__ __forceinline__ void decode_add(float2 (&x)[8], float sigma, const LaneCodes<BITS> &c)
 {
     const float2 s2 = make_float2(sigma, sigma);
-    if constexpr (BITS == 8) {   // lane copies: byte 64 code + 4 (lane mod 16)
-        const float *q = q8c();
-        const uint32_t c4 = (threadIdx.x & 15u) << 2;
+    if constexpr (BITS == 8) {   // lane copies: the level at byte 128 code + 8 (lane mod 16)
+        const float2 *q = qg8c();
+        const uint32_t c8 = (threadIdx.x & 15u) << 3;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int i0 = 2 * k, i1 = 2 * k + 1;
             const uint32_t w0 = c.w[i0 >> 2], w1 = c.w[i1 >> 2];
             const int b0 = 8 * (i0 & 3), b1 = 8 * (i1 & 3);
-            const uint32_t o0 = ((b0 >= 6 ? (w0 >> (b0 >= 6 ? b0 - 6 : 0)) : (w0 << 6)) & 0x3FC0u) | c4;
-            const uint32_t o1 = ((b1 >= 6 ? (w1 >> (b1 >= 6 ? b1 - 6 : 0)) : (w1 << 6)) & 0x3FC0u) | c4;
+            const uint32_t o0 = ((b0 >= 7 ? (w0 >> (b0 >= 7 ? b0 - 7 : 0)) : (w0 << 7)) & 0x7F80u) | c8;
+            const uint32_t o1 = ((b1 >= 7 ? (w1 >> (b1 >= 7 ? b1 - 7 : 0)) : (w1 << 7)) & 0x7F80u) | c8;
             x[k] = f2_fma(s2, make_float2(lds_at<float>(q, o0), lds_at<float>(q, o1)), x[k]);
         }
     } else if constexpr (BITS == 4 && !PAIR4) {   // one level load per code (16 entries: 16 banks)
@@ -319,11 +336,11 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
         B[i + 4] = B[i] ^ 0x80000000u;
     }
 
-    // 8 bits: lane copies, level byte offsets 64 k + 4 (lane mod 16), steps of 64
-    const float *q = BITS == 8 ? q8c() : Lvl<BITS>::q();
-    const float *g = BITS == 8 ? g8c() : Lvl<BITS>::g();
+    // 8 bits: lane copies, {level, gap} at byte offsets 128 k + 8 (lane mod 16), steps of 128
+    const float *q = BITS == 8 ? reinterpret_cast<const float *>(qg8c()) : Lvl<BITS>::q();
+    const float *g = BITS == 8 ? nullptr : Lvl<BITS>::g();
     const BucketEntry *bk = BITS == 8 ? bk8c() : Lvl<BITS>::bk();
-    constexpr uint32_t kStep = BITS == 8 ? 64u : 4u;
+    constexpr uint32_t kStep = BITS == 8 ? 128u : 4u;
     // byte offset of bucket b: 8b (2 bits: r = rint(8Hy), 8b = r & ~7) or,
     // for the lane-copied 4- and 8-bit tables, 128b + 8 (lane mod 16)
     // (r = rint(128Hy); 8 bits: b + 256)
@@ -345,29 +362,36 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
         const float2 tf = f2_fma(y, mul2, M2);                 // S*H*y is exact: one rounding = rint
         const BucketEntry b0 = lds_at<BucketEntry>(bk, (__float_as_uint(tf.x) & kB) | lane_copy);
         const BucketEntry b1 = lds_at<BucketEntry>(bk, (__float_as_uint(tf.y) & kB) | lane_copy);
-        uint32_t k40 = (uint32_t)b0.kb4 + (y.x >= b0.boundary ? kStep : 0u);
-        uint32_t k41 = (uint32_t)b1.kb4 + (y.y >= b1.boundary ? kStep : 0u);
-        if (BITS == 8) {   // a non-finite y reaches rows past 512: keep its offsets inside the tables
-            k40 &= 0x3FFCu;
-            k41 &= 0x3FFCu;
+        uint32_t k40 = add_if_ge<kStep>((uint32_t)b0.kb4, y.x, b0.boundary);
+        uint32_t k41 = add_if_ge<kStep>((uint32_t)b1.kb4, y.y, b1.boundary);
+        if (BITS == 8) {   // a non-finite y reaches rows past 512: keep its offsets inside the table
+            k40 &= 0x7FF8u;
+            k41 &= 0x7FF8u;
         }
         if (!ONE_LEVEL) {  // buckets wider than a gap: walk up (bounded by the top level)
             constexpr uint32_t kTop = kStep * ((1u << BITS) - 1u);
             while (k40 < kTop && y.x >= lds_at<float>(q, k40 + kStep)) k40 += kStep;
             while (k41 < kTop && y.y >= lds_at<float>(q, k41 + kStep)) k41 += kStep;
         }
-        const float2 qv = make_float2(lds_at<float>(q, k40), lds_at<float>(q, k41));
-        const float2 gv = make_float2(lds_at<float>(g, k40), lds_at<float>(g, k41));
-        const float2 t = f2_fma_rp(f2_sub(y, qv), gv, C2);     // 2^23 + ceil(d * G16)
+        float2 t;   // 2^23 + ceil(d * G16)
+        if (BITS == 8) {   // one 8-byte load gives the level and its gap
+            const float2 e0 = lds_at<float2>(q, k40), e1 = lds_at<float2>(q, k41);
+            t = make_float2(__fmaf_ru(__fsub_rn(y.x, e0.x), e0.y, 8388608.0f),
+                            __fmaf_ru(__fsub_rn(y.y, e1.x), e1.y, 8388608.0f));
+        } else {
+            const float2 qv = make_float2(lds_at<float>(q, k40), lds_at<float>(q, k41));
+            const float2 gv = make_float2(lds_at<float>(g, k40), lds_at<float>(g, k41));
+            t = f2_fma_rp(f2_sub(y, qv), gv, C2);
+        }
         const float U0 = __uint_as_float(__byte_perm(A[k], 0x4B00u, 0x5410u));   // 2^23 + U
         const float U1 = __uint_as_float(__byte_perm(B[k], 0x4B00u, 0x5432u));
-        k40 += U0 < t.x ? kStep : 0u;
-        k41 += U1 < t.y ? kStep : 0u;
+        k40 = add_if_lt<kStep>(k40, U0, t.x);
+        k41 = add_if_lt<kStep>(k41, U1, t.y);
         const int i0 = 2 * k, i1 = 2 * k + 1;
         const int s0 = (BITS * i0) & 31, s1 = (BITS * i1) & 31;
-        if (BITS == 8) {   // code = offset / 64 (the lane part is below bit 6)
-            out.w[(BITS * i0) >> 5] |= (k40 >> 6) << s0;
-            out.w[(BITS * i1) >> 5] |= (k41 >> 6) << s1;
+        if (BITS == 8) {   // code = offset / 128 (the lane part is below bit 7)
+            out.w[(BITS * i0) >> 5] |= (k40 >> 7) << s0;
+            out.w[(BITS * i1) >> 5] |= (k41 >> 7) << s1;
         } else {   // codes never overlap, so adding them packs (a shift-and-add each)
             out.w[(BITS * i0) >> 5] += s0 >= 2 ? (k40 << (s0 >= 2 ? s0 - 2 : 0)) : (k40 >> 2);
             out.w[(BITS * i1) >> 5] += s1 >= 2 ? (k41 << (s1 >= 2 ? s1 - 2 : 0)) : (k41 >> 2);
@@ -379,7 +403,12 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
 // Bytes of one staging slot (a pair of super-groups): addends, incoming
 // codes, incoming group scales.
 template <bool ADD_F32, bool SF32>
-__host__ __device__ constexpr int stage_bytes() { return (ADD_F32 ? 2048 : 1024) + 512 + (SF32 ? 128 : 32); }
+__host__ __device__ constexpr int stage_bytes() { return (ADD_F32 ? 2048 : 0) + 512 + (SF32 ? 128 : 32); }
+// 8-bit bucket rows up to 1023 (reached by a non-finite y) stay inside the
+// smallest dynamic allocation of a hop kernel
+static_assert(1024 * kCopies8 * 8 <= tab_bytes(false) + kWarps * kStages * stage_bytes<false, false>() &&
+                  1024 * kCopies8 * 8 <= tab_bytes(true) + kWarps * kStages * stage_bytes<true, false>(),
+              "garbage rows in bounds");
 
 // One work unit: super-groups j0 .. j0+cnt-1 (one task, one bitwidth).  PP
 // supplies perm, mu and the generator key and round.  Message bytes are
@@ -391,7 +420,7 @@ template <int BITS, bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32, bool O
 __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t *stg, int64_t j0, int cnt,
                                          int lane)
 {
-    constexpr int A_BYTES = ADD_F32 ? 2048 : 1024;
+    constexpr int A_BYTES = ADD_F32 ? 2048 : 0;   // bf16 addends bypass the staging
     constexpr int C_OFF = A_BYTES, U_OFF = A_BYTES + 512, STAGE = stage_bytes<ADD_F32, SF32>();
     constexpr int CB = 32 * BITS;                 // code bytes per super-group
     constexpr int UB = SF32 ? 64 : 16;            // scale bytes per super-group
@@ -435,10 +464,6 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
                 const char *src = add_f + (int64_t)s * 1024;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) cp_async16(st + half * 1024 + k * 256 + hl * 16, src + 16 * k);
-            } else {
-                const char *src = add_b + (int64_t)old * 512;
-                cp_async16(st + half * 512 + hl * 16, src);
-                cp_async16(st + half * 512 + 256 + hl * 16, src + 16);
             }
             if (HAS_IN) {
                 if (hl < 2 * BITS) cp_async16(st + C_OFF + half * 256 + hl * 16, in_c + (int64_t)s * CB);
@@ -452,10 +477,25 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
         cp_async_commit();
     };
 
+    // bf16 addends go straight to registers, one pair ahead (a lane's 32
+    // bytes are two 16-byte loads; no shared-memory round trip)
+    uint4 na = make_uint4(0u, 0u, 0u, 0u), nb = na;
+    auto load_add = [&](int pp) {
+        const int s = 2 * pp + half;
+        const int32_t old = __shfl_sync(kFull, old_i, s & 31);
+        if (!ADD_F32 && pp < npairs && s < cnt) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(add_b + (int64_t)old * 512);
+            na = __ldg(src);
+            nb = __ldg(src + 1);
+        }
+    };
+    if (!ADD_F32) load_add(0);
 #pragma unroll
     for (int pp = 0; pp < kStages - 1; ++pp) issue(pp);
     uint32_t e_out = 0;
     for (int p = 0; p < npairs; ++p) {
+        const uint4 ca = na, cb = nb;
+        if (!ADD_F32) load_add(p + 1);
         issue(p + kStages - 1);
         cp_async_wait<kStages - 1>();
         __syncwarp();
@@ -474,9 +514,7 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
                 x[2 * k + 1] = make_float2(v.z, v.w);
             }
         } else {
-            const uint4 a = *reinterpret_cast<const uint4 *>(st + half * 512 + hl * 16);
-            const uint4 b = *reinterpret_cast<const uint4 *>(st + half * 512 + 256 + hl * 16);
-            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            const uint32_t w[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
 #pragma unroll
             for (int k = 0; k < 8; ++k) x[k] = make_float2(bf16_lo_minus(w[k], mu), bf16_hi_minus(w[k], mu));
         }

@@ -32,9 +32,11 @@ def _sample(J, chunk_lo, n2, n4, rs, k=1500):
     return np.array(sorted(pts), dtype=np.int64)
 
 
-def _full_size(name, butterfly):
+def _full_size(name, butterfly, budget=None):
     build.build()
     w = synth.WORKLOADS[name]
+    if budget is not None:
+        w = w.scaled(w.n, budget=budget)
     N, J = w.n_ranks, w.n_sg
     grads = synth.generate(w, "cuda", seed=0)
     ar = DynamiQAllReduce(N, J, budget=w.budget, correlated=w.correlated, butterfly=butterfly, seed=0)
@@ -86,6 +88,12 @@ def test_gemma1b_ring16_full_size_sampled():
     """Gemma-1B-sized gradient, 16 workers, ring (the per-step exchange at
     this size), budget 5."""
     _full_size("gemma1b_ring16", butterfly=False)
+
+
+@pytest.mark.parametrize("B", [4.0, 6.0])
+def test_gemma1b_ring16_budget_sweep_full_size_sampled(B):
+    """The other budgets of the Gemma-1B workload's sweep, at full size."""
+    _full_size("gemma1b_ring16", butterfly=False, budget=B)
 
 
 def test_llama3_8b_buckets_full_size():
