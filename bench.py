@@ -332,9 +332,9 @@ KERNEL_NAMES = {"compress": "hop_kernel<false,false> (compress)", "dar": "hop_ke
                 "dar_bf16_final": "hop_kernel<true,false> (DAR, bf16 addend)",
                 "decode": "decode_kernel", "stats": "stats_kernel", "fused_ring": "fused_ring_kernel"}
 # the key under which profiles/dram_traffic.txt lists a kernel role
-TRAFFIC_KEY = {"dar": "hop_kernel<true,false>", "dar_bf16_split": "hop_kernel<true,false>",
-               "dar_bf16_final": "hop_kernel<true,false>", "dar_f32_split": "hop_kernel<true,true>",
-               "dar_f32_final": "hop_kernel<true,true>", "compress": "hop_kernel<false,false>",
+TRAFFIC_KEY = {"dar": "hop_kernel<true,false>", "dar_bf16_split": "hop_kernel<true,false>:split",
+               "dar_bf16_final": "hop_kernel<true,false>:final", "dar_f32_split": "hop_kernel<true,true>:split",
+               "dar_f32_final": "hop_kernel<true,true>:final", "compress": "hop_kernel<false,false>",
                "decode": "decode_kernel", "stats": "stats_kernel", "fused_ring": "fused_ring_kernel"}
 
 
@@ -547,7 +547,12 @@ def e2e_timing(args, w, ar, grads, outs, fused, dev, world):
 
     N, J = w.n_ranks, w.n_sg
     KE = args.e2e_steps or max(3, min(args.steps, 10))
-    hosts = [pinned_host_copy(g) for g in grads]
+    # one pinned host copy per simulated worker; under torchrun (one process
+    # per GPU, all on one node) the simulated workers of a process share one
+    # pinned copy, so the node's pinned memory stays one gradient per GPU (the
+    # bytes copied per step are the same)
+    shared = world > 1
+    hosts = [pinned_host_copy(grads[0])] * N if shared else [pinned_host_copy(g) for g in grads]
     out_host = torch.empty(J * SG, dtype=torch.float32, pin_memory=True)
     gbuf = [grads, [torch.empty_like(g) for g in grads]]
     main = torch.cuda.current_stream()
@@ -599,7 +604,9 @@ def e2e_timing(args, w, ar, grads, outs, fused, dev, world):
     h2d = N * J * SG * 2
     res = {"value": ms_e2e / (world * gb), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": J * SG * 4, "ms_per_step": ms_e2e, "steps": KE,
-           "h2d_gbs": h2d / (ms_e2e * 1e-3) / 1e9}
+           "h2d_gbs": h2d / (ms_e2e * 1e-3) / 1e9,
+           "host_buffers": "one pinned buffer shared by the simulated workers of each process" if shared
+           else "one pinned buffer per simulated worker"}
     del gbuf[1], hosts
     return res
 
@@ -823,10 +830,11 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
                 "note": "planning kernels of bucket k+1 run on a second stream under bucket k's exchange, so "
                         "the launch shares add up to more than the step"}
 
-    sq.run(seq, seq_out, round0=(W + K + 2) * nb)          # warm-up pass (workspace allocation)
-    ms_seq = timed(sq, 1, W + K + 3)
-    ms_alt = None
-    if alt is not None:
+    ms_seq = ms_alt = None
+    if not args.lean:
+        sq.run(seq, seq_out, round0=(W + K + 2) * nb)      # warm-up pass (workspace allocation)
+        ms_seq = timed(sq, 1, W + K + 3)
+    if alt is not None and not args.lean:
         alt.run(seq, seq_out, round0=(W + K + 4) * nb)
         ms_alt = timed(alt, 2, W + K + 5)
         if alt.fused:
@@ -837,9 +845,9 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
     ms_max = max_over_ranks(ms, world, dev)
     gb = w.n * 2 / 1e9
 
-    e2e = bucketed_e2e(args, w, ov, pool, pool_of, outs_pool, nb, dev, world, gb)
+    e2e = None if args.lean else bucketed_e2e(args, w, ov, pool, pool_of, outs_pool, nb, dev, world, gb)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.lean:
         cpu = bucketed_cpu_baseline(w, nb, gb)
     line = {
         "metric": METRIC, "value": ms_max / (world * gb), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
@@ -853,7 +861,7 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
                          "(about 0.6 GB) exceeds L2"},
         "per_bucket_ms": ms_max / nb,
         "two_streams": {"ms_per_pass_overlapped": ms, "ms_per_pass_one_stream": ms_seq,
-                        "saved_frac": 1.0 - ms / ms_seq},
+                        "saved_frac": (1.0 - ms / ms_seq) if ms_seq else None},
         "fused_exchange": {"used": ov.fused, "ms_per_pass_fused": ms_fused, "ms_per_pass_multi_launch": ms_ml},
         "kernels": kernels, "ms_per_step_logged": ms_logged, "roofline": roofline,
         "gpu_launches": n_launch, "clocks": clk, "cpu_baseline": cpu, "e2e": e2e,

@@ -23,7 +23,12 @@
  * Conventions (all entry points):
  *   - Device pointers are cudaMalloc/PyTorch device memory on the current
  *     device; "host" marks the few host pointers.  The caller owns every
- *     buffer; the library never allocates device memory.
+ *     buffer; the library never allocates device memory.  dq_plan and
+ *     dq_get_device_status read their results back through one small
+ *     pinned host buffer mapped into the device address space, one per
+ *     calling thread (under 64 bytes, allocated on the thread's first such
+ *     call, kept until the process exits): the readback is a one-thread
+ *     kernel write, so it never waits behind copies queued on other streams.
  *   - stream is a cudaStream_t (NULL = legacy default stream).  Work is
  *     enqueued asynchronously; only dq_plan synchronises (it reads three
  *     counts back to the host).

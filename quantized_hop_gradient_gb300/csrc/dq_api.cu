@@ -594,6 +594,94 @@ bool exchange_layout(const dq_config *cfg, int32_t butterfly, const dq_plan_info
 
 }  // namespace
 
+namespace {
+
+// What dq_plan reads back to the host: the stream counts, the threshold and
+// the non-finite flag.
+struct PlanReadback {
+    int64_t counts[3];
+    float T;
+    int32_t nonfinite;
+    int32_t status;   // dq_get_device_status
+};
+
+// One thread copies the plan's results into host memory mapped into the
+// device address space.  The host then reads them after synchronising the
+// plan's stream: no copy-engine transfer is involved, so the read cannot
+// queue behind large host<->device copies that other streams have in flight
+// (a pageable cudaMemcpyAsync could, and stalled the planning of a round
+// until the next round's gradient upload had finished).
+__global__ void plan_readback_kernel(const int64_t *counts, const float *T, const int32_t *nonfinite,
+                                     PlanReadback *out)
+{
+    if (threadIdx.x == 0) {
+        out->counts[0] = counts[0];
+        out->counts[1] = counts[1];
+        out->counts[2] = counts[2];
+        out->T = T ? *T : 0.0f;
+        out->nonfinite = *nonfinite;
+    }
+}
+
+// Zeroes up to two 32-bit words in stream order.  A kernel, not
+// cudaMemsetAsync: a small memset may be carried out by a copy engine and
+// then wait behind large host<->device copies queued by other streams.
+__global__ void zero_words_kernel(uint32_t *a, int na, uint32_t *b)
+{
+    if (threadIdx.x < na) a[threadIdx.x] = 0u;
+    if (threadIdx.x == 0 && b) *b = 0u;
+}
+
+// a[0 .. na) and, if b is not null, b[0] (na <= 32)
+cudaError_t zero_words(void *a, int na, void *b, cudaStream_t st)
+{
+    zero_words_kernel<<<1, 32, 0, st>>>(static_cast<uint32_t *>(a), na, static_cast<uint32_t *>(b));
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+// One thread copies a device status word into host memory mapped into the
+// device address space (the readback of dq_get_device_status).
+__global__ void status_readback_kernel(const int32_t *src, int32_t *out)
+{
+    if (threadIdx.x == 0) *out = *src;
+}
+
+// The calling thread's pinned, device-mapped readback buffer (allocated on
+// the thread's first dq_plan, kept until the process exits).
+PlanReadback *plan_readback_buffer()
+{
+    thread_local PlanReadback *buf = nullptr;
+    if (!buf) {
+        void *p = nullptr;
+        if (cudaHostAlloc(&p, sizeof(PlanReadback), cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess)
+            return nullptr;
+        buf = static_cast<PlanReadback *>(p);
+    }
+    return buf;
+}
+
+// Enqueues the readback on st, synchronises st and returns the host copy.
+dq_status plan_read(const int64_t *counts, const float *T, const int32_t *nonfinite, cudaStream_t st,
+                    PlanReadback *out)
+{
+    PlanReadback *buf = plan_readback_buffer();
+    if (!buf) return DQ_ERR_CUDA;
+    PlanReadback *dev = nullptr;
+    if (cudaHostGetDevicePointer(reinterpret_cast<void **>(&dev), buf, 0) != cudaSuccess) return DQ_ERR_CUDA;
+    plan_readback_kernel<<<1, 32, 0, st>>>(counts, T, nonfinite, dev);
+    note_launches(1);
+    if (cudaGetLastError() != cudaSuccess) return DQ_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return DQ_ERR_CUDA;
+    const volatile PlanReadback *v = buf;   // written by the device: read it afresh
+    for (int i = 0; i < 3; ++i) out->counts[i] = v->counts[i];
+    out->T = v->T;
+    out->nonfinite = v->nonfinite;
+    return DQ_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t dq_plan_workspace_bytes(int32_t n_ranks, int64_t n_sg)
@@ -627,7 +715,7 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
     int64_t *counts = reinterpret_cast<int64_t *>(w + L.counts);
     int32_t *nonfinite = reinterpret_cast<int32_t *>(w + L.counts + 32);   // inside the counts slot
     void *scratch = w + L.scratch;
-    if (cudaMemsetAsync(nonfinite, 0, sizeof(int32_t), st) != cudaSuccess) return DQ_ERR_CUDA;
+    if (zero_words(nonfinite, 1, nullptr, st) != cudaSuccess) return DQ_ERR_CUDA;
     if (rank_ready) {  // one launch per rank, each after its rank's event
         for (int32_t r = 0; r < N; ++r) {
             if (rank_ready[r] && cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(rank_ready[r]), 0) != cudaSuccess)
@@ -655,24 +743,20 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
     }
     const LogSlot slot = log_begin(log, DQ_LAUNCH_ALLOCATE_REORDER, n_sg, st);
     if (launch_stats_reduce(mean_all, sq_all, N, n_sg, M, F, mu, st, nonfinite) != cudaSuccess) return DQ_ERR_CUDA;
-    int32_t h_nonfinite = 0;
     if (n_sg <= small_plan_max_sg()) {
         // small problems: allocation and reorder in one launch
         const int64_t cap = (int64_t)floor((double)cfg->budget_bits * (double)n_sg);
         if (launch_plan_small(F, n_sg, cap, cfg->fixed_bits, b, T, counts, perm, st) != cudaSuccess)
             return DQ_ERR_CUDA;
         log_end(slot, st);
-        int64_t hc[5];   // counts[3], padding, the non-finite flag
-        float hT = 0.0f;
-        if (cudaMemcpyAsync(hc, counts, sizeof(hc), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DQ_ERR_CUDA;
-        if (cudaMemcpyAsync(&hT, T, sizeof(hT), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DQ_ERR_CUDA;
-        if (cudaStreamSynchronize(st) != cudaSuccess) return DQ_ERR_CUDA;
-        memcpy(&h_nonfinite, reinterpret_cast<const uint8_t *>(hc) + 32, sizeof(int32_t));
-        if (h_nonfinite) return DQ_ERR_NONFINITE;
-        info->T = cfg->fixed_bits ? NAN : hT;
-        info->n2 = hc[0];
-        info->n4 = hc[1];
-        info->n8 = hc[2];
+        PlanReadback h;
+        const dq_status rs = plan_read(counts, T, nonfinite, st, &h);
+        if (rs != DQ_OK) return rs;
+        if (h.nonfinite) return DQ_ERR_NONFINITE;
+        info->T = cfg->fixed_bits ? NAN : h.T;
+        info->n2 = h.counts[0];
+        info->n4 = h.counts[1];
+        info->n8 = h.counts[2];
         return DQ_OK;
     }
     if (cfg->fixed_bits) {
@@ -682,10 +766,12 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
         const dq_status s = dq_reorder(b, n_sg, perm, scratch, plan_scratch_bytes(n_sg), stream);
         if (s != DQ_OK) return s;
         log_end(slot, st);
-        if (cudaMemcpyAsync(&h_nonfinite, nonfinite, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-            return DQ_ERR_CUDA;
-        if (cudaStreamSynchronize(st) != cudaSuccess) return DQ_ERR_CUDA;
-        if (h_nonfinite) return DQ_ERR_NONFINITE;
+        // the counts slot is not written on this path: zeroed words stand in
+        if (zero_words(counts, 6, nullptr, st) != cudaSuccess) return DQ_ERR_CUDA;
+        PlanReadback h;
+        const dq_status rs = plan_read(counts, nullptr, nonfinite, st, &h);
+        if (rs != DQ_OK) return rs;
+        if (h.nonfinite) return DQ_ERR_NONFINITE;
         info->T = NAN;
         info->n2 = cfg->fixed_bits == 2 ? n_sg : 0;
         info->n4 = cfg->fixed_bits == 4 ? n_sg : 0;
@@ -697,17 +783,14 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
     s = dq_reorder(b, n_sg, perm, scratch, plan_scratch_bytes(n_sg), stream);
     if (s != DQ_OK) return s;
     log_end(slot, st);
-    int64_t hc[5];   // counts[3], padding, the non-finite flag
-    float hT = 0.0f;
-    if (cudaMemcpyAsync(hc, counts, sizeof(hc), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DQ_ERR_CUDA;
-    if (cudaMemcpyAsync(&hT, T, sizeof(hT), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DQ_ERR_CUDA;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return DQ_ERR_CUDA;
-    memcpy(&h_nonfinite, reinterpret_cast<const uint8_t *>(hc) + 32, sizeof(int32_t));
-    if (h_nonfinite) return DQ_ERR_NONFINITE;
-    info->T = hT;
-    info->n2 = hc[0];
-    info->n4 = hc[1];
-    info->n8 = hc[2];
+    PlanReadback h;
+    const dq_status rs = plan_read(counts, T, nonfinite, st, &h);
+    if (rs != DQ_OK) return rs;
+    if (h.nonfinite) return DQ_ERR_NONFINITE;
+    info->T = h.T;
+    info->n2 = h.counts[0];
+    info->n4 = h.counts[1];
+    info->n8 = h.counts[2];
     return DQ_OK;
 }
 
@@ -874,8 +957,7 @@ dq_status dq_exchange_fused(const dq_config *cfg, const void *const *grads, int6
     P->barrier = reinterpret_cast<unsigned int *>(w + X.total);
     P->status = status_dev;
     P->timeout_cycles = kBarrierTimeoutCycles;
-    if (cudaMemsetAsync(P->barrier, 0, sizeof(unsigned int), st) != cudaSuccess) return DQ_ERR_CUDA;
-    if (cudaMemsetAsync(status_dev, 0, sizeof(int32_t), st) != cudaSuccess) return DQ_ERR_CUDA;
+    if (zero_words(P->barrier, 1, status_dev, st) != cudaSuccess) return DQ_ERR_CUDA;
     const LogSlot slot = log_begin(log, DQ_LAUNCH_FUSED_RING, n_sg * (N + 1), st);
     const cudaError_t e = launch_fused_ring(*P, st);
     log_end(slot, st);
@@ -890,10 +972,15 @@ dq_status dq_get_device_status(const int32_t *status_dev, int32_t *status_host, 
     if (!status_dev || !status_host) return DQ_ERR_INVALID_ARG;
     if ((uintptr_t)status_dev & 3u) return DQ_ERR_ALIGNMENT;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int32_t v = 0;
-    if (cudaMemcpyAsync(&v, status_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DQ_ERR_CUDA;
+    PlanReadback *buf = plan_readback_buffer();
+    if (!buf) return DQ_ERR_CUDA;
+    PlanReadback *dev = nullptr;
+    if (cudaHostGetDevicePointer(reinterpret_cast<void **>(&dev), buf, 0) != cudaSuccess) return DQ_ERR_CUDA;
+    status_readback_kernel<<<1, 32, 0, st>>>(status_dev, &dev->status);
+    note_launches(1);
+    if (cudaGetLastError() != cudaSuccess) return DQ_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return DQ_ERR_CUDA;
-    *status_host = v;
+    *status_host = *reinterpret_cast<volatile int32_t *>(&buf->status);
     return DQ_OK;
 }
 
@@ -910,8 +997,7 @@ dq_status dq_barrier_selftest(int32_t n_blocks, int32_t missing, int64_t timeout
     if (n_blocks > sm_count()) return DQ_ERR_INVALID_ARG;   // one small CTA per SM at most: all resident
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned int *counter = static_cast<unsigned int *>(scratch);
-    if (cudaMemsetAsync(counter, 0, sizeof(unsigned int), st) != cudaSuccess) return DQ_ERR_CUDA;
-    if (cudaMemsetAsync(status_dev, 0, sizeof(int32_t), st) != cudaSuccess) return DQ_ERR_CUDA;
+    if (zero_words(counter, 1, status_dev, st) != cudaSuccess) return DQ_ERR_CUDA;
     return cuda_status(launch_barrier_selftest(n_blocks, missing, (long long)timeout_cycles, counter, status_dev, st));
 }
 

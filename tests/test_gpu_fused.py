@@ -94,7 +94,10 @@ def test_fused_is_one_launch():
     n0 = dq.dq_launch_count()
     ar.exchange(gd, outs, fused=True, log=log)
     torch.cuda.synchronize()
-    assert dq.dq_launch_count() - n0 == 1
+    # the exchange is one cooperative launch; a one-thread kernel before it
+    # zeroes its barrier counter and status word (in stream order, without
+    # a memset that a copy engine could hold behind other streams' copies)
+    assert dq.dq_launch_count() - n0 == 2
     assert [k for k, _, _ in log.launches()] == [dq.DQ_LAUNCH_FUSED_RING]
     ar.check_status()
 
