@@ -25,8 +25,13 @@
  *
  * Parity pins: every function here is checked by the CPU tests against
  * something other than itself (closed forms, published threshold ratios,
- * brute force on tiny inputs, an independent Philox implementation,
- * Monte-Carlo unbiasedness).  None is "parity unpinned".
+ * brute force on tiny inputs, the published Philox4x32-10 known-answer
+ * vectors and an independent Philox implementation, exact rational
+ * arithmetic for the single-rounding decode-accumulate, Monte-Carlo
+ * unbiasedness).  None is "parity unpinned".  The rounding rules (the
+ * exact-product comparison of the stochastic rounding, the single rounding
+ * of the decode-accumulate and of the final add-back) are fixed: a change to
+ * them must name the passage of the pages that requires it.
  */
 #include <math.h>
 #include <stdint.h>
