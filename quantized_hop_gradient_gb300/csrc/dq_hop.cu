@@ -10,9 +10,9 @@
 // permutation entries, means and exponent bytes are loaded once, coalesced,
 // and broadcast by shuffles; its message addresses and its send and keep
 // masks are computed once per unit.  The incoming codes and UINT8 scales
-// (and an fp32 partial sum) of a pair of super-groups are staged in shared
-// memory by cp.async, one pair ahead of the computation; a bf16 gradient
-// goes straight to registers, also one pair ahead.
+// of a pair of super-groups are staged in shared memory by cp.async, one
+// pair ahead of the computation; the addend (a bf16 gradient or an fp32
+// partial sum) goes straight to registers, also one pair ahead.
 //
 // Per coordinate the quantizer costs a packed fused multiply-add for y, one
 // for the bucket index, an AND, two or three shared-memory loads (the
@@ -57,10 +57,9 @@ __device__ __forceinline__ void expand_bk4()
 // of copy c sits at byte 128 k + 8c.  An 8-byte load is served per
 // half-warp, whose 16 lanes then always read 16 different bank pairs: one
 // conflict-free load per coordinate gives both the level and its gap.
-// After them, in the kernels whose addends are bf16 (fp32 addends leave no
-// room), the decoder's 4-bit pair table: entry p (a code byte: low nibble =
-// first coordinate's code) holds the two levels, one copy per half-warp
-// lane, copy c of entry p at byte 128 p + 8c.
+// After them, the decoder's 4-bit pair table: entry p (a code byte: low
+// nibble = first coordinate's code) holds the two levels, one copy per
+// half-warp lane, copy c of entry p at byte 128 p + 8c.
 extern __shared__ __align__(16) uint8_t g_dyn[];
 constexpr int kCopies8 = 16;
 constexpr int kRows8 = 2 * kOff8 + 1;
@@ -68,7 +67,7 @@ constexpr int kBk8cBytes = kRows8 * kCopies8 * 8;
 constexpr int kQG8cBytes = 256 * kCopies8 * 8;
 constexpr int kQ4pBytes = 256 * kCopies4 * 8;
 constexpr int kTab8Bytes = kBk8cBytes + kQG8cBytes;
-__host__ __device__ constexpr int tab_bytes(bool add_f32) { return kTab8Bytes + (add_f32 ? 0 : kQ4pBytes); }
+__host__ __device__ constexpr int tab_bytes(bool) { return kTab8Bytes + kQ4pBytes; }
 static_assert(kTab8Bytes % 16 == 0 && kQ4pBytes % 16 == 0, "16-byte aligned staging");
 __device__ __forceinline__ const BucketEntry *bk8c() { return reinterpret_cast<const BucketEntry *>(g_dyn); }
 __device__ __forceinline__ const float2 *qg8c() { return reinterpret_cast<const float2 *>(g_dyn + kBk8cBytes); }
@@ -403,7 +402,7 @@ __device__ __forceinline__ LaneCodes<BITS> quantize_group(const float2 (&x)[8], 
 // Bytes of one staging slot (a pair of super-groups): addends, incoming
 // codes, incoming group scales.
 template <bool ADD_F32, bool SF32>
-__host__ __device__ constexpr int stage_bytes() { return (ADD_F32 ? 2048 : 0) + 512 + (SF32 ? 128 : 32); }
+__host__ __device__ constexpr int stage_bytes() { return 512 + (SF32 ? 128 : 32); }
 // 8-bit bucket rows up to 1023 (reached by a non-finite y) stay inside the
 // smallest dynamic allocation of a hop kernel
 static_assert(1024 * kCopies8 * 8 <= tab_bytes(false) + kWarps * kStages * stage_bytes<false, false>() &&
@@ -420,7 +419,7 @@ template <int BITS, bool HAS_IN, bool ADD_F32, bool ONE_LEVEL, bool SF32, bool O
 __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t *stg, int64_t j0, int cnt,
                                          int lane)
 {
-    constexpr int A_BYTES = ADD_F32 ? 2048 : 0;   // bf16 addends bypass the staging
+    constexpr int A_BYTES = 0;   // addends bypass the staging
     constexpr int C_OFF = A_BYTES, U_OFF = A_BYTES + 512, STAGE = stage_bytes<ADD_F32, SF32>();
     constexpr int CB = 32 * BITS;                 // code bytes per super-group
     constexpr int UB = SF32 ? 64 : 16;            // scale bytes per super-group
@@ -463,11 +462,6 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
         if (!HAS_IN) (void)__shfl_sync(kFull, old_i, s & 31);
         if (pp < npairs && s < cnt) {
             const uint32_t st = stg_s + (uint32_t)((pp % kStages) * STAGE);
-            if (ADD_F32) {
-                const char *src = add_f + (int64_t)s * 1024;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) cp_async16(st + half * 1024 + k * 256 + hl * 16, src + 16 * k);
-            }
             if (HAS_IN) {
                 if (hl < 2 * BITS) cp_async16(st + C_OFF + half * 256 + hl * 16, in_c + (int64_t)s * CB);
                 if (SF32) {
@@ -483,25 +477,37 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
     // bf16 addends go straight to registers, one pair ahead (a lane's 32
     // bytes are two 16-byte loads; no shared-memory round trip)
     uint4 na = make_uint4(0u, 0u, 0u, 0u), nb = na;
+    float4 nf[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) nf[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     int32_t nold = 0;   // perm entry of the pair that load_add fetched
     auto load_add = [&](int pp) {
         const int s = 2 * pp + half;
-        const int32_t old = __shfl_sync(kFull, old_i, s & 31);
+        const int32_t old = ADD_F32 ? 0 : __shfl_sync(kFull, old_i, s & 31);
         nold = old;
-        if (!ADD_F32 && pp < npairs && s < cnt) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(add_b + (int64_t)old * 512);
-            na = __ldg(src);
-            nb = __ldg(src + 1);
+        if (pp < npairs && s < cnt) {
+            if (ADD_F32) {
+                const float4 *src = reinterpret_cast<const float4 *>(add_f + (int64_t)s * 1024);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) nf[k] = __ldg(src + k);
+            } else {
+                const uint4 *src = reinterpret_cast<const uint4 *>(add_b + (int64_t)old * 512);
+                na = __ldg(src);
+                nb = __ldg(src + 1);
+            }
         }
     };
-    if (!ADD_F32) load_add(0);
+    load_add(0);
 #pragma unroll
     for (int pp = 0; pp < kStages - 1; ++pp) issue(pp);
     uint32_t e_out = 0;
     for (int p = 0; p < npairs; ++p) {
         const uint4 ca = na, cb = nb;
+        float4 cf[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cf[k] = nf[k];
         const int32_t cold = nold;
-        if (!ADD_F32) load_add(p + 1);
+        load_add(p + 1);
         issue(p + kStages - 1);
         cp_async_wait<kStages - 1>();
         __syncwarp();
@@ -515,9 +521,8 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
         if (ADD_F32) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float4 v = *reinterpret_cast<const float4 *>(st + half * 1024 + k * 256 + hl * 16);
-                x[2 * k] = make_float2(v.x, v.y);
-                x[2 * k + 1] = make_float2(v.z, v.w);
+                x[2 * k] = make_float2(cf[k].x, cf[k].y);
+                x[2 * k + 1] = make_float2(cf[k].z, cf[k].w);
             }
         } else {
             const uint32_t w[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
@@ -533,7 +538,7 @@ __device__ __forceinline__ void hop_unit(const PP &P, const HopTask &t, uint8_t 
                 sigma = __fmul_rn((float)u, __uint_as_float(ein << 23));
             }
             const LaneCodes<BITS> c = lds_codes<BITS>(st + C_OFF + half * 256 + hl * 2 * BITS);
-            decode_add<BITS, !ADD_F32>(x, sigma, c);
+            decode_add<BITS, true>(x, sigma, c);
         }
         const bool send = (send_m >> s) & 1u;
         const bool keep = (keep_m >> s) & 1u;
@@ -570,7 +575,7 @@ __global__ void __launch_bounds__(kWarps * 32, kHopBlocksPerSM) hop_kernel(const
     block_copy(&g_tab, &P.tab);
     __syncthreads();
     expand_bk4();
-    expand_tables(!ADD_F32 && HAS_IN);
+    expand_tables(HAS_IN);
     __syncthreads();
     uint8_t *dyn = g_dyn + tab_bytes(ADD_F32);
     constexpr int STAGE = stage_bytes<ADD_F32, SF32>();
