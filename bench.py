@@ -47,10 +47,11 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=0, help="steps of the end-to-end timing (0: auto)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
-    p.add_argument("--exchange", choices=["auto", "fused", "multi"], default="auto",
-                   help="ring exchange as one cooperative launch (fused) or one launch per step (multi); "
-                        "auto: fused where it is the faster path (allreduce.use_fused: rings of up to 64 ranks, up to 2^17 "
-                        "super-groups per worker)")
+    p.add_argument("--exchange", choices=["auto", "fused", "multi", "pipelined"], default="auto",
+                   help="ring exchange as one cooperative launch (fused), one launch per step (multi) or pipelined "
+                        "over parts of the super-groups (pipelined); auto: the faster path for the size "
+                        "(allreduce.exchange_mode: fused up to 2^17 super-groups per worker, pipelined above, rings "
+                        "of up to 64 ranks; the butterfly runs step by step)")
     p.add_argument("--lean", action="store_true",
                    help="the timed rounds only: no end-to-end, MXFP8, budget-sweep or accuracy legs and no extra "
                         "workloads (for profiler captures, whose launch lists stay short)")
@@ -178,6 +179,7 @@ KERNEL_SOURCES = {
     "hop_kernel": ["dq_common.cuh", "dq_hop.cu"],
     "decode_kernel": ["dq_common.cuh", "dq_hop.cu"],
     "fused_ring_kernel": ["dq_common.cuh", "dq_hop.cu"],
+    "wave_ring_kernel": ["dq_common.cuh", "dq_hop.cu"],
     "stats_kernel": ["dq_common.cuh", "dq_codec.cu"],
     "mx_hop_kernel": ["dq_common.cuh", "dq_mx.cu"],
 }
@@ -241,7 +243,10 @@ def launch_bytes(kind: int, sgs: int, msg_per_sg: float, fp32_addend: bool = Fal
     allocate + reorder span: N x 8 B/SG of statistics read, M, F, mu written
     (12 B/SG), then about five passes over F (20 B/SG) and the bitwidths and
     permutation (about 7 B/SG); fused ring exchange: the compress, N-1 DARs
-    and a decode that reads each message once and writes N outputs."""
+    and a decode that reads each message once and writes N outputs;
+    pipelined ring exchange: the same bytes per round, each launch counted
+    by its share of the round's super-groups (its logged hop and decode
+    super-groups add up to J (N + 1) per round)."""
     if kind == 0:
         return sgs * (512 + send_frac * msg_per_sg + 8 + (1.0 - send_frac) * 1024)
     if kind == 1:
@@ -251,7 +256,7 @@ def launch_bytes(kind: int, sgs: int, msg_per_sg: float, fp32_addend: bool = Fal
         return sgs * 1024 + sgs / min(n_ranks, 16) * (msg_per_sg + 8)
     if kind == 3:
         return sgs * (512 + 8)
-    if kind == 7:   # fused ring: sgs = J (N + 1); compress, N - 1 DARs, one decode read, N outputs
+    if kind in (7, 8):   # fused or pipelined ring: J (N + 1) super-groups per round
         J = sgs / (n_ranks + 1)
         return J * ((512 + msg_per_sg + 8) + (n_ranks - 1) * (2 * msg_per_sg + 512 + 8) +
                     (msg_per_sg + 8 + 1024 * n_ranks))
@@ -330,12 +335,15 @@ KERNEL_NAMES = {"compress": "hop_kernel<false,false> (compress)", "dar": "hop_ke
                 "dar_f32_split": "hop_kernel<true,true> (DAR, fp32 addend, split)",
                 "dar_f32_final": "hop_kernel<true,true> (DAR, fp32 addend)",
                 "dar_bf16_final": "hop_kernel<true,false> (DAR, bf16 addend)",
-                "decode": "decode_kernel", "stats": "stats_kernel", "fused_ring": "fused_ring_kernel"}
+                "decode": "decode_kernel", "stats": "stats_kernel", "fused_ring": "fused_ring_kernel",
+                "pipelined": "wave_ring_kernel (pipelined ring exchange: hop steps of later parts and the final "
+                             "decode of an earlier part in each launch)"}
 # the key under which profiles/dram_traffic.txt lists a kernel role
 TRAFFIC_KEY = {"dar": "hop_kernel<true,false>", "dar_bf16_split": "hop_kernel<true,false>:split",
                "dar_bf16_final": "hop_kernel<true,false>:final", "dar_f32_split": "hop_kernel<true,true>:split",
                "dar_f32_final": "hop_kernel<true,true>:final", "compress": "hop_kernel<false,false>",
-               "decode": "decode_kernel", "stats": "stats_kernel", "fused_ring": "fused_ring_kernel"}
+               "decode": "decode_kernel", "stats": "stats_kernel", "fused_ring": "fused_ring_kernel",
+               "pipelined": "wave_ring_kernel"}
 
 
 def kernel_table(log, steps: int, ms_step: float, msg_per_sg: float, N: int, butterfly: bool):
@@ -344,7 +352,7 @@ def kernel_table(log, steps: int, ms_step: float, msg_per_sg: float, N: int, but
     algorithmic bytes and the GB/s and Gcoords/s they imply.  Hop launches
     are named by their role in the round (hop_roles)."""
     roles = hop_roles(butterfly, N)
-    other = {2: "decode", 3: "stats", 4: "allocate_reorder", 7: "fused_ring"}
+    other = {2: "decode", 3: "stats", 4: "allocate_reorder", 7: "fused_ring", 8: "pipelined"}
     per = {}
     hop_i = 0
     for kind, sgs, t in log.launches():
@@ -396,21 +404,24 @@ def measure_round(args, w, dev, world, K, W, full: bool, local: int = 0):
     import torch
 
     from quantized_hop_gradient_gb300 import dq, study, synth
-    from quantized_hop_gradient_gb300.allreduce import DynamiQAllReduce, use_fused
+    from quantized_hop_gradient_gb300.allreduce import DynamiQAllReduce, exchange_mode, pipeline_parts
 
     N, J = w.n_ranks, w.n_sg
     butterfly = w.topology == "butterfly"
     grads = synth.generate(w, dev, seed=0)
     ar = DynamiQAllReduce(N, J, budget=w.budget, correlated=w.correlated, butterfly=butterfly, seed=0)
     outs = ar.new_outputs()
-    fusable = not butterfly and N <= dq.MAX_FUSED_RANKS
-    fused = use_fused(N, butterfly, J) if args.exchange == "auto" else (args.exchange == "fused")
-    if fused and not fusable:
-        raise SystemExit("the fused exchange covers rings of up to 64 ranks")
+    ring64 = not butterfly and N <= dq.MAX_FUSED_RANKS
+    # (fused, parts) of the exchange
+    mode = {"auto": exchange_mode(N, butterfly, J), "fused": (True, None), "multi": (False, None),
+            "pipelined": (False, pipeline_parts(N, J))}[args.exchange]
+    if mode != (False, None) and not ring64:
+        raise SystemExit("the fused and pipelined exchanges cover rings of up to 64 ranks")
+    STEPWISE = (False, None)
 
-    def step(i, log=None, fused=fused, ar=ar):
+    def step(i, log=None, mode=mode, ar=ar):
         ar.plan(grads, round=i, log=log)
-        ar.exchange(grads, outs, round=i, log=log, fused=fused)
+        ar.exchange(grads, outs, round=i, log=log, fused=mode[0], parts=mode[1])
 
     def measure(fused_, steps, first, sample_clocks=False, ar_=ar):
         """Times `steps` rounds (CUDA events on the launching stream, a
@@ -431,7 +442,7 @@ def measure_round(args, w, dev, world, K, W, full: bool, local: int = 0):
         torch.cuda.synchronize()
         t1 = time.time()
         barrier(world, dev)
-        if fused_:
+        if fused_[0]:
             ar_.check_status()
         clk = clocks.stop(t0, t1) if clocks else None
         return e0.elapsed_time(e1) / steps, log, dq.dq_launch_count() - n0, clk
@@ -439,16 +450,16 @@ def measure_round(args, w, dev, world, K, W, full: bool, local: int = 0):
     for i in range(W):
         step(i)
     torch.cuda.synchronize()
-    ms, log, n_launch, clk = measure(fused, K, W, sample_clocks=full)
+    ms, log, n_launch, clk = measure(mode, K, W, sample_clocks=full)
     peak, peak_kind = measured_peaks()
     msg_per_sg = stream_message_bytes(dq, ar.info, N) / J
     kernels = kernel_table(log, K, ms, msg_per_sg, N, butterfly)
     kernels_multi = ms_multi = None
-    if fused:
+    if mode != STEPWISE:
         # the per-step kernels of the multi-launch exchange, for the hop breakdown
-        step(W + K, None, False)
+        step(W + K, None, STEPWISE)
         KM = max(3, min(K, 10))
-        ms_multi, log_m, _, _ = measure(False, KM, W + K + 1)
+        ms_multi, log_m, _, _ = measure(STEPWISE, KM, W + K + 1)
         kernels_multi = kernel_table(log_m, KM, ms_multi, msg_per_sg, N, butterfly)
     dominant = max((k for k in kernels if k != "allocate_reorder"), key=lambda k: kernels[k]["share_of_step"])
     dk = kernels[dominant]
@@ -461,7 +472,9 @@ def measure_round(args, w, dev, world, K, W, full: bool, local: int = 0):
            "simulated_workers": N, "topology": w.topology, "coords_per_worker": w.n, "super_groups": J,
            "budget_bits": w.budget, "correlated_rounding": w.correlated,
            "allocation": {"T": ar.info.T, "n2": ar.info.n2, "n4": ar.info.n4, "n8": ar.info.n8},
-           "exchange": "fused (one cooperative launch per round)" if fused else "one launch per step",
+           "exchange": ("fused (one cooperative launch per round)" if mode[0] else
+                        f"pipelined over {mode[1]} parts ({N + mode[1]} launches per round)" if mode[1] else
+                        "one launch per step"),
            "dar": dar_summary(kernels_multi or kernels, peak, w.name), "kernels": kernels,
            "kernels_multi_launch": kernels_multi, "ms_per_step_multi_launch": ms_multi, "roofline": roofline,
            "gpu_launches": n_launch, "clocks": clk, "steps": K, "warmup": W}
@@ -493,16 +506,17 @@ def measure_round(args, w, dev, world, K, W, full: bool, local: int = 0):
     res["accuracy"] = acc
 
     if full:
-        res["e2e"] = e2e_timing(args, w, ar, grads, outs, fused, dev, world)
+        res["e2e"] = e2e_timing(args, w, ar, grads, outs, mode, dev, world)
         res["accuracy"], res["mxfp8"] = compare_mxfp8(w, grads, outs, ar, dev, N, J, butterfly, peak, acc, s_exact)
-        res["budget_sweep"] = budget_sweep(w, grads, outs, dev, N, J, butterfly, peak, s_exact, fused)
+        res["budget_sweep"] = budget_sweep(w, grads, outs, dev, N, J, butterfly, peak, s_exact, mode)
     del s_exact
     return res, grads
 
 
-def budget_sweep(w, grads, outs, dev, N, J, butterfly, peak, s_exact, fused):
-    """The workload's other budgets (same gradients): ms per round, the DAR
-    hop and vNMSE at each."""
+def budget_sweep(w, grads, outs, dev, N, J, butterfly, peak, s_exact, mode):
+    """The workload's other budgets (same gradients): ms per round (exchange
+    `mode` = (fused, parts)), the DAR hop (one launch per step) and vNMSE at
+    each."""
     import torch
 
     from quantized_hop_gradient_gb300 import dq, study
@@ -513,22 +527,27 @@ def budget_sweep(w, grads, outs, dev, N, J, butterfly, peak, s_exact, fused):
         if B == w.budget:
             continue
         ar = DynamiQAllReduce(N, J, budget=B, correlated=w.correlated, butterfly=butterfly, seed=0)
-        for i in range(2):
-            ar(grads, round=i, outs=outs, fused=fused)
         KB = 5
+
+        def rounds(mode_, first, log=None):
+            for i in range(2):
+                ar(grads, round=i, outs=outs, fused=mode_[0], parts=mode_[1])
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for i in range(KB):
+                ar.plan(grads, round=first + i, log=log)
+                ar.exchange(grads, outs, round=first + i, log=log, fused=mode_[0], parts=mode_[1])
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / KB
+
+        ms = rounds(mode, 100)
         log = dq.LaunchLog(KB * (6 * N + 12))
         log.c.count = 0
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for i in range(KB):
-            ar.plan(grads, round=100 + i, log=log)
-            ar.exchange(grads, outs, round=100 + i, log=log, fused=fused)
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / KB
+        ms_steps = rounds((False, None), 200, log)
         msg = stream_message_bytes(dq, ar.info, N) / J
-        kt = kernel_table(log, KB, ms, msg, N, butterfly)
+        kt = kernel_table(log, KB, ms_steps, msg, N, butterfly)
         out[str(B)] = {"ms_per_step": ms, "ms_per_gb": ms / (J * SG * 2 / 1e9),
                        "wire_bytes_per_coord": msg / SG, "vnmse": study.vnmse(outs[0], s_exact),
                        "allocation": {"T": ar.info.T, "n2": ar.info.n2, "n4": ar.info.n4, "n8": ar.info.n8},
@@ -537,7 +556,7 @@ def budget_sweep(w, grads, outs, dev, N, J, butterfly, peak, s_exact, fused):
     return out
 
 
-def e2e_timing(args, w, ar, grads, outs, fused, dev, world):
+def e2e_timing(args, w, ar, grads, outs, mode, dev, world):
     """End to end: the gradients start in pinned host memory and rank 0's fp32
     result ends there; every copy is inside the timed region.  Round i+1's
     upload (copy stream) runs while round i computes, into the other of two
@@ -573,7 +592,7 @@ def e2e_timing(args, w, ar, grads, outs, fused, dev, world):
         b = i & 1
         ar.plan(gbuf[b], round=i, ready=ev_in[b])
         main.wait_event(ev_out)
-        ar.exchange(gbuf[b], outs, round=i, fused=fused)
+        ar.exchange(gbuf[b], outs, round=i, fused=mode[0], parts=mode[1])
         ev_free[b].record(main)
         ev_dec.record(main)
         cout.wait_event(ev_dec)

@@ -272,7 +272,9 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads_host, int64_t n
 enum { DQ_LAUNCH_COMPRESS = 0, DQ_LAUNCH_DAR = 1, DQ_LAUNCH_DECODE = 2, DQ_LAUNCH_STATS = 3,
        DQ_LAUNCH_ALLOCATE_REORDER = 4, /* statistics reduce, allocation and reorder, one bracket */
        DQ_LAUNCH_MX_HOP = 5, DQ_LAUNCH_MX_DECODE = 6, /* MXFP8 baseline; sgs = coordinates / 256 */
-       DQ_LAUNCH_FUSED_RING = 7 /* dq_exchange_fused: all hops and the decode; sgs = J * (N + 1) */ };
+       DQ_LAUNCH_FUSED_RING = 7, /* dq_exchange_fused: all hops and the decode; sgs = J * (N + 1) */
+       DQ_LAUNCH_PIPELINED = 8   /* one launch of dq_exchange_pipelined; sgs = super-groups its hop
+                                    units process plus super-groups it decodes (each once) */ };
 struct dq_launch_log {
     void   **events;
     int32_t *kinds;
@@ -333,6 +335,39 @@ dq_status dq_exchange_fused(const dq_config *cfg, const void *const *grads_host,
                             size_t ws_bytes, void *const *outs_host, int32_t out_is_bf16,
                             int32_t *status_dev, const uint8_t **final_msgs_host, dq_launch_log *log,
                             void *stream);
+
+/* ---- the ring exchange, pipelined over parts -------------------------------
+ * Device bytes dq_exchange_pipelined needs: N*N chunk messages and 2 KB of
+ * unit counters (ring; 1 <= N <= 64), 0 otherwise. */
+size_t dq_exchange_pipelined_workspace_bytes(const dq_config *cfg, int64_t n_sg, const dq_plan_info *info);
+
+/* The ring exchange of dq_exchange (same results, bit for bit: final
+ * messages and outputs) with the reduce-scatter pipelined over parts of the
+ * super-groups, the way a ring all-reduce is pipelined over slices of its
+ * chunks [S "Evaluation": ring all-reduce; S "Key idea and contribution":
+ * hop-by-hop fused decompress-accumulate-recompress, then restore order and
+ * add the mean].  The work units of one step (all chunks, 32 reordered
+ * super-groups each, in chunk order) are cut into n_parts parts of
+ * consecutive units; launch t (t = 0 .. N + n_parts - 1) runs step t - p of
+ * every part p with 0 <= t - p < N and the final decode of part t - N.  So
+ * the decode of early parts (bound by HBM writes: N outputs of 4 bytes per
+ * coordinate) runs in the same launches as the hops of later parts (bound by
+ * instruction issue), on every SM at once.
+ *   Ring only, 1 <= N <= 64; arguments as for dq_exchange.
+ *   n_parts: >= 1; cut to at most 256 and to the work units of one step.
+ *   n_parts = 1 is N + 1 launches with the per-step work of dq_exchange.
+ *   ws: dq_exchange_pipelined_workspace_bytes bytes (device, 16-byte
+ *   aligned): rank r's message of step s in its own buffer, so a launch never
+ *   overwrites bytes that another part has still to read, then one unit
+ *   counter per launch (zeroed by the call; one extra small launch).
+ *   final_msgs_host: as for dq_exchange (owner c's message of step N-1).
+ *   Errors: DQ_ERR_INVALID_ARG (bad config, N > 64, n_parts < 1, null
+ *   pointer, small ws), DQ_ERR_ALIGNMENT, DQ_ERR_CUDA (a launch failed).  No
+ *   sync. */
+dq_status dq_exchange_pipelined(const dq_config *cfg, const void *const *grads_host, int64_t n_sg,
+                                const float *mu, const int32_t *perm, const dq_plan_info *info, void *ws,
+                                size_t ws_bytes, void *const *outs_host, int32_t out_is_bf16, int32_t n_parts,
+                                const uint8_t **final_msgs_host, dq_launch_log *log, void *stream);
 
 /* Reads a device status word into host memory [boundary of the hot path:
  * device-side errors of an asynchronous call are reported through a status

@@ -27,6 +27,28 @@ def use_fused(n_ranks: int, butterfly: bool, n_sg: int) -> bool:
     return (not butterfly) and n_ranks <= dq.MAX_FUSED_RANKS and n_sg <= FUSED_MAX_SG
 
 
+def pipeline_parts(n_ranks: int, n_sg: int) -> int:
+    """Parts of the pipelined ring exchange: 2N, as long as each part keeps
+    at least 2048 work units (32 super-groups each) per step.  Measured on a
+    GB300 (exchange alone): Gemma-1B ring of 16, 26.2 ms per step-wise
+    exchange against 22.6, 22.5 and 22.6 ms at 32, 48 and 64 parts;
+    BERT-large ring of 8, 4.47 ms against 4.13 and 4.12 ms at 8 and 16."""
+    units = -(-n_sg // dq.UNIT)
+    return max(1, min(2 * n_ranks, units // 2048, dq.MAX_WAVE_PARTS))
+
+
+def exchange_mode(n_ranks: int, butterfly: bool, n_sg: int):
+    """(fused, parts) of the ring exchange that is fastest at this size: one
+    cooperative launch up to FUSED_MAX_SG super-groups per worker, the
+    pipelined exchange above (rings of up to 64 ranks); the butterfly runs
+    step by step: (False, None)."""
+    if butterfly or n_ranks > dq.MAX_FUSED_RANKS:
+        return False, None
+    if n_sg <= FUSED_MAX_SG:
+        return True, None
+    return False, pipeline_parts(n_ranks, n_sg)
+
+
 class DynamiQAllReduce:
     def __init__(self, n_ranks: int, n_sg: int, *, budget: float = 5.0, eps: float = 1.0,
                  correlated: bool = True, butterfly: bool = False, seed: int = 0,
@@ -71,16 +93,28 @@ class DynamiQAllReduce:
         if self.ws.numel() < nbytes:
             self.ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
 
-    def exchange(self, grads, outs, round: int = 0, stream=None, log=None, fused="auto"):
+    def exchange(self, grads, outs, round: int = 0, stream=None, log=None, fused="auto", parts=None):
         """``fused``: True runs the ring exchange as one cooperative launch
-        (ring, at most 64 ranks), "auto" does so where that is the faster
-        path (``use_fused``); its device status is in ``self.status`` (check
-        with ``check_status`` after synchronising)."""
+        (ring, at most 64 ranks); its device status is in ``self.status``
+        (check with ``check_status`` after synchronising).  ``parts``: run
+        the ring exchange pipelined over that many parts of the super-groups
+        (``dq_exchange_pipelined``) instead.  ``fused="auto"`` with no
+        ``parts`` picks the faster path for the size (``exchange_mode``)."""
         cfg = self.config(round)
         n_sg = getattr(self, "cur_sg", self.n_sg)
-        if fused == "auto":
-            fused = use_fused(self.n_ranks, self.butterfly, n_sg)
         bf16 = self.out_dtype == torch.bfloat16
+        if fused == "auto" and parts is None:
+            fused, parts = exchange_mode(self.n_ranks, self.butterfly, n_sg)
+        if parts is not None:
+            if self.butterfly:
+                raise ValueError("the pipelined exchange is the ring's")
+            need = dq.dq_exchange_pipelined_workspace_bytes(cfg, n_sg, self.info)
+            if need == 0:
+                raise dq.DQError(dq.DQ_ERR_INVALID_ARG, "dq_exchange_pipelined_workspace_bytes")
+            self.reserve(need)
+            self.final = dq.dq_exchange_pipelined(cfg, grads, n_sg, self.mu, self.perm, self.info, self.ws,
+                                                  self.ws.numel(), outs, parts, bf16, log, stream)
+            return outs
         if fused:
             if self.butterfly:
                 raise ValueError("the fused exchange is the ring's")
@@ -109,13 +143,13 @@ class DynamiQAllReduce:
         return [torch.empty(self.n_sg * SG, dtype=self.out_dtype, device=self.device)
                 for _ in range(self.n_ranks)]
 
-    def __call__(self, grads, round: int = 0, outs=None, stream=None, fused="auto"):
+    def __call__(self, grads, round: int = 0, outs=None, stream=None, fused="auto", parts=None):
         if len(grads) != self.n_ranks:
             raise ValueError("one gradient per rank")
         if outs is None:
             outs = self.new_outputs()
         self.plan(grads, round, stream)
-        return self.exchange(grads, outs, round, stream, fused=fused)
+        return self.exchange(grads, outs, round, stream, fused=fused, parts=parts)
 
     def chunk_lo(self):
         i = self.info

@@ -623,16 +623,16 @@ __global__ void plan_readback_kernel(const int64_t *counts, const float *T, cons
     }
 }
 
-// Zeroes up to two 32-bit words in stream order.  A kernel, not
+// Zeroes a few 32-bit words in stream order.  A kernel, not
 // cudaMemsetAsync: a small memset may be carried out by a copy engine and
 // then wait behind large host<->device copies queued by other streams.
 __global__ void zero_words_kernel(uint32_t *a, int na, uint32_t *b)
 {
-    if (threadIdx.x < na) a[threadIdx.x] = 0u;
+    for (int i = threadIdx.x; i < na; i += blockDim.x) a[i] = 0u;
     if (threadIdx.x == 0 && b) *b = 0u;
 }
 
-// a[0 .. na) and, if b is not null, b[0] (na <= 32)
+// a[0 .. na) and, if b is not null, b[0]
 cudaError_t zero_words(void *a, int na, void *b, cudaStream_t st)
 {
     zero_words_kernel<<<1, 32, 0, st>>>(static_cast<uint32_t *>(a), na, static_cast<uint32_t *>(b));
@@ -967,6 +967,115 @@ dq_status dq_exchange_fused(const dq_config *cfg, const void *const *grads, int6
     return DQ_OK;
 }
 
+size_t dq_exchange_pipelined_workspace_bytes(const dq_config *cfg, int64_t n_sg, const dq_plan_info *info)
+{
+    if (!fused_ok(cfg) || !info || n_sg < 1) return 0;
+    ExchangeLayout X;
+    if (!exchange_layout(cfg, 0, info, X)) return 0;
+    return (size_t)cfg->n_ranks * (size_t)cfg->n_ranks * X.msg_stride + kWaveCounterBytes;
+}
+
+dq_status dq_exchange_pipelined(const dq_config *cfg, const void *const *grads, int64_t n_sg, const float *mu,
+                                const int32_t *perm, const dq_plan_info *info, void *ws, size_t ws_bytes,
+                                void *const *outs, int32_t out_is_bf16, int32_t n_parts,
+                                const uint8_t **final_msgs, dq_launch_log *log, void *stream)
+{
+    if (!fused_ok(cfg) || !grads || !mu || !perm || !info || !ws || !outs || n_sg < 1 || n_sg >= kMaxSG ||
+        n_parts < 1)
+        return DQ_ERR_INVALID_ARG;
+    if (info->n2 < 0 || info->n4 < 0 || info->n8 < 0 || info->n2 + info->n4 + info->n8 != n_sg)
+        return DQ_ERR_INVALID_ARG;
+    const int32_t N = cfg->n_ranks;
+    ExchangeLayout X;
+    if (!exchange_layout(cfg, 0, info, X)) return DQ_ERR_INVALID_ARG;
+    const size_t msgs_bytes = (size_t)N * (size_t)N * X.msg_stride;
+    if (ws_bytes < msgs_bytes + kWaveCounterBytes) return DQ_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return DQ_ERR_ALIGNMENT;
+    for (int32_t r = 0; r < N; ++r) {
+        if (!grads[r] || !outs[r]) return DQ_ERR_INVALID_ARG;
+        if (!aligned16(grads[r]) || !aligned16(outs[r])) return DQ_ERR_ALIGNMENT;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t end2 = info->n2, end4 = info->n2 + info->n4;
+    const bool sf = cfg->scale_fp32 != 0;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+
+    std::unique_ptr<WaveRingParams> P(new WaveRingParams());
+    memset(P.get(), 0, sizeof(WaveRingParams));
+    if (!build_tables(cfg->eps, &P->tab)) return DQ_ERR_INVALID_ARG;
+    int64_t units = 0;
+    for (int32_t c = 0; c < N; ++c) {
+        const int64_t a = X.lo[c], b = X.lo[c + 1];
+        P->chunk[c] = msg_view(nullptr, a, b, end2, end4, sf);
+        P->lo[c] = a;
+        HopTask t;   // segment and unit bookkeeping of chunk c
+        memset(&t, 0, sizeof(t));
+        units += set_units(t, a, b, end2, end4, units);
+        for (int s = 0; s < 3; ++s) {
+            P->seg_lo[c][s] = t.seg_lo[s];
+            P->seg_hi[c][s] = t.seg_hi[s];
+            P->unit_begin[c][s] = t.unit_begin[s];
+        }
+        P->unit_begin[c][3] = t.unit_begin[3];
+        P->grads[c] = grads[c];
+        P->outs[c] = outs[c];
+    }
+    P->lo[N] = X.lo[N];
+    P->msgs = w;
+    P->msg_stride = (int64_t)X.msg_stride;
+    P->units = units;
+    const int32_t parts = (int32_t)std::min<int64_t>(std::min<int64_t>(n_parts, kMaxWaveParts), units);
+    P->n_parts = parts;
+    P->n_ranks = N;
+    P->correlated = cfg->correlated ? 1 : 0;
+    P->mu = mu;
+    P->perm = perm;
+    P->ph = philox_keys(cfg->seed, cfg->round);
+    P->out_is_bf16 = out_is_bf16 ? 1 : 0;
+    P->scale_fp32 = cfg->scale_fp32;
+
+    // first unit of part p, and the super-groups in units [ua, ub)
+    auto part_lo = [&](int64_t p) { return units * p / parts; };
+    auto sgs_in = [&](int64_t ua, int64_t ub) {
+        int64_t n = 0;
+        for (int32_t c = 0; c < N; ++c)
+            for (int s = 0; s < 3; ++s) {
+                const int64_t b0 = P->unit_begin[c][s], b1 = P->unit_begin[c][s + 1];
+                const int64_t x = std::max(ua, b0), y = std::min(ub, b1);
+                if (y > x)
+                    n += std::min(P->seg_hi[c][s], P->seg_lo[c][s] + kUnit * (y - b0)) -
+                         (P->seg_lo[c][s] + kUnit * (x - b0));
+            }
+        return n;
+    };
+    // one unit counter per launch, all zeroed here
+    unsigned int *next = reinterpret_cast<unsigned int *>(w + msgs_bytes);
+    if (zero_words(next, N + parts, nullptr, st) != cudaSuccess) return DQ_ERR_CUDA;
+    for (int32_t t = 0; t < N + parts; ++t) {
+        const int32_t plo = std::max(0, t - N + 1), phi = std::min(t, parts - 1), pd = t - N;
+        P->launch = t;
+        P->next = next + t;
+        P->h_lo = P->h_hi = 0;
+        if (plo <= phi) {
+            P->h_lo = part_lo(plo);
+            P->h_hi = part_lo(phi + 1);
+        }
+        P->d_lo = P->d_hi = 0;
+        if (pd >= 0 && pd < parts) {
+            P->d_lo = part_lo(pd);
+            P->d_hi = part_lo(pd + 1);
+        }
+        const LogSlot slot =
+            log_begin(log, DQ_LAUNCH_PIPELINED, sgs_in(P->h_lo, P->h_hi) + sgs_in(P->d_lo, P->d_hi), st);
+        const cudaError_t e = launch_wave_ring(*P, st);
+        log_end(slot, st);
+        if (e != cudaSuccess) return DQ_ERR_CUDA;
+    }
+    if (final_msgs)
+        for (int32_t c = 0; c < N; ++c) final_msgs[c] = w + ((size_t)c * N + (size_t)(N - 1)) * X.msg_stride;
+    return DQ_OK;
+}
+
 dq_status dq_get_device_status(const int32_t *status_dev, int32_t *status_host, void *stream)
 {
     if (!status_dev || !status_host) return DQ_ERR_INVALID_ARG;
@@ -1007,3 +1116,4 @@ dq_status dq_barrier_selftest(int32_t n_blocks, int32_t missing, int64_t timeout
 static_assert(sizeof(dq::HopParams) <= 32764, "HopParams exceeds the kernel parameter limit");
 static_assert(sizeof(dq::DecodeParams) <= 32764, "DecodeParams exceeds the kernel parameter limit");
 static_assert(sizeof(dq::FusedRingParams) <= 32764, "FusedRingParams exceeds the kernel parameter limit");
+static_assert(sizeof(dq::WaveRingParams) <= 32764, "WaveRingParams exceeds the kernel parameter limit");

@@ -187,6 +187,44 @@ struct FusedRingParams {
     long long timeout_cycles;                  // bound of every barrier wait (SM clock cycles)
 };
 
+// One launch of the pipelined ring exchange.  The work units of one step
+// (numbered across the chunks as in FusedRingParams) are cut into n_parts
+// parts of consecutive units, part p = [units*p/n_parts, units*(p+1)/n_parts);
+// launch t runs every part p at step t - p (0 <= t - p < N) and decodes part
+// t - N, so N + n_parts launches carry a round.  Warps take the launch's
+// units in turn from a counter, one unit ahead of their work.  A part's units go through
+// the steps in order, one launch apart; rank r's message of step s has its
+// own buffer (r*N + s), so no launch overwrites bytes another part has still
+// to read.
+constexpr int kMaxWaveParts = 256;
+constexpr int kWaveCounterBytes = 2048;   // one unit counter per launch: (kMaxFusedRanks + kMaxWaveParts) x 4 bytes
+static_assert((kMaxFusedRanks + kMaxWaveParts) * 4 <= kWaveCounterBytes, "wave counters");
+
+struct WaveRingParams {
+    Tables tab;
+    MsgView chunk[kMaxFusedRanks];             // message layout of chunk c (base unset)
+    int64_t lo[kMaxFusedRanks + 1];
+    int64_t seg_lo[kMaxFusedRanks][3], seg_hi[kMaxFusedRanks][3];
+    int64_t unit_begin[kMaxFusedRanks][4];
+    const void *grads[kMaxFusedRanks];
+    void *outs[kMaxFusedRanks];
+    uint8_t *msgs;                             // N*N message buffers, msg_stride apart
+    int64_t msg_stride;
+    int64_t units;                             // work units of one step (all chunks)
+    int64_t h_lo, h_hi;                        // this launch's hop units [h_lo, h_hi)
+    int64_t d_lo, d_hi;                        // this launch's decode units [d_lo, d_hi)
+    unsigned int *next;                        // this launch's unit counter, zero at launch
+    int32_t n_parts;
+    int32_t launch;                            // t
+    int32_t n_ranks;
+    int32_t correlated;
+    const float *mu;
+    const int32_t *perm;
+    PhiloxKeys ph;
+    int32_t out_is_bf16;
+    int32_t scale_fp32;
+};
+
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon et al., SC 2011): ten rounds; each multiplies words
 // 0 and 2 by the Philox constants (full 64-bit products), xors the high

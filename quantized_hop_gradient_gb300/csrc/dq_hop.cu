@@ -869,6 +869,226 @@ __global__ void __launch_bounds__(kWarps * 32, 1) fused_ring_kernel(const __grid
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // the decode's copies
 }
 
+// Codes of one lane read from global memory (a message written by an
+// earlier launch).
+template <int BITS>
+__device__ __forceinline__ LaneCodes<BITS> ldg_codes(const uint8_t *p)
+{
+    LaneCodes<BITS> c;
+    if (BITS == 2) {
+        c.w[0] = __ldcg(reinterpret_cast<const unsigned int *>(p));
+    } else if (BITS == 4) {
+        const uint2 v = __ldcg(reinterpret_cast<const uint2 *>(p));
+        c.w[0] = v.x; c.w[1] = v.y;
+    } else {
+        const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(p));
+        c.w[0] = v.x; c.w[1] = v.y; c.w[2] = v.z; c.w[3] = v.w;
+    }
+    return c;
+}
+
+constexpr int kRowBytes = 1024;   // row buffer of the in-launch decode, per half-warp
+constexpr int kDecodeSub = 4;     // in-launch decode pieces per work unit (8 super-groups each)
+
+// The final decode of up to kUnit super-groups of one chunk into all N
+// outputs: out = fl(sigma * q_code + fl(mu * N)).  The hop's mapping: lanes
+// 0-15 decode one super-group, lanes 16-31 the next, lane l of a half the
+// coordinates 16l .. 16l+15.  Each half writes its decoded row to its row
+// buffer (`rows`, 1 KB per half) and the warp hands the 2N row copies of the
+// pair to the bulk-copy engine, one (row, output) per lane; before a row
+// buffer is rewritten, each lane waits until its earlier copies have read
+// it.  The caller waits for all copies before the block exits.  The codes
+// and scales of the next four pairs load while a pair is decoded.  Meant to
+// run beside the hop units of a launch, whose shared-memory tables it uses.
+template <int BITS, bool SF32, typename PP>
+__device__ __forceinline__ void decode_unit_rows(const PP &P, const MsgView &m, int64_t lo, int64_t j0, int cnt,
+                                                 int lane, uint8_t *rows)
+{
+    constexpr int CB = 32 * BITS;
+    constexpr int UB = SF32 ? 64 : 16;
+    const int half = lane >> 4, hl = lane & 15;
+    const int N = P.n_ranks;
+    int32_t old_i = 0;
+    float back_i = 0.0f;
+    uint32_t ein_i = 0;
+    if (lane < cnt) {
+        old_i = __ldg(P.perm + j0 + lane);
+        back_i = __fmul_rn(__ldg(P.mu + old_i), (float)N);
+        if (!SF32) ein_i = __ldcg(m.base + (j0 + lane - lo));
+    }
+    const int64_t sl0 = j0 - lo;
+    const uint8_t *cp = m.base + code_block_off<BITS>(m, sl0) + hl * 2 * BITS;
+    const uint8_t *up = m.base + m.off_u + sl0 * UB + hl * (SF32 ? 4 : 1);
+    uint4 *row = reinterpret_cast<uint4 *>(rows + half * kRowBytes);
+    const uint32_t rows_s = smem_addr(rows);
+    const int row_bytes = P.out_is_bf16 ? 512 : 1024;
+    const int npairs = (cnt + 1) >> 1;
+    // codes and scale of pairs p .. p+3 in flight, rotated through q0 .. q3
+    LaneCodes<BITS> q0, q1, q2, q3;
+    uint32_t u0 = 0, u1 = 0, u2 = 0, u3 = 0;
+#pragma unroll
+    for (int w = 0; w < BITS / 2; ++w) q0.w[w] = q1.w[w] = q2.w[w] = q3.w[w] = 0u;
+    auto load = [&](int pp, LaneCodes<BITS> &qc, uint32_t &uu) {
+        const int s = 2 * pp + half;
+        if (pp < npairs && s < cnt) {
+            qc = ldg_codes<BITS>(cp + (int64_t)s * CB);
+            uu = SF32 ? __ldcg(reinterpret_cast<const unsigned int *>(up + (int64_t)s * UB))
+                      : (uint32_t)__ldcg(up + (int64_t)s * UB);
+        }
+    };
+    load(0, q0, u0);
+    load(1, q1, u1);
+    load(2, q2, u2);
+    load(3, q3, u3);
+    for (int p = 0; p < npairs; ++p) {
+        const LaneCodes<BITS> c = q0;
+        const uint32_t uc = u0;
+        q0 = q1; u0 = u1;
+        q1 = q2; u1 = u2;
+        q2 = q3; u2 = u3;
+        load(p + 4, q3, u3);
+        const int s = 2 * p + half;
+        const float back = __shfl_sync(kFull, back_i, s & 31);
+        const uint32_t E = __shfl_sync(kFull, ein_i, s & 31);
+        const float sigma = SF32 ? __uint_as_float(uc) : __fmul_rn((float)uc, __uint_as_float(E << 23));
+        float2 x[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = make_float2(back, back);
+        decode_add<BITS, true>(x, sigma, c);
+        // the row buffers are free once this lane's earlier copies have read them
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncwarp();
+        if (P.out_is_bf16) {   // lane l: bytes 32l .. 32l+31 of the 512-byte row
+            uint32_t h[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                h[k] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[k].x)) |
+                       ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[k].y)) << 16);
+            row[2 * hl] = make_uint4(h[0], h[1], h[2], h[3]);
+            row[2 * hl + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+        } else {               // lane l: bytes 64l .. 64l+63 of the 1 KB row
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                row[4 * hl + i] = make_uint4(__float_as_uint(x[2 * i].x), __float_as_uint(x[2 * i].y),
+                                             __float_as_uint(x[2 * i + 1].x), __float_as_uint(x[2 * i + 1].y));
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        // copies of the pair: row a (0: lanes 0-15's super-group) to output r
+        const int n_rows = 2 * p + 1 < cnt ? 2 : 1;
+        const int pairs = n_rows * N;
+        for (int pbase = 0; pbase < pairs; pbase += 32) {
+            const int pi = pbase + lane;
+            const int a = pi < pairs ? pi / N : 0;
+            const int32_t old = __shfl_sync(kFull, old_i, (2 * p + a) & 31);
+            if (pi < pairs) {
+                char *dst = static_cast<char *>(P.outs[pi - a * N]) + (int64_t)old * row_bytes;
+                bulk_store(dst, rows_s + (uint32_t)(a * kRowBytes), (uint32_t)row_bytes);
+            }
+        }
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+}
+
+// One launch of the pipelined ring exchange (WaveRingParams): hop units of
+// several parts, each at its own step, and the decode units of one part,
+// spread evenly through the launch's unit list so that every SM keeps
+// decoding (bound by HBM writes) beside the hops (bound by instruction
+// issue).  Step s of chunk c is handled by rank r = (c + 1 + s) mod N, which
+// reads rank r-1's message of step s-1 and writes its own of step s; step 0
+// quantizes the local gradient.  The decode reads owner c's message of step
+// N-1.  Results are those of the per-step exchange, bit for bit: every
+// super-group sees the same operations, only their order in time changes.
+template <bool ONE_LEVEL, bool SF32>
+__global__ void __launch_bounds__(kWarps * 32, 1) wave_ring_kernel(const __grid_constant__ WaveRingParams P)
+{
+    // Launched with programmatic stream serialization: the next launch may
+    // start its blocks (and their table setup) on the SMs this one frees, and
+    // this one's table setup overlaps the previous launch's last units.
+    // griddepcontrol.wait returns once the previous launch has completed and
+    // its writes are visible; nothing before it touches global memory other
+    // than the launch parameters.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    block_copy(&g_tab, &P.tab);
+    __syncthreads();
+    expand_bk4();
+    expand_tables(true);
+    __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    uint8_t *dyn = g_dyn + tab_bytes(false);
+    constexpr int STAGE = stage_bytes<false, SF32>();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t *stg = dyn + warp * kStages * STAGE;
+    uint8_t *rows = dyn + kWarps * kStages * STAGE + warp * 2 * kRowBytes;
+    const int N = P.n_ranks;
+    // each decode unit is cut into kDecodeSub pieces, so that the launches
+    // whose work is mostly decode end evenly
+    const int64_t H = P.h_hi - P.h_lo, D = (P.d_hi - P.d_lo) * kDecodeSub, T = H + D;
+    // units are taken in turn from the launch's counter, the next one claimed
+    // before the current one runs (a static stride would hand every decode
+    // unit to the same warps whenever the stride and the decode spacing
+    // share a factor)
+    auto claim = [&]() -> int64_t {
+        unsigned v = 0u;
+        if (lane == 0) v = atomicAdd(P.next, 1u);
+        return (int64_t)__shfl_sync(kFull, v, 0);
+    };
+    int64_t k_next = claim();
+    while (k_next < T) {
+        const int64_t k = k_next;
+        k_next = claim();
+        // position k is a decode piece when floor(k D / T) steps up at k + 1
+        const int64_t f0 = k * D / T, f1 = (k + 1) * D / T;
+        const bool dec = f1 > f0;
+        const int64_t u = dec ? P.d_lo + f0 / kDecodeSub : P.h_lo + (k - f0);
+        int c = 0;
+        while (c + 1 < N && u >= P.unit_begin[c + 1][0]) ++c;
+        int seg = 0;
+        while (seg < 2 && u >= P.unit_begin[c][seg + 1]) ++seg;
+        const int64_t j0 = P.seg_lo[c][seg] + (u - P.unit_begin[c][seg]) * kUnit +
+                           (dec ? (f0 % kDecodeSub) * (kUnit / kDecodeSub) : 0);
+        const int64_t rem = P.seg_hi[c][seg] - j0;
+        const int64_t len = dec ? kUnit / kDecodeSub : kUnit;
+        if (rem <= 0) continue;   // a piece past the end of a short unit
+        const int cnt = (int)(rem < len ? rem : len);
+        if (dec) {
+            MsgView m = P.chunk[c];
+            m.base = P.msgs + ((int64_t)c * N + (N - 1)) * P.msg_stride;
+            if (seg == 0) decode_unit_rows<2, SF32>(P, m, P.lo[c], j0, cnt, lane, rows);
+            else if (seg == 1) decode_unit_rows<4, SF32>(P, m, P.lo[c], j0, cnt, lane, rows);
+            else decode_unit_rows<8, SF32>(P, m, P.lo[c], j0, cnt, lane, rows);
+            continue;
+        }
+        // the part of unit u (largest p with units*p/n_parts <= u) and its step
+        const int64_t part = ((u + 1) * P.n_parts - 1) / P.units;
+        const int step = P.launch - (int)part;
+        const int r = (c + 1 + step) % N, src = (r - 1 + N) % N;
+        HopTask t;
+        t.in = P.chunk[c];
+        t.in.base = step > 0 ? P.msgs + ((int64_t)src * N + (step - 1)) * P.msg_stride : nullptr;
+        t.out = P.chunk[c];
+        t.out.base = P.msgs + ((int64_t)r * N + step) * P.msg_stride;
+        t.addend = P.grads[r];
+        t.keep_out = nullptr;
+        t.in_lo = P.lo[c];
+        t.send_lo = P.lo[c];
+        t.send_hi = P.lo[c + 1];
+        t.keep_lo = t.keep_hi = P.lo[c + 1];
+        t.stage_word = (uint32_t)step | (P.correlated ? 0xFFFF0000u : ((uint32_t)r << 16));
+        t.corr2 = 0u;   // one quantizer per ring stage: stratum offset 0
+        if (step == 0) {
+            if (seg == 0) hop_unit<2, false, false, ONE_LEVEL, SF32, false>(P, t, stg, j0, cnt, lane);
+            else if (seg == 1) hop_unit<4, false, false, ONE_LEVEL, SF32, false>(P, t, stg, j0, cnt, lane);
+            else hop_unit<8, false, false, ONE_LEVEL, SF32, false>(P, t, stg, j0, cnt, lane);
+        } else {
+            if (seg == 0) hop_unit<2, true, false, ONE_LEVEL, SF32, false>(P, t, stg, j0, cnt, lane);
+            else if (seg == 1) hop_unit<4, true, false, ONE_LEVEL, SF32, false>(P, t, stg, j0, cnt, lane);
+            else hop_unit<8, true, false, ONE_LEVEL, SF32, false>(P, t, stg, j0, cnt, lane);
+        }
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // the decode's copies
+}
+
 // Opts a kernel in to `dyn` bytes of dynamic shared memory (needed once its
 // static plus dynamic shared memory passes 48 KB), once per device; `done`
 // is the caller's per-kernel record.
@@ -999,6 +1219,44 @@ cudaError_t launch_fused_ring(const FusedRingParams &P, cudaStream_t st)
     const bool one = P.tab.one_level != 0;
     if (P.scale_fp32) return one ? launch_fused_t<true, true>(P, st) : launch_fused_t<false, true>(P, st);
     return one ? launch_fused_t<true, false>(P, st) : launch_fused_t<false, false>(P, st);
+}
+
+namespace {
+
+template <bool ONE_LEVEL, bool SF32>
+cudaError_t launch_wave_t(const WaveRingParams &P, int64_t units, cudaStream_t st)
+{
+    const size_t dyn = (size_t)tab_bytes(false) + (size_t)kWarps * kStages * stage_bytes<false, SF32>() +
+                       (size_t)kWarps * 2 * kRowBytes;
+    auto k = wave_ring_kernel<ONE_LEVEL, SF32>;
+    static bool opted[128] = {false};   // one record per instantiation of this launcher
+    const cudaError_t e = allow_dyn_smem(k, dyn, opted);
+    if (e != cudaSuccess) return e;
+    const int wpb = hop_block_warps(units);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid_for(k, wpb, dyn, units));
+    cfg.blockDim = dim3((unsigned)(wpb * 32));
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t el = cudaLaunchKernelEx(&cfg, k, P);
+    note_launches(1);
+    return el != cudaSuccess ? el : cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_wave_ring(const WaveRingParams &P, cudaStream_t st)
+{
+    const int64_t units = (P.h_hi - P.h_lo) + (P.d_hi - P.d_lo);
+    if (units <= 0) return cudaSuccess;
+    const bool one = P.tab.one_level != 0;
+    if (P.scale_fp32) return one ? launch_wave_t<true, true>(P, units, st) : launch_wave_t<false, true>(P, units, st);
+    return one ? launch_wave_t<true, false>(P, units, st) : launch_wave_t<false, false>(P, units, st);
 }
 
 cudaError_t launch_barrier_selftest(int32_t n_blocks, int32_t missing, long long timeout_cycles, unsigned *counter,

@@ -30,6 +30,8 @@ cudaError_t launch_decode(const DecodeParams &P, cudaStream_t st);
 cudaError_t launch_fused_ring(const FusedRingParams &P, cudaStream_t st);
 cudaError_t launch_barrier_selftest(int32_t n_blocks, int32_t missing, long long timeout_cycles,
                                     unsigned int *counter, int32_t *status, cudaStream_t st);
+// One launch of the pipelined ring exchange (ordinary launch).
+cudaError_t launch_wave_ring(const WaveRingParams &P, cudaStream_t st);
 
 // Allocation (radix select of T) and reordering; ws is device scratch.
 constexpr int kReorderTile = 2048;   // super-groups per reorder tile (4 int64 of scratch each)

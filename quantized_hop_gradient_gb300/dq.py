@@ -59,9 +59,11 @@ class dq_launch_log(C.Structure):
 
 
 DQ_LAUNCH_COMPRESS, DQ_LAUNCH_DAR, DQ_LAUNCH_DECODE, DQ_LAUNCH_STATS, DQ_LAUNCH_ALLOCATE_REORDER = 0, 1, 2, 3, 4
-DQ_LAUNCH_MX_HOP, DQ_LAUNCH_MX_DECODE, DQ_LAUNCH_FUSED_RING = 5, 6, 7
+DQ_LAUNCH_MX_HOP, DQ_LAUNCH_MX_DECODE, DQ_LAUNCH_FUSED_RING, DQ_LAUNCH_PIPELINED = 5, 6, 7, 8
 DQ_DEVICE_OK, DQ_DEVICE_BARRIER_TIMEOUT = 0, 1
 MAX_FUSED_RANKS = 64
+MAX_WAVE_PARTS = 256   # dq_exchange_pipelined cuts n_parts to this
+UNIT = 32              # super-groups per work unit of the kernels
 
 
 class dq_plan_info(C.Structure):
@@ -104,6 +106,11 @@ _SIGS = {
     "dq_exchange_fused": ([C.POINTER(dq_config), C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
                            C.POINTER(dq_plan_info), C.c_void_p, C.c_size_t, C.c_void_p, C.c_int32, C.c_void_p,
                            C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+    "dq_exchange_pipelined_workspace_bytes": ([C.POINTER(dq_config), C.c_int64, C.POINTER(dq_plan_info)],
+                                               C.c_size_t),
+    "dq_exchange_pipelined": ([C.POINTER(dq_config), C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
+                               C.POINTER(dq_plan_info), C.c_void_p, C.c_size_t, C.c_void_p, C.c_int32, C.c_int32,
+                               C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "dq_barrier_selftest": ([C.c_int32, C.c_int32, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "dq_mx_message_bytes": ([C.c_int64], C.c_size_t),
     "dq_mx_quantize": ([C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p], C.c_int),
@@ -361,6 +368,27 @@ def dq_exchange_fused(cfg, grads, n_sg, mu, perm, info, ws, ws_bytes, outs, stat
                                    _ptr(status), C.cast(fin, C.c_void_p),
                                    C.byref(log.c) if log is not None else None, _stream(stream)),
            "dq_exchange_fused")
+    return [fin[i] for i in range(n)]
+
+
+def dq_exchange_pipelined_workspace_bytes(cfg, n_sg, info) -> int:
+    return lib().dq_exchange_pipelined_workspace_bytes(C.byref(cfg), n_sg, C.byref(info))
+
+
+def dq_exchange_pipelined(cfg, grads, n_sg, mu, perm, info, ws, ws_bytes, outs, n_parts, out_is_bf16=False,
+                          log: LaunchLog = None, stream=None):
+    """The ring exchange pipelined over ``n_parts`` parts of the
+    super-groups (N + n_parts launches).  Returns the N device addresses of
+    the final chunk messages."""
+    n = len(grads)
+    gp = (C.c_void_p * n)(*[_ptr(g) for g in grads])
+    op = (C.c_void_p * n)(*[_ptr(o) for o in outs])
+    fin = (C.c_void_p * n)()
+    _check(lib().dq_exchange_pipelined(C.byref(cfg), C.cast(gp, C.c_void_p), n_sg, _ptr(mu), _ptr(perm),
+                                       C.byref(info), _ptr(ws), ws_bytes, C.cast(op, C.c_void_p),
+                                       int(out_is_bf16), int(n_parts), C.cast(fin, C.c_void_p),
+                                       C.byref(log.c) if log is not None else None, _stream(stream)),
+           "dq_exchange_pipelined")
     return [fin[i] for i in range(n)]
 
 

@@ -32,3 +32,26 @@ def test_message_bytes_per_super_group_at_five_bits():
     n4, n8 = 3 * 1024, 1024
     per = oracle.message_bytes(0, n4, n8) / (n4 + n8) / 256
     assert abs(per - (5 + 17 * 8 / 256) / 8) < 1e-3
+
+
+def test_pipelined_launches_count_the_fused_round_bytes():
+    # the logged super-groups of a pipelined round add up to J (N + 1), and
+    # the bytes are the fused ring's for the same round
+    J, N, m = 1000, 16, 177.0
+    assert bench.launch_bytes(8, J * (N + 1), m, n_ranks=N) == bench.launch_bytes(7, J * (N + 1), m, n_ranks=N)
+    parts = [J * (N + 1) // 5] * 4
+    parts.append(J * (N + 1) - sum(parts))
+    total = sum(bench.launch_bytes(8, p, m, n_ranks=N) for p in parts)
+    assert abs(total - bench.launch_bytes(8, J * (N + 1), m, n_ranks=N)) < 1e-6 * total
+
+
+def test_exchange_mode_picks_by_size():
+    from quantized_hop_gradient_gb300.allreduce import FUSED_MAX_SG, exchange_mode, pipeline_parts
+    assert exchange_mode(8, True, 1 << 20) == (False, None)          # butterfly: step by step
+    assert exchange_mode(65, False, 1 << 20) == (False, None)        # beyond 64 ranks
+    assert exchange_mode(8, False, FUSED_MAX_SG) == (True, None)
+    assert exchange_mode(16, False, 3905805) == (False, 32)          # Gemma-1B ring of 16: 2N parts
+    assert exchange_mode(8, False, 1309148) == (False, 16)           # BERT-large ring of 8
+    assert pipeline_parts(8, FUSED_MAX_SG + 1) == 2                  # parts keep >= 2048 units
+    assert pipeline_parts(64, 1 << 26) == 128
+    assert pipeline_parts(4, 1) == 1
