@@ -52,6 +52,8 @@ def parse_args(argv=None):
                         "over parts of the super-groups (pipelined); auto: the faster path for the size "
                         "(allreduce.exchange_mode: fused up to 2^17 super-groups per worker, pipelined above, rings "
                         "of up to 64 ranks; the butterfly runs step by step)")
+    p.add_argument("--parts", type=int, default=0,
+                   help="parts of the pipelined exchange (0: allreduce.pipeline_parts)")
     p.add_argument("--lean", action="store_true",
                    help="the timed rounds only: no end-to-end, MXFP8, budget-sweep or accuracy legs and no extra "
                         "workloads (for profiler captures, whose launch lists stay short)")
@@ -415,6 +417,8 @@ def measure_round(args, w, dev, world, K, W, full: bool, local: int = 0):
     # (fused, parts) of the exchange
     mode = {"auto": exchange_mode(N, butterfly, J), "fused": (True, None), "multi": (False, None),
             "pipelined": (False, pipeline_parts(N, J))}[args.exchange]
+    if mode[1] and args.parts > 0:
+        mode = (False, args.parts)
     if mode != (False, None) and not ring64:
         raise SystemExit("the fused and pipelined exchanges cover rings of up to 64 ranks")
     STEPWISE = (False, None)
