@@ -182,6 +182,7 @@ KERNEL_SOURCES = {
     "decode_kernel": ["dq_common.cuh", "dq_hop.cu"],
     "fused_ring_kernel": ["dq_common.cuh", "dq_hop.cu"],
     "wave_ring_kernel": ["dq_common.cuh", "dq_hop.cu"],
+    "stream_ring_kernel": ["dq_common.cuh", "dq_hop.cu"],
     "stats_kernel": ["dq_common.cuh", "dq_codec.cu"],
     "mx_hop_kernel": ["dq_common.cuh", "dq_mx.cu"],
 }
@@ -248,7 +249,9 @@ def launch_bytes(kind: int, sgs: int, msg_per_sg: float, fp32_addend: bool = Fal
     and a decode that reads each message once and writes N outputs;
     pipelined ring exchange: the same bytes per round, each launch counted
     by its share of the round's super-groups (its logged hop and decode
-    super-groups add up to J (N + 1) per round)."""
+    super-groups add up to J (N + 1) per round); bucket stream: likewise per
+    bucket (a bucket's J super-groups are logged by each of the N + 1
+    launches it takes part in)."""
     if kind == 0:
         return sgs * (512 + send_frac * msg_per_sg + 8 + (1.0 - send_frac) * 1024)
     if kind == 1:
@@ -258,7 +261,7 @@ def launch_bytes(kind: int, sgs: int, msg_per_sg: float, fp32_addend: bool = Fal
         return sgs * 1024 + sgs / min(n_ranks, 16) * (msg_per_sg + 8)
     if kind == 3:
         return sgs * (512 + 8)
-    if kind in (7, 8):   # fused or pipelined ring: J (N + 1) super-groups per round
+    if kind in (7, 8, 9):   # fused, pipelined or bucket-stream ring: J (N + 1) super-groups per bucket
         J = sgs / (n_ranks + 1)
         return J * ((512 + msg_per_sg + 8) + (n_ranks - 1) * (2 * msg_per_sg + 512 + 8) +
                     (msg_per_sg + 8 + 1024 * n_ranks))
@@ -339,13 +342,15 @@ KERNEL_NAMES = {"compress": "hop_kernel<false,false> (compress)", "dar": "hop_ke
                 "dar_bf16_final": "hop_kernel<true,false> (DAR, bf16 addend)",
                 "decode": "decode_kernel", "stats": "stats_kernel", "fused_ring": "fused_ring_kernel",
                 "pipelined": "wave_ring_kernel (pipelined ring exchange: hop steps of later parts and the final "
-                             "decode of an earlier part in each launch)"}
+                             "decode of an earlier part in each launch)",
+                "stream": "stream_ring_kernel (bucket stream: ring steps of N buckets and the final decode of one "
+                          "bucket in each launch)"}
 # the key under which profiles/dram_traffic.txt lists a kernel role
 TRAFFIC_KEY = {"dar": "hop_kernel<true,false>", "dar_bf16_split": "hop_kernel<true,false>:split",
                "dar_bf16_final": "hop_kernel<true,false>:final", "dar_f32_split": "hop_kernel<true,true>:split",
                "dar_f32_final": "hop_kernel<true,true>:final", "compress": "hop_kernel<false,false>",
                "decode": "decode_kernel", "stats": "stats_kernel", "fused_ring": "fused_ring_kernel",
-               "pipelined": "wave_ring_kernel"}
+               "pipelined": "wave_ring_kernel", "stream": "stream_ring_kernel"}
 
 
 def kernel_table(log, steps: int, ms_step: float, msg_per_sg: float, N: int, butterfly: bool):
@@ -761,15 +766,19 @@ def compare_mxfp8(w, grads, outs, ar, dev, N, J, butterfly, peak, acc, s_exact):
 # --------------------------------------------------------------------------- streamed workloads
 def run_gpu_bucketed(args, rank, world, local, w, dev):
     """A streamed workload (DDP buckets): one step is a full pass over the
-    model's buckets, each bucket a DynamiQ round; bucket k+1's planning runs
-    on a second stream under bucket k's hops.  The gradient data cycle
-    through a pool of resident buckets drawn from across the model (the
-    whole model does not fit in HBM with every worker's copy)."""
+    model's buckets, each bucket a DynamiQ round.  Rings of up to 8 ranks
+    run the bucket stream whose exchange is pipelined across buckets
+    (stream.BucketStream: each launch carries N buckets' ring steps and one
+    bucket's decode; planning a few buckets ahead on a second stream); the
+    per-bucket stream (one cooperative exchange launch per bucket, the next
+    bucket's planning on a second stream) is timed beside it.  The gradient
+    data cycle through a pool of resident buckets drawn from across the model
+    (the whole model does not fit in HBM with every worker's copy)."""
     import torch
 
     from quantized_hop_gradient_gb300 import dq, synth
     from quantized_hop_gradient_gb300.allreduce import use_fused
-    from quantized_hop_gradient_gb300.stream import BucketedAllReduce
+    from quantized_hop_gradient_gb300.stream import BucketedAllReduce, BucketStream
 
     N = w.n_ranks
     nb = synth.bucket_count(w)
@@ -783,13 +792,14 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
     seq_out = [outs_pool[i] for i in pool_of]
     bucket_sg = w.bucket // SG
     kw = dict(budget=w.budget, correlated=w.correlated, butterfly=w.topology == "butterfly", seed=0)
-    # the overlapped stream picks its exchange itself ("auto": the cooperative
-    # one-launch exchange for rings of up to 64 ranks and 2^17 super-groups);
-    # the other exchange is timed beside it for comparison
-    fusable = use_fused(N, w.topology == "butterfly", bucket_sg)
-    ov = BucketedAllReduce(N, bucket_sg, overlap=True, fused="auto", **kw)
-    alt = BucketedAllReduce(N, bucket_sg, overlap=True, fused=not ov.fused, **kw) \
-        if (fusable or ov.fused) else None
+    # the pipelined bucket stream where it applies (rings of up to 8 ranks);
+    # the per-bucket stream with its own choice of exchange ("auto": the
+    # cooperative one-launch exchange for rings of up to 64 ranks and 2^17
+    # super-groups) is timed beside it for comparison
+    piped = w.topology == "ring" and N <= dq.MAX_STREAM_RANKS
+    per_bucket = BucketedAllReduce(N, bucket_sg, overlap=True, fused="auto", **kw)
+    ov = BucketStream(N, bucket_sg, budget=w.budget, correlated=w.correlated, seed=0) if piped else per_bucket
+    alt = per_bucket if piped else None
     sq = BucketedAllReduce(N, bucket_sg, overlap=False, fused=False, **kw)
     K, W = args.steps, max(args.warmup, 0)
 
@@ -814,7 +824,7 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
     t1 = time.time()
     n_launch = dq.dq_launch_count() - n0
     clk = clocks.stop(t0, t1)
-    if ov.fused:
+    if getattr(ov, "fused", False):
         for s_ in ov.sets:
             s_.check_status()
     # one more pass with every launch recorded: per-kernel times and the roofline
@@ -823,8 +833,9 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
     ms_logged = timed(ov, 1, W + K, log=log)
     infos_msg = []
     per = {}
-    kind_name = {0: "compress", 1: "dar", 2: "decode", 3: "stats", 4: "allocate_reorder", 7: "fused_ring"}
-    ref_set = ov.sets[0]
+    kind_name = {0: "compress", 1: "dar", 2: "decode", 3: "stats", 4: "allocate_reorder", 7: "fused_ring",
+                 9: "stream"}
+    ref_set = per_bucket.sets[0]
     for kind, sgs, t in log.launches():
         d = per.setdefault(kind_name.get(kind, str(kind)), {"launches": 0, "ms": 0.0, "sgs": 0})
         d["launches"] += 1
@@ -850,8 +861,8 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
     roofline = {"bound": "hbm", "kernel": KERNEL_NAMES.get(dominant, dominant), "achieved": dk["achieved_gbs"],
                 "peak": peak, "unit": "GB/s", "frac": dk["achieved_gbs"] / peak, "peak_source": peak_kind,
                 "traffic": traffic, "alg_bytes_per_launch": dk["alg_bytes_per_launch"],
-                "note": "planning kernels of bucket k+1 run on a second stream under bucket k's exchange, so "
-                        "the launch shares add up to more than the step"}
+                "note": "planning kernels run on a second stream under the exchange's launches, so the "
+                        "launch shares add up to more than the step"}
 
     ms_seq = ms_alt = None
     if not args.lean:
@@ -863,8 +874,6 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
         if alt.fused:
             for s_ in alt.sets:
                 s_.check_status()
-    ms_fused = ms if ov.fused else ms_alt
-    ms_ml = ms_alt if ov.fused else ms
     ms_max = max_over_ranks(ms, world, dev)
     gb = w.n * 2 / 1e9
 
@@ -883,9 +892,14 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
                    "l2": "each pass streams 8 x 16 GB of gradients through the pool; one bucket's working set "
                          "(about 0.6 GB) exceeds L2"},
         "per_bucket_ms": ms_max / nb,
-        "two_streams": {"ms_per_pass_overlapped": ms, "ms_per_pass_one_stream": ms_seq,
-                        "saved_frac": (1.0 - ms / ms_seq) if ms_seq else None},
-        "fused_exchange": {"used": ov.fused, "ms_per_pass_fused": ms_fused, "ms_per_pass_multi_launch": ms_ml},
+        "exchange": ("pipelined across buckets (N + 1 buckets per launch; planning "
+                     f"{ov.lookahead} buckets ahead on a second stream with {ov.plan_sms} SMs left to it)"
+                     if piped else ("one cooperative launch per bucket" if ov.fused else "one launch per step")),
+        "per_bucket_stream": {"ms_per_pass": ms_alt if piped else ms,
+                              "exchange": "one cooperative launch per bucket" if per_bucket.fused
+                              else "one launch per step",
+                              "note": "the next bucket's planning on a second stream"},
+        "one_stream": {"ms_per_pass": ms_seq, "note": "per-bucket rounds, one launch per step, no overlap"},
         "kernels": kernels, "ms_per_step_logged": ms_logged, "roofline": roofline,
         "gpu_launches": n_launch, "clocks": clk, "cpu_baseline": cpu, "e2e": e2e,
     }
@@ -895,24 +909,28 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
 
 def bucketed_e2e(args, w, ar, pool, pool_of, outs_pool, nb, dev, world, gb):
     """End to end over a full pass: every bucket's N gradients are uploaded
-    from pinned host memory (a host copy of the resident pool) into one of two
-    device staging sets on a copy stream, bucket k+1's upload and planning
-    overlapping bucket k's exchange; rank 0's fp32 result of every bucket is
-    downloaded on a third stream.  All copies are inside the timed region."""
+    from pinned host memory (a host copy of the resident pool) into one of the
+    stream's device staging sets on a copy stream, later buckets' uploads and
+    planning overlapping earlier buckets' exchange; rank 0's fp32 result of
+    every bucket is downloaded on a third stream.  All copies are inside the
+    timed region."""
     import torch
 
     N = w.n_ranks
     hosts = [[pinned_host_copy(g) for g in b] for b in pool]
     out_host = [torch.empty(o[0].numel(), dtype=torch.float32, pin_memory=True) for o in outs_pool]
-    stage = [[torch.empty(g.numel(), dtype=g.dtype, device=dev) for g in pool[0]] for _ in range(2)]
-    stage_last = [[torch.empty(g.numel(), dtype=g.dtype, device=dev) for g in pool[-1]] for _ in range(2)]
+    # a bucket's gradients are read until its last ring step: the pipelined
+    # stream keeps `depth` buckets in flight, the per-bucket stream two
+    S = getattr(ar, "depth", 2)
+    stage = [[torch.empty(g.numel(), dtype=g.dtype, device=dev) for g in pool[0]] for _ in range(S)]
+    stage_last = [[torch.empty(g.numel(), dtype=g.dtype, device=dev) for g in pool[-1]] for _ in range(S)]
     cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [[torch.cuda.Event() for _ in range(N)] for _ in range(nb)]
     ev_out = [torch.cuda.Event() for _ in range(len(outs_pool))]
     ev_exch = [torch.cuda.Event() for _ in range(nb)]
     P = len(outs_pool)
     last = nb - 1
-    bufs = [stage_last[k & 1] if k == last else stage[k & 1] for k in range(nb)]
+    bufs = [stage_last[k % S] if k == last else stage[k % S] for k in range(nb)]
     outs = [outs_pool[pool_of[k]] for k in range(nb)]
 
     def before_plan(k, side):

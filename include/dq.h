@@ -261,6 +261,21 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads_host, int64_t n
                   dq_plan_info *info_host, void *const *rank_ready_host, dq_launch_log *log,
                   void *stream);
 
+/* dq_plan without the readback: the same launches, enqueued on `stream`, and
+ * no synchronisation.  The plan's 2/4/8 counts stay on the device, for
+ * dq_exchange_stream_step, which derives the bucket's chunk cuts from them.
+ *   counts_dev_host: host output: the device address (inside plan_ws) of the
+ *   three int64 counts n2, n4, n8, written by the enqueued work.
+ *   nonfinite_dev_host: NULL, or host output: the device address (inside
+ *   plan_ws) of an int32 that the enqueued work leaves nonzero when some M_j
+ *   or F_j is not finite (read it with dq_get_device_status after the work;
+ *   the round's results are then not meaningful, though no kernel faults).
+ *   Other arguments as for dq_plan.  Errors: as dq_plan's argument checks. */
+dq_status dq_plan_async(const dq_config *cfg, const void *const *grads_host, int64_t n_sg,
+                        float *mu, int32_t *perm, void *plan_ws, size_t plan_ws_bytes,
+                        const int64_t **counts_dev_host, const int32_t **nonfinite_dev_host,
+                        void *const *rank_ready_host, dq_launch_log *log, void *stream);
+
 /* Optional record of the kernel launches of dq_plan and dq_exchange, for timing them on
  * the launching stream.  events: host array of 2*capacity cudaEvent_t created
  * by the caller (timing enabled); launch i is bracketed by events[2i] and
@@ -273,8 +288,10 @@ enum { DQ_LAUNCH_COMPRESS = 0, DQ_LAUNCH_DAR = 1, DQ_LAUNCH_DECODE = 2, DQ_LAUNC
        DQ_LAUNCH_ALLOCATE_REORDER = 4, /* statistics reduce, allocation and reorder, one bracket */
        DQ_LAUNCH_MX_HOP = 5, DQ_LAUNCH_MX_DECODE = 6, /* MXFP8 baseline; sgs = coordinates / 256 */
        DQ_LAUNCH_FUSED_RING = 7, /* dq_exchange_fused: all hops and the decode; sgs = J * (N + 1) */
-       DQ_LAUNCH_PIPELINED = 8   /* one launch of dq_exchange_pipelined; sgs = super-groups its hop
-                                    units process plus super-groups it decodes (each once) */ };
+       DQ_LAUNCH_PIPELINED = 8,  /* one launch of dq_exchange_pipelined; sgs = super-groups its hop
+                                    units process plus super-groups it decodes (each once) */
+       DQ_LAUNCH_STREAM = 9      /* one dq_exchange_stream_step; sgs = the super-groups of its
+                                    buckets (each once) */ };
 struct dq_launch_log {
     void   **events;
     int32_t *kinds;
@@ -368,6 +385,99 @@ dq_status dq_exchange_pipelined(const dq_config *cfg, const void *const *grads_h
                                 const float *mu, const int32_t *perm, const dq_plan_info *info, void *ws,
                                 size_t ws_bytes, void *const *outs_host, int32_t out_is_bf16, int32_t n_parts,
                                 const uint8_t **final_msgs_host, dq_launch_log *log, void *stream);
+
+/* ---- DDP buckets: the ring exchange pipelined across buckets -------------
+ * Data-parallel training all-reduces its gradient as a stream of buckets
+ * [S "Evaluation": DDP gradient buckets; review "What carries the
+ * argument": each bucket is compressed with its own statistics and
+ * allocation].  A bucket of a 25 MB DDP stream gives each ring step too few
+ * work units to fill the GPU, so the exchange is pipelined across buckets:
+ * launch t runs ring step t - b of every bucket b in flight (N of them) and
+ * the final decode of bucket t - N, the way the ring pipelines its chunks.
+ * Each bucket's planning is dq_plan_async (no host round trip); the launch
+ * derives the bucket's chunk cuts and work units on the device from the
+ * counts the plan left there.  Results are those of dq_exchange for each
+ * bucket, bit for bit. */
+
+/* One bucket's part in a launch. */
+typedef struct {
+    int64_t            n_sg;        /* super-groups of the bucket (J), 1 .. 2^27-1 */
+    const int64_t     *counts_dev;  /* device: n2, n4, n8 (dq_plan_async's counts_dev) */
+    const void *const *grads_host;  /* host array of N device bf16 gradients (J*256) */
+    void *const       *outs_host;   /* host array of N device outputs (J*256 fp32 or bf16) */
+    const float       *mu;          /* device, J floats, from the bucket's plan */
+    const int32_t     *perm;        /* device, J int32, from the bucket's plan */
+    void              *msgs;        /* device, 16-byte aligned: the bucket's messages */
+    size_t             msgs_bytes;  /* >= dq_bucket_msgs_bytes(cfg, n_sg) */
+    uint64_t           round;       /* the bucket's generator round */
+    int32_t            step;        /* 0 .. N-1: this launch runs ring step `step` of
+                                       the bucket; N: its final decode */
+} dq_bucket_step;
+
+/* Device bytes of one bucket's message buffers (N*N chunk messages, sized
+ * for any allocation of n_sg super-groups); 0 for a bad config, a butterfly
+ * or more than 8 ranks. */
+size_t dq_bucket_msgs_bytes(const dq_config *cfg, int64_t n_sg);
+
+/* One launch of the bucket stream: the ring steps and the final decode
+ * listed in steps[0 .. n_steps) (1 <= n_steps <= N + 1, at most one decode,
+ * ring only, N <= 8; cfg's round is not used: each bucket carries its own).
+ * A bucket's step s must follow its step s-1 on the same stream (and its
+ * decode its step N-1); its plan must precede its step 0 (stream order or an
+ * event).  The bucket's messages, mu, perm and gradients must stay untouched
+ * from its step 0 to its decode.
+ *   counter_dev: device uint32, zero at the launch (one per launch; the
+ *   launch counts it up).
+ *   Errors: DQ_ERR_INVALID_ARG (bad config, N > 8, a bad step list, a null
+ *   pointer, small msgs), DQ_ERR_ALIGNMENT, DQ_ERR_CUDA.  No sync. */
+dq_status dq_exchange_stream_step(const dq_config *cfg, const dq_bucket_step *steps, int32_t n_steps,
+                                  unsigned int *counter_dev, int32_t out_is_bf16, dq_launch_log *log,
+                                  void *stream);
+
+/* A whole bucket stream in one call: every bucket's dq_plan_async on
+ * plan_stream (one bucket ahead of the exchange) and the N + n_buckets
+ * launches of dq_exchange_stream_step on `stream`, ordered by CUDA events
+ * the call creates and releases (no device memory is allocated, and the
+ * host never waits).  Each bucket's results equal a dq_plan + dq_exchange
+ * round of that bucket with cfg's round replaced by the bucket's.
+ *   buckets[k]: the bucket's size, its N gradients and outputs (host arrays
+ *   of device pointers, as for dq_plan and dq_exchange) and its round.
+ *   lookahead: >= 1, how many buckets ahead of the exchange the planning
+ *   is enqueued.
+ *   plan_sms: SMs the exchange's launches leave free for the planning
+ *   stream's kernels (0 .. SMs - 1).
+ *   sets[0 .. n_sets): caller-owned buffer sets, n_sets >= N + lookahead + 1:
+ *   bucket k uses set k % n_sets, which is reused once bucket k - n_sets has
+ *   been decoded.  A set holds
+ *   mu and perm (bucket_sg floats and int32), a plan workspace
+ *   (dq_plan_workspace_bytes(N, bucket_sg)) and the messages
+ *   (dq_bucket_msgs_bytes(cfg, bucket_sg)), bucket_sg >= every n_sg.
+ *   counters_dev: device, n_buckets + N uint32 (zeroed by the call).
+ *   plan_stream: the planning stream (NULL: `stream`); give it a higher
+ *   priority than `stream`, so that its short kernels take SMs as the
+ *   exchange's launches free them.
+ *   Errors: as dq_exchange_stream_step and dq_plan's argument checks, and
+ *   DQ_ERR_INVALID_ARG for a bad lookahead, plan_sms or n_sets.  No sync. */
+typedef struct {
+    int64_t            n_sg;
+    const void *const *grads_host;
+    void *const       *outs_host;
+    uint64_t           round;
+} dq_bucket;
+
+typedef struct {
+    float   *mu;
+    int32_t *perm;
+    void    *plan_ws;
+    size_t   plan_ws_bytes;
+    void    *msgs;
+    size_t   msgs_bytes;
+} dq_stream_set;
+
+dq_status dq_allreduce_stream(const dq_config *cfg, const dq_bucket *buckets, int32_t n_buckets,
+                              const dq_stream_set *sets, int32_t n_sets, int32_t lookahead, int32_t plan_sms,
+                              unsigned int *counters_dev, int32_t out_is_bf16, void *plan_stream, void *stream,
+                              dq_launch_log *log);
 
 /* Reads a device status word into host memory [boundary of the hot path:
  * device-side errors of an asynchronous call are reported through a status

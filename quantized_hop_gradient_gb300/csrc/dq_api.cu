@@ -640,6 +640,22 @@ cudaError_t zero_words(void *a, int na, void *b, cudaStream_t st)
     return cudaGetLastError();
 }
 
+// Zeroes n 32-bit words (any count) in one launch.
+__global__ void zero_many_kernel(uint32_t *p, int64_t n)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        p[i] = 0u;
+}
+
+cudaError_t zero_many(void *p, int64_t n, cudaStream_t st)
+{
+    if (n <= 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((n + 255) / 256, 4 * (int64_t)sm_count());
+    zero_many_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<uint32_t *>(p), n);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
 // One thread copies a device status word into host memory mapped into the
 // device address space (the readback of dq_get_device_status).
 __global__ void status_readback_kernel(const int32_t *src, int32_t *out)
@@ -690,11 +706,33 @@ size_t dq_plan_workspace_bytes(int32_t n_ranks, int64_t n_sg)
     return plan_layout(n_ranks, n_sg).total;
 }
 
-dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, float *mu, int32_t *perm, void *ws,
-                  size_t ws_bytes, dq_plan_info *info, void *const *rank_ready, dq_launch_log *log, void *stream)
+}  // extern "C"
+
+namespace {
+
+// Where a plan leaves its results on the device.
+struct PlanDev {
+    int64_t *counts;     // n2, n4, n8
+    float *T;
+    int32_t *nonfinite;
+};
+
+__global__ void set_counts_kernel(int64_t *counts, int64_t n2, int64_t n4, int64_t n8)
 {
-    if (!cfg_ok(cfg) || !grads || !mu || !perm || !ws || !info || n_sg < 1 || n_sg >= kMaxSG)
-        return DQ_ERR_INVALID_ARG;
+    if (threadIdx.x == 0) {
+        counts[0] = n2;
+        counts[1] = n4;
+        counts[2] = n8;
+    }
+}
+
+// Enqueues the whole plan (statistics, reduce, allocation, reorder) on st;
+// nothing is read back.
+dq_status plan_enqueue(const dq_config *cfg, const void *const *grads, int64_t n_sg, float *mu, int32_t *perm,
+                       void *ws, size_t ws_bytes, void *const *rank_ready, dq_launch_log *log, cudaStream_t st,
+                       PlanDev &out)
+{
+    if (!cfg_ok(cfg) || !grads || !mu || !perm || !ws || n_sg < 1 || n_sg >= kMaxSG) return DQ_ERR_INVALID_ARG;
     const int32_t N = cfg->n_ranks;
     const PlanLayout L = plan_layout(N, n_sg);
     if (ws_bytes < L.total) return DQ_ERR_INVALID_ARG;
@@ -704,7 +742,6 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
         if (!grads[r]) return DQ_ERR_INVALID_ARG;
         if (!aligned16(grads[r])) return DQ_ERR_ALIGNMENT;
     }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *w = static_cast<uint8_t *>(ws);
     float *mean_all = reinterpret_cast<float *>(w + L.mean_all);
     float *sq_all = reinterpret_cast<float *>(w + L.sq_all);
@@ -715,6 +752,7 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
     int64_t *counts = reinterpret_cast<int64_t *>(w + L.counts);
     int32_t *nonfinite = reinterpret_cast<int32_t *>(w + L.counts + 32);   // inside the counts slot
     void *scratch = w + L.scratch;
+    out = PlanDev{counts, T, nonfinite};
     if (zero_words(nonfinite, 1, nullptr, st) != cudaSuccess) return DQ_ERR_CUDA;
     if (rank_ready) {  // one launch per rank, each after its rank's event
         for (int32_t r = 0; r < N; ++r) {
@@ -749,48 +787,62 @@ dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, 
         if (launch_plan_small(F, n_sg, cap, cfg->fixed_bits, b, T, counts, perm, st) != cudaSuccess)
             return DQ_ERR_CUDA;
         log_end(slot, st);
-        PlanReadback h;
-        const dq_status rs = plan_read(counts, T, nonfinite, st, &h);
-        if (rs != DQ_OK) return rs;
-        if (h.nonfinite) return DQ_ERR_NONFINITE;
-        info->T = cfg->fixed_bits ? NAN : h.T;
-        info->n2 = h.counts[0];
-        info->n4 = h.counts[1];
-        info->n8 = h.counts[2];
         return DQ_OK;
     }
     if (cfg->fixed_bits) {
         // uniform-bitwidth ablation: every super-group gets fixed_bits (the
         // reorder of a uniform allocation is the identity permutation)
         if (cudaMemsetAsync(b, cfg->fixed_bits, (size_t)n_sg, st) != cudaSuccess) return DQ_ERR_CUDA;
-        const dq_status s = dq_reorder(b, n_sg, perm, scratch, plan_scratch_bytes(n_sg), stream);
+        const dq_status s = dq_reorder(b, n_sg, perm, scratch, plan_scratch_bytes(n_sg), st);
         if (s != DQ_OK) return s;
         log_end(slot, st);
-        // the counts slot is not written on this path: zeroed words stand in
-        if (zero_words(counts, 6, nullptr, st) != cudaSuccess) return DQ_ERR_CUDA;
-        PlanReadback h;
-        const dq_status rs = plan_read(counts, nullptr, nonfinite, st, &h);
-        if (rs != DQ_OK) return rs;
-        if (h.nonfinite) return DQ_ERR_NONFINITE;
-        info->T = NAN;
-        info->n2 = cfg->fixed_bits == 2 ? n_sg : 0;
-        info->n4 = cfg->fixed_bits == 4 ? n_sg : 0;
-        info->n8 = cfg->fixed_bits == 8 ? n_sg : 0;
-        return DQ_OK;
+        const int32_t f = cfg->fixed_bits;
+        set_counts_kernel<<<1, 32, 0, st>>>(counts, f == 2 ? n_sg : 0, f == 4 ? n_sg : 0, f == 8 ? n_sg : 0);
+        note_launches(1);
+        return cuda_status(cudaGetLastError());
     }
-    dq_status s = dq_allocate(F, n_sg, cfg->budget_bits, b, T, counts, scratch, plan_scratch_bytes(n_sg), stream);
+    dq_status s = dq_allocate(F, n_sg, cfg->budget_bits, b, T, counts, scratch, plan_scratch_bytes(n_sg), st);
     if (s != DQ_OK) return s;
-    s = dq_reorder(b, n_sg, perm, scratch, plan_scratch_bytes(n_sg), stream);
+    s = dq_reorder(b, n_sg, perm, scratch, plan_scratch_bytes(n_sg), st);
     if (s != DQ_OK) return s;
     log_end(slot, st);
+    return DQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dq_status dq_plan(const dq_config *cfg, const void *const *grads, int64_t n_sg, float *mu, int32_t *perm, void *ws,
+                  size_t ws_bytes, dq_plan_info *info, void *const *rank_ready, dq_launch_log *log, void *stream)
+{
+    if (!info) return DQ_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    PlanDev d;
+    const dq_status s = plan_enqueue(cfg, grads, n_sg, mu, perm, ws, ws_bytes, rank_ready, log, st, d);
+    if (s != DQ_OK) return s;
     PlanReadback h;
-    const dq_status rs = plan_read(counts, T, nonfinite, st, &h);
+    const dq_status rs = plan_read(d.counts, cfg->fixed_bits ? nullptr : d.T, d.nonfinite, st, &h);
     if (rs != DQ_OK) return rs;
     if (h.nonfinite) return DQ_ERR_NONFINITE;
-    info->T = h.T;
+    info->T = cfg->fixed_bits ? NAN : h.T;
     info->n2 = h.counts[0];
     info->n4 = h.counts[1];
     info->n8 = h.counts[2];
+    return DQ_OK;
+}
+
+dq_status dq_plan_async(const dq_config *cfg, const void *const *grads, int64_t n_sg, float *mu, int32_t *perm,
+                        void *ws, size_t ws_bytes, const int64_t **counts_dev, const int32_t **nonfinite_dev,
+                        void *const *rank_ready, dq_launch_log *log, void *stream)
+{
+    if (!counts_dev) return DQ_ERR_INVALID_ARG;
+    PlanDev d;
+    const dq_status s =
+        plan_enqueue(cfg, grads, n_sg, mu, perm, ws, ws_bytes, rank_ready, log, static_cast<cudaStream_t>(stream), d);
+    if (s != DQ_OK) return s;
+    *counts_dev = d.counts;
+    if (nonfinite_dev) *nonfinite_dev = d.nonfinite;
     return DQ_OK;
 }
 
@@ -1076,6 +1128,190 @@ dq_status dq_exchange_pipelined(const dq_config *cfg, const void *const *grads, 
     return DQ_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Bytes of one chunk message of a bucket of J super-groups, for any
+// allocation: at most J super-groups of scale metadata, and at most
+// 8J/N + 9 code bits per super-group-coordinate (the cut gives a chunk at
+// most ceil(total/N) + 8 of the bucket's total code bits), 32 bytes each.
+size_t bucket_msg_stride(int32_t N, int64_t J, bool sf)
+{
+    const int64_t meta = sf ? 64 * J : (J + 15) / 16 * 16 + 16 * J;
+    const int64_t codes = 32 * (8 * J / N + 9) + 256;
+    return round256((size_t)(meta + codes));
+}
+
+bool stream_cfg_ok(const dq_config *cfg) { return cfg_ok(cfg) && cfg->n_ranks <= kMaxStreamRanks; }
+
+}  // namespace
+
+extern "C" {
+
+size_t dq_bucket_msgs_bytes(const dq_config *cfg, int64_t n_sg)
+{
+    if (!stream_cfg_ok(cfg) || n_sg < 1 || n_sg >= kMaxSG) return 0;
+    const size_t N = (size_t)cfg->n_ranks;
+    return N * N * bucket_msg_stride(cfg->n_ranks, n_sg, cfg->scale_fp32 != 0);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Fills P (tables aside) for one launch of the bucket stream and launches it.
+dq_status stream_step(const dq_config *cfg, StreamRingParams *P, const dq_bucket_step *steps, int32_t n_steps,
+                      unsigned int *counter_dev, int32_t out_is_bf16, dq_launch_log *log, cudaStream_t st,
+                      int32_t free_sms = 0)
+{
+    const int32_t N = cfg->n_ranks;
+    if (n_steps < 1 || n_steps > N + 1) return DQ_ERR_INVALID_ARG;
+    if (!counter_dev) return DQ_ERR_INVALID_ARG;
+    if ((uintptr_t)counter_dev & 3u) return DQ_ERR_ALIGNMENT;
+    const bool sf = cfg->scale_fp32 != 0;
+    int decodes = 0;
+    int64_t tasks = 0, sgs = 0;
+    for (int32_t i = 0; i < n_steps; ++i) {
+        const dq_bucket_step &b = steps[i];
+        if (b.step < 0 || b.step > N || b.n_sg < 1 || b.n_sg >= kMaxSG || !b.counts_dev || !b.grads_host ||
+            !b.outs_host || !b.mu || !b.perm || !b.msgs)
+            return DQ_ERR_INVALID_ARG;
+        if (b.step == N && ++decodes > 1) return DQ_ERR_INVALID_ARG;
+        if (b.msgs_bytes < dq_bucket_msgs_bytes(cfg, b.n_sg)) return DQ_ERR_INVALID_ARG;
+        if (((uintptr_t)b.counts_dev & 7u) || !aligned16(b.mu) || !aligned16(b.perm) || !aligned16(b.msgs))
+            return DQ_ERR_ALIGNMENT;
+        BucketSlot &S = P->slot[i];
+        for (int32_t r = 0; r < N; ++r) {
+            if (!b.grads_host[r] || !b.outs_host[r]) return DQ_ERR_INVALID_ARG;
+            if (!aligned16(b.grads_host[r]) || !aligned16(b.outs_host[r])) return DQ_ERR_ALIGNMENT;
+            S.grads[r] = b.grads_host[r];
+            S.outs[r] = b.outs_host[r];
+        }
+        S.counts = b.counts_dev;
+        S.mu = b.mu;
+        S.perm = b.perm;
+        S.msgs = static_cast<uint8_t *>(b.msgs);
+        S.msg_stride = (int64_t)bucket_msg_stride(N, b.n_sg, sf);
+        S.ph = philox_keys(cfg->seed, b.round);
+        S.n_sg = (int32_t)b.n_sg;
+        S.step = b.step;
+        S.n_ranks = N;
+        S.out_is_bf16 = out_is_bf16 ? 1 : 0;
+        // grid sizing only: the units of one step (the device finds the exact count)
+        const int64_t units = (b.n_sg + kUnit - 1) / kUnit + 3 * N;
+        tasks += b.step == N ? units * kDecodeSub : units;
+        sgs += b.n_sg;
+    }
+    P->n_slots = n_steps;
+    P->n_ranks = N;
+    P->correlated = cfg->correlated ? 1 : 0;
+    P->scale_fp32 = cfg->scale_fp32;
+    P->next = counter_dev;
+    const LogSlot slot = log_begin(log, DQ_LAUNCH_STREAM, sgs, st);
+    const cudaError_t e = launch_stream_ring(*P, tasks, st, free_sms);
+    log_end(slot, st);
+    return cuda_status(e);
+}
+
+// CUDA events of one dq_allreduce_stream call, destroyed when it returns
+// (destruction waits for nothing: an event still pending in a stream is
+// released once it completes).
+struct EventPool {
+    std::vector<cudaEvent_t> ev;
+    ~EventPool()
+    {
+        for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    }
+    bool make(size_t n)
+    {
+        for (size_t i = 0; i < n; ++i) {
+            cudaEvent_t e = nullptr;
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return false;
+            ev.push_back(e);
+        }
+        return true;
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+dq_status dq_exchange_stream_step(const dq_config *cfg, const dq_bucket_step *steps, int32_t n_steps,
+                                  unsigned int *counter_dev, int32_t out_is_bf16, dq_launch_log *log, void *stream)
+{
+    if (!stream_cfg_ok(cfg) || !steps) return DQ_ERR_INVALID_ARG;
+    std::unique_ptr<StreamRingParams> P(new StreamRingParams());
+    memset(P.get(), 0, sizeof(StreamRingParams));
+    if (!build_tables(cfg->eps, &P->tab)) return DQ_ERR_INVALID_ARG;
+    return stream_step(cfg, P.get(), steps, n_steps, counter_dev, out_is_bf16, log, static_cast<cudaStream_t>(stream));
+}
+
+dq_status dq_allreduce_stream(const dq_config *cfg, const dq_bucket *buckets, int32_t n_buckets,
+                              const dq_stream_set *sets, int32_t n_sets, int32_t lookahead, int32_t plan_sms,
+                              unsigned int *counters_dev, int32_t out_is_bf16, void *plan_stream, void *stream,
+                              dq_launch_log *log)
+{
+    if (!stream_cfg_ok(cfg) || !buckets || !sets || !counters_dev || n_buckets < 1) return DQ_ERR_INVALID_ARG;
+    const int32_t N = cfg->n_ranks;
+    if (lookahead < 1 || n_sets < N + lookahead + 1 || plan_sms < 0 || plan_sms >= sm_count()) return DQ_ERR_INVALID_ARG;
+    if ((uintptr_t)counters_dev & 3u) return DQ_ERR_ALIGNMENT;
+    for (int32_t k = 0; k < n_buckets; ++k)
+        if (buckets[k].n_sg < 1 || buckets[k].n_sg >= kMaxSG || !buckets[k].grads_host || !buckets[k].outs_host)
+            return DQ_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n_sets; ++i)
+        if (!sets[i].mu || !sets[i].perm || !sets[i].plan_ws || !sets[i].msgs) return DQ_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStream_t ps = plan_stream ? static_cast<cudaStream_t>(plan_stream) : st;
+    EventPool E;   // per set: planned, free again; then the call's start
+    if (!E.make(2 * (size_t)n_sets + 1)) return DQ_ERR_CUDA;
+    // the planning stream starts after everything already enqueued on
+    // `stream` (earlier work may still use the sets)
+    if (ps != st && (cudaEventRecord(E.ev.back(), st) != cudaSuccess || cudaStreamWaitEvent(ps, E.ev.back(), 0) != cudaSuccess))
+        return DQ_ERR_CUDA;
+    auto ev_plan = [&](int32_t i) { return E.ev[2 * i]; };
+    auto ev_free = [&](int32_t i) { return E.ev[2 * i + 1]; };
+    std::unique_ptr<StreamRingParams> P(new StreamRingParams());
+    memset(P.get(), 0, sizeof(StreamRingParams));
+    if (!build_tables(cfg->eps, &P->tab)) return DQ_ERR_INVALID_ARG;
+    if (zero_many(counters_dev, (int64_t)n_buckets + N, st) != cudaSuccess) return DQ_ERR_CUDA;
+    std::vector<const int64_t *> counts((size_t)n_buckets, nullptr);
+    std::vector<uint8_t> used((size_t)n_sets, 0);
+    auto plan = [&](int32_t k) -> dq_status {
+        const int32_t si = k % n_sets;
+        if (used[si] && cudaStreamWaitEvent(ps, ev_free(si), 0) != cudaSuccess) return DQ_ERR_CUDA;
+        used[si] = 1;
+        dq_config c = *cfg;
+        c.round = buckets[k].round;
+        PlanDev d;
+        const dq_stream_set &S = sets[si];
+        const dq_status s = plan_enqueue(&c, buckets[k].grads_host, buckets[k].n_sg, S.mu, S.perm, S.plan_ws,
+                                         S.plan_ws_bytes, nullptr, log, ps, d);
+        if (s != DQ_OK) return s;
+        counts[k] = d.counts;
+        return cudaEventRecord(ev_plan(si), ps) == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
+    };
+    dq_status s = DQ_OK;
+    for (int32_t k = 0; k < std::min(lookahead, n_buckets); ++k)
+        if ((s = plan(k)) != DQ_OK) return s;
+    dq_bucket_step steps[kMaxStreamRanks + 1];
+    for (int32_t t = 0; t < n_buckets + N; ++t) {
+        if (t + lookahead < n_buckets && (s = plan(t + lookahead)) != DQ_OK) return s;
+        if (t < n_buckets && cudaStreamWaitEvent(st, ev_plan(t % n_sets), 0) != cudaSuccess) return DQ_ERR_CUDA;
+        int32_t n = 0;
+        for (int32_t b = std::max(0, t - N); b <= std::min(t, n_buckets - 1); ++b) {
+            const dq_stream_set &S = sets[b % n_sets];
+            steps[n++] = dq_bucket_step{buckets[b].n_sg, counts[b], buckets[b].grads_host, buckets[b].outs_host,
+                                        S.mu, S.perm, S.msgs, S.msgs_bytes, buckets[b].round, t - b};
+        }
+        if ((s = stream_step(cfg, P.get(), steps, n, counters_dev + t, out_is_bf16, log, st, plan_sms)) != DQ_OK)
+            return s;
+        if (t >= N && cudaEventRecord(ev_free((t - N) % n_sets), st) != cudaSuccess) return DQ_ERR_CUDA;
+    }
+    return DQ_OK;
+}
+
 dq_status dq_get_device_status(const int32_t *status_dev, int32_t *status_host, void *stream)
 {
     if (!status_dev || !status_host) return DQ_ERR_INVALID_ARG;
@@ -1117,3 +1353,4 @@ static_assert(sizeof(dq::HopParams) <= 32764, "HopParams exceeds the kernel para
 static_assert(sizeof(dq::DecodeParams) <= 32764, "DecodeParams exceeds the kernel parameter limit");
 static_assert(sizeof(dq::FusedRingParams) <= 32764, "FusedRingParams exceeds the kernel parameter limit");
 static_assert(sizeof(dq::WaveRingParams) <= 32764, "WaveRingParams exceeds the kernel parameter limit");
+static_assert(sizeof(dq::StreamRingParams) <= 32764, "StreamRingParams exceeds the kernel parameter limit");

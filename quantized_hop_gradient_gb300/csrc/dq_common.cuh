@@ -197,6 +197,7 @@ struct FusedRingParams {
 // own buffer (r*N + s), so no launch overwrites bytes another part has still
 // to read.
 constexpr int kMaxWaveParts = 256;
+constexpr int kDecodeSub = 4;   // decode pieces per work unit in the pipelined exchanges (8 super-groups each)
 constexpr int kWaveCounterBytes = 2048;   // one unit counter per launch: (kMaxFusedRanks + kMaxWaveParts) x 4 bytes
 static_assert((kMaxFusedRanks + kMaxWaveParts) * 4 <= kWaveCounterBytes, "wave counters");
 
@@ -223,6 +224,39 @@ struct WaveRingParams {
     PhiloxKeys ph;
     int32_t out_is_bf16;
     int32_t scale_fp32;
+};
+
+// One launch of the bucket stream (dq_exchange_stream_step): a ring
+// exchange pipelined across DDP buckets.  Launch t runs ring step t - b of
+// every bucket b in flight and the final decode of bucket t - N, so N + 1
+// buckets share each launch.  A bucket's chunk cuts and work units are
+// derived on the device from the 2/4/8 counts its (asynchronous) planning
+// left in device memory: the host never waits for a plan.
+constexpr int kMaxStreamRanks = 8;
+
+struct BucketSlot {
+    const void *grads[kMaxStreamRanks];
+    void *outs[kMaxStreamRanks];
+    const int64_t *counts;      // device: n2, n4, n8 of the bucket's plan
+    const float *mu;
+    const int32_t *perm;
+    uint8_t *msgs;              // N*N message buffers of the bucket, msg_stride apart
+    int64_t msg_stride;
+    PhiloxKeys ph;              // the bucket's generator round
+    int32_t n_sg;
+    int32_t step;               // 0 .. N-1: ring step; N: the final decode
+    int32_t n_ranks;            // the launch's, so that a slot serves as
+    int32_t out_is_bf16;        //   the kernels' parameter view
+};
+
+struct StreamRingParams {
+    Tables tab;
+    BucketSlot slot[kMaxStreamRanks + 1];
+    int32_t n_slots;
+    int32_t n_ranks;
+    int32_t correlated;
+    int32_t scale_fp32;
+    unsigned int *next;         // task counter, zero at launch
 };
 
 // ---------------------------------------------------------------------------

@@ -888,7 +888,6 @@ __device__ __forceinline__ LaneCodes<BITS> ldg_codes(const uint8_t *p)
 }
 
 constexpr int kRowBytes = 1024;   // row buffer of the in-launch decode, per half-warp
-constexpr int kDecodeSub = 4;     // in-launch decode pieces per work unit (8 super-groups each)
 
 // The final decode of up to kUnit super-groups of one chunk into all N
 // outputs: out = fl(sigma * q_code + fl(mu * N)).  The hop's mapping: lanes
@@ -1089,6 +1088,182 @@ __global__ void __launch_bounds__(kWarps * 32, 1) wave_ring_kernel(const __grid_
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // the decode's copies
 }
 
+// Chunk cuts and work units of one bucket, derived from its plan's counts
+// (32-bit: a bucket has fewer than 2^27 super-groups).  The cuts follow
+// dq_chunk_cuts: chunk c starts at the first super-group whose code bits
+// before it reach ceil(c * total / N).
+struct SlotGeom {
+    int32_t lo[kMaxStreamRanks + 1];
+    int32_t ub[kMaxStreamRanks][4];   // first unit of each segment of chunk c; [3] = its end
+    int32_t end2, end4, units, pad;
+};
+
+__device__ __forceinline__ void slot_geometry(const BucketSlot &S, int N, SlotGeom &g)
+{
+    const int64_t J = S.n_sg;
+    // counts from a plan whose input was not finite are not trusted: clamped,
+    // they still describe J super-groups, so every index stays in range
+    const int64_t n2 = min(max(S.counts[0], (int64_t)0), J);
+    const int64_t n4 = min(max(S.counts[1], (int64_t)0), J - n2);
+    const int64_t n8 = J - n2 - n4;
+    const int64_t total = 2 * n2 + 4 * n4 + 8 * n8;
+    g.lo[0] = 0;
+    for (int c = 1; c < N; ++c) {
+        const int64_t target = ((int64_t)c * total + N - 1) / N;
+        int64_t i;
+        if (target <= 2 * n2) i = (target + 1) / 2;
+        else if (target <= 2 * n2 + 4 * n4) i = n2 + (target - 2 * n2 + 3) / 4;
+        else i = n2 + n4 + (target - 2 * n2 - 4 * n4 + 7) / 8;
+        g.lo[c] = (int32_t)i;
+    }
+    g.lo[N] = (int32_t)J;
+    g.end2 = (int32_t)n2;
+    g.end4 = (int32_t)(n2 + n4);
+    int32_t u = 0;
+    for (int c = 0; c < N; ++c) {
+        const int32_t a = g.lo[c], b = g.lo[c + 1];
+        const int32_t cuts[4] = {a, max(a, min(b, g.end2)), max(a, min(b, g.end4)), b};
+        for (int s = 0; s < 3; ++s) {
+            g.ub[c][s] = u;
+            u += (cuts[s + 1] - cuts[s] + kUnit - 1) / kUnit;
+        }
+        g.ub[c][3] = u;
+    }
+    g.units = u;
+}
+
+// Message layout of chunk [a, b) of a bucket (msg_view on the device).
+__device__ __forceinline__ MsgView chunk_view(uint8_t *base, int32_t a, int32_t b, int32_t end2, int32_t end4,
+                                              bool sf32)
+{
+    auto overlap = [](int32_t x0, int32_t x1, int32_t y0, int32_t y1) {
+        const int32_t l = max(x0, y0), h = min(x1, y1);
+        return h > l ? h - l : 0;
+    };
+    MsgView m;
+    m.base = base;
+    m.c = b - a;
+    m.n2 = overlap(a, b, 0, end2);
+    m.n4 = overlap(a, b, end2, end4);
+    m.off_u = sf32 ? 0 : (m.c + 15) / 16 * 16;
+    m.off_c2 = m.off_u + (sf32 ? 64 : 16) * m.c;
+    m.off_c4 = m.off_c2 + 64 * m.n2;
+    m.off_c8 = m.off_c4 + 128 * m.n4;
+    return m;
+}
+
+// One launch of the bucket stream (StreamRingParams).  Every block first
+// derives the chunk cuts and work units of the launch's buckets from their
+// plans' counts (shared memory).  The tasks are the work units of every
+// bucket at a ring step and the decode pieces of the bucket at its final
+// decode, spread evenly through the task list; warps claim them in turn from
+// the launch's counter, one ahead.  Step s of chunk c of a bucket is handled
+// by rank r = (c + 1 + s) mod N, which reads rank r-1's message of step s-1
+// and writes its own of step s (step 0 quantizes the local gradient); the
+// decode reads owner c's message of step N-1.  Launched with programmatic
+// stream serialization, as the pipelined exchange's kernel.
+template <bool ONE_LEVEL, bool SF32>
+__global__ void __launch_bounds__(kWarps * 32, 1) stream_ring_kernel(const __grid_constant__ StreamRingParams P)
+{
+    __shared__ SlotGeom geo[kMaxStreamRanks + 1];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    block_copy(&g_tab, &P.tab);
+    __syncthreads();
+    expand_bk4();
+    expand_tables(true);
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the plans' counts and the previous launch's messages
+    const int N = P.n_ranks;
+    if (threadIdx.x < (unsigned)P.n_slots) slot_geometry(P.slot[threadIdx.x], N, geo[threadIdx.x]);
+    __syncthreads();
+    uint8_t *dyn = g_dyn + tab_bytes(false);
+    constexpr int STAGE = stage_bytes<false, SF32>();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t *stg = dyn + warp * kStages * STAGE;
+    uint8_t *rows = dyn + kWarps * kStages * STAGE + warp * 2 * kRowBytes;
+    // hop tasks H (units of the buckets at a ring step) and decode pieces D
+    uint32_t H = 0, D = 0;
+    int dslot = -1;
+    for (int i = 0; i < P.n_slots; ++i) {
+        if (P.slot[i].step == N) {
+            dslot = i;
+            D = (uint32_t)geo[i].units * kDecodeSub;
+        } else {
+            H += (uint32_t)geo[i].units;
+        }
+    }
+    const uint32_t T = H + D, stride = D > 0 ? T / D : 1u;
+    uint32_t k_next = 0u;
+    if (lane == 0) k_next = atomicAdd(P.next, 1u);
+    k_next = __shfl_sync(kFull, k_next, 0);
+    while (k_next < T) {
+        const uint32_t k = k_next;
+        if (lane == 0) k_next = atomicAdd(P.next, 1u);
+        k_next = __shfl_sync(kFull, k_next, 0);
+        // position k is a decode piece when k = i * stride + stride - 1 with i < D
+        const uint32_t q = k / stride, in_step = k - q * stride;
+        const bool dec = D > 0 && q < D && in_step == stride - 1;
+        int si;
+        uint32_t u, piece = 0;
+        if (dec) {
+            si = dslot;
+            u = q / kDecodeSub;
+            piece = q % kDecodeSub;
+        } else {
+            u = k - min(q, D);   // the hop tasks before k: k minus the pieces before it
+            si = 0;
+            while (si == dslot || u >= (uint32_t)geo[si].units) {
+                if (si != dslot) u -= (uint32_t)geo[si].units;
+                ++si;
+            }
+        }
+        const BucketSlot &S = P.slot[si];
+        const SlotGeom &g = geo[si];
+        int c = 0;
+        while (c + 1 < N && (int32_t)u >= g.ub[c + 1][0]) ++c;
+        int seg = 0;
+        while (seg < 2 && (int32_t)u >= g.ub[c][seg + 1]) ++seg;
+        const int32_t a = g.lo[c], b = g.lo[c + 1];
+        const int32_t c2 = max(a, min(b, g.end2)), c4 = max(a, min(b, g.end4));   // the segments' cuts
+        const int32_t seg_lo = seg == 0 ? a : (seg == 1 ? c2 : c4), seg_hi = seg == 0 ? c2 : (seg == 1 ? c4 : b);
+        const int32_t j0 = seg_lo + ((int32_t)u - g.ub[c][seg]) * kUnit + (int32_t)piece * (kUnit / kDecodeSub);
+        const int32_t len = dec ? kUnit / kDecodeSub : kUnit;
+        const int32_t rem = seg_hi - j0;
+        if (rem <= 0) continue;   // a piece past the end of a short unit
+        const int cnt = rem < len ? rem : len;
+        if (dec) {
+            const MsgView m = chunk_view(S.msgs + ((int64_t)c * N + (N - 1)) * S.msg_stride, a, b, g.end2, g.end4, SF32);
+            if (seg == 0) decode_unit_rows<2, SF32>(S, m, a, j0, cnt, lane, rows);
+            else if (seg == 1) decode_unit_rows<4, SF32>(S, m, a, j0, cnt, lane, rows);
+            else decode_unit_rows<8, SF32>(S, m, a, j0, cnt, lane, rows);
+            continue;
+        }
+        const int step = S.step;
+        const int r = (c + 1 + step) % N, src = (r - 1 + N) % N;
+        HopTask t;
+        t.in = chunk_view(step > 0 ? S.msgs + ((int64_t)src * N + (step - 1)) * S.msg_stride : nullptr, a, b, g.end2,
+                          g.end4, SF32);
+        t.out = chunk_view(S.msgs + ((int64_t)r * N + step) * S.msg_stride, a, b, g.end2, g.end4, SF32);
+        t.addend = S.grads[r];
+        t.keep_out = nullptr;
+        t.in_lo = a;
+        t.send_lo = a;
+        t.send_hi = b;
+        t.keep_lo = t.keep_hi = b;
+        t.stage_word = (uint32_t)step | (P.correlated ? 0xFFFF0000u : ((uint32_t)r << 16));
+        t.corr2 = 0u;   // one quantizer per ring stage: stratum offset 0
+        if (step == 0) {
+            if (seg == 0) hop_unit<2, false, false, ONE_LEVEL, SF32, false>(S, t, stg, j0, cnt, lane);
+            else if (seg == 1) hop_unit<4, false, false, ONE_LEVEL, SF32, false>(S, t, stg, j0, cnt, lane);
+            else hop_unit<8, false, false, ONE_LEVEL, SF32, false>(S, t, stg, j0, cnt, lane);
+        } else {
+            if (seg == 0) hop_unit<2, true, false, ONE_LEVEL, SF32, false>(S, t, stg, j0, cnt, lane);
+            else if (seg == 1) hop_unit<4, true, false, ONE_LEVEL, SF32, false>(S, t, stg, j0, cnt, lane);
+            else hop_unit<8, true, false, ONE_LEVEL, SF32, false>(S, t, stg, j0, cnt, lane);
+        }
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // the decode's copies
+}
+
 // Opts a kernel in to `dyn` bytes of dynamic shared memory (needed once its
 // static plus dynamic shared memory passes 48 KB), once per device; `done`
 // is the caller's per-kernel record.
@@ -1249,6 +1424,46 @@ cudaError_t launch_wave_t(const WaveRingParams &P, int64_t units, cudaStream_t s
 }
 
 }  // namespace
+
+namespace {
+
+template <bool ONE_LEVEL, bool SF32>
+cudaError_t launch_stream_t(const StreamRingParams &P, int64_t tasks, cudaStream_t st, int free_sms)
+{
+    const size_t dyn = (size_t)tab_bytes(false) + (size_t)kWarps * kStages * stage_bytes<false, SF32>() +
+                       (size_t)kWarps * 2 * kRowBytes;
+    auto k = stream_ring_kernel<ONE_LEVEL, SF32>;
+    static bool opted[128] = {false};   // one record per instantiation of this launcher
+    const cudaError_t e = allow_dyn_smem(k, dyn, opted);
+    if (e != cudaSuccess) return e;
+    const int wpb = hop_block_warps(tasks);
+    cudaLaunchConfig_t cfg = {};
+    // one block per SM; free_sms SMs are left to other streams' kernels
+    cfg.gridDim = dim3((unsigned)std::max(1, std::min(grid_for(k, wpb, dyn, tasks), sm_count() - free_sms)));
+    cfg.blockDim = dim3((unsigned)(wpb * 32));
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t el = cudaLaunchKernelEx(&cfg, k, P);
+    note_launches(1);
+    return el != cudaSuccess ? el : cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_stream_ring(const StreamRingParams &P, int64_t tasks_hint, cudaStream_t st, int free_sms)
+{
+    const bool one = P.tab.one_level != 0;
+    if (P.scale_fp32)
+        return one ? launch_stream_t<true, true>(P, tasks_hint, st, free_sms)
+                   : launch_stream_t<false, true>(P, tasks_hint, st, free_sms);
+    return one ? launch_stream_t<true, false>(P, tasks_hint, st, free_sms)
+               : launch_stream_t<false, false>(P, tasks_hint, st, free_sms);
+}
 
 cudaError_t launch_wave_ring(const WaveRingParams &P, cudaStream_t st)
 {

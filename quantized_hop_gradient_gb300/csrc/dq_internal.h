@@ -32,6 +32,9 @@ cudaError_t launch_barrier_selftest(int32_t n_blocks, int32_t missing, long long
                                     unsigned int *counter, int32_t *status, cudaStream_t st);
 // One launch of the pipelined ring exchange (ordinary launch).
 cudaError_t launch_wave_ring(const WaveRingParams &P, cudaStream_t st);
+// One launch of the bucket stream; tasks_hint sizes the grid (the exact
+// task count is known only on the device), free_sms SMs are left free.
+cudaError_t launch_stream_ring(const StreamRingParams &P, int64_t tasks_hint, cudaStream_t st, int free_sms = 0);
 
 // Allocation (radix select of T) and reordering; ws is device scratch.
 constexpr int kReorderTile = 2048;   // super-groups per reorder tile (4 int64 of scratch each)

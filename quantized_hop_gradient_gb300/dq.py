@@ -60,6 +60,8 @@ class dq_launch_log(C.Structure):
 
 DQ_LAUNCH_COMPRESS, DQ_LAUNCH_DAR, DQ_LAUNCH_DECODE, DQ_LAUNCH_STATS, DQ_LAUNCH_ALLOCATE_REORDER = 0, 1, 2, 3, 4
 DQ_LAUNCH_MX_HOP, DQ_LAUNCH_MX_DECODE, DQ_LAUNCH_FUSED_RING, DQ_LAUNCH_PIPELINED = 5, 6, 7, 8
+DQ_LAUNCH_STREAM = 9
+MAX_STREAM_RANKS = 8   # dq_exchange_stream_step: rings of up to 8 ranks
 DQ_DEVICE_OK, DQ_DEVICE_BARRIER_TIMEOUT = 0, 1
 MAX_FUSED_RANKS = 64
 MAX_WAVE_PARTS = 256   # dq_exchange_pipelined cuts n_parts to this
@@ -68,6 +70,21 @@ UNIT = 32              # super-groups per work unit of the kernels
 
 class dq_plan_info(C.Structure):
     _fields_ = [("T", C.c_float), ("n2", C.c_int64), ("n4", C.c_int64), ("n8", C.c_int64)]
+
+
+class dq_bucket(C.Structure):
+    _fields_ = [("n_sg", C.c_int64), ("grads_host", C.c_void_p), ("outs_host", C.c_void_p), ("round", C.c_uint64)]
+
+
+class dq_stream_set(C.Structure):
+    _fields_ = [("mu", C.c_void_p), ("perm", C.c_void_p), ("plan_ws", C.c_void_p), ("plan_ws_bytes", C.c_size_t),
+                ("msgs", C.c_void_p), ("msgs_bytes", C.c_size_t)]
+
+
+class dq_bucket_step(C.Structure):
+    _fields_ = [("n_sg", C.c_int64), ("counts_dev", C.c_void_p), ("grads_host", C.c_void_p),
+                ("outs_host", C.c_void_p), ("mu", C.c_void_p), ("perm", C.c_void_p), ("msgs", C.c_void_p),
+                ("msgs_bytes", C.c_size_t), ("round", C.c_uint64), ("step", C.c_int32)]
 
 
 _SIGS = {
@@ -111,6 +128,13 @@ _SIGS = {
     "dq_exchange_pipelined": ([C.POINTER(dq_config), C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
                                C.POINTER(dq_plan_info), C.c_void_p, C.c_size_t, C.c_void_p, C.c_int32, C.c_int32,
                                C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+    "dq_plan_async": ([C.POINTER(dq_config), C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p,
+                       C.c_size_t, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+    "dq_bucket_msgs_bytes": ([C.POINTER(dq_config), C.c_int64], C.c_size_t),
+    "dq_allreduce_stream": ([C.POINTER(dq_config), C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_int32,
+                             C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+    "dq_exchange_stream_step": ([C.POINTER(dq_config), C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p,
+                                 C.c_void_p], C.c_int),
     "dq_barrier_selftest": ([C.c_int32, C.c_int32, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "dq_mx_message_bytes": ([C.c_int64], C.c_size_t),
     "dq_mx_quantize": ([C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p], C.c_int),
@@ -277,6 +301,47 @@ def dq_plan(cfg, grads, n_sg, mu, perm, ws, ws_bytes, log=None, stream=None, rea
                          ws_bytes, C.byref(info), C.cast(ev, C.c_void_p) if ev is not None else None,
                          C.byref(log.c) if log is not None else None, _stream(stream)), "dq_plan")
     return info
+
+
+def dq_plan_async(cfg, grads, n_sg, mu, perm, ws, ws_bytes, log=None, stream=None, ready=None):
+    """dq_plan without the readback or the sync.  Returns the device
+    addresses (ints) of the plan's three int64 counts and of its non-finite
+    flag."""
+    ptrs = (C.c_void_p * len(grads))(*[_ptr(g) for g in grads])
+    ev = None
+    if ready is not None:
+        ev = (C.c_void_p * len(grads))(*[(e.cuda_event if e is not None else None) for e in ready])
+    counts, nonfinite = C.c_void_p(), C.c_void_p()
+    _check(lib().dq_plan_async(C.byref(cfg), C.cast(ptrs, C.c_void_p), n_sg, _ptr(mu), _ptr(perm), _ptr(ws),
+                               ws_bytes, C.byref(counts), C.byref(nonfinite),
+                               C.cast(ev, C.c_void_p) if ev is not None else None,
+                               C.byref(log.c) if log is not None else None, _stream(stream)), "dq_plan_async")
+    return counts.value, nonfinite.value
+
+
+def dq_bucket_msgs_bytes(cfg, n_sg) -> int:
+    return lib().dq_bucket_msgs_bytes(C.byref(cfg), n_sg)
+
+
+def dq_allreduce_stream(cfg, buckets, sets, counters, out_is_bf16=False, plan_stream=None, stream=None,
+                        log: "LaunchLog" = None, lookahead: int = 1, plan_sms: int = 0):
+    """A whole bucket stream in one call.  ``buckets``: a ctypes array of
+    dq_bucket; ``sets``: a ctypes array of dq_stream_set; ``counters``: a
+    device int32 tensor of at least len(buckets) + N words."""
+    _check(lib().dq_allreduce_stream(C.byref(cfg), C.cast(buckets, C.c_void_p), len(buckets),
+                                     C.cast(sets, C.c_void_p), len(sets), int(lookahead), int(plan_sms),
+                                     _ptr(counters), int(out_is_bf16),
+                                     _stream(plan_stream) if plan_stream is not None else None, _stream(stream),
+                                     C.byref(log.c) if log is not None else None), "dq_allreduce_stream")
+
+
+def dq_exchange_stream_step(cfg, steps, counter, out_is_bf16=False, log: "LaunchLog" = None, stream=None):
+    """One launch of the bucket stream.  ``steps``: a ctypes array of
+    dq_bucket_step; ``counter``: a device uint32 (tensor or address), zero at
+    the launch."""
+    _check(lib().dq_exchange_stream_step(C.byref(cfg), C.cast(steps, C.c_void_p), len(steps), _ptr(counter),
+                                         int(out_is_bf16), C.byref(log.c) if log is not None else None,
+                                         _stream(stream)), "dq_exchange_stream_step")
 
 
 def dq_exchange_workspace_bytes(cfg, butterfly, n_sg, info) -> int:

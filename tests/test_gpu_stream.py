@@ -1,13 +1,15 @@
 """The bucketed (DDP-style) all-reduce: every bucket's result equals the
 oracle's all-reduce of that bucket (bit for bit), with and without the
-two-stream overlap, including a short last bucket."""
+two-stream overlap, including a short last bucket; and the same for the
+bucket stream whose ring exchange is pipelined across buckets
+(dq_exchange_stream_step), with more buckets than buffer sets."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from quantized_hop_gradient_gb300 import build, synth
-from quantized_hop_gradient_gb300.stream import BucketedAllReduce
+from quantized_hop_gradient_gb300.stream import BucketedAllReduce, BucketStream
 
 pytestmark = pytest.mark.gpu
 
@@ -78,3 +80,97 @@ def test_buckets_uploaded_through_hooks_match_oracle(fused):
         assert np.array_equal(res[k].numpy().view(np.int32), exp.view(np.int32)), k
         for r in range(N):
             assert np.array_equal(outs[k][r].cpu().numpy().view(np.int32), exp.view(np.int32)), (k, r)
+
+
+@pytest.mark.parametrize("lookahead,plan_sms", [(3, -1), (1, 0), (2, 16)])
+@pytest.mark.parametrize("N,n_full", [(1, 3), (2, 5), (4, 9), (8, 13)])
+def test_bucket_stream_matches_oracle(N, n_full, lookahead, plan_sms):
+    """Every bucket of the cross-bucket pipelined stream equals the oracle's
+    all-reduce of that bucket, bit for bit: outputs of every rank, with a
+    short last bucket and more buckets than the stream's buffer sets."""
+    build.build()
+    bucket_sg = 37
+    w = synth.WORKLOADS["llama3_8b_ring8_buckets"]
+    w = w.__class__(**{**w.__dict__, "n_ranks": N, "n": 256 * (n_full * bucket_sg + 11), "bucket": 256 * bucket_sg})
+    nb = synth.bucket_count(w)
+    buckets = [synth.generate_bucket(w, k, "cuda", seed=3) for k in range(nb)]
+    outs = [[torch.empty(g.numel(), dtype=torch.float32, device="cuda") for g in b] for b in buckets]
+    bs = BucketStream(N, bucket_sg, budget=5.0, correlated=True, lookahead=lookahead, plan_sms=plan_sms)
+    assert nb > bs.depth or N < 8
+    bs.run(buckets, outs, round0=30)
+    torch.cuda.synchronize()
+    for k, b in enumerate(buckets):
+        gu = [synth.as_u16(g) for g in b]
+        _, exp = oracle.allreduce(oracle.Config(N, 5.0, correlated=True, round=30 + k), gu)
+        for r in range(N):
+            assert np.array_equal(outs[k][r].cpu().numpy().view(np.int32), exp.view(np.int32)), (k, r)
+
+
+@pytest.mark.parametrize("kw", [dict(eps=0.3), dict(scale_fp32=True), dict(fixed_bits=4, budget=4.0),
+                                dict(out_dtype=torch.bfloat16)])
+def test_bucket_stream_modes_match_per_bucket_rounds(kw):
+    """The stream in every mode equals one DynamiQ round per bucket through
+    the per-step exchange (itself pinned to the oracle), bit for bit."""
+    build.build()
+    N, bucket_sg = 4, 53
+    w = synth.WORKLOADS["llama3_8b_ring8_buckets"]
+    w = w.__class__(**{**w.__dict__, "n_ranks": N, "n": 256 * (6 * bucket_sg + 5), "bucket": 256 * bucket_sg})
+    nb = synth.bucket_count(w)
+    buckets = [synth.generate_bucket(w, k, "cuda", seed=4) for k in range(nb)]
+    dt = kw.get("out_dtype", torch.float32)
+    outs = [[torch.empty(g.numel(), dtype=dt, device="cuda") for g in b] for b in buckets]
+    BucketStream(N, bucket_sg, seed=2, **kw).run(buckets, outs, round0=7)
+    torch.cuda.synchronize()
+    from quantized_hop_gradient_gb300.allreduce import DynamiQAllReduce
+    for k, b in enumerate(buckets):
+        J = b[0].numel() // 256
+        ar = DynamiQAllReduce(N, J, seed=2, **kw)
+        exp = ar(b, round=7 + k, fused=False)
+        torch.cuda.synchronize()
+        for r in range(N):
+            bits = torch.int16 if dt == torch.bfloat16 else torch.int32
+            assert torch.equal(outs[k][r].view(bits), exp[r].view(bits)), (k, r)
+
+
+def test_bucket_stream_uploaded_through_hooks_matches_oracle():
+    """The stream as the end-to-end benchmark drives it: every bucket's
+    gradients come from pinned host memory into one of `depth` staging sets
+    on a copy stream, enqueued by the planning hook and waited on through
+    per-rank ready events; rank 0's result goes back to the host after each
+    bucket's decode.  Results equal the oracle's."""
+    build.build()
+    N, bucket_sg = 4, 29
+    w = synth.WORKLOADS["llama3_8b_ring8_buckets"]
+    w = w.__class__(**{**w.__dict__, "n_ranks": N, "n": 256 * (11 * bucket_sg + 7), "bucket": 256 * bucket_sg})
+    nb = synth.bucket_count(w)
+    buckets = [synth.generate_bucket(w, k, "cpu", seed=6) for k in range(nb)]
+    hosts = [[g.pin_memory() for g in b] for b in buckets]
+    bs = BucketStream(N, bucket_sg, budget=5.0, correlated=True)
+    stage = [[torch.empty(256 * bucket_sg, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+             for _ in range(bs.depth)]
+    bufs = [[s[:g.numel()] for s, g in zip(stage[k % bs.depth], buckets[k])] for k in range(nb)]
+    outs = [[torch.empty(g.numel(), dtype=torch.float32, device="cuda") for g in b] for b in buckets]
+    res = [torch.empty(g[0].numel(), dtype=torch.float32, pin_memory=True) for g in buckets]
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    ready = [[torch.cuda.Event() for _ in range(N)] for _ in range(nb)]
+    done = [torch.cuda.Event() for _ in range(nb)]
+
+    def before_plan(k, side):
+        cin.wait_stream(side)
+        with torch.cuda.stream(cin):
+            for r in range(N):
+                bufs[k][r].copy_(hosts[k][r], non_blocking=True)
+                ready[k][r].record(cin)
+
+    def after_exchange(k, main):
+        done[k].record(main)
+        cout.wait_event(done[k])
+        with torch.cuda.stream(cout):
+            res[k].copy_(outs[k][0], non_blocking=True)
+
+    bs.run(bufs, outs, round0=40, ready=ready, before_plan=before_plan, after_exchange=after_exchange)
+    torch.cuda.synchronize()
+    for k in range(nb):
+        gu = [synth.as_u16(g) for g in buckets[k]]
+        _, exp = oracle.allreduce(oracle.Config(N, 5.0, correlated=True, round=40 + k), gu)
+        assert np.array_equal(res[k].numpy().view(np.int32), exp.view(np.int32)), k
