@@ -307,3 +307,21 @@ def test_plan_single_block_and_multi_kernel_paths(J, B):
     assert bits32(np.array([info.T], np.float32))[0] == bits32(np.array([p.T], np.float32))[0]
     assert np.array_equal(host(ar.perm), p.perm)
     assert np.array_equal(bits32(host(ar.mu)), bits32(p.M / np.float32(N)))
+
+
+@pytest.mark.parametrize("N", [2, 8, 16, 32])
+def test_butterfly_decode_outputs_match_fp32_rounded(N):
+    """The butterfly's outputs, fp32 and bf16, in every rank equal: bf16 is
+    the fp32 result rounded to nearest-even (one decode launch per 16
+    outputs: 32 ranks take two)."""
+    _, gr = grads_for("llama1b_butterfly8", 256 * 900 + 31, N, seed=N)
+    J = gr[0].size // 256
+    gd = [dev_u16(g) for g in gr]
+    res = {}
+    for dt in (torch.float32, torch.bfloat16):
+        ar = DynamiQAllReduce(N, J, budget=5.0, correlated=True, butterfly=True, seed=4, out_dtype=dt)
+        res[dt] = [o.clone() for o in ar(gd, round=3)]
+    torch.cuda.synchronize()
+    for a, b in zip(res[torch.float32], res[torch.bfloat16]):
+        assert torch.equal(a.to(torch.bfloat16).view(torch.int16), b.view(torch.int16))
+        assert torch.equal(a.view(torch.int32), res[torch.float32][0].view(torch.int32))
