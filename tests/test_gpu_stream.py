@@ -174,3 +174,23 @@ def test_bucket_stream_uploaded_through_hooks_matches_oracle():
         gu = [synth.as_u16(g) for g in buckets[k]]
         _, exp = oracle.allreduce(oracle.Config(N, 5.0, correlated=True, round=40 + k), gu)
         assert np.array_equal(res[k].numpy().view(np.int32), exp.view(np.int32)), k
+
+
+def test_bucket_stream_large_buckets_match_oracle():
+    """Buckets above 16,384 super-groups (planned by the multi-kernel
+    allocation and reorder, not the single-block one): every bucket equals
+    the oracle's all-reduce of it, bit for bit."""
+    build.build()
+    N, bucket_sg = 2, 20000
+    w = synth.WORKLOADS["llama3_8b_ring8_buckets"]
+    w = w.__class__(**{**w.__dict__, "n_ranks": N, "n": 256 * (2 * bucket_sg + 999), "bucket": 256 * bucket_sg})
+    nb = synth.bucket_count(w)
+    buckets = [synth.generate_bucket(w, k, "cuda", seed=8) for k in range(nb)]
+    outs = [[torch.empty(g.numel(), dtype=torch.float32, device="cuda") for g in b] for b in buckets]
+    BucketStream(N, bucket_sg, budget=5.0, correlated=True).run(buckets, outs, round0=50)
+    torch.cuda.synchronize()
+    for k, b in enumerate(buckets):
+        gu = [synth.as_u16(g) for g in b]
+        _, exp = oracle.allreduce(oracle.Config(N, 5.0, correlated=True, round=50 + k), gu)
+        for r in range(N):
+            assert np.array_equal(outs[k][r].cpu().numpy().view(np.int32), exp.view(np.int32)), (k, r)
