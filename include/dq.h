@@ -234,7 +234,7 @@ dq_status dq_decode(const dq_config *cfg, dq_range r, const uint8_t *msg, const 
 
 /* Result of the planning phase, filled by dq_plan. */
 typedef struct {
-    float   T;            /* the threshold T_{2,4} */
+    float   T;            /* the threshold T_{2,4}; NaN when fixed_bits is set */
     int64_t n2, n4, n8;   /* SGs per bitwidth */
 } dq_plan_info;
 

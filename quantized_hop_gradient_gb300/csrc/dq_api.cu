@@ -717,15 +717,6 @@ struct PlanDev {
     int32_t *nonfinite;
 };
 
-__global__ void set_counts_kernel(int64_t *counts, int64_t n2, int64_t n4, int64_t n8)
-{
-    if (threadIdx.x == 0) {
-        counts[0] = n2;
-        counts[1] = n4;
-        counts[2] = n8;
-    }
-}
-
 // Enqueues the whole plan (statistics, reduce, allocation, reorder) on st;
 // nothing is read back.
 dq_status plan_enqueue(const dq_config *cfg, const void *const *grads, int64_t n_sg, float *mu, int32_t *perm,
@@ -753,7 +744,9 @@ dq_status plan_enqueue(const dq_config *cfg, const void *const *grads, int64_t n
     int32_t *nonfinite = reinterpret_cast<int32_t *>(w + L.counts + 32);   // inside the counts slot
     void *scratch = w + L.scratch;
     out = PlanDev{counts, T, nonfinite};
-    if (zero_words(nonfinite, 1, nullptr, st) != cudaSuccess) return DQ_ERR_CUDA;
+    const bool small = n_sg <= small_plan_max_sg();
+    // the flag is cleared before the statistics reduce sets it (the chain clears it itself)
+    if (small && zero_words(nonfinite, 1, nullptr, st) != cudaSuccess) return DQ_ERR_CUDA;
     if (rank_ready) {  // one launch per rank, each after its rank's event
         for (int32_t r = 0; r < N; ++r) {
             if (rank_ready[r] && cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(rank_ready[r]), 0) != cudaSuccess)
@@ -779,32 +772,17 @@ dq_status plan_enqueue(const dq_config *cfg, const void *const *grads, int64_t n
             if (e != cudaSuccess) return DQ_ERR_CUDA;
         }
     }
+    const int64_t cap = (int64_t)floor((double)cfg->budget_bits * (double)n_sg);
     const LogSlot slot = log_begin(log, DQ_LAUNCH_ALLOCATE_REORDER, n_sg, st);
-    if (launch_stats_reduce(mean_all, sq_all, N, n_sg, M, F, mu, st, nonfinite) != cudaSuccess) return DQ_ERR_CUDA;
-    if (n_sg <= small_plan_max_sg()) {
-        // small problems: allocation and reorder in one launch
-        const int64_t cap = (int64_t)floor((double)cfg->budget_bits * (double)n_sg);
+    if (small) {
+        // small problems: the metadata all-reduce, then allocation and reorder in one launch
+        if (launch_stats_reduce(mean_all, sq_all, N, n_sg, M, F, mu, st, nonfinite) != cudaSuccess) return DQ_ERR_CUDA;
         if (launch_plan_small(F, n_sg, cap, cfg->fixed_bits, b, T, counts, perm, st) != cudaSuccess)
             return DQ_ERR_CUDA;
-        log_end(slot, st);
-        return DQ_OK;
+    } else if (launch_plan_chain(mean_all, sq_all, N, n_sg, cap, cfg->fixed_bits, M, F, mu, nonfinite, b, T, counts,
+                                 perm, scratch, st) != cudaSuccess) {
+        return DQ_ERR_CUDA;
     }
-    if (cfg->fixed_bits) {
-        // uniform-bitwidth ablation: every super-group gets fixed_bits (the
-        // reorder of a uniform allocation is the identity permutation)
-        if (cudaMemsetAsync(b, cfg->fixed_bits, (size_t)n_sg, st) != cudaSuccess) return DQ_ERR_CUDA;
-        const dq_status s = dq_reorder(b, n_sg, perm, scratch, plan_scratch_bytes(n_sg), st);
-        if (s != DQ_OK) return s;
-        log_end(slot, st);
-        const int32_t f = cfg->fixed_bits;
-        set_counts_kernel<<<1, 32, 0, st>>>(counts, f == 2 ? n_sg : 0, f == 4 ? n_sg : 0, f == 8 ? n_sg : 0);
-        note_launches(1);
-        return cuda_status(cudaGetLastError());
-    }
-    dq_status s = dq_allocate(F, n_sg, cfg->budget_bits, b, T, counts, scratch, plan_scratch_bytes(n_sg), st);
-    if (s != DQ_OK) return s;
-    s = dq_reorder(b, n_sg, perm, scratch, plan_scratch_bytes(n_sg), st);
-    if (s != DQ_OK) return s;
     log_end(slot, st);
     return DQ_OK;
 }

@@ -43,6 +43,14 @@ size_t reorder_scratch_bytes(int64_t n_sg);   // bytes of ws that launch_reorder
 cudaError_t launch_allocate(const float *F, int64_t n_sg, int64_t cap_bits, uint8_t *b, float *T,
                             int64_t *counts, void *ws, cudaStream_t st);
 cudaError_t launch_reorder(const uint8_t *b, int64_t n_sg, int32_t *perm, void *ws, cudaStream_t st);
+// The planning after the statistics, for any size: metadata all-reduce
+// (M, F, mu from the ranks' per-super-group statistics), allocation and
+// reorder in 3 + passes launches; ws holds plan_scratch_bytes(n_sg).
+// fixed_bits != 0 gives every super-group that width.
+cudaError_t launch_plan_chain(const float *mean_all, const float *sq_all, int32_t n_ranks, int64_t n_sg,
+                              int64_t cap_bits, int32_t fixed_bits, float *M, float *F, float *mu,
+                              int32_t *nonfinite, uint8_t *b, float *T, int64_t *counts, int32_t *perm, void *ws,
+                              cudaStream_t st);
 // allocation and reorder of up to small_plan_max_sg() super-groups in one launch
 int64_t small_plan_max_sg();
 cudaError_t launch_plan_small(const float *F, int64_t n_sg, int64_t cap_bits, int32_t fixed_bits, uint8_t *b,

@@ -10,10 +10,15 @@
 // are W(t) = 2 #{key4 >= t} + 4 #{key8 >= t}, non-increasing in t.  The
 // smallest t with W(t) <= R = floor(B J) - 2J is v + 1, where v is the
 // largest key at which the weight of keys >= v first exceeds R: a weighted
-// radix select over the 2J keys, four passes of 8-bit digits from the top.
+// radix select over the 2J keys, three passes of 11-, 11- and 10-bit digits
+// from the top.  Each pass is one launch: every block adds its histogram to
+// a global one, and the block that arrives last picks the digit (no block
+// waits for another).
 //
 // Reordering.  A stable counting sort of the super-groups by bitwidth
 // (2, 4, 8): per-tile counts, one scan over tiles, then a stable scatter.
+// In the planning chain the bitwidths and the per-tile counts come from one
+// launch whose last block also scans the tiles.
 #include <mutex>
 
 #include "dq_common.cuh"
@@ -27,115 +32,194 @@ constexpr int kAllocThreads = 256;
 constexpr int kTile = kReorderTile;    // super-groups per reorder tile
 constexpr int kTileThreads = 256;      // 8 super-groups per thread
 constexpr int64_t kSmallPlanMaxSG = 16384;   // single-block plan: F in 64 KB of shared memory; above this the multi-kernel path is faster
+constexpr int kBins = 2048;            // digits of up to 11 bits
+constexpr int kSelectPasses = 3;
+
+// first bit and width mask of the digit of each pass (bits 21..31, 10..20, 0..9)
+__host__ __device__ constexpr int digit_shift(int pass) { return pass == 0 ? 21 : (pass == 1 ? 10 : 0); }
+__host__ __device__ constexpr uint32_t digit_mask(int pass) { return pass == 2 ? 1023u : 2047u; }
 
 struct AllocState {
-    unsigned long long hist[256];
+    unsigned int hist[kBins];          // weights by digit of the current pass (zero between passes)
     long long above;                   // weight of keys above the current prefix
     long long R;                       // remaining budget of extra code bits
     uint32_t prefix;                   // determined high digits of v
     uint32_t t;                        // final threshold bit pattern
     int32_t all8;                      // 1: budget >= 8 bits, T = 0
-    int32_t pad_;
+    unsigned int arrived;              // blocks of the current launch that have finished their part
 };
+constexpr size_t kAllocStateBytes = (sizeof(AllocState) + 255) / 256 * 256;
 
 __device__ __forceinline__ uint32_t key4_of(float F) { return __float_as_uint(F); }
 __device__ __forceinline__ uint32_t key8_of(float F) { return __float_as_uint(__fmul_rd(F, 0.033203125f)); }
 
-__global__ void alloc_init_kernel(AllocState *st, long long R, int all8, int64_t *counts)
+// Bin of a key in pass `pass` (kBins: not in this pass, its higher digits
+// differ from the prefix found so far).
+__device__ __forceinline__ uint32_t bin_of(uint32_t key, uint32_t prefix, int pass)
 {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) st->hist[i] = 0ull;
+    const int shift = digit_shift(pass);
+    if (pass > 0) {
+        const int hs = digit_shift(pass - 1);
+        if ((key >> hs) != (prefix >> hs)) return (uint32_t)kBins;
+    }
+    return (key >> shift) & digit_mask(pass);
+}
+
+__global__ void alloc_init_kernel(AllocState *st, long long R, int all8, int64_t *counts, int32_t *flag)
+{
+    for (int i = threadIdx.x; i < kBins; i += blockDim.x) st->hist[i] = 0u;
     if (threadIdx.x == 0) {
         st->above = 0;
         st->R = R;
         st->prefix = 0u;
         st->t = 0u;
         st->all8 = all8;
-        counts[0] = counts[1] = counts[2] = 0;
+        st->arrived = 0u;
+        if (counts) counts[0] = counts[1] = counts[2] = 0;
+        if (flag) *flag = 0;
     }
 }
 
-// Histogram (by the digit at `pass`) of the weights of keys whose higher
-// digits equal the prefix found so far.
-__global__ void __launch_bounds__(kAllocThreads) alloc_hist_kernel(const float *__restrict__ F, int64_t n,
-                                                                   AllocState *st, int pass)
+// Called by the last block of a pass: the largest digit d with
+// above + sum_{d' >= d} hist[d'] > R becomes the pass's digit of v; the
+// histogram and the arrival count are cleared for the next pass.  Thread i
+// owns bins 8i .. 8i+7 (blockDim = kAllocThreads).
+__device__ void select_digit(AllocState *st, int pass)
 {
-    __shared__ unsigned int h[256];
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0u;
+    static_assert(kAllocThreads * 8 == kBins, "8 bins per thread");
+    __shared__ long long warp_tot[kAllocThreads / 32];
+    __shared__ int dstar;
+    __shared__ long long dhigher;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    unsigned int h[8];
+    long long loc = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        h[i] = __ldcg(&st->hist[8 * tid + i]);
+        loc += h[i];
+    }
+    // weight of the bins of this thread and every thread above it
+    long long incl = loc;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long o = __shfl_down_sync(kFull, incl, off);
+        if (lane + off < 32) incl += o;
+    }
+    if (lane == 0) warp_tot[wid] = incl;
+    if (tid == 0) dstar = -1;
     __syncthreads();
-    if (!st->all8) {
-        const uint32_t prefix = st->prefix;
-        const int shift = 24 - 8 * pass;
-        const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-        for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n; j += stride) {
-            const float f = __ldg(F + j);
-            const uint32_t k4 = key4_of(f), k8 = key8_of(f);
-            if (pass == 0 || (k4 >> (shift + 8)) == (prefix >> (shift + 8)))
-                atomicAdd(&h[(k4 >> shift) & 255u], 2u);
-            if (pass == 0 || (k8 >> (shift + 8)) == (prefix >> (shift + 8)))
-                atomicAdd(&h[(k8 >> shift) & 255u], 4u);
+    for (int w = wid + 1; w < kAllocThreads / 32; ++w) incl += warp_tot[w];
+    const long long above = __ldcg(&st->above), R = __ldcg(&st->R);
+    long long gt = incl - loc;   // weight of the bins above 8*tid + i
+    int best = -1;
+    long long best_gt = 0;
+#pragma unroll
+    for (int i = 7; i >= 0; --i) {
+        if (best < 0 && above + gt + (long long)h[i] > R) {
+            best = 8 * tid + i;
+            best_gt = gt;
+        }
+        gt += h[i];
+    }
+    if (best >= 0) atomicMax(&dstar, best);
+    __syncthreads();
+    if (best >= 0 && best == dstar) dhigher = best_gt;
+    if (tid == 0 && dstar < 0) dhigher = incl - (long long)h[0];   // no digit qualifies: d = 0 (cannot happen unless all8)
+    __syncthreads();
+    if (tid == 0) {
+        const int d = dstar < 0 ? 0 : dstar;
+        st->above = above + dhigher;
+        const uint32_t prefix = __ldcg(&st->prefix) | ((uint32_t)d << digit_shift(pass));
+        st->prefix = prefix;
+        if (pass == kSelectPasses - 1) st->t = prefix + 1u;
+        st->arrived = 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) st->hist[8 * tid + i] = 0u;
+}
+
+// One pass of the select: the weighted histogram (by the digit at `pass`) of
+// the keys whose higher digits equal the prefix, added into the global one;
+// the last block to finish picks the digit.  REDUCE (pass 0 of the planning
+// chain): F is first computed from the ranks' per-super-group statistics,
+// as the metadata all-reduce does (M_j, F_j summed over ranks 0..N-1 in
+// order, mu_j = fl(M_j / N)), and written with M and mu.  hist = false
+// (REDUCE only: budget >= 8 bits or a fixed bitwidth) skips the histogram.
+template <bool REDUCE>
+__global__ void __launch_bounds__(kAllocThreads) alloc_pass_kernel(const float *__restrict__ Fin, int64_t n,
+                                                                   AllocState *st, int pass, bool hist,
+                                                                   const float *__restrict__ mean_all,
+                                                                   const float *__restrict__ sq_all, int32_t n_ranks,
+                                                                   float *__restrict__ M, float *__restrict__ Fout,
+                                                                   float *__restrict__ mu,
+                                                                   int32_t *__restrict__ nonfinite)
+{
+    __shared__ unsigned int h[kBins];
+    __shared__ bool last;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const bool do_hist = hist && !st->all8;
+    if (do_hist)
+        for (int i = tid; i < kBins; i += blockDim.x) h[i] = 0u;
+    __syncthreads();
+    const uint32_t prefix = do_hist ? st->prefix : 0u;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    // whole warps run every iteration (the match below needs all 32 lanes)
+    const int64_t n_warp = (n + 31) & ~(int64_t)31;
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + tid; j < n_warp; j += stride) {
+        uint32_t b4 = (uint32_t)kBins, b8 = (uint32_t)kBins;
+        if (j < n) {
+            float f;
+            if (REDUCE) {
+                float m = mean_all[j];
+                f = sq_all[j];
+                int32_t w = 1;
+                for (; w + 4 <= n_ranks; w += 4) {   // four ranks' loads in flight, then the sums in rank order
+                    float a[4], c[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        a[k] = mean_all[(int64_t)(w + k) * n + j];
+                        c[k] = sq_all[(int64_t)(w + k) * n + j];
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        m = __fadd_rn(m, a[k]);
+                        f = __fadd_rn(f, c[k]);
+                    }
+                }
+                for (; w < n_ranks; ++w) {
+                    m = __fadd_rn(m, mean_all[(int64_t)w * n + j]);
+                    f = __fadd_rn(f, sq_all[(int64_t)w * n + j]);
+                }
+                if (M) M[j] = m;
+                Fout[j] = f;
+                mu[j] = __fdiv_rn(m, (float)n_ranks);
+                if (nonfinite && !(isfinite(m) && isfinite(f))) atomicOr(nonfinite, 1);
+            } else {
+                f = __ldg(Fin + j);
+            }
+            if (do_hist) {
+                b4 = bin_of(key4_of(f), prefix, pass);
+                b8 = bin_of(key8_of(f), prefix, pass);
+            }
+        }
+        if (do_hist) {   // the top digits are mostly the exponent: combine equal bins of a warp first
+            const unsigned p4 = __match_any_sync(kFull, b4);
+            if (b4 < (uint32_t)kBins && lane == __ffs(p4) - 1) atomicAdd(&h[b4], 2u * (unsigned)__popc(p4));
+            const unsigned p8 = __match_any_sync(kFull, b8);
+            if (b8 < (uint32_t)kBins && lane == __ffs(p8) - 1) atomicAdd(&h[b8], 4u * (unsigned)__popc(p8));
         }
     }
+    if (!do_hist) return;
     __syncthreads();
-    for (int i = threadIdx.x; i < 256; i += blockDim.x)
-        if (h[i]) atomicAdd(&st->hist[i], (unsigned long long)h[i]);
-}
-
-// Picks the digit at `pass`: the largest d with above + sum_{d' >= d} h[d'] > R.
-__global__ void __launch_bounds__(256) alloc_select_kernel(AllocState *st, int pass)
-{
-    __shared__ unsigned long long suf[256];
-    __shared__ int dstar;
-    const int d = threadIdx.x;
-    if (st->all8) return;
-    suf[d] = st->hist[d];
-    if (d == 0) dstar = -1;
+    for (int i = tid; i < kBins; i += blockDim.x)
+        if (h[i]) atomicAdd(&st->hist[i], h[i]);
+    __threadfence();
     __syncthreads();
-    // suffix sums (Hillis-Steele over 256 entries)
-    for (int off = 1; off < 256; off <<= 1) {
-        const unsigned long long v = d + off < 256 ? suf[d + off] : 0ull;
-        __syncthreads();
-        suf[d] += v;
-        __syncthreads();
-    }
-    const long long above = st->above, R = st->R;
-    if (above + (long long)suf[d] > R) atomicMax(&dstar, d);
+    if (tid == 0) last = atomicAdd(&st->arrived, 1u) == gridDim.x - 1;
     __syncthreads();
-    if (d == 0) {
-        const int ds = dstar < 0 ? 0 : dstar;
-        const unsigned long long higher = ds + 1 < 256 ? suf[ds + 1] : 0ull;
-        st->above = above + (long long)higher;
-        st->prefix |= (uint32_t)ds << (24 - 8 * pass);
-        if (pass == 3) st->t = st->prefix + 1u;
-    }
-    __syncthreads();
-    st->hist[d] = 0ull;
-}
-
-__global__ void __launch_bounds__(kAllocThreads) alloc_assign_kernel(const float *__restrict__ F, int64_t n,
-                                                                     const AllocState *st, uint8_t *__restrict__ b,
-                                                                     float *T, int64_t *counts)
-{
-    __shared__ unsigned long long cnt[3];
-    if (threadIdx.x < 3) cnt[threadIdx.x] = 0ull;
-    __syncthreads();
-    const uint32_t t = st->all8 ? 0u : st->t;
-    if (blockIdx.x == 0 && threadIdx.x == 0) *T = __uint_as_float(t);
-    unsigned int c2 = 0, c4 = 0, c8 = 0;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n; j += stride) {
-        const float f = __ldg(F + j);
-        uint8_t bits = 2;
-        if (key8_of(f) >= t) { bits = 8; ++c8; }
-        else if (key4_of(f) >= t) { bits = 4; ++c4; }
-        else ++c2;
-        b[j] = bits;
-    }
-    atomicAdd(&cnt[0], (unsigned long long)c2);
-    atomicAdd(&cnt[1], (unsigned long long)c4);
-    atomicAdd(&cnt[2], (unsigned long long)c8);
-    __syncthreads();
-    if (threadIdx.x < 3 && cnt[threadIdx.x])
-        atomicAdd(reinterpret_cast<unsigned long long *>(counts) + threadIdx.x, cnt[threadIdx.x]);
+    if (!last) return;
+    __threadfence();
+    select_digit(st, pass);
 }
 
 // --------------------------------------------------------------------------- reorder
@@ -158,18 +242,19 @@ __global__ void __launch_bounds__(kTileThreads) reorder_count_kernel(const uint8
     if (threadIdx.x < 3) tile_counts[(int64_t)blockIdx.x * 4 + threadIdx.x] = c[threadIdx.x];
 }
 
-// Exclusive scan over tiles, per class, plus the class bases: writes the
-// first output position of each (tile, class) into tile_counts[tile*4+c].
-__global__ void __launch_bounds__(1024) reorder_scan_kernel(long long *tile_counts, int64_t n_tiles)
+// Exclusive scan over tiles, per class, plus the class bases: replaces
+// tile_counts[tile*4+c] by the first output position of (tile, class) and
+// returns the class totals.  Any block size that is a multiple of 32 (up to
+// 1024); the whole block calls it.
+__device__ void scan_tiles(long long *tile_counts, int64_t n_tiles, long long (&tot)[3])
 {
-    __shared__ long long tot[3];
+    __shared__ long long s_tot[3];
     __shared__ long long warp_sum[32][3];
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    long long carry[3] = {0, 0, 0};
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = (int)(blockDim.x >> 5);
     // pass 1: class totals
     long long part[3] = {0, 0, 0};
     for (int64_t i = tid; i < n_tiles; i += blockDim.x)
-        for (int k = 0; k < 3; ++k) part[k] += tile_counts[i * 4 + k];
+        for (int k = 0; k < 3; ++k) part[k] += __ldcg(&tile_counts[i * 4 + k]);
     for (int k = 0; k < 3; ++k)
         for (int m = 16; m >= 1; m >>= 1) part[k] += __shfl_xor_sync(kFull, part[k], m);
     if (lane == 0)
@@ -178,31 +263,30 @@ __global__ void __launch_bounds__(1024) reorder_scan_kernel(long long *tile_coun
     if (tid == 0) {
         for (int k = 0; k < 3; ++k) {
             long long s = 0;
-            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += warp_sum[w][k];
-            tot[k] = s;
+            for (int w = 0; w < nw; ++w) s += warp_sum[w][k];
+            s_tot[k] = s;
         }
     }
     __syncthreads();
-    carry[0] = 0;
-    carry[1] = tot[0];
-    carry[2] = tot[0] + tot[1];
-    __syncthreads();
+    for (int k = 0; k < 3; ++k) tot[k] = s_tot[k];
+    long long carry[3] = {0, tot[0], tot[0] + tot[1]};
     // pass 2: chunked exclusive scan
     for (int64_t base = 0; base < n_tiles; base += blockDim.x) {
         const int64_t i = base + tid;
         long long v[3];
-        for (int k = 0; k < 3; ++k) v[k] = i < n_tiles ? tile_counts[i * 4 + k] : 0;
+        for (int k = 0; k < 3; ++k) v[k] = i < n_tiles ? __ldcg(&tile_counts[i * 4 + k]) : 0;
         long long inc[3] = {v[0], v[1], v[2]};
         for (int off = 1; off < 32; off <<= 1)
             for (int k = 0; k < 3; ++k) {
                 const long long o = __shfl_up_sync(kFull, inc[k], off);
                 if (lane >= off) inc[k] += o;
             }
+        __syncthreads();   // the previous chunk's reads of warp_sum are done
         if (lane == 31)
             for (int k = 0; k < 3; ++k) warp_sum[wid][k] = inc[k];
         __syncthreads();
         long long wpre[3] = {0, 0, 0}, chunk[3] = {0, 0, 0};
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
+        for (int w = 0; w < nw; ++w)
             for (int k = 0; k < 3; ++k) {
                 if (w < wid) wpre[k] += warp_sum[w][k];
                 chunk[k] += warp_sum[w][k];
@@ -210,7 +294,66 @@ __global__ void __launch_bounds__(1024) reorder_scan_kernel(long long *tile_coun
         if (i < n_tiles)
             for (int k = 0; k < 3; ++k) tile_counts[i * 4 + k] = carry[k] + wpre[k] + inc[k] - v[k];
         for (int k = 0; k < 3; ++k) carry[k] += chunk[k];
-        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(1024) reorder_scan_kernel(long long *tile_counts, int64_t n_tiles)
+{
+    long long tot[3];
+    scan_tiles(tile_counts, n_tiles, tot);
+}
+
+// Bitwidths of one tile of super-groups (from F and the threshold, or the
+// fixed width) and the tile's count per class; the block that finishes last
+// scans the tiles (the first output position of each tile and class, as
+// reorder_scan_kernel) and writes the class totals and T.
+__global__ void __launch_bounds__(kTileThreads) tile_assign_kernel(const float *__restrict__ F, int64_t n,
+                                                                   AllocState *st, int32_t fixed_bits,
+                                                                   uint8_t *__restrict__ b, long long *tile_counts,
+                                                                   int64_t *counts, float *T)
+{
+    constexpr int kPer = kTile / kTileThreads;  // 8 consecutive super-groups per thread
+    __shared__ unsigned long long warp_tot[kTileThreads / 32];
+    __shared__ bool last;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const uint32_t t = st->all8 ? 0u : st->t;
+    const int64_t base = (int64_t)blockIdx.x * kTile + (int64_t)tid * kPer;
+    unsigned long long mine = 0ull;  // packed counts: class k in bits [21k, 21k+21)
+    for (int i = 0; i < kPer; ++i) {
+        const int64_t j = base + i;
+        if (j < n) {
+            uint8_t bits;
+            if (fixed_bits) {
+                bits = (uint8_t)fixed_bits;
+            } else {
+                const float f = __ldg(F + j);
+                bits = key8_of(f) >= t ? 8 : (key4_of(f) >= t ? 4 : 2);
+            }
+            b[j] = bits;
+            mine += 1ull << (21 * class_of(bits));
+        }
+    }
+    for (int off = 16; off >= 1; off >>= 1) mine += __shfl_xor_sync(kFull, mine, off);
+    if (lane == 0) warp_tot[wid] = mine;
+    __syncthreads();
+    if (tid == 0) {
+        unsigned long long all = 0ull;
+        for (int w = 0; w < kTileThreads / 32; ++w) all += warp_tot[w];
+        for (int k = 0; k < 3; ++k) tile_counts[(int64_t)blockIdx.x * 4 + k] = (long long)((all >> (21 * k)) & 0x1FFFFFull);
+        __threadfence();
+        last = atomicAdd(&st->arrived, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    long long tot[3];
+    scan_tiles(tile_counts, (int64_t)gridDim.x, tot);
+    if (tid == 0) {
+        counts[0] = tot[0];
+        counts[1] = tot[1];
+        counts[2] = tot[2];
+        *T = __uint_as_float(t);
+        st->arrived = 0u;
     }
 }
 
@@ -248,8 +391,9 @@ __global__ void __launch_bounds__(kTileThreads) reorder_scatter_kernel(const uin
 
 // --------------------------------------------------------------------------- small problems
 // Allocation and reorder in one block, for up to kSmallPlanMaxSG super-groups
-// (F held in shared memory): the same weighted radix select and stable
-// partition as the kernels above, without their 12 launches.  Histogram
+// (F held in shared memory): a weighted radix select (four passes of 8-bit
+// digits, the threshold the chain above finds) and the same stable
+// partition, without the chain's launches.  Histogram
 // updates are combined per warp (__match_any_sync) before the shared
 // atomic, since the top digit of F is mostly its exponent and few bins
 // take most keys.  fixed_bits != 0 gives every super-group that width.
@@ -381,32 +525,34 @@ size_t reorder_scratch_bytes(int64_t n_sg)
     return (size_t)(n_tiles > 0 ? n_tiles : 1) * 4 * sizeof(long long);
 }
 
-size_t plan_scratch_bytes(int64_t n_sg)
+// [allocation state][per-tile counts]
+size_t plan_scratch_bytes(int64_t n_sg) { return kAllocStateBytes + (reorder_scratch_bytes(n_sg) + 255) / 256 * 256; }
+
+static int alloc_blocks(int64_t n_sg)
 {
-    const size_t reorder = reorder_scratch_bytes(n_sg);
-    const size_t alloc = sizeof(AllocState);
-    const size_t m = reorder > alloc ? reorder : alloc;
-    return (m + 255) / 256 * 256;
+    // about two super-groups per thread, at most eight blocks per SM
+    int64_t blocks = (n_sg + 2 * kAllocThreads - 1) / (2 * kAllocThreads);
+    const int64_t cap = (int64_t)sm_count() * 8;
+    return (int)(blocks < 1 ? 1 : (blocks < cap ? blocks : cap));
 }
 
 cudaError_t launch_allocate(const float *F, int64_t n_sg, int64_t cap_bits, uint8_t *b, float *T,
                             int64_t *counts, void *ws, cudaStream_t st)
 {
     AllocState *s = static_cast<AllocState *>(ws);
+    long long *tiles = reinterpret_cast<long long *>(static_cast<uint8_t *>(ws) + kAllocStateBytes);
     const long long R = (long long)(cap_bits - 2 * n_sg);
     const int all8 = R >= 6 * (long long)n_sg ? 1 : 0;
-    alloc_init_kernel<<<1, 256, 0, st>>>(s, R, all8, counts);
-    int64_t blocks = (n_sg + kAllocThreads - 1) / kAllocThreads;
-    const int64_t cap = (int64_t)sm_count() * 4;
-    blocks = blocks < 1 ? 1 : (blocks < cap ? blocks : cap);
+    alloc_init_kernel<<<1, 256, 0, st>>>(s, R, all8, counts, nullptr);
     if (!all8) {
-        for (int pass = 0; pass < 4; ++pass) {
-            alloc_hist_kernel<<<(int)blocks, kAllocThreads, 0, st>>>(F, n_sg, s, pass);
-            alloc_select_kernel<<<1, 256, 0, st>>>(s, pass);
-        }
+        const int blocks = alloc_blocks(n_sg);
+        for (int pass = 0; pass < kSelectPasses; ++pass)
+            alloc_pass_kernel<false><<<blocks, kAllocThreads, 0, st>>>(F, n_sg, s, pass, true, nullptr, nullptr, 0,
+                                                                       nullptr, nullptr, nullptr, nullptr);
     }
-    alloc_assign_kernel<<<(int)blocks, kAllocThreads, 0, st>>>(F, n_sg, s, b, T, counts);
-    note_launches(all8 ? 2 : 10);
+    const int64_t n_tiles = (n_sg + kTile - 1) / kTile;
+    tile_assign_kernel<<<(unsigned)n_tiles, kTileThreads, 0, st>>>(F, n_sg, s, 0, b, tiles, counts, T);
+    note_launches(all8 ? 2 : 2 + kSelectPasses);
     return cudaGetLastError();
 }
 
@@ -418,6 +564,29 @@ cudaError_t launch_reorder(const uint8_t *b, int64_t n_sg, int32_t *perm, void *
     reorder_scan_kernel<<<1, 1024, 0, st>>>(tiles, n_tiles);
     reorder_scatter_kernel<<<(int)n_tiles, kTileThreads, 0, st>>>(b, n_sg, tiles, perm);
     note_launches(3);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan_chain(const float *mean_all, const float *sq_all, int32_t n_ranks, int64_t n_sg,
+                              int64_t cap_bits, int32_t fixed_bits, float *M, float *F, float *mu,
+                              int32_t *nonfinite, uint8_t *b, float *T, int64_t *counts, int32_t *perm, void *ws,
+                              cudaStream_t st)
+{
+    AllocState *s = static_cast<AllocState *>(ws);
+    long long *tiles = reinterpret_cast<long long *>(static_cast<uint8_t *>(ws) + kAllocStateBytes);
+    const long long R = (long long)(cap_bits - 2 * n_sg);
+    const int all8 = (fixed_bits || R >= 6 * (long long)n_sg) ? 1 : 0;
+    const int blocks = alloc_blocks(n_sg);
+    const int64_t n_tiles = (n_sg + kTile - 1) / kTile;
+    alloc_init_kernel<<<1, 256, 0, st>>>(s, R, all8, counts, nonfinite);
+    alloc_pass_kernel<true><<<blocks, kAllocThreads, 0, st>>>(nullptr, n_sg, s, 0, !all8, mean_all, sq_all, n_ranks,
+                                                              M, F, mu, nonfinite);
+    for (int pass = 1; pass < kSelectPasses && !all8; ++pass)
+        alloc_pass_kernel<false><<<blocks, kAllocThreads, 0, st>>>(F, n_sg, s, pass, true, nullptr, nullptr, 0,
+                                                                   nullptr, nullptr, nullptr, nullptr);
+    tile_assign_kernel<<<(unsigned)n_tiles, kTileThreads, 0, st>>>(F, n_sg, s, fixed_bits, b, tiles, counts, T);
+    reorder_scatter_kernel<<<(unsigned)n_tiles, kTileThreads, 0, st>>>(b, n_sg, tiles, perm);
+    note_launches(all8 ? 4 : 3 + kSelectPasses);
     return cudaGetLastError();
 }
 

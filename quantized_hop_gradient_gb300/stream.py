@@ -98,16 +98,16 @@ class BucketStream:
         self.fixed_bits, self.scale_fp32 = fixed_bits, scale_fp32
         self.out_is_bf16 = out_dtype == torch.bfloat16
         # N + 1 buckets in the exchange at once and `lookahead` planned ahead.
-        # The planning (its statistics read every rank's bucket) needs about a
-        # quarter of the SMs beside the exchange: measured on the Llama-3-8B
-        # stream of 8 ranks (613 buckets of 25 MB, ms per pass): lookahead 3
-        # with 32, 40, 48 and 64 of 152 SMs left to it, 143.8, 132.8, 138.1
-        # and 156.0; lookahead 1 with none, 180.4 (the per-bucket fused
-        # exchange: 181.2).  The ratio of planning to exchange work does not
+        # The planning (its statistics read every rank's bucket) runs beside
+        # the exchange on SMs the exchange's launches leave free.  Measured
+        # on the Llama-3-8B stream of 8 ranks (613 buckets of 25 MB, ms per
+        # pass), lookahead 3: with 8 to 28 of 152 SMs left free, 125.1 to
+        # 127.3; with 32, 137.8; with 40, 143.7.  Lookahead 2 and 4 measure
+        # the same as 3.  The ratio of planning to exchange work does not
         # depend on N.
         if plan_sms < 0:
             sms = torch.cuda.get_device_properties(torch.device(device)).multi_processor_count
-            plan_sms = round(sms * 40 / 152)
+            plan_sms = round(sms * 16 / 152)
         self.lookahead, self.plan_sms = lookahead, plan_sms
         self.depth = depth or n_ranks + lookahead + 1
         if self.depth < n_ranks + lookahead + 1:

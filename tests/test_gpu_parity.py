@@ -290,14 +290,18 @@ def test_exchange_outputs_16_byte_aligned(fused):
 
 
 
-# --------------------------------------------------------------------------- planning: one launch or twelve
-@pytest.mark.parametrize("J,B", [(1, 5.0), (4097, 2.0), (4097, 8.0), (3000, 3.3), (16384, 5.0), (16385, 5.0)])
-def test_plan_single_block_and_multi_kernel_paths(J, B):
+# --------------------------------------------------------------------------- planning: one launch or a chain
+@pytest.mark.parametrize("J,B,N", [(1, 5.0, 2), (4097, 2.0, 2), (4097, 8.0, 2), (3000, 3.3, 2), (16384, 5.0, 2),
+                                   (16385, 5.0, 2), (40001, 2.0, 3), (40001, 8.0, 3), (40001, 2.37, 3),
+                                   (51200, 5.0, 8), (70000, 6.5, 4)])
+def test_plan_single_block_and_multi_kernel_paths(J, B, N):
     """dq_plan allocates and reorders up to 16,384 super-groups in one
-    single-block launch and above that with the multi-kernel radix select;
-    both give the oracle's threshold, bitwidth counts and permutation (the
-    two sizes around the switch, and the all-2-bit and all-8-bit budgets)."""
-    N = 2
+    single-block launch and above that with a chain of launches (metadata
+    all-reduce with the first pass of the radix select, two more passes,
+    the bitwidths with the tile scan, the scatter); both give the oracle's
+    threshold, bitwidth counts, permutation and means (the two sizes around
+    the switch, the all-2-bit and all-8-bit budgets on both sides, and a
+    25 MB bucket of 8 ranks)."""
     _, gr = grads_for("bert_large_ring8", J * 256, N=N, seed=J)
     ar = DynamiQAllReduce(N, J, budget=B, correlated=True, seed=0)
     info = ar.plan([dev_u16(g) for g in gr], round=1)
@@ -307,6 +311,44 @@ def test_plan_single_block_and_multi_kernel_paths(J, B):
     assert bits32(np.array([info.T], np.float32))[0] == bits32(np.array([p.T], np.float32))[0]
     assert np.array_equal(host(ar.perm), p.perm)
     assert np.array_equal(bits32(host(ar.mu)), bits32(p.M / np.float32(N)))
+
+
+@pytest.mark.parametrize("J", [900, 40001])
+@pytest.mark.parametrize("fixed_bits", [2, 4, 8])
+def test_plan_fixed_bits(J, fixed_bits):
+    """The uniform-bitwidth ablation on both planning paths: every
+    super-group gets the fixed width, the permutation is the identity, the
+    counts are (J, 0, 0), (0, J, 0) or (0, 0, J) and T is reported as NaN
+    (no threshold applies)."""
+    N = 3
+    _, gr = grads_for("bert_large_ring8", J * 256, N=N, seed=J + fixed_bits)
+    ar = DynamiQAllReduce(N, J, budget=float(fixed_bits), fixed_bits=fixed_bits)
+    info = ar.plan([dev_u16(g) for g in gr], round=1)
+    torch.cuda.synchronize()
+    assert (info.n2, info.n4, info.n8) == tuple(J if fixed_bits == w else 0 for w in (2, 4, 8))
+    assert math.isnan(info.T)
+    assert np.array_equal(host(ar.perm), np.arange(J, dtype=np.int32))
+    p = oracle.plan(oracle.Config(N, float(fixed_bits), fixed_bits=fixed_bits), gr)
+    assert np.array_equal(host(ar.perm), p.perm)
+    assert np.array_equal(bits32(host(ar.mu)), bits32(p.M / np.float32(N)))
+
+
+def test_plan_chain_reports_nonfinite_and_recovers():
+    """Above the single-block size the chain's metadata all-reduce raises the
+    non-finite flag (a NaN in one rank's gradient), and the next clean plan
+    on the same workspace succeeds and equals the oracle's."""
+    N, J = 2, 20000
+    _, gr = grads_for("bert_large_ring8", J * 256, N=N, seed=11)
+    ar = DynamiQAllReduce(N, J, budget=5.0)
+    gd = [dev_u16(g) for g in gr]
+    gd[1][256 * 17000 + 3] = float("nan")
+    with pytest.raises(dq.NonFinite):
+        ar.plan(gd, round=1)
+    info = ar.plan([dev_u16(g) for g in gr], round=1)
+    torch.cuda.synchronize()
+    p = oracle.plan(oracle.Config(N, 5.0, round=1), gr)
+    assert (info.n2, info.n4, info.n8) == tuple(int(c) for c in p.counts)
+    assert np.array_equal(host(ar.perm), p.perm)
 
 
 @pytest.mark.parametrize("N", [2, 8, 16, 32])
