@@ -85,8 +85,8 @@ def test_llama1b_butterfly8_full_size_sampled():
 
 
 def test_gemma1b_ring16_full_size_sampled():
-    """Gemma-1B-sized gradient, 16 workers, ring (the per-step exchange at
-    this size), budget 5."""
+    """Gemma-1B-sized gradient, 16 workers, ring (the pipelined exchange
+    over 32 parts that the bench times at this size), budget 5."""
     _full_size("gemma1b_ring16", butterfly=False)
 
 
@@ -97,14 +97,15 @@ def test_gemma1b_ring16_budget_sweep_full_size_sampled(B):
 
 
 def test_llama3_8b_buckets_full_size():
-    """The streamed Llama-3-8B workload in its bench configuration: 25 MB
-    buckets of 13,107,200 coordinates, two streams, with the exchange the
-    stream picks (the cooperative one-launch exchange) and with per-step
-    launches.  The first bucket, one from
-    the middle and the short last bucket (of 613) are reduced as one stream
-    and compared with the oracle in full."""
+    """The streamed Llama-3-8B workload at full bucket size: 25 MB buckets of
+    13,107,200 coordinates, 8 ranks.  The first bucket, one from the middle
+    and the short last bucket (of 613) are reduced as one pass of the bucket
+    stream in the bench's configuration (BucketStream: lookahead 3, the
+    default share of SMs left to the planning stream), and as one stream of
+    per-bucket rounds (the cooperative one-launch exchange, and per-step
+    launches); every result is compared with the oracle in full."""
     from quantized_hop_gradient_gb300.allreduce import use_fused
-    from quantized_hop_gradient_gb300.stream import BucketedAllReduce
+    from quantized_hop_gradient_gb300.stream import BucketedAllReduce, BucketStream
     build.build()
     w = synth.WORKLOADS["llama3_8b_ring8_buckets"]
     N = w.n_ranks
@@ -117,18 +118,22 @@ def test_llama3_8b_buckets_full_size():
         gu = [synth.as_u16(g) for g in b]
         cfg = oracle.Config(N, w.budget, correlated=w.correlated, seed=0, round=100 + i)
         exps.append(oracle.allreduce(cfg, gu)[1])
-    for fused in (False, "auto"):
+    for mode in ("stream", False, "auto"):
         outs = [[torch.empty(g.numel(), dtype=torch.float32, device="cuda") for g in b] for b in buckets]
-        ar = BucketedAllReduce(N, w.bucket // 256, overlap=True, fused=fused, budget=w.budget,
-                               correlated=w.correlated, seed=0)
-        assert ar.fused == (fused == "auto")   # "auto" takes the one-launch exchange at this size
-        assert all(use_fused(N, False, s.n_sg) for s in ar.sets)   # the size allows the one-launch exchange
+        if mode == "stream":
+            ar = BucketStream(N, w.bucket // 256, budget=w.budget, correlated=w.correlated, seed=0)
+            assert ar.lookahead == 3
+        else:
+            ar = BucketedAllReduce(N, w.bucket // 256, overlap=True, fused=mode, budget=w.budget,
+                                   correlated=w.correlated, seed=0)
+            assert ar.fused == (mode == "auto")   # "auto" takes the one-launch exchange at this size
+            assert all(use_fused(N, False, s.n_sg) for s in ar.sets)   # the size allows the one-launch exchange
         ar.run(buckets, outs, round0=100)
         torch.cuda.synchronize()
-        if ar.fused:
+        if mode == "auto":
             for s in ar.sets:
                 s.check_status()
         for i in range(len(buckets)):
             for r in (0, N - 1):
                 got = outs[i][r].cpu().numpy()
-                assert np.array_equal(got.view(np.int32), exps[i].view(np.int32)), (fused, picks[i], r)
+                assert np.array_equal(got.view(np.int32), exps[i].view(np.int32)), (mode, picks[i], r)
