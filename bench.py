@@ -617,6 +617,19 @@ def e2e_timing(args, w, ar, grads, outs, mode, dev, world):
             compute(i)
         main.wait_event(ev_out)
 
+    # the host link's rate on this machine now: plain uploads of the same buffers
+    # (the first one warms the path; the second is timed)
+    link = []
+    for _ in range(2):
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0.record(cin)
+        with torch.cuda.stream(cin):
+            for r in range(N):
+                gbuf[1][r].copy_(hosts[r], non_blocking=True)
+        l1.record(cin)
+        cin.synchronize()
+        link.append(l0.elapsed_time(l1))
+    link_gbs = N * J * SG * 2 / (link[-1] * 1e-3) / 1e9
     e2e_run(0, 2)
     torch.cuda.synchronize()
     barrier(world, dev)
@@ -635,7 +648,9 @@ def e2e_timing(args, w, ar, grads, outs, mode, dev, world):
            "h2d_gbs": h2d / (ms_e2e * 1e-3) / 1e9,
            "host_buffers": "one pinned buffer shared by the simulated workers of each process" if shared
            else "the simulated workers' gradients as slices of one pinned allocation",
-           "link_floor_ms": h2d / 211.6e9 * 1e3}
+           "link_gbs": link_gbs, "link_floor_ms": h2d / (link_gbs * 1e9) * 1e3,
+           "link_note": "link_gbs: a plain upload of the same pinned buffers timed just before; the end-to-end "
+                        "step cannot be shorter than link_floor_ms, the upload of every rank's gradient at that rate"}
     del gbuf[1], hosts
     return res
 
@@ -924,7 +939,8 @@ def bucketed_e2e(args, w, ar, pool, pool_of, outs_pool, nb, dev, world, gb):
     stream's device staging sets on a copy stream, later buckets' uploads and
     planning overlapping earlier buckets' exchange; rank 0's fp32 result of
     every bucket is downloaded on a third stream.  All copies are inside the
-    timed region."""
+    timed region.  The bucket stream enqueues the copies itself
+    (dq_allreduce_stream_io); the per-bucket stream through its hooks."""
     import torch
 
     N = w.n_ranks
@@ -962,11 +978,36 @@ def bucketed_e2e(args, w, ar, pool, pool_of, outs_pool, nb, dev, world, gb):
             out_host[pool_of[k]].copy_(outs[k][0], non_blocking=True)
             ev_out[pool_of[k]].record(cout)
 
+    # the bucket stream stages natively: the library enqueues every upload and
+    # download itself (dq_allreduce_stream_io), no Python per bucket
+    native = hasattr(ar, "copy_streams")
+    if native:
+        src = [hosts[pool_of[k]] for k in range(nb)]
+        dst = [out_host[pool_of[k]] for k in range(nb)]
+
     def one_pass(first):
+        if native:
+            ar.run(bufs, outs, round0=first * nb, src_host=src, dst_host=dst, copy_in=cin, copy_out=cout)
+            return
         ar.run(bufs, outs, round0=first * nb, ready=ev_in, before_plan=before_plan,
                before_exchange=before_exchange, after_exchange=after_exchange)
         torch.cuda.current_stream().wait_stream(cout)
 
+    # the host link's rate on this machine now: plain uploads of the pool's host
+    # copies into the staging sets (the first round warms the path)
+    link = []
+    for _ in range(2):
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0.record(cin)
+        with torch.cuda.stream(cin):
+            for i in range(len(pool)):
+                into = stage_last[0] if i == len(pool) - 1 else stage[i % S]
+                for r in range(N):
+                    into[r].copy_(hosts[i][r], non_blocking=True)
+        l1.record(cin)
+        cin.synchronize()
+        link.append(l0.elapsed_time(l1))
+    link_gbs = sum(g.numel() * 2 for b in pool for g in b) / (link[-1] * 1e-3) / 1e9
     one_pass(1_000)
     torch.cuda.synchronize()
     barrier(world, dev)
@@ -985,7 +1026,12 @@ def bucketed_e2e(args, w, ar, pool, pool_of, outs_pool, nb, dev, world, gb):
     d2h = sum(outs_pool[pool_of[k]][0].numel() * 4 for k in range(nb))
     del hosts, out_host, stage, stage_last
     return {"value": ms / (world * gb), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": ms, "steps": KE, "h2d_gbs": h2d / (ms * 1e-3) / 1e9}
+            "ms_per_step": ms, "steps": KE, "h2d_gbs": h2d / (ms * 1e-3) / 1e9,
+            "link_gbs": link_gbs, "link_floor_ms": h2d / (link_gbs * 1e9) * 1e3,
+            "link_note": "link_gbs: a plain upload of the pool's pinned buffers timed just before; the pass "
+                         "cannot be shorter than link_floor_ms, the upload of every bucket at that rate",
+            "staging": "copies enqueued by the library (dq_allreduce_stream_io)" if native
+                       else "copies enqueued by Python hooks per bucket"}
 
 
 def bucketed_cpu_baseline(w, nb: int, gb: float):

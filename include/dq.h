@@ -435,7 +435,7 @@ dq_status dq_exchange_stream_step(const dq_config *cfg, const dq_bucket_step *st
                                   void *stream);
 
 /* A whole bucket stream in one call: every bucket's dq_plan_async on
- * plan_stream (one bucket ahead of the exchange) and the N + n_buckets
+ * plan_stream (lookahead buckets ahead of the exchange) and the N + n_buckets
  * launches of dq_exchange_stream_step on `stream`, ordered by CUDA events
  * the call creates and releases (no device memory is allocated, and the
  * host never waits).  Each bucket's results equal a dq_plan + dq_exchange
@@ -478,6 +478,42 @@ dq_status dq_allreduce_stream(const dq_config *cfg, const dq_bucket *buckets, in
                               const dq_stream_set *sets, int32_t n_sets, int32_t lookahead, int32_t plan_sms,
                               unsigned int *counters_dev, int32_t out_is_bf16, void *plan_stream, void *stream,
                               dq_launch_log *log);
+
+/* dq_allreduce_stream with the host staging of every bucket done by the
+ * library: the DDP bucket stream end to end, gradients arriving from host
+ * memory and rank 0's result leaving to it (the paper's all-reduce runs on
+ * gradients each worker holds and hands back [S "Key idea and
+ * contribution"]; here the host side of that hand-over is part of the
+ * call, with no host round trip per bucket).
+ *   io[k].src_host: host array of N pinned host pointers; rank r's bf16
+ *   gradient of bucket k (n_sg * 256 values) is copied into
+ *   buckets[k].grads_host[r] on copy_in_stream, right before the bucket's
+ *   planning is enqueued (lookahead buckets ahead of the exchange), and the
+ *   planning waits for it.  NULL: the gradients are already on the device.
+ *   A device gradient buffer used by an earlier bucket b is refilled once
+ *   b's last ring step has run; that launch must come before the planning
+ *   of bucket k in the call's order, i.e. k >= b + N + lookahead (e.g.
+ *   staging sets cycled k mod S with S >= N + lookahead), else
+ *   DQ_ERR_INVALID_ARG.
+ *   io[k].dst_host: pinned host buffer for rank 0's result of bucket k
+ *   (n_sg * 256 fp32, or bf16 with out_is_bf16), copied on copy_out_stream
+ *   after the bucket's decode; a later decode that writes the same device
+ *   buffer waits for that copy.  NULL: no download.
+ *   copy_in_stream, copy_out_stream: the copy streams (NULL: plan_stream
+ *   and `stream`).  Everything the call enqueues on the other streams
+ *   starts after the work already on `stream`, and `stream` ends after the
+ *   last download, so one synchronisation of `stream` covers the pass.
+ *   Other arguments and errors: as dq_allreduce_stream.  No sync. */
+typedef struct {
+    const void *const *src_host;
+    void              *dst_host;
+} dq_bucket_io;
+
+dq_status dq_allreduce_stream_io(const dq_config *cfg, const dq_bucket *buckets, const dq_bucket_io *io,
+                                 int32_t n_buckets, const dq_stream_set *sets, int32_t n_sets, int32_t lookahead,
+                                 int32_t plan_sms, unsigned int *counters_dev, int32_t out_is_bf16,
+                                 void *copy_in_stream, void *copy_out_stream, void *plan_stream, void *stream,
+                                 dq_launch_log *log);
 
 /* Reads a device status word into host memory [boundary of the hot path:
  * device-side errors of an asynchronous call are reported through a status

@@ -8,6 +8,7 @@
 #include <map>
 #include <memory>
 #include <mutex>
+#include <unordered_map>
 #include <vector>
 
 #include "dq_common.cuh"
@@ -1226,10 +1227,17 @@ dq_status dq_exchange_stream_step(const dq_config *cfg, const dq_bucket_step *st
     return stream_step(cfg, P.get(), steps, n_steps, counter_dev, out_is_bf16, log, static_cast<cudaStream_t>(stream));
 }
 
-dq_status dq_allreduce_stream(const dq_config *cfg, const dq_bucket *buckets, int32_t n_buckets,
-                              const dq_stream_set *sets, int32_t n_sets, int32_t lookahead, int32_t plan_sms,
-                              unsigned int *counters_dev, int32_t out_is_bf16, void *plan_stream, void *stream,
-                              dq_launch_log *log)
+}  // extern "C"
+
+namespace {
+
+// The bucket stream's driver (dq_allreduce_stream, and with host staging
+// dq_allreduce_stream_io).  Host iteration t enqueues the planning of bucket
+// t + lookahead (after its upload, if any) and exchange launch t.
+dq_status allreduce_stream(const dq_config *cfg, const dq_bucket *buckets, const dq_bucket_io *io,
+                           int32_t n_buckets, const dq_stream_set *sets, int32_t n_sets, int32_t lookahead,
+                           int32_t plan_sms, unsigned int *counters_dev, int32_t out_is_bf16, cudaStream_t cin,
+                           cudaStream_t cout, cudaStream_t ps, cudaStream_t st, dq_launch_log *log)
 {
     if (!stream_cfg_ok(cfg) || !buckets || !sets || !counters_dev || n_buckets < 1) return DQ_ERR_INVALID_ARG;
     const int32_t N = cfg->n_ranks;
@@ -1240,32 +1248,85 @@ dq_status dq_allreduce_stream(const dq_config *cfg, const dq_bucket *buckets, in
             return DQ_ERR_INVALID_ARG;
     for (int32_t i = 0; i < n_sets; ++i)
         if (!sets[i].mu || !sets[i].perm || !sets[i].plan_ws || !sets[i].msgs) return DQ_ERR_INVALID_ARG;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaStream_t ps = plan_stream ? static_cast<cudaStream_t>(plan_stream) : st;
-    EventPool E;   // per set: planned, free again; then the call's start
-    if (!E.make(2 * (size_t)n_sets + 1)) return DQ_ERR_CUDA;
-    // the planning stream starts after everything already enqueued on
-    // `stream` (earlier work may still use the sets)
-    if (ps != st && (cudaEventRecord(E.ev.back(), st) != cudaSuccess || cudaStreamWaitEvent(ps, E.ev.back(), 0) != cudaSuccess))
-        return DQ_ERR_CUDA;
+    // host staging: which earlier bucket last read each device gradient
+    // buffer (up to the launch of its last ring step), and which earlier
+    // download last read each output buffer a decode writes; the reuse
+    // waits for it, and an upload must be enqueued after that launch
+    const int64_t out_elem = out_is_bf16 ? 2 : 4;
+    std::vector<int32_t> reads_done_by((size_t)n_buckets, -1), out_prev((size_t)n_buckets, -1);
+    if (io) {
+        std::unordered_map<const void *, int32_t> last_grad, last_out;
+        for (int32_t k = 0; k < n_buckets; ++k) {
+            if (io[k].src_host) {
+                for (int32_t r = 0; r < N; ++r) {
+                    if (!io[k].src_host[r] || !buckets[k].grads_host[r]) return DQ_ERR_INVALID_ARG;
+                    auto it = last_grad.find(buckets[k].grads_host[r]);
+                    if (it != last_grad.end()) {
+                        // that bucket's last read (launch b + N - 1) precedes this planning's enqueue (k - lookahead)
+                        if (it->second + N - 1 >= k - lookahead) return DQ_ERR_INVALID_ARG;
+                        reads_done_by[k] = std::max(reads_done_by[k], it->second);
+                    }
+                }
+            }
+            for (int32_t r = 0; r < N; ++r) last_grad[buckets[k].grads_host[r]] = k;
+            // any output this bucket's decode writes may be a buffer an earlier download still reads
+            for (int32_t r = 0; r < N; ++r) {
+                auto it = last_out.find(buckets[k].outs_host[r]);
+                if (it != last_out.end()) out_prev[k] = std::max(out_prev[k], it->second);
+            }
+            if (io[k].dst_host) {
+                if (!buckets[k].outs_host[0]) return DQ_ERR_INVALID_ARG;
+                last_out[buckets[k].outs_host[0]] = k;
+            }
+        }
+    }
+    const int32_t R = n_sets;   // ring of events per kind (a wait on a later record of a slot waits longer, never less)
+    EventPool E;   // per set: planned, free again; rings: uploaded, last read, decoded, downloaded; the call's start; the end
+    if (!E.make(2 * (size_t)n_sets + (io ? 4 * (size_t)R : 0) + 2)) return DQ_ERR_CUDA;
     auto ev_plan = [&](int32_t i) { return E.ev[2 * i]; };
     auto ev_free = [&](int32_t i) { return E.ev[2 * i + 1]; };
+    auto ev_up = [&](int32_t k) { return E.ev[2 * n_sets + (k % R)]; };
+    auto ev_read = [&](int32_t k) { return E.ev[2 * n_sets + R + (k % R)]; };
+    auto ev_dec = [&](int32_t k) { return E.ev[2 * n_sets + 2 * R + (k % R)]; };
+    auto ev_out = [&](int32_t k) { return E.ev[2 * n_sets + 3 * R + (k % R)]; };
+    cudaEvent_t ev_start = E.ev[E.ev.size() - 2], ev_end = E.ev.back();
+    // the other streams start after everything already enqueued on `stream`
+    // (earlier work may still use the sets, the staging or the outputs)
+    if (cudaEventRecord(ev_start, st) != cudaSuccess) return DQ_ERR_CUDA;
+    for (cudaStream_t o : {ps, cin, cout})
+        if (io && o != st && cudaStreamWaitEvent(o, ev_start, 0) != cudaSuccess) return DQ_ERR_CUDA;
+    if (!io && ps != st && cudaStreamWaitEvent(ps, ev_start, 0) != cudaSuccess) return DQ_ERR_CUDA;
     std::unique_ptr<StreamRingParams> P(new StreamRingParams());
     memset(P.get(), 0, sizeof(StreamRingParams));
     if (!build_tables(cfg->eps, &P->tab)) return DQ_ERR_INVALID_ARG;
     if (zero_many(counters_dev, (int64_t)n_buckets + N, st) != cudaSuccess) return DQ_ERR_CUDA;
     std::vector<const int64_t *> counts((size_t)n_buckets, nullptr);
     std::vector<uint8_t> used((size_t)n_sets, 0);
+    auto upload = [&](int32_t k) -> dq_status {
+        if (!io || !io[k].src_host) return DQ_OK;
+        if (reads_done_by[k] >= 0 && cudaStreamWaitEvent(cin, ev_read(reads_done_by[k]), 0) != cudaSuccess)
+            return DQ_ERR_CUDA;
+        const size_t bytes = (size_t)buckets[k].n_sg * kSG * 2;
+        for (int32_t r = 0; r < N; ++r)
+            if (cudaMemcpyAsync(const_cast<void *>(buckets[k].grads_host[r]), io[k].src_host[r], bytes,
+                                cudaMemcpyHostToDevice, cin) != cudaSuccess)
+                return DQ_ERR_CUDA;
+        if (cudaEventRecord(ev_up(k), cin) != cudaSuccess || cudaStreamWaitEvent(ps, ev_up(k), 0) != cudaSuccess)
+            return DQ_ERR_CUDA;
+        return DQ_OK;
+    };
     auto plan = [&](int32_t k) -> dq_status {
         const int32_t si = k % n_sets;
         if (used[si] && cudaStreamWaitEvent(ps, ev_free(si), 0) != cudaSuccess) return DQ_ERR_CUDA;
         used[si] = 1;
+        dq_status s = upload(k);
+        if (s != DQ_OK) return s;
         dq_config c = *cfg;
         c.round = buckets[k].round;
         PlanDev d;
         const dq_stream_set &S = sets[si];
-        const dq_status s = plan_enqueue(&c, buckets[k].grads_host, buckets[k].n_sg, S.mu, S.perm, S.plan_ws,
-                                         S.plan_ws_bytes, nullptr, log, ps, d);
+        s = plan_enqueue(&c, buckets[k].grads_host, buckets[k].n_sg, S.mu, S.perm, S.plan_ws, S.plan_ws_bytes,
+                         nullptr, log, ps, d);
         if (s != DQ_OK) return s;
         counts[k] = d.counts;
         return cudaEventRecord(ev_plan(si), ps) == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
@@ -1277,6 +1338,9 @@ dq_status dq_allreduce_stream(const dq_config *cfg, const dq_bucket *buckets, in
     for (int32_t t = 0; t < n_buckets + N; ++t) {
         if (t + lookahead < n_buckets && (s = plan(t + lookahead)) != DQ_OK) return s;
         if (t < n_buckets && cudaStreamWaitEvent(st, ev_plan(t % n_sets), 0) != cudaSuccess) return DQ_ERR_CUDA;
+        // this launch decodes bucket t - N: a download of its rank-0 output buffer still in flight comes first
+        if (io && t >= N && out_prev[t - N] >= 0 && cudaStreamWaitEvent(st, ev_out(out_prev[t - N]), 0) != cudaSuccess)
+            return DQ_ERR_CUDA;
         int32_t n = 0;
         for (int32_t b = std::max(0, t - N); b <= std::min(t, n_buckets - 1); ++b) {
             const dq_stream_set &S = sets[b % n_sets];
@@ -1286,8 +1350,54 @@ dq_status dq_allreduce_stream(const dq_config *cfg, const dq_bucket *buckets, in
         if ((s = stream_step(cfg, P.get(), steps, n, counters_dev + t, out_is_bf16, log, st, plan_sms)) != DQ_OK)
             return s;
         if (t >= N && cudaEventRecord(ev_free((t - N) % n_sets), st) != cudaSuccess) return DQ_ERR_CUDA;
+        if (!io) continue;
+        // bucket t - N + 1 ran its last ring step: its gradients are no longer read
+        if (t - N + 1 >= 0 && t - N + 1 < n_buckets && cudaEventRecord(ev_read(t - N + 1), st) != cudaSuccess)
+            return DQ_ERR_CUDA;
+        const int32_t b = t - N;   // decoded by this launch
+        if (b >= 0 && io[b].dst_host) {
+            if (cudaEventRecord(ev_dec(b), st) != cudaSuccess || cudaStreamWaitEvent(cout, ev_dec(b), 0) != cudaSuccess ||
+                cudaMemcpyAsync(io[b].dst_host, buckets[b].outs_host[0], (size_t)buckets[b].n_sg * kSG * out_elem,
+                                cudaMemcpyDeviceToHost, cout) != cudaSuccess ||
+                cudaEventRecord(ev_out(b), cout) != cudaSuccess)
+                return DQ_ERR_CUDA;
+        }
     }
+    // `stream` covers the whole call: the downloads join it at the end
+    if (io && cout != st &&
+        (cudaEventRecord(ev_end, cout) != cudaSuccess || cudaStreamWaitEvent(st, ev_end, 0) != cudaSuccess))
+        return DQ_ERR_CUDA;
     return DQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dq_status dq_allreduce_stream(const dq_config *cfg, const dq_bucket *buckets, int32_t n_buckets,
+                              const dq_stream_set *sets, int32_t n_sets, int32_t lookahead, int32_t plan_sms,
+                              unsigned int *counters_dev, int32_t out_is_bf16, void *plan_stream, void *stream,
+                              dq_launch_log *log)
+{
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStream_t ps = plan_stream ? static_cast<cudaStream_t>(plan_stream) : st;
+    return allreduce_stream(cfg, buckets, nullptr, n_buckets, sets, n_sets, lookahead, plan_sms, counters_dev,
+                            out_is_bf16, st, st, ps, st, log);
+}
+
+dq_status dq_allreduce_stream_io(const dq_config *cfg, const dq_bucket *buckets, const dq_bucket_io *io,
+                                 int32_t n_buckets, const dq_stream_set *sets, int32_t n_sets, int32_t lookahead,
+                                 int32_t plan_sms, unsigned int *counters_dev, int32_t out_is_bf16,
+                                 void *copy_in_stream, void *copy_out_stream, void *plan_stream, void *stream,
+                                 dq_launch_log *log)
+{
+    if (!io) return DQ_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStream_t ps = plan_stream ? static_cast<cudaStream_t>(plan_stream) : st;
+    cudaStream_t cin = copy_in_stream ? static_cast<cudaStream_t>(copy_in_stream) : ps;
+    cudaStream_t cout = copy_out_stream ? static_cast<cudaStream_t>(copy_out_stream) : st;
+    return allreduce_stream(cfg, buckets, io, n_buckets, sets, n_sets, lookahead, plan_sms, counters_dev, out_is_bf16,
+                            cin, cout, ps, st, log);
 }
 
 dq_status dq_get_device_status(const int32_t *status_dev, int32_t *status_host, void *stream)

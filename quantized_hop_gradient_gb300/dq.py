@@ -81,6 +81,10 @@ class dq_stream_set(C.Structure):
                 ("msgs", C.c_void_p), ("msgs_bytes", C.c_size_t)]
 
 
+class dq_bucket_io(C.Structure):
+    _fields_ = [("src_host", C.c_void_p), ("dst_host", C.c_void_p)]
+
+
 class dq_bucket_step(C.Structure):
     _fields_ = [("n_sg", C.c_int64), ("counts_dev", C.c_void_p), ("grads_host", C.c_void_p),
                 ("outs_host", C.c_void_p), ("mu", C.c_void_p), ("perm", C.c_void_p), ("msgs", C.c_void_p),
@@ -133,6 +137,9 @@ _SIGS = {
     "dq_bucket_msgs_bytes": ([C.POINTER(dq_config), C.c_int64], C.c_size_t),
     "dq_allreduce_stream": ([C.POINTER(dq_config), C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_int32,
                              C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+    "dq_allreduce_stream_io": ([C.POINTER(dq_config), C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_int32,
+                                C.c_int32, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
+                                C.c_void_p, C.c_void_p], C.c_int),
     "dq_exchange_stream_step": ([C.POINTER(dq_config), C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p,
                                  C.c_void_p], C.c_int),
     "dq_barrier_selftest": ([C.c_int32, C.c_int32, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
@@ -333,6 +340,21 @@ def dq_allreduce_stream(cfg, buckets, sets, counters, out_is_bf16=False, plan_st
                                      _ptr(counters), int(out_is_bf16),
                                      _stream(plan_stream) if plan_stream is not None else None, _stream(stream),
                                      C.byref(log.c) if log is not None else None), "dq_allreduce_stream")
+
+
+def dq_allreduce_stream_io(cfg, buckets, io, sets, counters, out_is_bf16=False, copy_in_stream=None,
+                           copy_out_stream=None, plan_stream=None, stream=None, log: "LaunchLog" = None,
+                           lookahead: int = 1, plan_sms: int = 0):
+    """dq_allreduce_stream with each bucket's upload and download done by the
+    library.  ``io``: a ctypes array of dq_bucket_io, one per bucket."""
+    if len(io) != len(buckets):
+        raise ValueError("one dq_bucket_io per bucket")
+    opt = lambda st: _stream(st) if st is not None else None
+    _check(lib().dq_allreduce_stream_io(C.byref(cfg), C.cast(buckets, C.c_void_p), C.cast(io, C.c_void_p),
+                                        len(buckets), C.cast(sets, C.c_void_p), len(sets), int(lookahead),
+                                        int(plan_sms), _ptr(counters), int(out_is_bf16), opt(copy_in_stream),
+                                        opt(copy_out_stream), opt(plan_stream), _stream(stream),
+                                        C.byref(log.c) if log is not None else None), "dq_allreduce_stream_io")
 
 
 def dq_exchange_stream_step(cfg, steps, counter, out_is_bf16=False, log: "LaunchLog" = None, stream=None):

@@ -133,8 +133,15 @@ class BucketStream:
         return self.dq.config(self.n_ranks, self.budget, self.eps, self.correlated, self.seed, round,
                               self.fixed_bits, self.scale_fp32)
 
+    def copy_streams(self):
+        """The (upload, download) streams of the library's host staging."""
+        if getattr(self, "_copy_streams", None) is None:
+            self._copy_streams = (torch.cuda.Stream(device=self.counters.device),
+                                  torch.cuda.Stream(device=self.counters.device))
+        return self._copy_streams
+
     def run(self, buckets, outs, round0: int = 0, log=None, ready=None, before_plan=None, before_exchange=None,
-            after_exchange=None):
+            after_exchange=None, src_host=None, dst_host=None, copy_in=None, copy_out=None):
         """As ``BucketedAllReduce.run``: buckets[k][r] is rank r's bf16
         gradient of bucket k (a multiple of 256 coordinates, at most
         bucket_sg super-groups), outs[k][r] its result; bucket k is round
@@ -143,7 +150,14 @@ class BucketStream:
         previous bucket has finished: its staging may be reused), before its
         first launch and after its decode (on the exchange stream).  A
         bucket's gradients are read until its last ring step, so a caller
-        that stages them needs ``depth`` staging sets (set k % depth)."""
+        that stages them needs ``depth`` staging sets (set k % depth).
+
+        Host staging without hooks: ``src_host[k][r]`` (pinned host tensors)
+        are copied into buckets[k][r] before bucket k's planning, and rank
+        0's result of bucket k into ``dst_host[k]`` (a pinned host tensor)
+        after its decode, all by the library (dq_allreduce_stream_io) on the
+        copy streams ``copy_in`` and ``copy_out`` (None: streams of its
+        own); staging sets must be at least N + lookahead apart."""
         import ctypes as C
         dq = self.dq
         N, nb, D = self.n_ranks, len(buckets), self.depth
@@ -165,9 +179,39 @@ class BucketStream:
                                                                  s["plan_ws"].data_ptr(), s["plan_ws"].numel(),
                                                                  s["msgs"].data_ptr(), s["msgs"].numel())
                                             for s in self.sets])
-            dq.dq_allreduce_stream(self.config(0), arr, sets, self.counters, self.out_is_bf16, side, main, log,
-                                   lookahead=self.lookahead, plan_sms=self.plan_sms)
+            if src_host is None and dst_host is None:
+                dq.dq_allreduce_stream(self.config(0), arr, sets, self.counters, self.out_is_bf16, side, main, log,
+                                       lookahead=self.lookahead, plan_sms=self.plan_sms)
+                return
+            io = (dq.dq_bucket_io * nb)()
+            for k in range(nb):
+                # the library copies whole buffers: sizes must match the device sides
+                if src_host is not None and any(h.device.type != "cpu" or h.numel() != g.numel() or
+                                                h.element_size() != 2 for h, g in zip(src_host[k], buckets[k])):
+                    raise ValueError(f"src_host[{k}]: host bf16 buffers of the device gradients' sizes "
+                                     f"({[(h.device.type, h.numel(), h.element_size()) for h in src_host[k]]} "
+                                     f"against {[g.numel() for g in buckets[k]]})")
+                if dst_host is not None and (dst_host[k].device.type != "cpu" or
+                                             dst_host[k].numel() != outs[k][0].numel() or
+                                             dst_host[k].element_size() != outs[k][0].element_size()):
+                    raise ValueError(f"dst_host[{k}]: a host buffer of rank 0's output size and type "
+                                     f"({dst_host[k].device}, {dst_host[k].numel()} x {dst_host[k].element_size()} "
+                                     f"bytes against {outs[k][0].numel()} x {outs[k][0].element_size()})")
+                sp = None
+                if src_host is not None:
+                    sp = (C.c_void_p * N)(*[h.data_ptr() for h in src_host[k]])
+                    keep.append(sp)
+                io[k] = dq.dq_bucket_io(C.cast(sp, C.c_void_p) if sp is not None else None,
+                                        dst_host[k].data_ptr() if dst_host is not None else None)
+            if copy_in is None:
+                copy_in = self.copy_streams()[0]
+            if copy_out is None:
+                copy_out = self.copy_streams()[1]
+            dq.dq_allreduce_stream_io(self.config(0), arr, io, sets, self.counters, self.out_is_bf16, copy_in,
+                                      copy_out, side, main, log, lookahead=self.lookahead, plan_sms=self.plan_sms)
             return
+        if src_host is not None or dst_host is not None:
+            raise ValueError("host staging by the library cannot be combined with hooks or ready events")
         self.counters[: nb + N].zero_()
         live = {}
 

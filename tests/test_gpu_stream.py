@@ -194,3 +194,61 @@ def test_bucket_stream_large_buckets_match_oracle():
         _, exp = oracle.allreduce(oracle.Config(N, 5.0, correlated=True, round=50 + k), gu)
         for r in range(N):
             assert np.array_equal(outs[k][r].cpu().numpy().view(np.int32), exp.view(np.int32)), (k, r)
+
+
+@pytest.mark.parametrize("N,lookahead,n_out,dt", [(4, 3, 3, torch.float32), (8, 1, 2, torch.float32),
+                                                   (2, 2, 1, torch.bfloat16)])
+def test_bucket_stream_library_staging_matches_oracle(N, lookahead, n_out, dt):
+    """The stream with its host staging done by the library
+    (dq_allreduce_stream_io): every bucket's gradients are copied from pinned
+    host memory into device staging sets cycled at the smallest allowed
+    distance (N + lookahead buckets), and rank 0's result of every bucket is
+    copied to its own pinned host buffer while only n_out device output sets
+    are cycled (a decode waits for the download that still reads its
+    buffer).  The host results equal the oracle's, bit for bit (bf16: the
+    fp32 result rounded to nearest-even)."""
+    build.build()
+    bucket_sg = 31
+    w = synth.WORKLOADS["llama3_8b_ring8_buckets"]
+    w = w.__class__(**{**w.__dict__, "n_ranks": N, "n": 256 * (14 * bucket_sg + 9), "bucket": 256 * bucket_sg})
+    nb = synth.bucket_count(w)
+    buckets = [synth.generate_bucket(w, k, "cpu", seed=9) for k in range(nb)]
+    hosts = [[g.pin_memory() for g in b] for b in buckets]
+    bs = BucketStream(N, bucket_sg, budget=5.0, correlated=True, lookahead=lookahead, out_dtype=dt)
+    S = N + lookahead
+    stage = [[torch.empty(256 * bucket_sg, dtype=torch.bfloat16, device="cuda") for _ in range(N)] for _ in range(S)]
+    bufs = [[s[:g.numel()] for s, g in zip(stage[k % S], buckets[k])] for k in range(nb)]
+    oset = [[torch.empty(256 * bucket_sg, dtype=dt, device="cuda") for _ in range(N)] for _ in range(n_out)]
+    outs = [[o[:g.numel()] for o, g in zip(oset[k % n_out], buckets[k])] for k in range(nb)]
+    res = [torch.full((g[0].numel(),), -1.0, dtype=dt).pin_memory() for g in buckets]
+    bs.run(bufs, outs, round0=60, src_host=hosts, dst_host=res)
+    torch.cuda.current_stream().synchronize()   # the call joins its copy streams to this one
+    for k in range(nb):
+        gu = [synth.as_u16(g) for g in buckets[k]]
+        _, exp = oracle.allreduce(oracle.Config(N, 5.0, correlated=True, round=60 + k), gu)
+        if dt == torch.bfloat16:
+            got = res[k].view(torch.int16).numpy()
+            want = torch.from_numpy(exp).to(torch.bfloat16).view(torch.int16).numpy()
+        else:
+            got, want = res[k].numpy().view(np.int32), exp.view(np.int32)
+        assert np.array_equal(got, want), k
+
+
+def test_bucket_stream_library_staging_rejects_close_reuse():
+    """Staging sets closer than N + lookahead buckets apart cannot be
+    refilled in time: the call is refused before anything is enqueued."""
+    from quantized_hop_gradient_gb300 import dq
+    build.build()
+    N, lookahead, bucket_sg = 4, 3, 17
+    w = synth.WORKLOADS["llama3_8b_ring8_buckets"]
+    w = w.__class__(**{**w.__dict__, "n_ranks": N, "n": 256 * 10 * bucket_sg, "bucket": 256 * bucket_sg})
+    nb = synth.bucket_count(w)
+    buckets = [synth.generate_bucket(w, k, "cpu", seed=10) for k in range(nb)]
+    hosts = [[g.pin_memory() for g in b] for b in buckets]
+    S = N + lookahead - 1
+    stage = [[torch.empty(256 * bucket_sg, dtype=torch.bfloat16, device="cuda") for _ in range(N)] for _ in range(S)]
+    bufs = [stage[k % S] for k in range(nb)]
+    outs = [[torch.empty(256 * bucket_sg, device="cuda") for _ in range(N)] for _ in range(nb)]
+    bs = BucketStream(N, bucket_sg, lookahead=lookahead)
+    with pytest.raises(dq.DQError):
+        bs.run(bufs, outs, src_host=hosts)
