@@ -125,3 +125,30 @@ def test_bad_arguments_rejected_on_the_host(L):
     assert L.dq_get_device_status(None, ctypes.addressof(host), st) == dq.DQ_ERR_INVALID_ARG
     assert L.dq_get_device_status(P, None, st) == dq.DQ_ERR_INVALID_ARG
     assert L.dq_get_device_status(P + 2, ctypes.addressof(host), st) == dq.DQ_ERR_ALIGNMENT
+
+
+def test_bucket_stream_arguments_rejected_on_the_host(L):
+    """The whole-pass bucket stream drivers refuse bad arguments before they
+    touch the GPU: no buckets, a ring above 8 ranks, a lookahead below 1,
+    too few buffer sets, and (for the staged driver) no staging list."""
+    P = 4096
+    st = 0
+    ptrs = (ctypes.c_void_p * 4)(*([P] * 4))
+    b = (dq.dq_bucket * 2)(*[dq.dq_bucket(100, ctypes.cast(ptrs, ctypes.c_void_p), ctypes.cast(ptrs, ctypes.c_void_p), k)
+                             for k in range(2)])
+    sets = (dq.dq_stream_set * 8)(*[dq.dq_stream_set(P, P, P, 1 << 20, P, 1 << 20) for _ in range(8)])
+    io = (dq.dq_bucket_io * 2)(*[dq.dq_bucket_io(ctypes.cast(ptrs, ctypes.c_void_p), P) for _ in range(2)])
+    cfg4, cfg9 = dq.config(4), dq.config(9)
+    # dq_allreduce_stream(cfg, buckets, n, sets, n_sets, lookahead, plan_sms, counters, bf16, plan_stream, stream, log)
+    assert L.dq_allreduce_stream(cfg4, b, 0, sets, 8, 3, 0, P, 0, None, st, None) == dq.DQ_ERR_INVALID_ARG
+    assert L.dq_allreduce_stream(cfg9, b, 2, sets, 8, 3, 0, P, 0, None, st, None) == dq.DQ_ERR_INVALID_ARG
+    assert L.dq_allreduce_stream(cfg4, b, 2, sets, 8, 0, 0, P, 0, None, st, None) == dq.DQ_ERR_INVALID_ARG
+    assert L.dq_allreduce_stream(cfg4, b, 2, sets, 7, 3, 0, P, 0, None, st, None) == dq.DQ_ERR_INVALID_ARG
+    # dq_allreduce_stream_io(cfg, buckets, io, n, sets, n_sets, lookahead, plan_sms, counters, bf16,
+    #                        copy_in, copy_out, plan_stream, stream, log)
+    assert L.dq_allreduce_stream_io(cfg4, b, None, 2, sets, 8, 3, 0, P, 0, None, None, None, st,
+                                    None) == dq.DQ_ERR_INVALID_ARG
+    assert L.dq_allreduce_stream_io(cfg4, b, io, 2, sets, 7, 3, 0, P, 0, None, None, None, st,
+                                    None) == dq.DQ_ERR_INVALID_ARG
+    assert L.dq_allreduce_stream_io(cfg9, b, io, 2, sets, 8, 3, 0, P, 0, None, None, None, st,
+                                    None) == dq.DQ_ERR_INVALID_ARG
