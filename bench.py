@@ -649,8 +649,9 @@ def e2e_timing(args, w, ar, grads, outs, mode, dev, world):
            "host_buffers": "one pinned buffer shared by the simulated workers of each process" if shared
            else "the simulated workers' gradients as slices of one pinned allocation",
            "link_gbs": link_gbs, "link_floor_ms": h2d / (link_gbs * 1e9) * 1e3,
-           "link_note": "link_gbs: a plain upload of the same pinned buffers timed just before; the end-to-end "
-                        "step cannot be shorter than link_floor_ms, the upload of every rank's gradient at that rate"}
+           "link_note": "link_gbs: a plain upload of the same pinned buffers timed just before; link_floor_ms: "
+                        "the upload of every rank's gradient at that rate, which bounds the end-to-end step (the "
+                        "link's rate varies from box to box and over time on some)"}
     del gbuf[1], hosts
     return res
 
@@ -1028,8 +1029,9 @@ def bucketed_e2e(args, w, ar, pool, pool_of, outs_pool, nb, dev, world, gb):
     return {"value": ms / (world * gb), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms, "steps": KE, "h2d_gbs": h2d / (ms * 1e-3) / 1e9,
             "link_gbs": link_gbs, "link_floor_ms": h2d / (link_gbs * 1e9) * 1e3,
-            "link_note": "link_gbs: a plain upload of the pool's pinned buffers timed just before; the pass "
-                         "cannot be shorter than link_floor_ms, the upload of every bucket at that rate",
+            "link_note": "link_gbs: a plain upload of the pool's pinned buffers timed just before; "
+                         "link_floor_ms: the upload of every bucket at that rate, which bounds the pass (the link's "
+                         "rate varies from box to box and over time on some)",
             "staging": "copies enqueued by the library (dq_allreduce_stream_io)" if native
                        else "copies enqueued by Python hooks per bucket"}
 
