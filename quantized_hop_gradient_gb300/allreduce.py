@@ -7,6 +7,8 @@ from one simulated rank to the next inside the exchange workspace.
 """
 from __future__ import annotations
 
+import math
+
 import torch
 
 from . import dq
@@ -14,12 +16,13 @@ from . import dq
 SG = dq.SG
 
 # Largest per-worker size (super-groups) at which the fused ring exchange is
-# the faster one on a GB300 (BERT-large distribution, 8 ranks, exchange
-# alone): 0.332 vs 0.377 ms at 2^24 coordinates per worker, 0.620 vs 0.637 ms
-# at 2^25; behind above that (1.173 vs 1.137 ms at 2^26, 4.91 vs 4.64 ms at
-# 335 M coordinates), where the per-step path's flat launches stream HBM
-# faster than the persistent cooperative kernel.
-FUSED_MAX_SG = 1 << 17
+# the faster one on a GB300 (BERT-large distribution, exchange alone, ms):
+# at 2^16 super-groups 0.164 / 0.315 / 0.617 for rings of 4 / 8 / 16 against
+# 0.228 / 0.436 / 0.866 pipelined (one part) and 0.174 / 0.344 / 0.690 step
+# by step; at 1.25 * 2^16 the fused exchange jumps to 0.278 / 0.543 / 1.074
+# (its messages no longer stay in L2) and the one-part pipeline leads with
+# 0.241 / 0.468 / 0.931.
+FUSED_MAX_SG = 1 << 16
 
 
 def use_fused(n_ranks: int, butterfly: bool, n_sg: int) -> bool:
@@ -28,13 +31,20 @@ def use_fused(n_ranks: int, butterfly: bool, n_sg: int) -> bool:
 
 
 def pipeline_parts(n_ranks: int, n_sg: int) -> int:
-    """Parts of the pipelined ring exchange: 2N, as long as each part keeps
-    at least 2048 work units (32 super-groups each) per step.  Measured on a
-    GB300 (exchange alone): Gemma-1B ring of 16, 26.2 ms per step-wise
-    exchange against 22.6, 22.5 and 22.6 ms at 32, 48 and 64 parts;
-    BERT-large ring of 8, 4.47 ms against 4.13 and 4.12 ms at 8 and 16."""
+    """Parts of the pipelined ring exchange.  More parts shorten the first
+    N launches, which carry hop steps only (no part has finished its ring
+    yet), to (N + 1) / 2P of the hop work; each part adds a launch.  The
+    best count measured on a GB300 (exchange alone) grows like N times the
+    square root of the work units (32 super-groups each): N = 8: 16,385
+    units 4 (4 to 8 within 0.5%), 32,769 units 12, 40,911 (BERT-large)
+    8 to 10 (16: 2.3% slower), 65,537 units 16; N = 16: 32,769 units 24,
+    65,537 units 32, 122,057 (Gemma-1B) 32 to 40.  Up to 16,384 units one
+    part is best (8,193 units: 1.013 ms at one part, 1.026 at four, N = 8).
+    At most 2N parts."""
     units = -(-n_sg // dq.UNIT)
-    return max(1, min(2 * n_ranks, units // 2048, dq.MAX_WAVE_PARTS))
+    if units <= 16384:
+        return 1
+    return max(1, min(2 * n_ranks, round(n_ranks * math.sqrt(units) / 144), dq.MAX_WAVE_PARTS))
 
 
 def exchange_mode(n_ranks: int, butterfly: bool, n_sg: int):

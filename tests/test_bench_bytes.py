@@ -51,7 +51,10 @@ def test_exchange_mode_picks_by_size():
     assert exchange_mode(65, False, 1 << 20) == (False, None)        # beyond 64 ranks
     assert exchange_mode(8, False, FUSED_MAX_SG) == (True, None)
     assert exchange_mode(16, False, 3905805) == (False, 32)          # Gemma-1B ring of 16: 2N parts
-    assert exchange_mode(8, False, 1309148) == (False, 16)           # BERT-large ring of 8
-    assert pipeline_parts(8, FUSED_MAX_SG + 1) == 2                  # parts keep >= 2048 units
+    assert exchange_mode(8, False, 1309148) == (False, 11)           # BERT-large ring of 8: about N sqrt(units) / 144
+    assert FUSED_MAX_SG == 1 << 16
+    assert pipeline_parts(8, FUSED_MAX_SG + 1) == 1                  # one part up to 16,384 units
+    assert pipeline_parts(16, 32 * 16384) == 1 and pipeline_parts(16, 32 * 16385) == 14
+    assert pipeline_parts(8, 1 << 20) == 10 and pipeline_parts(16, 1 << 21) == 28
     assert pipeline_parts(64, 1 << 26) == 128
     assert pipeline_parts(4, 1) == 1
