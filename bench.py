@@ -225,6 +225,17 @@ def ncu_counters(kernel: str, workload: str):
 
 
 # --------------------------------------------------------------------------- algorithmic bytes
+def step_roofline(kernels, per_step_key, ms_step, peak):
+    """The whole step against the HBM roofline: the algorithmic bytes of every
+    kernel launched in one step (each kernel's bytes per launch times its
+    launches per step) over the step's time."""
+    by = sum(k["alg_bytes_per_launch"] * k[per_step_key] for k in kernels.values())
+    gbs = by / (ms_step * 1e-3) / 1e9
+    return {"alg_bytes": by, "achieved": gbs, "frac": gbs / peak,
+            "note": "every kernel of one step: its algorithmic bytes per launch times its launches per step, over "
+                    "the step's time"}
+
+
 def stream_message_bytes(dq, info, N):
     lo = dq.dq_chunk_cuts(info.n2, info.n4, info.n8, N)
     e2, e4 = info.n2, info.n2 + info.n4
@@ -475,7 +486,8 @@ def measure_round(args, w, dev, world, K, W, full: bool, local: int = 0):
     traffic, _ = ncu_counters(TRAFFIC_KEY[dominant], w.name)
     roofline = {"bound": "hbm", "kernel": KERNEL_NAMES[dominant], "achieved": dk["achieved_gbs"], "peak": peak,
                 "unit": "GB/s", "frac": dk["achieved_gbs"] / peak, "peak_source": peak_kind,
-                "traffic": traffic, "alg_bytes_per_launch": dk["alg_bytes_per_launch"]}
+                "traffic": traffic, "alg_bytes_per_launch": dk["alg_bytes_per_launch"],
+                "step": step_roofline(kernels, "launches_per_step", ms, peak)}
     gb = J * SG * 2 / 1e9
     res = {"workload": w.name, "ms_per_step": ms, "ms_per_gb": ms / gb, "grad_gb_per_worker": gb,
            "simulated_workers": N, "topology": w.topology, "coords_per_worker": w.n, "super_groups": J,
@@ -889,7 +901,8 @@ def run_gpu_bucketed(args, rank, world, local, w, dev):
                 "peak": peak, "unit": "GB/s", "frac": dk["achieved_gbs"] / peak, "peak_source": peak_kind,
                 "traffic": traffic, "alg_bytes_per_launch": dk["alg_bytes_per_launch"],
                 "note": "planning kernels run on a second stream under the exchange's launches, so the "
-                        "launch shares add up to more than the step"}
+                        "launch shares add up to more than the step",
+                "step": step_roofline(kernels, "launches_per_step", ms, peak)}
 
     ms_seq = ms_alt = None
     if not args.lean:
