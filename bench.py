@@ -255,8 +255,9 @@ def launch_bytes(kind: int, sgs: int, msg_per_sg: float, fp32_addend: bool = Fal
     super-group read (once for up to 16 outputs);
     stats: bf16 gradient 512 B/SG + mean and squared norm 8 B/SG;
     allocate + reorder span: N x 8 B/SG of statistics read, M, F, mu written
-    (12 B/SG), then about five passes over F (20 B/SG) and the bitwidths and
-    permutation (about 7 B/SG); fused ring exchange: the compress, N-1 DARs
+    (12 B/SG), then two more select passes and the bitwidth pass over F
+    (12 B/SG), the bitwidths written and read back (2 B/SG) and the
+    permutation written (4 B/SG); fused ring exchange: the compress, N-1 DARs
     and a decode that reads each message once and writes N outputs;
     pipelined ring exchange: the same bytes per round, each launch counted
     by its share of the round's super-groups (its logged hop and decode
@@ -276,7 +277,7 @@ def launch_bytes(kind: int, sgs: int, msg_per_sg: float, fp32_addend: bool = Fal
         J = sgs / (n_ranks + 1)
         return J * ((512 + msg_per_sg + 8) + (n_ranks - 1) * (2 * msg_per_sg + 512 + 8) +
                     (msg_per_sg + 8 + 1024 * n_ranks))
-    return sgs * (8 * n_ranks + 12 + 20 + 7)
+    return sgs * (8 * n_ranks + 12 + 12 + 2 + 4)
 
 
 def hop_roles(butterfly: bool, n_ranks: int):
