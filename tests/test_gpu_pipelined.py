@@ -65,6 +65,20 @@ def test_pipelined_equals_oracle_and_per_step(N, parts):
         assert np.array_equal(o.numpy().view(np.int32), np.ascontiguousarray(exp, np.float32).view(np.int32))
 
 
+@pytest.mark.parametrize("N,parts", [(32, 1), (32, 7), (64, 3), (64, 40)])
+def test_pipelined_many_ranks_equals_oracle(N, parts):
+    """Rings of 32 and 64 ranks (up to the exchange's limit): N x N message
+    buffers, decodes into more than 16 outputs per launch (2N row copies per
+    pair of super-groups), and more parts than a chunk has units."""
+    gr = grads_for("gemma1b_ring16", 256 * 400 + 13, N, seed=N * 7 + parts)
+    _, outs, _ = _run(gr, N, parts, budget=5.0, correlated=True)
+    cfg = oracle.Config(N, 5.0, correlated=True, seed=1, round=2)
+    _, exp = oracle.allreduce(cfg, gr)
+    want = np.ascontiguousarray(exp, np.float32).view(np.int32)
+    for r in (0, 1, N // 2, N - 1):
+        assert np.array_equal(outs[r].numpy().view(np.int32), want), r
+
+
 @pytest.mark.parametrize("kw", [dict(eps=0.3), dict(eps=math.inf, correlated=False), dict(scale_fp32=True),
                                 dict(fixed_bits=2, budget=2.0), dict(fixed_bits=8, budget=8.0),
                                 dict(out_dtype=torch.bfloat16)])

@@ -252,3 +252,25 @@ def test_bucket_stream_library_staging_rejects_close_reuse():
     bs = BucketStream(N, bucket_sg, lookahead=lookahead)
     with pytest.raises(dq.DQError):
         bs.run(bufs, outs, src_host=hosts)
+
+
+@pytest.mark.parametrize("last_sg", [1, 3, 7])
+def test_bucket_stream_last_bucket_smaller_than_ring(last_sg):
+    """A last bucket with fewer super-groups than the ring has ranks (8):
+    some chunks are empty, which the device-side chunk geometry must cut the
+    same way as the host's; every bucket equals the oracle's all-reduce."""
+    build.build()
+    N, bucket_sg = 8, 23
+    w = synth.WORKLOADS["llama3_8b_ring8_buckets"]
+    w = w.__class__(**{**w.__dict__, "n_ranks": N, "n": 256 * (4 * bucket_sg + last_sg), "bucket": 256 * bucket_sg})
+    nb = synth.bucket_count(w)
+    buckets = [synth.generate_bucket(w, k, "cuda", seed=11 + last_sg) for k in range(nb)]
+    assert buckets[-1][0].numel() == 256 * last_sg
+    outs = [[torch.empty(g.numel(), dtype=torch.float32, device="cuda") for g in b] for b in buckets]
+    BucketStream(N, bucket_sg, budget=5.0, correlated=True).run(buckets, outs, round0=70)
+    torch.cuda.synchronize()
+    for k, b in enumerate(buckets):
+        gu = [synth.as_u16(g) for g in b]
+        _, exp = oracle.allreduce(oracle.Config(N, 5.0, correlated=True, round=70 + k), gu)
+        for r in range(N):
+            assert np.array_equal(outs[k][r].cpu().numpy().view(np.int32), exp.view(np.int32)), (k, r)
