@@ -453,6 +453,11 @@ dq_status dq_exchange_stream_step(const dq_config *cfg, const dq_bucket_step *st
  *   (dq_plan_workspace_bytes(N, bucket_sg)) and the messages
  *   (dq_bucket_msgs_bytes(cfg, bucket_sg)), bucket_sg >= every n_sg.
  *   counters_dev: device, n_buckets + N uint32 (zeroed by the call).
+ *   nonfinite_dev: NULL, or a device int32 (4-byte aligned) that the call
+ *   clears and that becomes 1 when any bucket's statistics are not finite
+ *   (what dq_plan reports as DQ_ERR_NONFINITE: that bucket's results are
+ *   meaningless, the others are unaffected); read it after the work, e.g.
+ *   with dq_get_device_status.
  *   plan_stream: the planning stream (NULL: `stream`); give it a higher
  *   priority than `stream`, so that its short kernels take SMs as the
  *   exchange's launches free them.
@@ -476,8 +481,8 @@ typedef struct {
 
 dq_status dq_allreduce_stream(const dq_config *cfg, const dq_bucket *buckets, int32_t n_buckets,
                               const dq_stream_set *sets, int32_t n_sets, int32_t lookahead, int32_t plan_sms,
-                              unsigned int *counters_dev, int32_t out_is_bf16, void *plan_stream, void *stream,
-                              dq_launch_log *log);
+                              unsigned int *counters_dev, int32_t out_is_bf16, int32_t *nonfinite_dev,
+                              void *plan_stream, void *stream, dq_launch_log *log);
 
 /* dq_allreduce_stream with the host staging of every bucket done by the
  * library: the DDP bucket stream end to end, gradients arriving from host
@@ -512,8 +517,8 @@ typedef struct {
 dq_status dq_allreduce_stream_io(const dq_config *cfg, const dq_bucket *buckets, const dq_bucket_io *io,
                                  int32_t n_buckets, const dq_stream_set *sets, int32_t n_sets, int32_t lookahead,
                                  int32_t plan_sms, unsigned int *counters_dev, int32_t out_is_bf16,
-                                 void *copy_in_stream, void *copy_out_stream, void *plan_stream, void *stream,
-                                 dq_launch_log *log);
+                                 int32_t *nonfinite_dev, void *copy_in_stream, void *copy_out_stream,
+                                 void *plan_stream, void *stream, dq_launch_log *log);
 
 /* Reads a device status word into host memory [boundary of the hot path:
  * device-side errors of an asynchronous call are reported through a status

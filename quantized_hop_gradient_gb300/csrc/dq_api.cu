@@ -722,7 +722,7 @@ struct PlanDev {
 // nothing is read back.
 dq_status plan_enqueue(const dq_config *cfg, const void *const *grads, int64_t n_sg, float *mu, int32_t *perm,
                        void *ws, size_t ws_bytes, void *const *rank_ready, dq_launch_log *log, cudaStream_t st,
-                       PlanDev &out)
+                       PlanDev &out, int32_t *sticky = nullptr)
 {
     if (!cfg_ok(cfg) || !grads || !mu || !perm || !ws || n_sg < 1 || n_sg >= kMaxSG) return DQ_ERR_INVALID_ARG;
     const int32_t N = cfg->n_ranks;
@@ -778,10 +778,10 @@ dq_status plan_enqueue(const dq_config *cfg, const void *const *grads, int64_t n
     if (small) {
         // small problems: the metadata all-reduce, then allocation and reorder in one launch
         if (launch_stats_reduce(mean_all, sq_all, N, n_sg, M, F, mu, st, nonfinite) != cudaSuccess) return DQ_ERR_CUDA;
-        if (launch_plan_small(F, n_sg, cap, cfg->fixed_bits, b, T, counts, perm, st) != cudaSuccess)
+        if (launch_plan_small(F, n_sg, cap, cfg->fixed_bits, b, T, counts, perm, st, nonfinite, sticky) != cudaSuccess)
             return DQ_ERR_CUDA;
     } else if (launch_plan_chain(mean_all, sq_all, N, n_sg, cap, cfg->fixed_bits, M, F, mu, nonfinite, b, T, counts,
-                                 perm, scratch, st) != cudaSuccess) {
+                                 perm, scratch, st, sticky) != cudaSuccess) {
         return DQ_ERR_CUDA;
     }
     log_end(slot, st);
@@ -1236,13 +1236,13 @@ namespace {
 // t + lookahead (after its upload, if any) and exchange launch t.
 dq_status allreduce_stream(const dq_config *cfg, const dq_bucket *buckets, const dq_bucket_io *io,
                            int32_t n_buckets, const dq_stream_set *sets, int32_t n_sets, int32_t lookahead,
-                           int32_t plan_sms, unsigned int *counters_dev, int32_t out_is_bf16, cudaStream_t cin,
-                           cudaStream_t cout, cudaStream_t ps, cudaStream_t st, dq_launch_log *log)
+                           int32_t plan_sms, unsigned int *counters_dev, int32_t out_is_bf16, int32_t *nonfinite_dev,
+                           cudaStream_t cin, cudaStream_t cout, cudaStream_t ps, cudaStream_t st, dq_launch_log *log)
 {
     if (!stream_cfg_ok(cfg) || !buckets || !sets || !counters_dev || n_buckets < 1) return DQ_ERR_INVALID_ARG;
     const int32_t N = cfg->n_ranks;
     if (lookahead < 1 || n_sets < N + lookahead + 1 || plan_sms < 0 || plan_sms >= sm_count()) return DQ_ERR_INVALID_ARG;
-    if ((uintptr_t)counters_dev & 3u) return DQ_ERR_ALIGNMENT;
+    if (((uintptr_t)counters_dev & 3u) || ((uintptr_t)nonfinite_dev & 3u)) return DQ_ERR_ALIGNMENT;
     for (int32_t k = 0; k < n_buckets; ++k)
         if (buckets[k].n_sg < 1 || buckets[k].n_sg >= kMaxSG || !buckets[k].grads_host || !buckets[k].outs_host)
             return DQ_ERR_INVALID_ARG;
@@ -1290,6 +1290,8 @@ dq_status allreduce_stream(const dq_config *cfg, const dq_bucket *buckets, const
     auto ev_dec = [&](int32_t k) { return E.ev[2 * n_sets + 2 * R + (k % R)]; };
     auto ev_out = [&](int32_t k) { return E.ev[2 * n_sets + 3 * R + (k % R)]; };
     cudaEvent_t ev_start = E.ev[E.ev.size() - 2], ev_end = E.ev.back();
+    // the pass's non-finite flag is cleared before any planning starts
+    if (nonfinite_dev && zero_words(nonfinite_dev, 1, nullptr, st) != cudaSuccess) return DQ_ERR_CUDA;
     // the other streams start after everything already enqueued on `stream`
     // (earlier work may still use the sets, the staging or the outputs)
     if (cudaEventRecord(ev_start, st) != cudaSuccess) return DQ_ERR_CUDA;
@@ -1326,7 +1328,7 @@ dq_status allreduce_stream(const dq_config *cfg, const dq_bucket *buckets, const
         PlanDev d;
         const dq_stream_set &S = sets[si];
         s = plan_enqueue(&c, buckets[k].grads_host, buckets[k].n_sg, S.mu, S.perm, S.plan_ws, S.plan_ws_bytes,
-                         nullptr, log, ps, d);
+                         nullptr, log, ps, d, nonfinite_dev);
         if (s != DQ_OK) return s;
         counts[k] = d.counts;
         return cudaEventRecord(ev_plan(si), ps) == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
@@ -1376,20 +1378,20 @@ extern "C" {
 
 dq_status dq_allreduce_stream(const dq_config *cfg, const dq_bucket *buckets, int32_t n_buckets,
                               const dq_stream_set *sets, int32_t n_sets, int32_t lookahead, int32_t plan_sms,
-                              unsigned int *counters_dev, int32_t out_is_bf16, void *plan_stream, void *stream,
-                              dq_launch_log *log)
+                              unsigned int *counters_dev, int32_t out_is_bf16, int32_t *nonfinite_dev,
+                              void *plan_stream, void *stream, dq_launch_log *log)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaStream_t ps = plan_stream ? static_cast<cudaStream_t>(plan_stream) : st;
     return allreduce_stream(cfg, buckets, nullptr, n_buckets, sets, n_sets, lookahead, plan_sms, counters_dev,
-                            out_is_bf16, st, st, ps, st, log);
+                            out_is_bf16, nonfinite_dev, st, st, ps, st, log);
 }
 
 dq_status dq_allreduce_stream_io(const dq_config *cfg, const dq_bucket *buckets, const dq_bucket_io *io,
                                  int32_t n_buckets, const dq_stream_set *sets, int32_t n_sets, int32_t lookahead,
                                  int32_t plan_sms, unsigned int *counters_dev, int32_t out_is_bf16,
-                                 void *copy_in_stream, void *copy_out_stream, void *plan_stream, void *stream,
-                                 dq_launch_log *log)
+                                 int32_t *nonfinite_dev, void *copy_in_stream, void *copy_out_stream,
+                                 void *plan_stream, void *stream, dq_launch_log *log)
 {
     if (!io) return DQ_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1397,7 +1399,7 @@ dq_status dq_allreduce_stream_io(const dq_config *cfg, const dq_bucket *buckets,
     cudaStream_t cin = copy_in_stream ? static_cast<cudaStream_t>(copy_in_stream) : ps;
     cudaStream_t cout = copy_out_stream ? static_cast<cudaStream_t>(copy_out_stream) : st;
     return allreduce_stream(cfg, buckets, io, n_buckets, sets, n_sets, lookahead, plan_sms, counters_dev, out_is_bf16,
-                            cin, cout, ps, st, log);
+                            nonfinite_dev, cin, cout, ps, st, log);
 }
 
 dq_status dq_get_device_status(const int32_t *status_dev, int32_t *status_host, void *stream)

@@ -46,15 +46,19 @@ cudaError_t launch_reorder(const uint8_t *b, int64_t n_sg, int32_t *perm, void *
 // The planning after the statistics, for any size: metadata all-reduce
 // (M, F, mu from the ranks' per-super-group statistics), allocation and
 // reorder in 3 + passes launches; ws holds plan_scratch_bytes(n_sg).
-// fixed_bits != 0 gives every super-group that width.
+// fixed_bits != 0 gives every super-group that width.  sticky (optional):
+// set to 1, and never cleared, when the statistics are not finite.
 cudaError_t launch_plan_chain(const float *mean_all, const float *sq_all, int32_t n_ranks, int64_t n_sg,
                               int64_t cap_bits, int32_t fixed_bits, float *M, float *F, float *mu,
                               int32_t *nonfinite, uint8_t *b, float *T, int64_t *counts, int32_t *perm, void *ws,
-                              cudaStream_t st);
+                              cudaStream_t st, int32_t *sticky = nullptr);
 // allocation and reorder of up to small_plan_max_sg() super-groups in one launch
 int64_t small_plan_max_sg();
+// nonfinite: the flag the statistics reduce before this launch set;
+// sticky (optional) receives it as launch_plan_chain's.
 cudaError_t launch_plan_small(const float *F, int64_t n_sg, int64_t cap_bits, int32_t fixed_bits, uint8_t *b,
-                              float *T, int64_t *counts, int32_t *perm, cudaStream_t st);
+                              float *T, int64_t *counts, int32_t *perm, cudaStream_t st,
+                              const int32_t *nonfinite = nullptr, int32_t *sticky = nullptr);
 
 // Brackets one launch with the caller's events (if a log has room).
 struct LogSlot {

@@ -143,8 +143,10 @@ __device__ void select_digit(AllocState *st, int pass)
 // the last block to finish picks the digit.  REDUCE (pass 0 of the planning
 // chain): F is first computed from the ranks' per-super-group statistics,
 // as the metadata all-reduce does (M_j, F_j summed over ranks 0..N-1 in
-// order, mu_j = fl(M_j / N)), and written with M and mu.  hist = false
-// (REDUCE only: budget >= 8 bits or a fixed bitwidth) skips the histogram.
+// order, mu_j = fl(M_j / N)), and written with M and mu; a non-finite M_j
+// or F_j sets *nonfinite and, if given, the caller's *sticky flag (which
+// collects the planning of many buckets).  hist = false (REDUCE only:
+// budget >= 8 bits or a fixed bitwidth) skips the histogram.
 template <bool REDUCE>
 __global__ void __launch_bounds__(kAllocThreads) alloc_pass_kernel(const float *__restrict__ Fin, int64_t n,
                                                                    AllocState *st, int pass, bool hist,
@@ -152,7 +154,8 @@ __global__ void __launch_bounds__(kAllocThreads) alloc_pass_kernel(const float *
                                                                    const float *__restrict__ sq_all, int32_t n_ranks,
                                                                    float *__restrict__ M, float *__restrict__ Fout,
                                                                    float *__restrict__ mu,
-                                                                   int32_t *__restrict__ nonfinite)
+                                                                   int32_t *__restrict__ nonfinite,
+                                                                   int32_t *__restrict__ sticky)
 {
     __shared__ unsigned int h[kBins];
     __shared__ bool last;
@@ -193,7 +196,10 @@ __global__ void __launch_bounds__(kAllocThreads) alloc_pass_kernel(const float *
                 if (M) M[j] = m;
                 Fout[j] = f;
                 mu[j] = __fdiv_rn(m, (float)n_ranks);
-                if (nonfinite && !(isfinite(m) && isfinite(f))) atomicOr(nonfinite, 1);
+                if (nonfinite && !(isfinite(m) && isfinite(f))) {
+                    atomicOr(nonfinite, 1);
+                    if (sticky) atomicOr(sticky, 1);
+                }
             } else {
                 f = __ldg(Fin + j);
             }
@@ -402,7 +408,8 @@ constexpr int kSmallPlanThreads = 1024;
 __global__ void __launch_bounds__(kSmallPlanThreads) plan_small_kernel(const float *__restrict__ F, int32_t n,
                                                                        long long R, int32_t all8, int32_t fixed_bits,
                                                                        uint8_t *__restrict__ b, float *T,
-                                                                       int64_t *counts, int32_t *__restrict__ perm)
+                                                                       int64_t *counts, int32_t *__restrict__ perm,
+                                                                       const int32_t *nonfinite, int32_t *sticky)
 {
     extern __shared__ float sF[];
     __shared__ unsigned int hist[256];
@@ -514,6 +521,7 @@ __global__ void __launch_bounds__(kSmallPlanThreads) plan_small_kernel(const flo
         counts[1] = tot1;
         counts[2] = tot2;
         *T = __uint_as_float(t);
+        if (sticky && nonfinite && *nonfinite) atomicOr(sticky, 1);   // the reduce before this launch set it
     }
 }
 
@@ -548,7 +556,7 @@ cudaError_t launch_allocate(const float *F, int64_t n_sg, int64_t cap_bits, uint
         const int blocks = alloc_blocks(n_sg);
         for (int pass = 0; pass < kSelectPasses; ++pass)
             alloc_pass_kernel<false><<<blocks, kAllocThreads, 0, st>>>(F, n_sg, s, pass, true, nullptr, nullptr, 0,
-                                                                       nullptr, nullptr, nullptr, nullptr);
+                                                                       nullptr, nullptr, nullptr, nullptr, nullptr);
     }
     const int64_t n_tiles = (n_sg + kTile - 1) / kTile;
     tile_assign_kernel<<<(unsigned)n_tiles, kTileThreads, 0, st>>>(F, n_sg, s, 0, b, tiles, counts, T);
@@ -570,7 +578,7 @@ cudaError_t launch_reorder(const uint8_t *b, int64_t n_sg, int32_t *perm, void *
 cudaError_t launch_plan_chain(const float *mean_all, const float *sq_all, int32_t n_ranks, int64_t n_sg,
                               int64_t cap_bits, int32_t fixed_bits, float *M, float *F, float *mu,
                               int32_t *nonfinite, uint8_t *b, float *T, int64_t *counts, int32_t *perm, void *ws,
-                              cudaStream_t st)
+                              cudaStream_t st, int32_t *sticky)
 {
     AllocState *s = static_cast<AllocState *>(ws);
     long long *tiles = reinterpret_cast<long long *>(static_cast<uint8_t *>(ws) + kAllocStateBytes);
@@ -580,10 +588,10 @@ cudaError_t launch_plan_chain(const float *mean_all, const float *sq_all, int32_
     const int64_t n_tiles = (n_sg + kTile - 1) / kTile;
     alloc_init_kernel<<<1, 256, 0, st>>>(s, R, all8, counts, nonfinite);
     alloc_pass_kernel<true><<<blocks, kAllocThreads, 0, st>>>(nullptr, n_sg, s, 0, !all8, mean_all, sq_all, n_ranks,
-                                                              M, F, mu, nonfinite);
+                                                              M, F, mu, nonfinite, sticky);
     for (int pass = 1; pass < kSelectPasses && !all8; ++pass)
         alloc_pass_kernel<false><<<blocks, kAllocThreads, 0, st>>>(F, n_sg, s, pass, true, nullptr, nullptr, 0,
-                                                                   nullptr, nullptr, nullptr, nullptr);
+                                                                   nullptr, nullptr, nullptr, nullptr, nullptr);
     tile_assign_kernel<<<(unsigned)n_tiles, kTileThreads, 0, st>>>(F, n_sg, s, fixed_bits, b, tiles, counts, T);
     reorder_scatter_kernel<<<(unsigned)n_tiles, kTileThreads, 0, st>>>(b, n_sg, tiles, perm);
     note_launches(all8 ? 4 : 3 + kSelectPasses);
@@ -593,7 +601,8 @@ cudaError_t launch_plan_chain(const float *mean_all, const float *sq_all, int32_
 int64_t small_plan_max_sg() { return kSmallPlanMaxSG; }
 
 cudaError_t launch_plan_small(const float *F, int64_t n_sg, int64_t cap_bits, int32_t fixed_bits, uint8_t *b,
-                              float *T, int64_t *counts, int32_t *perm, cudaStream_t st)
+                              float *T, int64_t *counts, int32_t *perm, cudaStream_t st, const int32_t *nonfinite,
+                              int32_t *sticky)
 {
     if (n_sg < 1 || n_sg > kSmallPlanMaxSG) return cudaErrorInvalidValue;
     const size_t smem = (size_t)n_sg * sizeof(float);
@@ -614,7 +623,8 @@ cudaError_t launch_plan_small(const float *F, int64_t n_sg, int64_t cap_bits, in
     }
     const long long R = (long long)(cap_bits - 2 * n_sg);
     const int all8 = R >= 6 * (long long)n_sg ? 1 : 0;
-    plan_small_kernel<<<1, kSmallPlanThreads, smem, st>>>(F, (int32_t)n_sg, R, all8, fixed_bits, b, T, counts, perm);
+    plan_small_kernel<<<1, kSmallPlanThreads, smem, st>>>(F, (int32_t)n_sg, R, all8, fixed_bits, b, T, counts, perm,
+                                                          nonfinite, sticky);
     note_launches(1);
     return cudaGetLastError();
 }

@@ -136,10 +136,11 @@ _SIGS = {
                        C.c_size_t, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "dq_bucket_msgs_bytes": ([C.POINTER(dq_config), C.c_int64], C.c_size_t),
     "dq_allreduce_stream": ([C.POINTER(dq_config), C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_int32,
-                             C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
+                             C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p],
+                            C.c_int),
     "dq_allreduce_stream_io": ([C.POINTER(dq_config), C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_int32,
                                 C.c_int32, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
-                                C.c_void_p, C.c_void_p], C.c_int),
+                                C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
     "dq_exchange_stream_step": ([C.POINTER(dq_config), C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p,
                                  C.c_void_p], C.c_int),
     "dq_barrier_selftest": ([C.c_int32, C.c_int32, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p], C.c_int),
@@ -331,20 +332,23 @@ def dq_bucket_msgs_bytes(cfg, n_sg) -> int:
 
 
 def dq_allreduce_stream(cfg, buckets, sets, counters, out_is_bf16=False, plan_stream=None, stream=None,
-                        log: "LaunchLog" = None, lookahead: int = 1, plan_sms: int = 0):
+                        log: "LaunchLog" = None, lookahead: int = 1, plan_sms: int = 0, nonfinite=None):
     """A whole bucket stream in one call.  ``buckets``: a ctypes array of
     dq_bucket; ``sets``: a ctypes array of dq_stream_set; ``counters``: a
-    device int32 tensor of at least len(buckets) + N words."""
+    device int32 tensor of at least len(buckets) + N words; ``nonfinite``:
+    None or a device int32 that becomes 1 if some bucket's statistics are
+    not finite."""
     _check(lib().dq_allreduce_stream(C.byref(cfg), C.cast(buckets, C.c_void_p), len(buckets),
                                      C.cast(sets, C.c_void_p), len(sets), int(lookahead), int(plan_sms),
                                      _ptr(counters), int(out_is_bf16),
+                                     _ptr(nonfinite) if nonfinite is not None else None,
                                      _stream(plan_stream) if plan_stream is not None else None, _stream(stream),
                                      C.byref(log.c) if log is not None else None), "dq_allreduce_stream")
 
 
 def dq_allreduce_stream_io(cfg, buckets, io, sets, counters, out_is_bf16=False, copy_in_stream=None,
                            copy_out_stream=None, plan_stream=None, stream=None, log: "LaunchLog" = None,
-                           lookahead: int = 1, plan_sms: int = 0):
+                           lookahead: int = 1, plan_sms: int = 0, nonfinite=None):
     """dq_allreduce_stream with each bucket's upload and download done by the
     library.  ``io``: a ctypes array of dq_bucket_io, one per bucket."""
     if len(io) != len(buckets):
@@ -352,7 +356,8 @@ def dq_allreduce_stream_io(cfg, buckets, io, sets, counters, out_is_bf16=False, 
     opt = lambda st: _stream(st) if st is not None else None
     _check(lib().dq_allreduce_stream_io(C.byref(cfg), C.cast(buckets, C.c_void_p), C.cast(io, C.c_void_p),
                                         len(buckets), C.cast(sets, C.c_void_p), len(sets), int(lookahead),
-                                        int(plan_sms), _ptr(counters), int(out_is_bf16), opt(copy_in_stream),
+                                        int(plan_sms), _ptr(counters), int(out_is_bf16),
+                                        _ptr(nonfinite) if nonfinite is not None else None, opt(copy_in_stream),
                                         opt(copy_out_stream), opt(plan_stream), _stream(stream),
                                         C.byref(log.c) if log is not None else None), "dq_allreduce_stream_io")
 

@@ -128,10 +128,20 @@ class BucketStream:
         self.ev_free = [torch.cuda.Event() for _ in range(self.depth)]
         self.counters = torch.zeros(1024, dtype=torch.int32, device=dev)
         self.nonfinite = [None] * self.depth
+        # set by the library when some bucket of the last pass had non-finite statistics
+        self.pass_nonfinite = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def config(self, round: int = 0):
         return self.dq.config(self.n_ranks, self.budget, self.eps, self.correlated, self.seed, round,
                               self.fixed_bits, self.scale_fp32)
+
+    def check(self):
+        """Raises dq.NonFinite if some bucket of the last pass driven by the
+        library had non-finite statistics (a NaN or infinite gradient, or
+        squares beyond fp32); synchronises the current stream.  The passes
+        with hooks plan bucket by bucket and are not covered."""
+        if self.dq.dq_get_device_status(self.pass_nonfinite) != 0:
+            raise self.dq.NonFinite(self.dq.DQ_ERR_NONFINITE, "bucket stream: non-finite gradient statistics")
 
     def copy_streams(self):
         """The (upload, download) streams of the library's host staging."""
@@ -181,7 +191,8 @@ class BucketStream:
                                             for s in self.sets])
             if src_host is None and dst_host is None:
                 dq.dq_allreduce_stream(self.config(0), arr, sets, self.counters, self.out_is_bf16, side, main, log,
-                                       lookahead=self.lookahead, plan_sms=self.plan_sms)
+                                       lookahead=self.lookahead, plan_sms=self.plan_sms,
+                                       nonfinite=self.pass_nonfinite)
                 return
             io = (dq.dq_bucket_io * nb)()
             for k in range(nb):
@@ -208,7 +219,8 @@ class BucketStream:
             if copy_out is None:
                 copy_out = self.copy_streams()[1]
             dq.dq_allreduce_stream_io(self.config(0), arr, io, sets, self.counters, self.out_is_bf16, copy_in,
-                                      copy_out, side, main, log, lookahead=self.lookahead, plan_sms=self.plan_sms)
+                                      copy_out, side, main, log, lookahead=self.lookahead, plan_sms=self.plan_sms,
+                                      nonfinite=self.pass_nonfinite)
             return
         if src_host is not None or dst_host is not None:
             raise ValueError("host staging by the library cannot be combined with hooks or ready events")

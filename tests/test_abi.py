@@ -139,16 +139,17 @@ def test_bucket_stream_arguments_rejected_on_the_host(L):
     sets = (dq.dq_stream_set * 8)(*[dq.dq_stream_set(P, P, P, 1 << 20, P, 1 << 20) for _ in range(8)])
     io = (dq.dq_bucket_io * 2)(*[dq.dq_bucket_io(ctypes.cast(ptrs, ctypes.c_void_p), P) for _ in range(2)])
     cfg4, cfg9 = dq.config(4), dq.config(9)
-    # dq_allreduce_stream(cfg, buckets, n, sets, n_sets, lookahead, plan_sms, counters, bf16, plan_stream, stream, log)
-    assert L.dq_allreduce_stream(cfg4, b, 0, sets, 8, 3, 0, P, 0, None, st, None) == dq.DQ_ERR_INVALID_ARG
-    assert L.dq_allreduce_stream(cfg9, b, 2, sets, 8, 3, 0, P, 0, None, st, None) == dq.DQ_ERR_INVALID_ARG
-    assert L.dq_allreduce_stream(cfg4, b, 2, sets, 8, 0, 0, P, 0, None, st, None) == dq.DQ_ERR_INVALID_ARG
-    assert L.dq_allreduce_stream(cfg4, b, 2, sets, 7, 3, 0, P, 0, None, st, None) == dq.DQ_ERR_INVALID_ARG
-    # dq_allreduce_stream_io(cfg, buckets, io, n, sets, n_sets, lookahead, plan_sms, counters, bf16,
+    # dq_allreduce_stream(cfg, buckets, n, sets, n_sets, lookahead, plan_sms, counters, bf16, nonfinite,
+    #                     plan_stream, stream, log)
+    assert L.dq_allreduce_stream(cfg4, b, 0, sets, 8, 3, 0, P, 0, P, None, st, None) == dq.DQ_ERR_INVALID_ARG
+    assert L.dq_allreduce_stream(cfg9, b, 2, sets, 8, 3, 0, P, 0, P, None, st, None) == dq.DQ_ERR_INVALID_ARG
+    assert L.dq_allreduce_stream(cfg4, b, 2, sets, 8, 0, 0, P, 0, P, None, st, None) == dq.DQ_ERR_INVALID_ARG
+    assert L.dq_allreduce_stream(cfg4, b, 2, sets, 7, 3, 0, P, 0, None, None, st, None) == dq.DQ_ERR_INVALID_ARG
+    # dq_allreduce_stream_io(cfg, buckets, io, n, sets, n_sets, lookahead, plan_sms, counters, bf16, nonfinite,
     #                        copy_in, copy_out, plan_stream, stream, log)
-    assert L.dq_allreduce_stream_io(cfg4, b, None, 2, sets, 8, 3, 0, P, 0, None, None, None, st,
+    assert L.dq_allreduce_stream_io(cfg4, b, None, 2, sets, 8, 3, 0, P, 0, P, None, None, None, st,
                                     None) == dq.DQ_ERR_INVALID_ARG
-    assert L.dq_allreduce_stream_io(cfg4, b, io, 2, sets, 7, 3, 0, P, 0, None, None, None, st,
+    assert L.dq_allreduce_stream_io(cfg4, b, io, 2, sets, 7, 3, 0, P, 0, None, None, None, None, st,
                                     None) == dq.DQ_ERR_INVALID_ARG
-    assert L.dq_allreduce_stream_io(cfg9, b, io, 2, sets, 8, 3, 0, P, 0, None, None, None, st,
+    assert L.dq_allreduce_stream_io(cfg9, b, io, 2, sets, 8, 3, 0, P, 0, P, None, None, None, st,
                                     None) == dq.DQ_ERR_INVALID_ARG

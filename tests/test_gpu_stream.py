@@ -274,3 +274,50 @@ def test_bucket_stream_last_bucket_smaller_than_ring(last_sg):
         _, exp = oracle.allreduce(oracle.Config(N, 5.0, correlated=True, round=70 + k), gu)
         for r in range(N):
             assert np.array_equal(outs[k][r].cpu().numpy().view(np.int32), exp.view(np.int32)), (k, r)
+
+
+@pytest.mark.parametrize("bucket_sg,staged", [(29, False), (20000, False), (29, True)])
+def test_bucket_stream_reports_nonfinite(bucket_sg, staged):
+    """A NaN in one rank's gradient of one bucket makes the pass's flag read
+    non-finite (BucketStream.check raises dq.NonFinite), on both planning
+    paths (single-block up to 16,384 super-groups, the launch chain above)
+    and with the library's host staging; the other buckets still equal the
+    oracle's, and a clean pass afterwards checks clean."""
+    from quantized_hop_gradient_gb300 import dq
+    build.build()
+    N = 2
+    w = synth.WORKLOADS["llama3_8b_ring8_buckets"]
+    w = w.__class__(**{**w.__dict__, "n_ranks": N, "n": 256 * (5 * bucket_sg + 3), "bucket": 256 * bucket_sg})
+    nb = synth.bucket_count(w)
+    clean = [synth.generate_bucket(w, k, "cpu", seed=12) for k in range(nb)]
+    bad = [[g.clone() for g in b] for b in clean]
+    bad[2][1][256 * (bucket_sg // 2) + 5] = float("nan")
+    bs = BucketStream(N, bucket_sg, budget=5.0, correlated=True)
+
+    def run(src):
+        outs = [[torch.empty(g.numel(), dtype=torch.float32, device="cuda") for g in b] for b in src]
+        if staged:
+            S = bs.depth
+            stage = [[torch.empty(256 * bucket_sg, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+                     for _ in range(S)]
+            bufs = [[t[:g.numel()] for t, g in zip(stage[k % S], src[k])] for k in range(nb)]
+            hosts = [[g.pin_memory() for g in b] for b in src]
+            res = [torch.empty(b[0].numel(), dtype=torch.float32).pin_memory() for b in src]
+            bs.run(bufs, outs, round0=80, src_host=hosts, dst_host=res)
+            torch.cuda.current_stream().synchronize()
+            return [r.numpy() for r in res]
+        bs.run([[g.cuda() for g in b] for b in src], outs, round0=80)
+        torch.cuda.synchronize()
+        return [o[0].cpu().numpy() for o in outs]
+
+    got = run(bad)
+    with pytest.raises(dq.NonFinite):
+        bs.check()
+    for k in range(nb):
+        if k == 2:
+            continue
+        gu = [synth.as_u16(g) for g in clean[k]]
+        _, exp = oracle.allreduce(oracle.Config(N, 5.0, correlated=True, round=80 + k), gu)
+        assert np.array_equal(got[k].view(np.int32), exp.view(np.int32)), k
+    run(clean)
+    bs.check()
